@@ -1,0 +1,307 @@
+#!/usr/bin/env python3
+"""Throughput of the S_up (FO) calibration pass for one layer.
+
+A step is one affinity_up(FO) call over one batch of T synthetic tokens of a
+Qwen3-0.6B-shaped layer (by default): fp16 operand staging, the fold of
+W_o^(h) diag(gamma) [W_g | W_u], the operating-point + per-head tensor-core
+kernel, and the deterministic reductions.  Inputs are resident in HBM when
+the timed region starts; they are larger than L2 (402 MB of a and x per
+step), so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle on a token sample
+
+Under torchrun (N > 1) every rank processes its own token batch (weak
+scaling, no collective in the timed region); rank 0 prints the JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "calibration tokens/sec for S^up fo affinity per layer; % of GB300 bf16 tensor peak"
+
+
+def fo_flops(s) -> dict:
+    """Algorithmic flops (multiply-add = 2) of the S_up FO pass."""
+    fold = 2 * 2 * s.I * s.D * s.H * s.dh            # [Wg;Wu] diag(gamma) Wo^(h): (2I x D)(D x H dh)
+    gate_up = 2 * s.T * s.D * 2 * s.I                  # (gamma x / r) [Wg;Wu]^T
+    heads = 2 * s.T * s.H * s.dh * 2 * s.I             # a_h M_h for gate and up
+    return {"fold": fold, "gate_up": gate_up, "heads": heads, "total": fold + gate_up + heads,
+            "tile_kernel": gate_up + heads}
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"bf16_tflops": d["bf16_tflops"], "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_rate(shape, layer, budget_s: float = 10.0, max_tokens: int | None = None) -> dict:
+    """Time the fp64 oracle (as it stands) on the first tokens of the same layer."""
+    from oracle import affinity_oracle as O
+    cores = len(os.sched_getaffinity(0))
+
+    def run(n):
+        t0 = time.perf_counter()
+        O.s_up(layer["a"][:n], layer["x"][:n], layer["Wo"], layer["gamma"], layer["Wg"], layer["Wu"], layer["Wd"],
+               shape.H, shape.G, shape.dh, shape.eps, "fo")
+        return time.perf_counter() - t0
+
+    n0 = 32
+    t_probe = run(n0)
+    n = int(max(n0, min(shape.T, n0 * budget_s / max(t_probe, 1e-6))))
+    if max_tokens:
+        n = min(n, max_tokens)
+    t = run(n)
+    return {"value": n / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 numpy oracle, FO S_up over all {shape.I} neurons for the first {n} of {shape.T} tokens "
+                      f"({t:.1f} s wall, numpy BLAS threads over {cores} host cores)"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args) -> None:
+    from transformer_sharding_affinity_gb300 import workloads as W
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    shape = W.CONFIGS[args.workload]
+    sample = W.make_layer(shape.scaled(T=max(64, args.ref_tokens)))
+    tok = sample["a"].shape[0]
+    from oracle import affinity_oracle as O
+    for _ in range(args.warmup):
+        O.s_up(sample["a"][:8], sample["x"][:8], sample["Wo"], sample["gamma"], sample["Wg"], sample["Wu"],
+               sample["Wd"], shape.H, shape.G, shape.dh, shape.eps, "fo")
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.s_up(sample["a"], sample["x"], sample["Wo"], sample["gamma"], sample["Wg"], sample["Wu"], sample["Wd"],
+               shape.H, shape.G, shape.dh, shape.eps, "fo")
+    dt = time.perf_counter() - t0
+    v = tok * args.steps / dt
+    cores = len(os.sched_getaffinity(0))
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "T": shape.T, "D": shape.D, "H": shape.H, "G": shape.G,
+                       "d_head": shape.dh, "I": shape.I, "mode": "fo", "tokens_per_step": tok},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"each step: fp64 oracle FO S_up over all {shape.I} neurons for {tok} tokens "
+                                       f"of the {args.workload} workload"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3_0p6b_layer")
+    ap.add_argument("--mode", default="fo", choices=["fo", "add"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-tokens", type=int, default=256)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    from transformer_sharding_affinity_gb300 import binding as B
+    from transformer_sharding_affinity_gb300 import device as DV
+    from transformer_sharding_affinity_gb300 import workloads as W
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    B.load()
+
+    base = W.CONFIGS[args.workload]
+    shape = base.scaled(seed=base.seed + 1000 * rank)     # each rank: its own token batch
+    layer = W.make_layer(shape)
+    host = {k: DV.host_tensor(layer, k, shape.dtype).pin_memory() for k in DV.UP_KEYS}
+    dev = {k: v.to("cuda") for k, v in host.items()}
+    d = B.dims(shape.T, shape.D, shape.H, shape.G, shape.dh, shape.I, shape.eps)
+    mode = B.MODES[args.mode]
+    work = torch.empty(B.workspace_size(d, mode), dtype=torch.uint8, device="cuda")
+    S = torch.empty(shape.G, shape.I, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    ev_k0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_k1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for e in ev_k0 + ev_k1:
+        e.record()
+    torch.cuda.synchronize()
+
+    def step(i=None):
+        if i is not None:
+            B.set_timing_events(ev_k0[i], ev_k1[i])
+        B.affinity_up(dev["a"], dev["x"], dev["Wo"], dev["gamma"], dev["Wg"], dev["Wu"], dev["Wd"], d, mode, S,
+                      None, work, stream)
+        if i is not None:
+            B.set_timing_events(None, None)
+
+    for _ in range(args.warmup):
+        step()
+    st = B.device_status(work)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {B.strerror(st)}")
+
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0.record()
+        for i in range(args.steps):
+            step(i)
+        t1.record()
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    ms = t0.elapsed_time(t1)
+    kern_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(ev_k0, ev_k1)]))
+    st = B.device_status(work)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {B.strerror(st)}")
+    if ws > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+
+    # end to end: pinned host inputs -> device, the call, S back to the host, every step
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    S_host = torch.empty(shape.G, shape.I, pin_memory=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(args.e2e_steps):
+        for k in DV.UP_KEYS:
+            dev[k].copy_(host[k], non_blocking=True)
+        step()
+        S_host.copy_(S, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+    pk = peaks()
+    fl = fo_flops(shape)
+    flops_per_step = fl["total"] if args.mode == "fo" else fl["fold"] + 2 * shape.T * shape.H * shape.dh * 2 * shape.I
+    tile_flops = fl["tile_kernel"] if args.mode == "fo" else 2 * shape.T * shape.H * shape.dh * 2 * shape.I
+    achieved = tile_flops / (kern_ms * 1e-3) / 1e12
+    tokens = shape.T * ws
+    line = {
+        "metric": METRIC, "value": tokens / (ms_step * 1e-3), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp16 operands, fp32 accumulate (bf16 inputs)",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "T": shape.T, "D": shape.D, "H": shape.H, "G": shape.G,
+                   "d_head": shape.dh, "I": shape.I, "mode": args.mode, "parallelism": f"dp{ws} (token shards)",
+                   "l2": "inputs larger than L2 (a + x = %.0f MB per step); no flush" %
+                         ((shape.T * (shape.H * shape.dh + shape.D) * 2) / 2**20)},
+        "step_flops": flops_per_step,
+        "step_tflops": flops_per_step / (ms_step * 1e-3) / 1e12,
+        "step_frac_of_peak": flops_per_step / (ms_step * 1e-3) / 1e12 / pk["bf16_tflops"],
+        "roofline": {"bound": "tensor", "kernel": "affinity_tile_kernel<FO> (operating point + per-head contraction)",
+                     "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / pk["bf16_tflops"],
+                     "frac_sustained": achieved / pk["bf16_tflops_sustained"] if pk["bf16_tflops_sustained"] else None,
+                     "peak_source": pk["source"] + " bf16 dense (fp16 runs at the bf16 rate)",
+                     "kernel_ms": kern_ms, "algorithmic_flops_per_launch": tile_flops, "traffic": None},
+        "gpu_launches": 8 * args.steps,
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": shape.G * shape.I * 4, "ms_per_step": e2e_ms},
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        line["cpu_baseline"] = cpu_oracle_rate(shape, layer, args.cpu_budget)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,223 @@
+/*
+ * affinity.h -- C ABI of libaffinity, the GB300 (sm_103a) calibration pass
+ * that scores head->neuron and neuron->next-layer-KV-group affinity for
+ * affinity-aware sharding under Delayed Tensor Parallelism.
+ *
+ * Method: "Affinity-Aware Sharding for Delayed Tensor Parallelism"
+ * (de Reynal, 2026), §3 "Method: affinity-aware layouts":
+ *   - "Affinity scores": S_up in R^{G x I} (FO and ADD), S_down in R^{I x G},
+ *     equation (5) for the first-order damage Delta_hk;
+ *   - "Objective": unit-mass normalisation and J(h, nu), equation (6);
+ *   - "Optimiser": scoring the G!/((G/L)!)^L labelled balanced partitions
+ *     of the KV groups given the neighbouring neuron assignments.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  Tensors are dense, row-major, in PyTorch nn.Linear storage (out x in):
+ *    a     [T, H*d_head]  attention output of every head; head h owns columns
+ *                         h*d_head .. (h+1)*d_head-1
+ *    x     [T, D]         residual entering the FFN's pre-norm
+ *    Wo    [D, H*d_head]  attention output projection (W_o^(h) = its columns of head h)
+ *    gamma [D]            FFN pre-norm gain
+ *    Wg,Wu [I, D]         gate / up projections (row k = w^g_k, w^u_k)
+ *    Wd    [D, I]         down projection (column k = w^d_k)
+ *    gamma_next [D]       next layer's attention pre-norm gain
+ *    Wq_next [H*d_head, D], Wk_next [G*d_head, D], Wv_next [G*d_head, D]
+ *                         next layer's query / key / value projections
+ *  Element type: dims->dtype (AFF_BF16 or AFF_FP32) for every tensor.
+ *  Query head h belongs to KV group h / (H/G).
+ *  Device pointers are caller-owned (e.g. allocated through PyTorch); the
+ *  library never allocates, frees or keeps them.  Inputs are read-only.
+ *  Every device pointer must be 16-byte aligned.
+ *  Outputs are overwritten, never accumulated into.
+ *  All device work is enqueued on `stream` in order; no call synchronises
+ *  the device or the stream.  A call returns AFF_OK once its work is
+ *  enqueued; errors found on the device are latched into a status word in
+ *  the workspace and read with affinity_device_status().
+ *  Validation happens before any launch: a call that returns an error code
+ *  other than AFF_ERR_CUDA has enqueued nothing.
+ *  For fixed inputs, shapes and library build the outputs are bit-identical
+ *  from run to run (fixed reduction orders, no floating-point atomics).
+ *
+ *  bf16 path numerics: operands are staged as fp16 (the normalised FFN
+ *  input gamma*x/r, a/r, the folded per-head matrices, the SwiGLU operating
+ *  point) and contracted on the tensor cores with fp32 accumulation; token
+ *  sums are finished in fp64.  Intermediates must fit fp16's range
+ *  (|value| < 65504); an overflow latches AFF_ERR_RANGE.  fp32 path: fp32
+ *  arithmetic on the CUDA cores (meant for small shapes).
+ */
+#ifndef AFFINITY_H
+#define AFFINITY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define AFF_API __attribute__((visibility("default")))
+#else
+#define AFF_API
+#endif
+
+/* Same type as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st* aff_stream_t;
+
+typedef enum {
+  AFF_OK = 0,
+  AFF_ERR_INVALID_ARG = 1,        /* NULL pointer, bad enum, non-positive size */
+  AFF_ERR_UNSUPPORTED_SHAPE = 2,  /* shape outside the constraints listed below */
+  AFF_ERR_UNSUPPORTED_DTYPE = 3,
+  AFF_ERR_ARCH = 4,               /* current device is not sm_103 / no device */
+  AFF_ERR_WORKSPACE = 5,          /* workspace NULL, too small or misaligned */
+  AFF_ERR_CUDA = 6,               /* a CUDA call failed; see affinity_last_cuda_error() */
+  AFF_ERR_DEVICE_TIMEOUT = 7,     /* a kernel's bounded wait expired (device-latched) */
+  AFF_ERR_RANGE = 8,              /* an fp16 intermediate overflowed (device-latched) */
+  AFF_ERR_ALIGNMENT = 9           /* a pointer is not 16-byte aligned */
+} aff_status;
+
+typedef enum {
+  AFF_MODE_FO = 0,   /* S_hk = E_t[Delta_hk^2] * ||w^d_k||^2, Delta from eq. (5) */
+  AFF_MODE_ADD = 1   /* S_hk = E_t[(p_h.w^g_k)^2 + (p_h.w^u_k)^2] */
+} aff_mode;
+
+typedef enum { AFF_BF16 = 0, AFF_FP32 = 1 } aff_dtype;
+
+/*
+ * Layer shape.  T tokens, model width D, H query heads in G KV groups of
+ * H/G heads, head width d_head, I FFN neurons; eps is the rms epsilon
+ * (r = sqrt(mean_d x_d^2 + eps)); dtype an aff_dtype; flags must be 0.
+ *
+ * Constraints: all sizes >= 1, H % G == 0.  AFF_BF16 additionally needs
+ * D % 8 == 0, d_head % 8 == 0 and I % 8 == 0 (16-byte row strides for the
+ * tensor-memory copies); any T >= 1 (a ragged last token tile is handled).
+ * AFF_FP32 has no further constraint.  eps must be finite and >= 0.
+ */
+typedef struct {
+  int64_t T, D, H, G, d_head, I;
+  float eps;
+  int32_t dtype;
+  uint32_t flags;
+} aff_dims;
+
+/*
+ * Bytes of device workspace that affinity_up (down == 0) or affinity_down
+ * (down != 0) needs for this shape and mode (mode is ignored when down != 0).
+ * The workspace must be 256-byte aligned.  Returns AFF_ERR_INVALID_ARG /
+ * AFF_ERR_UNSUPPORTED_SHAPE / AFF_ERR_UNSUPPORTED_DTYPE for bad dims.
+ */
+AFF_API aff_status affinity_workspace_size(const aff_dims* dims, int32_t mode, int32_t down, size_t* bytes);
+
+/*
+ * S_up for one layer ("Affinity scores", §3; equation (5)).
+ *   FO : S_up[g, k] = sum_{h in g} E_t[Delta_hk^2] * ||w^d_k||^2
+ *        Delta_hk = silu'(g_k) u_k (p_h.w^g_k) + silu(g_k) (p_h.w^u_k),
+ *        p_h = gamma * (a_h W_o^(h)) / r,  r = rms(x),
+ *        g_k = (gamma*x/r).w^g_k,  u_k = (gamma*x/r).w^u_k.
+ *   ADD: S_up[g, k] = sum_{h in g} E_t[(p_h.w^g_k)^2 + (p_h.w^u_k)^2].
+ * E_t is the mean over the T tokens.  Wd is read only in FO mode (it may be
+ * NULL in ADD mode).
+ * Outputs (device, fp32): S_out [G, I] row-major; S_head_out [H, I] (the
+ * per-query-head scores before the group sum) or NULL.
+ * workspace: device, >= affinity_workspace_size(dims, mode, 0) bytes,
+ * 256-byte aligned; its contents are scratch (no state between calls except
+ * the status word); two calls must not use one workspace concurrently.
+ */
+AFF_API aff_status affinity_up(const void* a, const void* x, const void* Wo, const void* gamma,
+                       const void* Wg, const void* Wu, const void* Wd,
+                       const aff_dims* dims, int32_t mode,
+                       float* S_out, float* S_head_out,
+                       void* workspace, size_t workspace_bytes, aff_stream_t stream);
+
+/*
+ * S_down for one layer ("Affinity scores", §3, down edge):
+ *   S_down[k, g] = E_t[alpha_k^2 / r'^2] * ||b_gk||^2,
+ *   alpha_k = silu(g_k) u_k,  b_gk = W^qkv_g (gamma_next * w^d_k),
+ *   W^qkv_g = [query rows of g's H/G heads; key rows of g; value rows of g],
+ *   r' = rms(x') with x' = x + sum_k alpha_k w^d_k (the residual after this
+ *   FFN, which is the next attention's pre-norm input) and the same eps.
+ * Output S_out [I, G] row-major fp32 (device).  Workspace as for affinity_up
+ * with down != 0.
+ */
+AFF_API aff_status affinity_down(const void* x, const void* gamma, const void* Wg, const void* Wu,
+                         const void* Wd, const void* gamma_next, const void* Wq_next,
+                         const void* Wk_next, const void* Wv_next,
+                         const aff_dims* dims, float* S_out,
+                         void* workspace, size_t workspace_bytes, aff_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the status word that kernels
+ * of the previous affinity_up / affinity_down call on this workspace latch
+ * (AFF_ERR_DEVICE_TIMEOUT, AFF_ERR_RANGE); returns AFF_OK if none was set.
+ */
+AFF_API aff_status affinity_device_status(void* workspace, aff_stream_t stream);
+
+/*
+ * Host-only helper ("Optimiser", §3): score every labelled balanced
+ * partition h of G KV groups onto L devices (G/L groups per device) by
+ * sum_g C[g, h(g)], where C [G, L] (host, row-major, fp64) is the gain of
+ * putting group g on device l.  Partitions are enumerated in lexicographic
+ * order of (h(0), ..., h(G-1)); the first maximum wins ties.
+ *   scores      host [count] or NULL
+ *   count       number of partitions, G! / ((G/L)!)^L (2520 for G=8, L=4)
+ *   best_index  index of the best partition in that order
+ *   best_assign host [G]: the best partition's device of each group, or NULL
+ * Requires 1 <= L <= G <= 16 and G % L == 0 (AFF_ERR_INVALID_ARG otherwise)
+ * and at most 1e8 partitions (AFF_ERR_UNSUPPORTED_SHAPE otherwise); when
+ * scores != NULL the caller must size it with a first call that passes
+ * scores == NULL.
+ */
+AFF_API aff_status affinity_score_partitions(const double* C, int32_t G, int32_t L, double* scores,
+                                     int64_t* count, int64_t* best_index, int32_t* best_assign);
+
+/*
+ * Host-only helper ("Optimiser", §3): the gain C [G, L] (fp64) of placing
+ * group g of layer i on device l given the neuron maps, from unit-mass
+ * matrices:  C[g, l] = sum_{k: nu_i(k) = l} Shat_up_i[g, k]
+ *                    + sum_{k: nu_prev(k) = l} Shat_down_prev[k, g].
+ * Shat_up_i [G, I], Shat_down_prev [I, G] (NULL for the first layer),
+ * nu_i / nu_prev [I] device indices in [0, L).  All host memory.
+ */
+AFF_API aff_status affinity_group_gain(const double* Shat_up_i, const int32_t* nu_i,
+                               const double* Shat_down_prev, const int32_t* nu_prev,
+                               int32_t G, int64_t I, int32_t L, double* C);
+
+/*
+ * Host-only helper ("Objective", equation (6)): total co-located affinity
+ *   J = sum_i sum_{g,k: h_i(g) = nu_i(k)} Shat_up_i[g, k]
+ *     + sum_{i < N-1} sum_{k,g: nu_i(k) = h_{i+1}(g)} Shat_down_i[k, g]
+ * for N layers.  Shat_up: N contiguous [G, I] fp64 blocks; Shat_down: N-1
+ * contiguous [I, G] blocks (may be NULL when N == 1); h: N x [G];
+ * nu: N x [I]; all host memory.
+ */
+AFF_API aff_status affinity_objective(const double* Shat_up, const double* Shat_down,
+                              const int32_t* h, const int32_t* nu,
+                              int32_t N, int32_t G, int64_t I, double* J);
+
+/*
+ * Profiling hook (no effect on results): register two caller-created CUDA
+ * events (cudaEvent_t handles) that later affinity_up / affinity_down calls
+ * made from this host thread record on their stream immediately before and
+ * after their dominant tensor-core kernel -- the operating point + per-head
+ * contraction kernel for affinity_up, the gate/up (alpha) kernel for
+ * affinity_down.  Pass two NULLs to stop recording.  The events must outlive
+ * the calls that record them.
+ */
+AFF_API aff_status affinity_set_timing_events(void* start_event, void* stop_event);
+
+/* Static text for a status code. */
+AFF_API const char* affinity_strerror(aff_status status);
+
+/* Text of the last CUDA error seen by this thread (empty if none). */
+AFF_API const char* affinity_last_cuda_error(void);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+AFF_API int32_t affinity_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AFFINITY_H */

@@ -1,0 +1,177 @@
+"""The C ABI without a GPU: the library loads and exports every entry point
+include/affinity.h declares, argument validation returns the documented codes
+before touching a device, and the host-only helpers (partition scoring, group
+gain, objective J) agree with the oracle exactly."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import partitions as P
+from transformer_sharding_affinity_gb300 import binding as B
+from transformer_sharding_affinity_gb300 import build as BUILD
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(B.LIB_PATH):
+        BUILD.build()
+    return B.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "affinity.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"AFF_API\s+[\w\s\*]+?\b(affinity_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/affinity.h but not exported"
+
+
+def test_version_and_strerror(lib):
+    assert B.version() >= 100
+    for code in range(0, 10):
+        assert len(B.strerror(code)) > 0
+    assert B.strerror(123) == "unknown status"
+
+
+def _d(**kw):
+    base = dict(T=256, D=64, H=4, G=2, d_head=16, I=128, eps=1e-6, dtype=B.AFF_BF16)
+    base.update(kw)
+    return B.dims(**base)
+
+
+def _ws(d, mode=0, down=0):
+    n = ctypes.c_size_t(0)
+    st = B.load().affinity_workspace_size(ctypes.byref(d), mode, down, ctypes.byref(n))
+    return st, n.value
+
+
+def test_workspace_size(lib):
+    st, n_fo = _ws(_d())
+    assert st == B.AFF_OK and n_fo > 0 and n_fo % 1024 == 0
+    st, n_add = _ws(_d(), 1)
+    assert st == B.AFF_OK and 0 < n_add < n_fo          # ADD needs no operating point / Wd norms
+    st, n_dn = _ws(_d(), 0, 1)
+    assert st == B.AFF_OK and n_dn > 0
+    st, n_big = _ws(_d(T=65536, D=1024, H=16, G=8, d_head=128, I=3072))
+    assert st == B.AFF_OK and n_big > 400 * 2**20
+    st, n_f32 = _ws(_d(dtype=B.AFF_FP32))
+    assert st == B.AFF_OK and n_f32 > 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=0), B.AFF_ERR_INVALID_ARG),
+    (dict(I=-1), B.AFF_ERR_INVALID_ARG),
+    (dict(H=3, G=2), B.AFF_ERR_UNSUPPORTED_SHAPE),
+    (dict(D=60), B.AFF_ERR_UNSUPPORTED_SHAPE),
+    (dict(d_head=12), B.AFF_ERR_UNSUPPORTED_SHAPE),
+    (dict(I=100), B.AFF_ERR_UNSUPPORTED_SHAPE),
+    (dict(H=256, G=1), B.AFF_ERR_UNSUPPORTED_SHAPE),
+    (dict(dtype=7), B.AFF_ERR_UNSUPPORTED_DTYPE),
+    (dict(eps=float("nan")), B.AFF_ERR_INVALID_ARG),
+    (dict(eps=-1.0), B.AFF_ERR_INVALID_ARG),
+])
+def test_bad_dims(lib, kw, code):
+    assert _ws(_d(**kw))[0] == code
+
+
+def test_fp32_relaxes_alignment_constraints(lib):
+    assert _ws(_d(D=60, d_head=12, I=100, dtype=B.AFF_FP32))[0] == B.AFF_OK
+
+
+def test_flags_and_mode_are_checked(lib):
+    d = _d()
+    d.flags = 1
+    assert _ws(d)[0] == B.AFF_ERR_INVALID_ARG
+    assert _ws(_d(), 5)[0] == B.AFF_ERR_INVALID_ARG
+
+
+def _up(lib, d, ptrs, mode=0, ws=1 << 20, ws_bytes=1 << 40, S=1 << 20):
+    return lib.affinity_up(*ptrs, ctypes.byref(d), mode, S, None, ws, ws_bytes, None)
+
+
+def test_up_argument_errors_before_any_launch(lib):
+    d = _d()
+    good = [0x10000 * (i + 1) for i in range(7)]
+    assert _up(lib, d, [None] + good[1:]) == B.AFF_ERR_INVALID_ARG
+    assert _up(lib, d, good, S=None) == B.AFF_ERR_INVALID_ARG
+    assert _up(lib, d, good[:6] + [None]) == B.AFF_ERR_INVALID_ARG            # FO reads Wd
+    assert _up(lib, d, good[:1] + [good[1] + 8] + good[2:]) == B.AFF_ERR_ALIGNMENT
+    assert _up(lib, d, good, ws=None) == B.AFF_ERR_WORKSPACE
+    assert _up(lib, d, good, ws=(1 << 20) + 128) == B.AFF_ERR_WORKSPACE       # 256-byte alignment
+    assert _up(lib, d, good, ws_bytes=1024) == B.AFF_ERR_WORKSPACE
+    assert _up(lib, d, good, mode=3) == B.AFF_ERR_INVALID_ARG
+    bad = _d(T=0)
+    assert _up(lib, bad, good) == B.AFF_ERR_INVALID_ARG
+
+
+def test_up_without_a_device_reports_arch(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    d = _d()
+    good = [0x10000 * (i + 1) for i in range(7)]
+    assert _up(lib, d, good) == B.AFF_ERR_ARCH
+
+
+def test_down_argument_errors(lib):
+    d = _d()
+    good = [0x10000 * (i + 1) for i in range(9)]
+    f = lib.affinity_down
+    assert f(*([None] + good[1:]), ctypes.byref(d), 1 << 20, 1 << 20, 1 << 40, None) == B.AFF_ERR_INVALID_ARG
+    assert f(*good, ctypes.byref(d), None, 1 << 20, 1 << 40, None) == B.AFF_ERR_INVALID_ARG
+    assert f(*good, ctypes.byref(d), (1 << 20) + 4, 1 << 20, 1 << 40, None) == B.AFF_ERR_ALIGNMENT
+    assert f(*good, ctypes.byref(d), 1 << 20, 1 << 20, 16, None) == B.AFF_ERR_WORKSPACE
+
+
+# ---------------------------------------------------------------- host helpers vs the oracle
+
+@pytest.mark.parametrize("G,L", [(8, 4), (8, 2), (6, 3), (4, 4), (4, 1), (12, 4), (10, 5)])
+def test_score_partitions_matches_oracle(lib, G, L):
+    rng = np.random.default_rng(G * 100 + L)
+    C = rng.random((G, L))
+    scores, count, best, assign = B.score_partitions(C)
+    assert count == P.partition_count(G, L)
+    o_scores, o_best, o_assign = P.score_partitions(C)
+    np.testing.assert_array_equal(scores, o_scores)
+    assert best == o_best and assign == tuple(o_assign)
+
+
+def test_score_partitions_paper_count_and_ties(lib):
+    scores, count, best, assign = B.score_partitions(np.zeros((8, 4)))
+    assert count == 2520 and best == 0 and assign == (0, 0, 1, 1, 2, 2, 3, 3)
+    for G, L in [(0, 1), (8, 3), (4, 8), (17, 1)]:
+        cnt, bi = ctypes.c_int64(0), ctypes.c_int64(0)
+        C = np.zeros((max(G, 1), max(L, 1)))
+        assert lib.affinity_score_partitions(C.ctypes.data, G, L, None, ctypes.byref(cnt), ctypes.byref(bi),
+                                             None) == B.AFF_ERR_INVALID_ARG
+    C = np.zeros((16, 8))   # 16!/2^8 ~ 8e10 partitions: refused
+    assert lib.affinity_score_partitions(C.ctypes.data, 16, 8, None, ctypes.byref(cnt), ctypes.byref(bi),
+                                         None) == B.AFF_ERR_UNSUPPORTED_SHAPE
+
+
+def test_group_gain_and_objective_match_oracle(lib):
+    rng = np.random.default_rng(3)
+    N, G, I, L = 4, 8, 64, 4
+    ups = [P.unit_mass(rng.random((G, I))) for _ in range(N)]
+    downs = [P.unit_mass(rng.random((I, G))) for _ in range(N - 1)]
+    hs = [rng.permutation(P.contiguous_heads(G, L)) for _ in range(N)]
+    ns = [rng.permutation(P.contiguous_neurons(I, L)) for _ in range(N)]
+    np.testing.assert_allclose(B.objective(ups, downs, hs, ns), P.objective_J(ups, downs, hs, ns), rtol=1e-13)
+    for i in range(N):
+        got = B.group_gain(ups[i], ns[i], L, downs[i - 1] if i else None, ns[i - 1] if i else None)
+        ref = P.group_gain(ups[i], L, ns[i], downs[i - 1] if i else None, ns[i - 1] if i else None)
+        np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-16)
+    bad = np.array(ns[0])
+    bad[0] = L
+    with pytest.raises(B.AffinityError):
+        B.group_gain(ups[0], bad, L)

@@ -1,0 +1,614 @@
+// api.cu -- the C ABI declared in include/affinity.h: argument validation,
+// workspace layout, TMA descriptor encoding and the launch sequence of the
+// affinity pass ("Affinity-Aware Sharding for Delayed Tensor Parallelism",
+// §3 "Affinity scores", "Objective", "Optimiser").
+#include "affinity.h"
+#include "aux_kernels.cuh"
+#include "tile_kernel.cuh"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+namespace aff {
+cudaError_t launch_tile_kernel(const CUtensorMap* maps, const TileParams& p, int grid, cudaStream_t stream);
+size_t tile_smem_bytes(int mode, int stages, int H);
+}  // namespace aff
+
+using namespace aff;
+
+namespace {
+
+thread_local std::string g_last_cuda_error;
+thread_local cudaEvent_t g_timing_start = nullptr;  // see affinity_set_timing_events
+thread_local cudaEvent_t g_timing_stop = nullptr;
+
+aff_status cuda_fail(cudaError_t e, const char* where) {
+  g_last_cuda_error = std::string(where) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return AFF_ERR_CUDA;
+}
+
+#define AFF_CUDA(call)                                   \
+  do {                                                   \
+    cudaError_t e_ = (call);                             \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call);  \
+  } while (0)
+
+constexpr int64_t kMaxDim = (int64_t)1 << 30;
+constexpr int kTilesPerUnit = 2;      // token tiles (of 128) per FO / ADD unit
+constexpr int kDownTokenChunk = 256;  // tokens per partial sum of E_t[alpha^2 / r'^2]
+
+inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+inline int64_t ceil_div(int64_t v, int64_t m) { return (v + m - 1) / m; }
+
+aff_status check_dims(const aff_dims* d) {
+  if (!d) return AFF_ERR_INVALID_ARG;
+  if (d->dtype != AFF_BF16 && d->dtype != AFF_FP32) return AFF_ERR_UNSUPPORTED_DTYPE;
+  if (d->flags != 0) return AFF_ERR_INVALID_ARG;
+  if (d->T < 1 || d->D < 1 || d->H < 1 || d->G < 1 || d->d_head < 1 || d->I < 1) return AFF_ERR_INVALID_ARG;
+  if (!(std::isfinite(d->eps) && d->eps >= 0.f)) return AFF_ERR_INVALID_ARG;
+  if (d->T > kMaxDim || d->D > kMaxDim || d->H > 4096 || d->d_head > 4096 || d->I > kMaxDim)
+    return AFF_ERR_UNSUPPORTED_SHAPE;
+  if (d->H % d->G) return AFF_ERR_UNSUPPORTED_SHAPE;
+  if (d->dtype == AFF_BF16) {
+    if (d->D % 8 || d->d_head % 8 || d->I % 8) return AFF_ERR_UNSUPPORTED_SHAPE;
+    // per-thread head sums live in shared memory next to 2+ pipeline stages
+    if (tile_smem_bytes(kModeFO, 2, (int)d->H) > (size_t)kMaxDynSmem) return AFF_ERR_UNSUPPORTED_SHAPE;
+    if (d->H * d->d_head > kMaxDim) return AFF_ERR_UNSUPPORTED_SHAPE;
+  }
+  return AFF_OK;
+}
+
+// Workspace carve-up; every buffer starts on a 1024-byte boundary.
+struct Layout {
+  size_t total = 0;
+  size_t status = 0;
+  // bf16 path
+  size_t W16 = 0, GWo16 = 0, M16 = 0, n16 = 0, a16 = 0, partial = 0, headsum = 0, wdn = 0;
+  size_t alpha16 = 0, Wd16 = 0, WdT16 = 0, Wqkv16 = 0, ssx = 0, cpart = 0, bnorm = 0;
+  // fp32 path
+  size_t n32 = 0, a32 = 0, M32 = 0, ab = 0, alpha32 = 0;
+  int64_t I_pad = 0, T_pad = 0, n_chunks = 0, n_tchunks = 0, Rg = 0;
+
+  size_t take(size_t bytes) {
+    total = (size_t)round_up((int64_t)total, 1024);
+    size_t off = total;
+    total += bytes;
+    return off;
+  }
+};
+
+Layout make_layout(const aff_dims& d, int mode, bool down) {
+  Layout L;
+  const int64_t T = d.T, D = d.D, H = d.H, G = d.G, dh = d.d_head, I = d.I;
+  L.status = L.take(256);
+  if (d.dtype == AFF_BF16) {
+    L.I_pad = round_up(I, 128);
+    L.T_pad = round_up(T, 128);
+    L.W16 = L.take((size_t)2 * L.I_pad * D * 2);
+    L.n16 = L.take((size_t)T * D * 2);
+    if (!down) {
+      L.n_chunks = ceil_div(L.T_pad / 128, kTilesPerUnit);
+      L.GWo16 = L.take((size_t)H * dh * 2 * D * 2);
+      L.M16 = L.take((size_t)2 * H * L.I_pad * dh * 2);
+      L.a16 = L.take((size_t)T * H * dh * 2);
+      L.partial = L.take((size_t)L.n_chunks * 2 * H * L.I_pad * 4);
+      L.headsum = L.take((size_t)H * L.I_pad * 8);
+      if (mode == AFF_MODE_FO) L.wdn = L.take((size_t)L.I_pad * 4);
+    } else {
+      L.Rg = (H / G + 2) * dh;
+      L.n_tchunks = ceil_div(T, kDownTokenChunk);
+      L.alpha16 = L.take((size_t)L.T_pad * L.I_pad * 2);
+      L.Wd16 = L.take((size_t)D * L.I_pad * 2);
+      L.WdT16 = L.take((size_t)L.I_pad * D * 2);
+      L.Wqkv16 = L.take((size_t)G * L.Rg * 2 * D * 2);
+      L.ssx = L.take((size_t)2 * L.T_pad * 4);
+      L.cpart = L.take((size_t)L.n_tchunks * L.I_pad * 4);
+      L.bnorm = L.take((size_t)2 * L.I_pad * G * 4);
+    }
+  } else {
+    L.I_pad = I;
+    L.T_pad = T;
+    L.n32 = L.take((size_t)T * D * 4);
+    if (!down) {
+      L.n_chunks = ceil_div(T, 128);
+      L.a32 = L.take((size_t)T * H * dh * 4);
+      L.M32 = L.take((size_t)2 * H * I * dh * 4);
+      if (mode == AFF_MODE_FO) L.ab = L.take((size_t)T * I * 8);
+      L.partial = L.take((size_t)L.n_chunks * H * I * 4);
+      L.headsum = L.take((size_t)H * I * 8);
+      if (mode == AFF_MODE_FO) L.wdn = L.take((size_t)I * 4);
+    } else {
+      L.n_tchunks = ceil_div(T, kDownTokenChunk);
+      L.alpha32 = L.take((size_t)T * I * 4);
+      L.ssx = L.take((size_t)2 * T * 4);
+      L.cpart = L.take((size_t)L.n_tchunks * I * 4);
+      L.bnorm = L.take((size_t)I * G * 4);
+    }
+  }
+  L.total = (size_t)round_up((int64_t)L.total, 1024);
+  return L;
+}
+
+// ---------------------------------------------------------------- device checks
+aff_status check_device(int* sm_count) {
+  static std::mutex mu;
+  static std::vector<int> sms;  // per device: 0 unknown, -1 wrong arch, >0 SM count
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return AFF_ERR_ARCH;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if ((int)sms.size() <= dev) sms.resize(dev + 1, 0);
+  if (sms[dev] == 0) {
+    int maj = 0, min = 0, n = 0;
+    if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return AFF_ERR_ARCH;
+    }
+    sms[dev] = (maj == 10 && min == 3) ? n : -1;
+  }
+  if (sms[dev] < 0) return AFF_ERR_ARCH;
+  *sm_count = sms[dev];
+  return AFF_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// fp16 tensor of `rank` dims (dims[0] innermost, contiguous), 128 B swizzle,
+// box = 64 innermost elements x box1 (x 1 in the other dims); OOB reads zero.
+aff_status make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, const uint64_t* strides,
+                    uint32_t box1, int box1_dim) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    g_last_cuda_error = "cuTensorMapEncodeTiled unavailable";
+    return AFF_ERR_CUDA;
+  }
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = 1;
+    es[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
+  bx[0] = 64;
+  bx[box1_dim] = box1;
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), gd, gs, bx, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[96];
+    std::snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    g_last_cuda_error = buf;
+    return AFF_ERR_CUDA;
+  }
+  return AFF_OK;
+}
+
+aff_status map2(CUtensorMap* m, const void* p, uint64_t inner, uint64_t rows) {
+  uint64_t d[2] = {inner, rows}, s[1] = {inner * 2};
+  return make_map(m, p, 2, d, s, 128, 1);
+}
+
+int pick_stages(int mode, int H) {
+  for (int s = 4; s >= 2; --s)
+    if (tile_smem_bytes(mode, s, H) <= (size_t)kMaxDynSmem) return s;
+  return 0;
+}
+
+TileParams base_params(const aff_dims& d, const Layout& L, uint8_t* ws, int mode) {
+  TileParams p{};
+  p.mode = mode;
+  p.T = (int)d.T;
+  p.D = (int)d.D;
+  p.H = (int)d.H;
+  p.G = (int)d.G;
+  p.dh = (int)d.d_head;
+  p.I = (int)d.I;
+  p.I_pad = (int)L.I_pad;
+  p.T_pad = (int)L.T_pad;
+  p.n_ktiles = (int)(L.I_pad / 128);
+  p.n_ttiles = (int)(L.T_pad / 128);
+  p.tiles_per_unit = kTilesPerUnit;
+  p.nkb_D = (int)ceil_div(d.D, 64);
+  p.nkb_dh = (int)ceil_div(d.d_head, 64);
+  p.nkb_I = (int)(L.I_pad / 64);
+  p.stages = pick_stages(mode, p.H);
+  p.status = reinterpret_cast<uint32_t*>(ws + L.status);
+  p.eps = d.eps;
+  return p;
+}
+
+aff_status run_tile(const CUtensorMap* maps, TileParams& p, int sm_count, cudaStream_t s, bool dominant = false) {
+  if (p.n_units <= 0) return AFF_OK;
+  const int grid = p.n_units < sm_count ? p.n_units : sm_count;
+  const bool timed = dominant && g_timing_start && g_timing_stop;
+  if (timed) AFF_CUDA(cudaEventRecord(g_timing_start, s));
+  cudaError_t e = launch_tile_kernel(maps, p, grid, s);
+  if (e != cudaSuccess) return cuda_fail(e, "affinity_tile_kernel");
+  if (timed) AFF_CUDA(cudaEventRecord(g_timing_stop, s));
+  return AFF_OK;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+aff_status check_ws(const Layout& L, void* ws, size_t bytes) {
+  if (!ws) return AFF_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return AFF_ERR_WORKSPACE;
+  if (bytes < L.total) return AFF_ERR_WORKSPACE;
+  return AFF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t affinity_version(void) { return 100; }
+
+aff_status affinity_set_timing_events(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr)) return AFF_ERR_INVALID_ARG;
+  g_timing_start = static_cast<cudaEvent_t>(start_event);
+  g_timing_stop = static_cast<cudaEvent_t>(stop_event);
+  return AFF_OK;
+}
+
+const char* affinity_strerror(aff_status s) {
+  switch (s) {
+    case AFF_OK: return "success";
+    case AFF_ERR_INVALID_ARG: return "invalid argument (NULL pointer, bad enum value or non-positive size)";
+    case AFF_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case AFF_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+    case AFF_ERR_ARCH: return "no sm_103 (GB300) device is current";
+    case AFF_ERR_WORKSPACE: return "workspace missing, misaligned (256 B) or smaller than affinity_workspace_size()";
+    case AFF_ERR_CUDA: return "a CUDA call failed (see affinity_last_cuda_error())";
+    case AFF_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait expired";
+    case AFF_ERR_RANGE: return "an fp16 intermediate overflowed (|value| >= 65504)";
+    case AFF_ERR_ALIGNMENT: return "a device pointer is not 16-byte aligned";
+  }
+  return "unknown status";
+}
+
+const char* affinity_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+aff_status affinity_workspace_size(const aff_dims* dims, int32_t mode, int32_t down, size_t* bytes) {
+  if (!bytes) return AFF_ERR_INVALID_ARG;
+  aff_status st = check_dims(dims);
+  if (st != AFF_OK) return st;
+  if (!down && mode != AFF_MODE_FO && mode != AFF_MODE_ADD) return AFF_ERR_INVALID_ARG;
+  *bytes = make_layout(*dims, mode, down != 0).total;
+  return AFF_OK;
+}
+
+aff_status affinity_up(const void* a, const void* x, const void* Wo, const void* gamma, const void* Wg,
+                       const void* Wu, const void* Wd, const aff_dims* dims, int32_t mode, float* S_out,
+                       float* S_head_out, void* workspace, size_t workspace_bytes, aff_stream_t stream) {
+  aff_status st = check_dims(dims);
+  if (st != AFF_OK) return st;
+  if (mode != AFF_MODE_FO && mode != AFF_MODE_ADD) return AFF_ERR_INVALID_ARG;
+  const bool fo = mode == AFF_MODE_FO;
+  if (!a || !x || !Wo || !gamma || !Wg || !Wu || (fo && !Wd) || !S_out) return AFF_ERR_INVALID_ARG;
+  const void* ptrs[] = {a, x, Wo, gamma, Wg, Wu, fo ? Wd : nullptr, S_out, S_head_out};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return AFF_ERR_ALIGNMENT;
+  const aff_dims& d = *dims;
+  Layout L = make_layout(d, mode, false);
+  if ((st = check_ws(L, workspace, workspace_bytes)) != AFF_OK) return st;
+  int sm_count = 0;
+  if ((st = check_device(&sm_count)) != AFF_OK) return st;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
+  AFF_CUDA(cudaMemsetAsync(status, 0, 4, s));
+  const int T = (int)d.T, D = (int)d.D, H = (int)d.H, G = (int)d.G, dh = (int)d.d_head, I = (int)d.I;
+  const int I_pad = (int)L.I_pad;
+  float* wdn = fo ? reinterpret_cast<float*>(ws + L.wdn) : nullptr;
+  double* headsum = reinterpret_cast<double*>(ws + L.headsum);
+
+  if (d.dtype == AFF_FP32) {
+    F32UpArgs A{};
+    A.a = (const float*)a; A.x = (const float*)x; A.Wo = (const float*)Wo; A.gamma = (const float*)gamma;
+    A.Wg = (const float*)Wg; A.Wu = (const float*)Wu;
+    A.n32 = reinterpret_cast<float*>(ws + L.n32); A.a32 = reinterpret_cast<float*>(ws + L.a32);
+    A.M32 = reinterpret_cast<float*>(ws + L.M32); A.partial = reinterpret_cast<float*>(ws + L.partial);
+    A.ab = fo ? reinterpret_cast<float2*>(ws + L.ab) : nullptr;
+    A.T = T; A.D = D; A.H = H; A.dh = dh; A.I = I; A.n_chunks = (int)L.n_chunks; A.chunk = 128; A.fo = fo;
+    A.eps = d.eps;
+    AFF_CUDA(launch_f32_up(A, s));
+    AFF_CUDA(launch_reduce_partials(A.partial, headsum, (int)L.n_chunks, 1, H, I, s));
+    if (fo) AFF_CUDA(launch_wd_colnorm_f32((const float*)Wd, wdn, D, I, s));
+    AFF_CUDA(launch_finalize_up(headsum, wdn, fo, T, H, G, I, I, S_out, S_head_out, s));
+    return AFF_OK;
+  }
+
+  // ---- bf16 path: stage fp16 operands, fold, contract, reduce
+  __half* W16 = reinterpret_cast<__half*>(ws + L.W16);
+  __half* GWo16 = reinterpret_cast<__half*>(ws + L.GWo16);
+  __half* M16 = reinterpret_cast<__half*>(ws + L.M16);
+  __half* n16 = reinterpret_cast<__half*>(ws + L.n16);
+  __half* a16 = reinterpret_cast<__half*>(ws + L.a16);
+  float* partial = reinterpret_cast<float*>(ws + L.partial);
+  const uint16_t* a_b = static_cast<const uint16_t*>(a);
+  const uint16_t* x_b = static_cast<const uint16_t*>(x);
+  const uint16_t* g_b = static_cast<const uint16_t*>(gamma);
+
+  AFF_CUDA(launch_prep_gate_up((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, status, s));
+  AFF_CUDA(launch_scaled_transpose_split((const uint16_t*)Wo, g_b, GWo16, D, H * dh, status, s));
+  if (fo) AFF_CUDA(launch_wd_colnorm((const uint16_t*)Wd, wdn, D, I, I_pad, s));
+  AFF_CUDA(launch_prep_tokens(x_b, a_b, g_b, fo ? n16 : nullptr, a16, nullptr, T, D, H * dh, d.eps, status, s));
+
+  CUtensorMap maps[4];
+  std::memset(maps, 0, sizeof maps);
+  // fold: M_h = [Wg; Wu] diag(gamma) Wo^(h)
+  {
+    if ((st = map2(&maps[0], W16, (uint64_t)D, (uint64_t)2 * I_pad)) != AFF_OK) return st;
+    uint64_t dm[3] = {(uint64_t)D, 2, (uint64_t)H * dh}, sd[2] = {(uint64_t)D * 2, (uint64_t)D * 4};
+    if ((st = make_map(&maps[1], GWo16, 3, dm, sd, 128, 2)) != AFF_OK) return st;
+    maps[2] = maps[0];
+    maps[3] = maps[0];
+    TileParams p = base_params(d, L, ws, kModeFold);
+    p.n_ntiles = (int)ceil_div((int64_t)H * dh, 128);
+    p.n_units = p.n_ktiles * p.n_ntiles;
+    p.M16 = M16;
+    if ((st = run_tile(maps, p, sm_count, s)) != AFF_OK) return st;
+  }
+  // FO / ADD: per token tile, operating point (FO) then every head
+  {
+    if ((st = map2(&maps[0], W16, (uint64_t)D, (uint64_t)2 * I_pad)) != AFF_OK) return st;
+    if (fo) {
+      if ((st = map2(&maps[1], n16, (uint64_t)D, (uint64_t)T)) != AFF_OK) return st;
+    } else {
+      maps[1] = maps[0];
+    }
+    uint64_t dm[3] = {(uint64_t)dh, (uint64_t)I_pad, (uint64_t)2 * H};
+    uint64_t sd[2] = {(uint64_t)dh * 2, (uint64_t)I_pad * dh * 2};
+    if ((st = make_map(&maps[2], M16, 3, dm, sd, 128, 1)) != AFF_OK) return st;
+    uint64_t da[3] = {(uint64_t)dh, (uint64_t)H, (uint64_t)T};
+    uint64_t sa[2] = {(uint64_t)dh * 2, (uint64_t)H * dh * 2};
+    if ((st = make_map(&maps[3], a16, 3, da, sa, 128, 2)) != AFF_OK) return st;
+    TileParams p = base_params(d, L, ws, fo ? kModeFO : kModeADD);
+    p.n_units = (int)(L.n_chunks * p.n_ktiles);
+    p.partial = partial;
+    if ((st = run_tile(maps, p, sm_count, s, true)) != AFF_OK) return st;
+  }
+  AFF_CUDA(launch_reduce_partials(partial, headsum, (int)L.n_chunks, 2, H, I_pad, s));
+  AFF_CUDA(launch_finalize_up(headsum, wdn, fo, T, H, G, I, I_pad, S_out, S_head_out, s));
+  return AFF_OK;
+}
+
+aff_status affinity_down(const void* x, const void* gamma, const void* Wg, const void* Wu, const void* Wd,
+                         const void* gamma_next, const void* Wq_next, const void* Wk_next, const void* Wv_next,
+                         const aff_dims* dims, float* S_out, void* workspace, size_t workspace_bytes,
+                         aff_stream_t stream) {
+  aff_status st = check_dims(dims);
+  if (st != AFF_OK) return st;
+  if (!x || !gamma || !Wg || !Wu || !Wd || !gamma_next || !Wq_next || !Wk_next || !Wv_next || !S_out)
+    return AFF_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, gamma, Wg, Wu, Wd, gamma_next, Wq_next, Wk_next, Wv_next, S_out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return AFF_ERR_ALIGNMENT;
+  const aff_dims& d = *dims;
+  Layout L = make_layout(d, 0, true);
+  if ((st = check_ws(L, workspace, workspace_bytes)) != AFF_OK) return st;
+  int sm_count = 0;
+  if ((st = check_device(&sm_count)) != AFF_OK) return st;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
+  AFF_CUDA(cudaMemsetAsync(status, 0, 4, s));
+  const int T = (int)d.T, D = (int)d.D, H = (int)d.H, G = (int)d.G, dh = (int)d.d_head, I = (int)d.I;
+  const int I_pad = (int)L.I_pad, T_pad = (int)L.T_pad;
+  float* ssx = reinterpret_cast<float*>(ws + L.ssx);
+  float* cpart = reinterpret_cast<float*>(ws + L.cpart);
+  float* bnorm = reinterpret_cast<float*>(ws + L.bnorm);
+
+  if (d.dtype == AFF_FP32) {
+    F32DownArgs A{};
+    A.x = (const float*)x; A.gamma = (const float*)gamma; A.Wg = (const float*)Wg; A.Wu = (const float*)Wu;
+    A.Wd = (const float*)Wd; A.gamma_next = (const float*)gamma_next; A.Wq = (const float*)Wq_next;
+    A.Wk = (const float*)Wk_next; A.Wv = (const float*)Wv_next;
+    A.n32 = reinterpret_cast<float*>(ws + L.n32); A.alpha32 = reinterpret_cast<float*>(ws + L.alpha32);
+    A.ssx = ssx; A.cpart = cpart; A.bnorm = bnorm;
+    A.T = T; A.D = D; A.H = H; A.G = G; A.dh = dh; A.I = I; A.n_chunks = (int)L.n_tchunks;
+    A.chunk = kDownTokenChunk; A.eps = d.eps;
+    AFF_CUDA(launch_f32_down(A, s));
+    AFF_CUDA(launch_finalize_down(cpart, bnorm, (int)L.n_tchunks, 1, T, I, I, G, S_out, s));
+    return AFF_OK;
+  }
+
+  __half* W16 = reinterpret_cast<__half*>(ws + L.W16);
+  __half* n16 = reinterpret_cast<__half*>(ws + L.n16);
+  __half* alpha16 = reinterpret_cast<__half*>(ws + L.alpha16);
+  __half* Wd16 = reinterpret_cast<__half*>(ws + L.Wd16);
+  __half* WdT16 = reinterpret_cast<__half*>(ws + L.WdT16);
+  __half* Wqkv16 = reinterpret_cast<__half*>(ws + L.Wqkv16);
+
+  AFF_CUDA(launch_prep_gate_up((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, status, s));
+  AFF_CUDA(launch_prep_tokens((const uint16_t*)x, nullptr, (const uint16_t*)gamma, n16, nullptr, nullptr, T, D, 0,
+                              d.eps, status, s));
+  AFF_CUDA(launch_prep_wd((const uint16_t*)Wd, Wd16, WdT16, D, I, I_pad, status, s));
+  AFF_CUDA(launch_prep_qkv((const uint16_t*)Wq_next, (const uint16_t*)Wk_next, (const uint16_t*)Wv_next,
+                           (const uint16_t*)gamma_next, Wqkv16, G, H / G, dh, D, status, s));
+  CUtensorMap maps[4];
+  std::memset(maps, 0, sizeof maps);
+  // alpha = silu(g) u for every (token, neuron)
+  {
+    if ((st = map2(&maps[0], W16, (uint64_t)D, (uint64_t)2 * I_pad)) != AFF_OK) return st;
+    if ((st = map2(&maps[1], n16, (uint64_t)D, (uint64_t)T)) != AFF_OK) return st;
+    maps[2] = maps[0];
+    maps[3] = maps[0];
+    TileParams p = base_params(d, L, ws, kModeAlpha);
+    p.n_units = (int)(ceil_div(p.n_ttiles, kTilesPerUnit) * p.n_ktiles);
+    p.alpha16 = alpha16;
+    if ((st = run_tile(maps, p, sm_count, s, true)) != AFF_OK) return st;
+  }
+  // x' = x + alpha Wd^T and sum_d x'^2 per token
+  {
+    if ((st = map2(&maps[0], alpha16, (uint64_t)I_pad, (uint64_t)T_pad)) != AFF_OK) return st;
+    if ((st = map2(&maps[1], Wd16, (uint64_t)I_pad, (uint64_t)D)) != AFF_OK) return st;
+    maps[2] = maps[0];
+    maps[3] = maps[0];
+    TileParams p = base_params(d, L, ws, kModeXPrime);
+    p.n_ntiles = (int)ceil_div(D, 128);
+    p.n_units = (int)ceil_div(T_pad, 256);
+    p.partial = ssx;
+    p.x_bf16 = (const uint16_t*)x;
+    if ((st = run_tile(maps, p, sm_count, s)) != AFF_OK) return st;
+  }
+  AFF_CUDA(launch_down_token_weights(alpha16, ssx, cpart, T, T_pad, D, I_pad, kDownTokenChunk, d.eps, s));
+  // ||b_gk||^2 for every neuron and group
+  {
+    if ((st = map2(&maps[0], WdT16, (uint64_t)D, (uint64_t)I_pad)) != AFF_OK) return st;
+    uint64_t dm[4] = {(uint64_t)D, 2, (uint64_t)L.Rg, (uint64_t)G};
+    uint64_t sd[3] = {(uint64_t)D * 2, (uint64_t)D * 4, (uint64_t)L.Rg * D * 4};
+    if ((st = make_map(&maps[1], Wqkv16, 4, dm, sd, 128, 2)) != AFF_OK) return st;
+    maps[2] = maps[0];
+    maps[3] = maps[0];
+    TileParams p = base_params(d, L, ws, kModeQNorm);
+    p.n_ntiles = (int)ceil_div(L.Rg, 128);
+    p.rows_per_group = (int)L.Rg;
+    p.n_units = (int)ceil_div(I_pad, 256);
+    p.bnorm = bnorm;
+    if ((st = run_tile(maps, p, sm_count, s)) != AFF_OK) return st;
+  }
+  AFF_CUDA(launch_finalize_down(cpart, bnorm, (int)L.n_tchunks, 2, T, I, I_pad, G, S_out, s));
+  return AFF_OK;
+}
+
+aff_status affinity_device_status(void* workspace, aff_stream_t stream) {
+  if (!workspace) return AFF_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  AFF_CUDA(cudaStreamSynchronize(s));
+  AFF_CUDA(cudaMemcpy(&v, workspace, 4, cudaMemcpyDeviceToHost));
+  AFF_CUDA(cudaMemset(workspace, 0, 4));
+  return static_cast<aff_status>(v);
+}
+
+// ---------------------------------------------------------------- host helpers
+aff_status affinity_score_partitions(const double* C, int32_t G, int32_t L, double* scores, int64_t* count,
+                                     int64_t* best_index, int32_t* best_assign) {
+  if (!C || !count || !best_index || G < 1 || L < 1 || G > 16 || L > G || G % L) return AFF_ERR_INVALID_ARG;
+  const int cap = G / L;
+  {
+    // G! / ((G/L)!)^L as a running product of binomials; refuse enumerations past 1e8.
+    double total = 1.0, rem = G;
+    for (int l = 0; l < L; ++l) {
+      double b = 1.0;
+      for (int i = 0; i < cap; ++i) b = b * (rem - i) / (i + 1);
+      total *= b;
+      rem -= cap;
+    }
+    if (total > 1e8) return AFF_ERR_UNSUPPORTED_SHAPE;
+  }
+  int h[16], used[16] = {0};
+  int64_t n = 0, best = -1;
+  double best_score = 0.0;
+  // depth-first, devices tried in increasing order: lexicographic order of (h(0), ..., h(G-1))
+  int g = 0;
+  for (int i = 0; i < G; ++i) h[i] = -1;
+  while (g >= 0) {
+    if (g == G) {
+      double sc = 0.0;
+      for (int i = 0; i < G; ++i) sc += C[(size_t)i * L + h[i]];
+      if (scores) scores[n] = sc;
+      if (best < 0 || sc > best_score) {
+        best = n;
+        best_score = sc;
+        if (best_assign)
+          for (int i = 0; i < G; ++i) best_assign[i] = h[i];
+      }
+      ++n;
+      --g;
+      continue;
+    }
+    if (h[g] >= 0) used[h[g]]--;
+    int l = h[g] + 1;
+    while (l < L && used[l] >= cap) ++l;
+    if (l < L) {
+      h[g] = l;
+      used[l]++;
+      ++g;
+      if (g < G) h[g] = -1;
+    } else {
+      h[g] = -1;
+      --g;
+    }
+  }
+  *count = n;
+  *best_index = best;
+  return AFF_OK;
+}
+
+aff_status affinity_group_gain(const double* Shat_up_i, const int32_t* nu_i, const double* Shat_down_prev,
+                               const int32_t* nu_prev, int32_t G, int64_t I, int32_t L, double* C) {
+  if (!Shat_up_i || !nu_i || !C || G < 1 || I < 1 || L < 1) return AFF_ERR_INVALID_ARG;
+  if ((Shat_down_prev == nullptr) != (nu_prev == nullptr)) return AFF_ERR_INVALID_ARG;
+  for (int64_t k = 0; k < I; ++k) {
+    if (nu_i[k] < 0 || nu_i[k] >= L) return AFF_ERR_INVALID_ARG;
+    if (nu_prev && (nu_prev[k] < 0 || nu_prev[k] >= L)) return AFF_ERR_INVALID_ARG;
+  }
+  for (int64_t i = 0; i < (int64_t)G * L; ++i) C[i] = 0.0;
+  for (int g = 0; g < G; ++g)
+    for (int64_t k = 0; k < I; ++k) C[(size_t)g * L + nu_i[k]] += Shat_up_i[(size_t)g * I + k];
+  if (Shat_down_prev)
+    for (int64_t k = 0; k < I; ++k)
+      for (int g = 0; g < G; ++g) C[(size_t)g * L + nu_prev[k]] += Shat_down_prev[(size_t)k * G + g];
+  return AFF_OK;
+}
+
+aff_status affinity_objective(const double* Shat_up, const double* Shat_down, const int32_t* h, const int32_t* nu,
+                              int32_t N, int32_t G, int64_t I, double* J) {
+  if (!Shat_up || !h || !nu || !J || N < 1 || G < 1 || I < 1) return AFF_ERR_INVALID_ARG;
+  if (N > 1 && !Shat_down) return AFF_ERR_INVALID_ARG;
+  double s = 0.0;
+  for (int i = 0; i < N; ++i) {
+    const double* S = Shat_up + (size_t)i * G * I;
+    const int32_t* hi = h + (size_t)i * G;
+    const int32_t* ni = nu + (size_t)i * I;
+    for (int g = 0; g < G; ++g)
+      for (int64_t k = 0; k < I; ++k)
+        if (hi[g] == ni[k]) s += S[(size_t)g * I + k];
+  }
+  for (int i = 0; i + 1 < N; ++i) {
+    const double* S = Shat_down + (size_t)i * I * G;
+    const int32_t* ni = nu + (size_t)i * I;
+    const int32_t* hn = h + (size_t)(i + 1) * G;
+    for (int64_t k = 0; k < I; ++k)
+      for (int g = 0; g < G; ++g)
+        if (ni[k] == hn[g]) s += S[(size_t)k * G + g];
+  }
+  *J = s;
+  return AFF_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,533 @@
+// aux_kernels.cu -- the memory-bound and small kernels around the tcgen05
+// tile kernel: operand staging in fp16, the deterministic cross-unit
+// reductions, the down-edge finishing steps, and the fp32 CUDA-core path.
+// Paper: "Affinity-Aware Sharding for Delayed Tensor Parallelism", §3
+// "Affinity scores" (eq. 5 and the FO / ADD / down definitions after it).
+#include "aux_kernels.cuh"
+#include "sm103_primitives.cuh"
+
+#include <cuda_fp16.h>
+
+namespace aff {
+
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+__device__ __forceinline__ __half to_h(float v, bool& bad) {
+  if (!(fabsf(v) <= 65504.f)) bad = true;
+  return __float2half_rn(v);
+}
+
+// ---------------------------------------------------------------- token rows
+// One warp per token: r_t = sqrt(mean_d x_td^2 + eps); n16 = gamma*x/r (the
+// FFN's normalised input) and a16 = a/r (so that the head contraction with
+// the folded matrices yields p_h.w directly), both rounded to fp16.
+__global__ void prep_tokens_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ a,
+                                   const uint16_t* __restrict__ gamma, __half* __restrict__ n16,
+                                   __half* __restrict__ a16, float* __restrict__ inv_r, int T, int D, int HD,
+                                   float eps, uint32_t* status) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= T) return;
+  const size_t t = (size_t)warp;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + t * D);
+  float ss = 0.f;
+  for (int v = lane; v < D / 8; v += 32) {
+    uint4 q = xr[v];
+    const uint16_t* e = reinterpret_cast<const uint16_t*>(&q);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float f = bf2f(e[i]);
+      ss = fmaf(f, f, ss);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float ir = rsqrtf(ss / (float)D + eps);
+  if (lane == 0 && inv_r) inv_r[t] = ir;
+  bool bad = false;
+  if (n16) {
+    const uint4* gr = reinterpret_cast<const uint4*>(gamma);
+    uint4* nr = reinterpret_cast<uint4*>(n16 + t * D);
+    for (int v = lane; v < D / 8; v += 32) {
+      uint4 q = xr[v], g = gr[v];
+      const uint16_t* e = reinterpret_cast<const uint16_t*>(&q);
+      const uint16_t* ge = reinterpret_cast<const uint16_t*>(&g);
+      __align__(16) __half o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = to_h(bf2f(ge[i]) * bf2f(e[i]) * ir, bad);
+      nr[v] = *reinterpret_cast<uint4*>(o);
+    }
+  }
+  if (a16) {
+    const uint4* ar = reinterpret_cast<const uint4*>(a + t * HD);
+    uint4* orow = reinterpret_cast<uint4*>(a16 + t * HD);
+    for (int v = lane; v < HD / 8; v += 32) {
+      uint4 q = ar[v];
+      const uint16_t* e = reinterpret_cast<const uint16_t*>(&q);
+      __align__(16) __half o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = to_h(bf2f(e[i]) * ir, bad);
+      orow[v] = *reinterpret_cast<uint4*>(o);
+    }
+  }
+  if (bad) latch_status(status, kStatusRange);
+}
+
+// ---------------------------------------------------------------- weights
+// W16 = fp16 copy of [Wg; Wu] with each block padded to I_pad rows of zeros.
+__global__ void prep_gate_up_kernel(const uint16_t* __restrict__ Wg, const uint16_t* __restrict__ Wu,
+                                    __half* __restrict__ W16, int I, int I_pad, int D, uint32_t* status) {
+  const size_t n8 = (size_t)2 * I_pad * D / 8;
+  bool bad = false;
+  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8; v += (size_t)gridDim.x * blockDim.x) {
+    const size_t e0 = v * 8;
+    const int r = (int)(e0 / D), d = (int)(e0 % D);
+    const int blk = r / I_pad, k = r % I_pad;
+    __align__(16) __half o[8];
+    if (k < I) {
+      const uint16_t* src = (blk == 0 ? Wg : Wu) + (size_t)k * D + d;
+      uint4 q = *reinterpret_cast<const uint4*>(src);
+      const uint16_t* e = reinterpret_cast<const uint16_t*>(&q);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = to_h(bf2f(e[i]), bad);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = __float2half_rn(0.f);
+    }
+    *reinterpret_cast<uint4*>(W16 + e0) = *reinterpret_cast<uint4*>(o);
+  }
+  if (bad) latch_status(status, kStatusRange);
+}
+
+// out[n][part][d] for part 0/1 = fp16 hi / lo of scale_d * W[d][n] (a transposed,
+// split copy: hi + lo carries ~22 significant bits of the exact fp32 product).
+// W is [Drows][Ncols] bf16 row-major.  Tiled through shared memory.
+__global__ void scaled_transpose_split_kernel(const uint16_t* __restrict__ W, const uint16_t* __restrict__ scale,
+                                              __half* __restrict__ out, int Drows, int Ncols, uint32_t* status) {
+  __shared__ float tile[32][33];
+  const int d0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int d = d0 + i, n = n0 + threadIdx.x;
+    tile[i][threadIdx.x] = (d < Drows && n < Ncols) ? bf2f(scale[d]) * bf2f(W[(size_t)d * Ncols + n]) : 0.f;
+  }
+  __syncthreads();
+  bool bad = false;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int n = n0 + i, d = d0 + threadIdx.x;
+    if (n < Ncols && d < Drows) {
+      const float v = tile[threadIdx.x][i];
+      const __half hi = to_h(v, bad);
+      const __half lo = __float2half_rn(v - __half2float(hi));
+      out[((size_t)n * 2 + 0) * Drows + d] = hi;
+      out[((size_t)n * 2 + 1) * Drows + d] = lo;
+    }
+  }
+  if (bad) latch_status(status, kStatusRange);
+}
+
+// wdn[k] = ||w^d_k||^2 = sum_d Wd[d][k]^2 (fp32; fixed order: 8 row phases, then in order).
+__global__ void wd_colnorm_kernel(const uint16_t* __restrict__ Wd, float* __restrict__ wdn, int D, int I, int I_pad) {
+  __shared__ float part[8][33];
+  const int k = blockIdx.x * 32 + threadIdx.x;
+  float s = 0.f;
+  if (k < I)
+    for (int d = threadIdx.y; d < D; d += 8) {
+      const float v = bf2f(Wd[(size_t)d * I + k]);
+      s = fmaf(v, v, s);
+    }
+  part[threadIdx.y][threadIdx.x] = s;
+  __syncthreads();
+  if (threadIdx.y == 0 && k < I_pad) {
+    float t = 0.f;
+    for (int i = 0; i < 8; ++i) t += part[i][threadIdx.x];
+    wdn[k] = (k < I) ? t : 0.f;
+  }
+}
+
+// fp32 twin of wd_colnorm_kernel for the fp32 path.
+__global__ void wd_colnorm_f32_kernel(const float* __restrict__ Wd, float* __restrict__ wdn, int D, int I) {
+  __shared__ float part[8][33];
+  const int k = blockIdx.x * 32 + threadIdx.x;
+  float s = 0.f;
+  if (k < I)
+    for (int d = threadIdx.y; d < D; d += 8) s = fmaf(Wd[(size_t)d * I + k], Wd[(size_t)d * I + k], s);
+  part[threadIdx.y][threadIdx.x] = s;
+  __syncthreads();
+  if (threadIdx.y == 0 && k < I) {
+    float t = 0.f;
+    for (int i = 0; i < 8; ++i) t += part[i][threadIdx.x];
+    wdn[k] = t;
+  }
+}
+
+// ---------------------------------------------------------------- reductions
+// S_head_d[h][k] = sum over chunks and halves of partial[c][hf][h][k], in fp64,
+// in a fixed order (8 interleaved chunk phases, then phases in order).
+__global__ void reduce_partials_kernel(const float* __restrict__ partial, double* __restrict__ out, int n_chunks,
+                                       int halves, int H, int I_pad) {
+  __shared__ double part[8][33];
+  const int k = blockIdx.x * 32 + threadIdx.x;
+  const int h = blockIdx.y;
+  double s = 0.0;
+  if (k < I_pad)
+    for (int c = threadIdx.y; c < n_chunks; c += 8)
+      for (int hf = 0; hf < halves; ++hf) s += (double)partial[((size_t)(c * halves + hf) * H + h) * I_pad + k];
+  part[threadIdx.y][threadIdx.x] = s;
+  __syncthreads();
+  if (threadIdx.y == 0 && k < I_pad) {
+    double t = 0.0;
+    for (int i = 0; i < 8; ++i) t += part[i][threadIdx.x];
+    out[(size_t)h * I_pad + k] = t;
+  }
+}
+
+// S_head[h][k] = sum_t(...) / T (x ||w^d_k||^2 for FO); S_up[g][k] = sum_{h in g} S_head[h][k].
+__global__ void finalize_up_kernel(const double* __restrict__ sh, const float* __restrict__ wdn, int fo, int T,
+                                   int H, int G, int I, int I_pad, float* __restrict__ S_out,
+                                   float* __restrict__ S_head_out) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  const int g = blockIdx.y;
+  if (k >= I) return;
+  const int hpg = H / G;
+  const double scale = (fo ? (double)wdn[k] : 1.0) / (double)T;
+  double s = 0.0;
+  for (int h = g * hpg; h < (g + 1) * hpg; ++h) {
+    const double v = sh[(size_t)h * I_pad + k] * scale;
+    if (S_head_out) S_head_out[(size_t)h * I + k] = (float)v;
+    s += v;
+  }
+  S_out[(size_t)g * I + k] = (float)s;
+}
+
+// ---------------------------------------------------------------- down edge
+// Wd16 [D][I_pad] and WdT16 [I_pad][D]: fp16 copies of Wd (zero padded).
+__global__ void prep_wd_kernel(const uint16_t* __restrict__ Wd, __half* __restrict__ Wd16,
+                               __half* __restrict__ WdT16, int D, int I, int I_pad, uint32_t* status) {
+  __shared__ float tile[32][33];
+  const int d0 = blockIdx.y * 32, k0 = blockIdx.x * 32;
+  bool bad = false;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int d = d0 + i, k = k0 + threadIdx.x;
+    float v = 0.f;
+    if (d < D && k < I) v = bf2f(Wd[(size_t)d * I + k]);
+    tile[i][threadIdx.x] = v;
+    if (d < D && k < I_pad) Wd16[(size_t)d * I_pad + k] = to_h(v, bad);
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int k = k0 + i, d = d0 + threadIdx.x;
+    if (k < I_pad && d < D) WdT16[(size_t)k * D + d] = __float2half_rn(tile[threadIdx.x][i]);
+  }
+  if (bad) latch_status(status, kStatusRange);
+}
+
+// Wqkv16 [G][R_g][2][D]: rows of W^qkv_g (query rows of g's heads, then key, then
+// value rows) times gamma', split into fp16 hi / lo.
+__global__ void prep_qkv_kernel(const uint16_t* __restrict__ Wq, const uint16_t* __restrict__ Wk,
+                                const uint16_t* __restrict__ Wv, const uint16_t* __restrict__ gamma_next,
+                                __half* __restrict__ out, int G, int hpg, int dh, int D, uint32_t* status) {
+  const int Rg = (hpg + 2) * dh;
+  const size_t total = (size_t)G * Rg * D;
+  bool bad = false;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
+    const int d = (int)(e % D);
+    const size_t rr = e / D;
+    const int r = (int)(rr % Rg), g = (int)(rr / Rg);
+    const uint16_t* src;
+    if (r < hpg * dh) src = Wq + ((size_t)g * hpg * dh + r) * D;
+    else if (r < (hpg + 1) * dh) src = Wk + ((size_t)g * dh + (r - hpg * dh)) * D;
+    else src = Wv + ((size_t)g * dh + (r - (hpg + 1) * dh)) * D;
+    const float v = bf2f(gamma_next[d]) * bf2f(src[d]);
+    const __half hi = to_h(v, bad);
+    out[(rr * 2 + 0) * D + d] = hi;
+    out[(rr * 2 + 1) * D + d] = __float2half_rn(v - __half2float(hi));
+  }
+  if (bad) latch_status(status, kStatusRange);
+}
+
+// cpart[c][k] = sum over the tokens t of chunk c of alpha_tk^2 / r'_t^2, with
+// 1/r'^2 = 1 / ((ss0 + ss1)/D + eps) from the two halves of sum_d x'^2.
+__global__ void down_token_weights_kernel(const __half* __restrict__ alpha16, const float* __restrict__ ssx,
+                                          float* __restrict__ cpart, int T, int T_pad, int D, int I_pad,
+                                          int chunk, float eps) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  const int c = blockIdx.y;
+  if (k >= I_pad) return;
+  const int t0 = c * chunk, t1 = min(T, t0 + chunk);
+  float s = 0.f;
+  for (int t = t0; t < t1; ++t) {
+    const float ssum = ssx[t] + ssx[(size_t)T_pad + t];
+    const float w = 1.0f / (ssum / (float)D + eps);
+    const float al = __half2float(alpha16[(size_t)t * I_pad + k]);
+    s = fmaf(al * al, w, s);
+  }
+  cpart[(size_t)c * I_pad + k] = s;
+}
+
+// S_down[k][g] = (sum_c cpart[c][k] / T) * (bn[0][k][g] + bn[1][k][g])  (fp64 sums, fixed order)
+__global__ void finalize_down_kernel(const float* __restrict__ cpart, const float* __restrict__ bnorm, int n_chunks,
+                                     int bhalves, int T, int I, int I_pad, int G, float* __restrict__ S_out) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= I) return;
+  double c = 0.0;
+  for (int i = 0; i < n_chunks; ++i) c += (double)cpart[(size_t)i * I_pad + k];
+  c /= (double)T;
+  for (int g = 0; g < G; ++g) {
+    double b = 0.0;
+    for (int hf = 0; hf < bhalves; ++hf) b += (double)bnorm[((size_t)hf * I_pad + k) * G + g];
+    S_out[(size_t)k * G + g] = (float)(c * b);
+  }
+}
+
+// ---------------------------------------------------------------- fp32 path (CUDA cores)
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
+
+// inv_r[t]; n32 = gamma*x/r; a32 = a/r.  One block per token.
+__global__ void f32_rows_kernel(const float* __restrict__ x, const float* __restrict__ a, const float* __restrict__ gamma,
+                                float* __restrict__ n32, float* __restrict__ a32, float* __restrict__ inv_r, int D,
+                                int HD, float eps) {
+  __shared__ float red[32];
+  const size_t t = blockIdx.x;
+  float ss = 0.f;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) ss = fmaf(x[t * D + d], x[t * D + d], ss);
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += red[i];
+    red[0] = s;
+  }
+  __syncthreads();
+  const float ir = 1.0f / sqrtf(red[0] / (float)D + eps);
+  if (threadIdx.x == 0 && inv_r) inv_r[t] = ir;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) n32[t * D + d] = gamma[d] * x[t * D + d] * ir;
+  if (a32)
+    for (int i = threadIdx.x; i < HD; i += blockDim.x) a32[t * HD + i] = a[t * HD + i] * ir;
+}
+
+// M32[2h + gu][k][j] = sum_d W[k][d] * gamma_d * Wo[d][h*dh + j]
+__global__ void f32_fold_kernel(const float* __restrict__ Wg, const float* __restrict__ Wu, const float* __restrict__ gamma,
+                                const float* __restrict__ Wo, float* __restrict__ M32, int H, int dh, int I, int D) {
+  const size_t total = (size_t)2 * H * I * dh;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
+    const int j = (int)(e % dh);
+    const int k = (int)((e / dh) % I);
+    const int hg = (int)(e / ((size_t)dh * I));
+    const int h = hg >> 1;
+    const float* w = ((hg & 1) ? Wu : Wg) + (size_t)k * D;
+    float s = 0.f;
+    for (int d = 0; d < D; ++d) s = fmaf(w[d] * gamma[d], Wo[(size_t)d * H * dh + h * dh + j], s);
+    M32[e] = s;
+  }
+}
+
+// Per (t, k): g, u from n32; FO: ab[t][k] = (silu'(g) u, silu(g)); alpha32[t][k] = silu(g) u.
+__global__ void f32_opoint_kernel(const float* __restrict__ n32, const float* __restrict__ Wg, const float* __restrict__ Wu,
+                                  float2* __restrict__ ab, float* __restrict__ alpha32, int T, int D, int I) {
+  const size_t total = (size_t)T * I;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
+    const int k = (int)(e % I);
+    const size_t t = e / I;
+    float g = 0.f, u = 0.f;
+    for (int d = 0; d < D; ++d) {
+      g = fmaf(n32[t * D + d], Wg[(size_t)k * D + d], g);
+      u = fmaf(n32[t * D + d], Wu[(size_t)k * D + d], u);
+    }
+    const float s = sigmoidf_(g);
+    if (ab) ab[e] = make_float2(s * (1.0f + g * (1.0f - s)) * u, g * s);
+    if (alpha32) alpha32[e] = g * s * u;
+  }
+}
+
+// partial[c][0][h][k] = sum_{t in chunk c} Delta^2 (FO) or pg^2 + pu^2 (ADD),
+// with pg = sum_j a32[t][h*dh+j] M32[2h][k][j] (a32 already carries 1/r).
+__global__ void f32_heads_kernel(const float* __restrict__ a32, const float* __restrict__ M32, const float2* __restrict__ ab,
+                                 float* __restrict__ partial, int T, int H, int dh, int I, int chunk, int fo) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  const int h = blockIdx.y, c = blockIdx.z;
+  if (k >= I) return;
+  const float* mg = M32 + ((size_t)(2 * h) * I + k) * dh;
+  const float* mu = M32 + ((size_t)(2 * h + 1) * I + k) * dh;
+  float acc = 0.f;
+  for (int t = c * chunk; t < min(T, (c + 1) * chunk); ++t) {
+    const float* ar = a32 + (size_t)t * H * dh + h * dh;
+    float pg = 0.f, pu = 0.f;
+    for (int j = 0; j < dh; ++j) {
+      pg = fmaf(ar[j], mg[j], pg);
+      pu = fmaf(ar[j], mu[j], pu);
+    }
+    if (fo) {
+      const float2 w = ab[(size_t)t * I + k];
+      const float d = w.x * pg + w.y * pu;
+      acc = fmaf(d, d, acc);
+    } else {
+      acc = fmaf(pg, pg, fmaf(pu, pu, acc));
+    }
+  }
+  partial[((size_t)c * H + h) * I + k] = acc;
+}
+
+// ssx[t] = sum_d (x[t][d] + sum_k alpha[t][k] Wd[d][k])^2; the second half row stays 0.
+__global__ void f32_xprime_kernel(const float* __restrict__ x, const float* __restrict__ alpha32, const float* __restrict__ Wd,
+                                  float* __restrict__ ssx, int T, int T_pad, int D, int I) {
+  __shared__ float red[32];
+  const size_t t = blockIdx.x;
+  float ss = 0.f;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float v = x[t * D + d];
+    for (int k = 0; k < I; ++k) v = fmaf(alpha32[t * I + k], Wd[(size_t)d * I + k], v);
+    ss = fmaf(v, v, ss);
+  }
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += red[i];
+    ssx[t] = s;
+    ssx[(size_t)T_pad + t] = 0.f;
+  }
+}
+
+// cpart[c][k] = sum_{t in chunk} alpha^2 / r'^2 for the fp32 path.
+__global__ void f32_down_token_weights_kernel(const float* __restrict__ alpha32, const float* __restrict__ ssx,
+                                              float* __restrict__ cpart, int T, int D, int I, int chunk, float eps) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  const int c = blockIdx.y;
+  if (k >= I) return;
+  float s = 0.f;
+  for (int t = c * chunk; t < min(T, (c + 1) * chunk); ++t) {
+    const float w = 1.0f / (ssx[t] / (float)D + eps);
+    const float al = alpha32[(size_t)t * I + k];
+    s = fmaf(al * al, w, s);
+  }
+  cpart[(size_t)c * I + k] = s;
+}
+
+// bnorm[0][k][g] = sum over W^qkv_g rows r of (sum_d Wrow[d] gamma'_d Wd[d][k])^2
+__global__ void f32_qnorm_kernel(const float* __restrict__ Wq, const float* __restrict__ Wk, const float* __restrict__ Wv,
+                                 const float* __restrict__ gamma_next, const float* __restrict__ Wd,
+                                 float* __restrict__ bnorm, int hpg, int dh, int D, int I, int G) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  const int g = blockIdx.y;
+  if (k >= I) return;
+  const int Rg = (hpg + 2) * dh;
+  float s = 0.f;
+  for (int r = 0; r < Rg; ++r) {
+    const float* row;
+    if (r < hpg * dh) row = Wq + ((size_t)g * hpg * dh + r) * D;
+    else if (r < (hpg + 1) * dh) row = Wk + ((size_t)g * dh + (r - hpg * dh)) * D;
+    else row = Wv + ((size_t)g * dh + (r - (hpg + 1) * dh)) * D;
+    float b = 0.f;
+    for (int d = 0; d < D; ++d) b = fmaf(row[d] * gamma_next[d], Wd[(size_t)d * I + k], b);
+    s = fmaf(b, b, s);
+  }
+  bnorm[(size_t)k * G + g] = s;
+}
+
+// ---------------------------------------------------------------- launchers
+static inline int blocks_for(size_t n, int threads, int cap = 8192) {
+  size_t b = (n + threads - 1) / threads;
+  return (int)(b < (size_t)cap ? (b > 0 ? b : 1) : cap);
+}
+
+cudaError_t launch_prep_tokens(const uint16_t* x, const uint16_t* a, const uint16_t* gamma, __half* n16, __half* a16,
+                               float* inv_r, int T, int D, int HD, float eps, uint32_t* status, cudaStream_t s) {
+  const int warps_per_block = 8;
+  prep_tokens_kernel<<<(T + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0, s>>>(
+      x, a, gamma, n16, a16, inv_r, T, D, HD, eps, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep_gate_up(const uint16_t* Wg, const uint16_t* Wu, __half* W16, int I, int I_pad, int D,
+                                uint32_t* status, cudaStream_t s) {
+  prep_gate_up_kernel<<<blocks_for((size_t)2 * I_pad * D / 8, 256), 256, 0, s>>>(Wg, Wu, W16, I, I_pad, D, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scaled_transpose_split(const uint16_t* W, const uint16_t* scale, __half* out, int Drows, int Ncols,
+                                          uint32_t* status, cudaStream_t s) {
+  dim3 grid((Ncols + 31) / 32, (Drows + 31) / 32), block(32, 8);
+  scaled_transpose_split_kernel<<<grid, block, 0, s>>>(W, scale, out, Drows, Ncols, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wd_colnorm(const uint16_t* Wd, float* wdn, int D, int I, int I_pad, cudaStream_t s) {
+  dim3 grid((I_pad + 31) / 32), block(32, 8);
+  wd_colnorm_kernel<<<grid, block, 0, s>>>(Wd, wdn, D, I, I_pad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wd_colnorm_f32(const float* Wd, float* wdn, int D, int I, cudaStream_t s) {
+  dim3 grid((I + 31) / 32), block(32, 8);
+  wd_colnorm_f32_kernel<<<grid, block, 0, s>>>(Wd, wdn, D, I);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_partials(const float* partial, double* out, int n_chunks, int halves, int H, int I_pad,
+                                   cudaStream_t s) {
+  dim3 grid((I_pad + 31) / 32, H), block(32, 8);
+  reduce_partials_kernel<<<grid, block, 0, s>>>(partial, out, n_chunks, halves, H, I_pad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_up(const double* sh, const float* wdn, int fo, int T, int H, int G, int I, int I_pad,
+                               float* S_out, float* S_head_out, cudaStream_t s) {
+  dim3 grid((I + 127) / 128, G);
+  finalize_up_kernel<<<grid, 128, 0, s>>>(sh, wdn, fo, T, H, G, I, I_pad, S_out, S_head_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep_wd(const uint16_t* Wd, __half* Wd16, __half* WdT16, int D, int I, int I_pad, uint32_t* status,
+                           cudaStream_t s) {
+  dim3 grid((I_pad + 31) / 32, (D + 31) / 32), block(32, 8);
+  prep_wd_kernel<<<grid, block, 0, s>>>(Wd, Wd16, WdT16, D, I, I_pad, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep_qkv(const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* gamma_next,
+                            __half* out, int G, int hpg, int dh, int D, uint32_t* status, cudaStream_t s) {
+  prep_qkv_kernel<<<blocks_for((size_t)G * (hpg + 2) * dh * D, 256), 256, 0, s>>>(Wq, Wk, Wv, gamma_next, out, G, hpg,
+                                                                                 dh, D, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_down_token_weights(const __half* alpha16, const float* ssx, float* cpart, int T, int T_pad, int D,
+                                      int I_pad, int chunk, float eps, cudaStream_t s) {
+  dim3 grid((I_pad + 127) / 128, (T + chunk - 1) / chunk);
+  down_token_weights_kernel<<<grid, 128, 0, s>>>(alpha16, ssx, cpart, T, T_pad, D, I_pad, chunk, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_down(const float* cpart, const float* bnorm, int n_chunks, int bhalves, int T, int I,
+                                 int I_pad, int G, float* S_out, cudaStream_t s) {
+  finalize_down_kernel<<<(I + 127) / 128, 128, 0, s>>>(cpart, bnorm, n_chunks, bhalves, T, I, I_pad, G, S_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_f32_up(const F32UpArgs& A, cudaStream_t s) {
+  f32_rows_kernel<<<A.T, 128, 0, s>>>(A.x, A.a, A.gamma, A.n32, A.a32, nullptr, A.D, A.H * A.dh, A.eps);
+  f32_fold_kernel<<<blocks_for((size_t)2 * A.H * A.I * A.dh, 128), 128, 0, s>>>(A.Wg, A.Wu, A.gamma, A.Wo, A.M32, A.H,
+                                                                                 A.dh, A.I, A.D);
+  if (A.fo)
+    f32_opoint_kernel<<<blocks_for((size_t)A.T * A.I, 128), 128, 0, s>>>(A.n32, A.Wg, A.Wu, A.ab, nullptr, A.T, A.D,
+                                                                          A.I);
+  dim3 grid((A.I + 127) / 128, A.H, A.n_chunks);
+  f32_heads_kernel<<<grid, 128, 0, s>>>(A.a32, A.M32, A.ab, A.partial, A.T, A.H, A.dh, A.I, A.chunk, A.fo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_f32_down(const F32DownArgs& A, cudaStream_t s) {
+  f32_rows_kernel<<<A.T, 128, 0, s>>>(A.x, nullptr, A.gamma, A.n32, nullptr, nullptr, A.D, 0, A.eps);
+  f32_opoint_kernel<<<blocks_for((size_t)A.T * A.I, 128), 128, 0, s>>>(A.n32, A.Wg, A.Wu, nullptr, A.alpha32, A.T,
+                                                                        A.D, A.I);
+  f32_xprime_kernel<<<A.T, 128, 0, s>>>(A.x, A.alpha32, A.Wd, A.ssx, A.T, A.T, A.D, A.I);
+  dim3 g1((A.I + 127) / 128, A.n_chunks);
+  f32_down_token_weights_kernel<<<g1, 128, 0, s>>>(A.alpha32, A.ssx, A.cpart, A.T, A.D, A.I, A.chunk, A.eps);
+  dim3 g2((A.I + 127) / 128, A.G);
+  f32_qnorm_kernel<<<g2, 128, 0, s>>>(A.Wq, A.Wk, A.Wv, A.gamma_next, A.Wd, A.bnorm, A.H / A.G, A.dh, A.D, A.I, A.G);
+  return cudaGetLastError();
+}
+
+}  // namespace aff

@@ -1,0 +1,53 @@
+// tile_kernel.cuh -- parameters shared by the tcgen05 tile kernel and its host launcher.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+namespace aff {
+
+// Every job of the tile kernel is "two 128-row A tiles against one shared
+// 128-row B tile": D1 = A1 * B^T and D2 = A2 * B^T accumulate in tensor
+// memory over K in blocks of 64 fp16 elements (128-byte rows).
+constexpr int kBlockM = 128;      // rows per A tile  (TMEM lanes)
+constexpr int kBlockN = 128;      // rows per B tile  (TMEM columns per accumulator)
+constexpr int kBlockK = 64;       // fp16 elements per K block (one 128 B swizzle row)
+constexpr int kTileBytes = kBlockM * kBlockK * 2;     // 16 KB
+constexpr int kStageBytes = 3 * kTileBytes;           // A1 + A2 + B = 48 KB
+constexpr int kThreads = 320;                         // TMA warp, MMA warp, 8 epilogue warps
+constexpr int kEpiWarps = 8;
+constexpr int kTmemCols = 512;                        // 2 buffers x (D1 128 + D2 128)
+constexpr int kMaxDynSmem = 232448;                   // 227 KB opt-in limit per block
+
+enum TileMode : int {
+  kModeFold = 0,   // M_h = Wg/Wu * diag(gamma) * Wo^(h)   -> fp16 [2H][I_pad][dh]
+  kModeFO = 1,     // per token tile: operating point, then every head's Delta^2
+  kModeADD = 2,    // per token tile: every head's (p.w^g)^2 + (p.w^u)^2
+  kModeAlpha = 3,  // per token tile: alpha = silu(g) u  -> fp16 [T_pad][I_pad]
+  kModeXPrime = 4, // x' = x + alpha Wd^T for 256 tokens, sum_d x'^2 -> 1/r'^2
+  kModeQNorm = 5   // ||b_gk||^2 = sum over group g's q/k/v rows r of ((Wqkv' diag(gamma'))_r . w^d_k)^2
+};
+
+struct TileParams {
+  int32_t mode;
+  int32_t n_units;
+  int32_t stages;
+  int32_t T, D, H, G, dh, I, I_pad, T_pad;
+  int32_t n_ktiles;        // neuron tiles of 128 (I_pad / 128)
+  int32_t n_ttiles;        // token tiles of 128 (T_pad / 128)
+  int32_t tiles_per_unit;  // token tiles per FO/ADD/alpha unit
+  int32_t n_ntiles;        // fold: column tiles of 128 over H*dh; x': over D; qnorm: row tiles per group
+  int32_t rows_per_group;  // qnorm: (H/G + 2) * dh
+  int32_t nkb_D, nkb_dh, nkb_I;
+  uint32_t* status;
+  float* partial;          // FO/ADD: [n_chunks][2][H][I_pad]; x': [T_pad] sum x'^2 parts
+  __half* M16;             // fold output
+  __half* alpha16;         // alpha output
+  const uint16_t* x_bf16;  // x' epilogue reads x (bf16 bits) [T][D]
+  float* inv_rp2;          // x' output 1/r'^2 [T_pad]
+  float* bnorm;            // qnorm output [I_pad][G]
+  float eps;
+};
+
+}  // namespace aff

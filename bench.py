@@ -175,6 +175,7 @@ def main() -> None:
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=256)
+    ap.add_argument("--tokens", type=int, default=0, help="override T (profiling runs on a smaller case)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -195,6 +196,8 @@ def main() -> None:
     B.load()
 
     base = W.CONFIGS[args.workload]
+    if args.tokens:
+        base = base.scaled(T=args.tokens)
     shape = base.scaled(seed=base.seed + 1000 * rank)     # each rank: its own token batch
     layer = W.make_layer(shape)
     host = {k: DV.host_tensor(layer, k, shape.dtype).pin_memory() for k in DV.UP_KEYS}
@@ -261,7 +264,7 @@ def main() -> None:
         S_host.copy_(S, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps if args.e2e_steps > 0 else float("nan")
 
     if rank != 0:
         if ws > 1:

@@ -132,6 +132,32 @@ AFF_API aff_status affinity_up(const void* a, const void* x, const void* Wo, con
                        void* workspace, size_t workspace_bytes, aff_stream_t stream);
 
 /*
+ * affinity_up without a workspace argument.  The paper has no counterpart:
+ * this entry point serves callers that cannot allocate device memory --
+ * for example a plugin hosted by a framework that owns every device
+ * allocation and hands plugins no scratch, or a process whose memory pool
+ * has already reserved the whole device.  It computes exactly what
+ * affinity_up computes (same arguments minus the workspace) and calls no
+ * allocator; its scratch is one 64 MiB array compiled into the library,
+ * which every GPU that loads the library holds until the process exits.
+ *   - Shapes whose affinity_workspace_size(dims, mode, 0) exceeds 64 MiB
+ *     (67108864 bytes) are refused with AFF_ERR_WORKSPACE; nothing is
+ *     enqueued.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents
+ *     (each call writes every part it reads).  Calls whose work overlaps on
+ *     the GPU -- on different streams, or from different host threads --
+ *     race on it: serialise them.  The device status word lives in the
+ *     array too; affinity_device_status() does not apply to it.
+ */
+AFF_API aff_status affinity_up_static(const void* a, const void* x, const void* Wo, const void* gamma,
+                              const void* Wg, const void* Wu, const void* Wd,
+                              const aff_dims* dims, int32_t mode,
+                              float* S_out, float* S_head_out, aff_stream_t stream);
+
+/*
  * S_down for one layer ("Affinity scores", §3, down edge):
  *   S_down[k, g] = E_t[alpha_k^2 / r'^2] * ||b_gk||^2,
  *   alpha_k = silu(g_k) u_k,  b_gk = W^qkv_g (gamma_next * w^d_k),

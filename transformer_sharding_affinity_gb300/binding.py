@@ -66,6 +66,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.affinity_workspace_size.restype = st
     lib.affinity_up.argtypes = [_P] * 7 + [ctypes.POINTER(aff_dims), ctypes.c_int32, _P, _P, _P, ctypes.c_size_t, _P]
     lib.affinity_up.restype = st
+    lib.affinity_up_static.argtypes = [_P] * 7 + [ctypes.POINTER(aff_dims), ctypes.c_int32, _P, _P, _P]
+    lib.affinity_up_static.restype = st
     lib.affinity_down.argtypes = [_P] * 9 + [ctypes.POINTER(aff_dims), _P, _P, ctypes.c_size_t, _P]
     lib.affinity_down.restype = st
     lib.affinity_device_status.argtypes = [_P, _P]
@@ -145,6 +147,14 @@ def affinity_up(a, x, Wo, gamma, Wg, Wu, Wd, d: aff_dims, mode: int, S_out, S_he
     _check(load().affinity_up(_ptr(a), _ptr(x), _ptr(Wo), _ptr(gamma), _ptr(Wg), _ptr(Wu), _ptr(Wd),
                               ctypes.byref(d), int(mode), _ptr(S_out), _ptr(S_head_out), _ptr(workspace), nbytes,
                               _stream(stream)), "affinity_up")
+
+
+def affinity_up_static(a, x, Wo, gamma, Wg, Wu, Wd, d: aff_dims, mode: int, S_out, S_head_out,
+                       stream=None) -> None:
+    """Enqueue S_up using the library's built-in 64 MiB scratch instead of a workspace."""
+    _check(load().affinity_up_static(_ptr(a), _ptr(x), _ptr(Wo), _ptr(gamma), _ptr(Wg), _ptr(Wu), _ptr(Wd),
+                                     ctypes.byref(d), int(mode), _ptr(S_out), _ptr(S_head_out), _stream(stream)),
+           "affinity_up_static")
 
 
 def affinity_down(x, gamma, Wg, Wu, Wd, gamma_next, Wq_next, Wk_next, Wv_next, d: aff_dims, S_out, workspace,

@@ -1,0 +1,59 @@
+// noalloc.cu -- affinity_up_static: affinity_up for callers that cannot
+// allocate device memory, with its scratch space compiled into the library.
+#include "affinity.h"
+
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <vector>
+
+namespace {
+
+// Scratch used in place of a caller-provided workspace.  Every GPU that loads
+// the library holds these bytes until the process exits.
+constexpr size_t kStaticScratchBytes = 64ull << 20;  // 64 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch on the current device.  In host code the
+// array's name only stands in for the symbol; a kernel must be given this
+// address instead.  Looked up once per device, with that device current.
+aff_status scratch_on_current_device(void** out) {
+  static std::mutex mu;
+  static std::vector<void*> addr;  // per device ordinal; nullptr until looked up
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return AFF_ERR_ARCH;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if ((int)addr.size() <= dev) addr.resize(dev + 1, nullptr);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return AFF_ERR_CUDA;
+    }
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return AFF_OK;
+}
+
+}  // namespace
+
+extern "C" aff_status affinity_up_static(const void* a, const void* x, const void* Wo, const void* gamma,
+                                         const void* Wg, const void* Wu, const void* Wd, const aff_dims* dims,
+                                         int32_t mode, float* S_out, float* S_head_out, aff_stream_t stream) {
+  size_t need = 0;
+  aff_status st = affinity_workspace_size(dims, mode, 0, &need);
+  if (st != AFF_OK) return st;
+  if (need > kStaticScratchBytes) return AFF_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if ((st = scratch_on_current_device(&scratch)) != AFF_OK) return st;
+  // Every buffer the pass reads is written earlier in the same call (the
+  // status word is cleared at its start), so leftovers of a previous call
+  // in the shared array never reach the result.
+  return affinity_up(a, x, Wo, gamma, Wg, Wu, Wd, dims, mode, S_out, S_head_out, scratch, kStaticScratchBytes,
+                     stream);
+}

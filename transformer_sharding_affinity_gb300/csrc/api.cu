@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -17,8 +18,8 @@
 #include <vector>
 
 namespace aff {
-cudaError_t launch_tile_kernel(const CUtensorMap* maps, const TileParams& p, int grid, cudaStream_t stream);
-size_t tile_smem_bytes(int mode, int stages, int H);
+cudaError_t launch_tile_kernel(const CUtensorMap* maps, const TileParams& p, int* grid, cudaStream_t stream);
+size_t tile_smem_bytes(int mode, int stages, int H, bool pair);
 }  // namespace aff
 
 using namespace aff;
@@ -59,7 +60,7 @@ aff_status check_dims(const aff_dims* d) {
   if (d->dtype == AFF_BF16) {
     if (d->D % 8 || d->d_head % 8 || d->I % 8) return AFF_ERR_UNSUPPORTED_SHAPE;
     // per-thread head sums live in shared memory next to 2+ pipeline stages
-    if (tile_smem_bytes(kModeFO, 2, (int)d->H) > (size_t)kMaxDynSmem) return AFF_ERR_UNSUPPORTED_SHAPE;
+    if (tile_smem_bytes(kModeFO, 2, (int)d->H, false) > (size_t)kMaxDynSmem) return AFF_ERR_UNSUPPORTED_SHAPE;
     if (d->H * d->d_head > kMaxDim) return AFF_ERR_UNSUPPORTED_SHAPE;
   }
   return AFF_OK;
@@ -89,7 +90,7 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
   const int64_t T = d.T, D = d.D, H = d.H, G = d.G, dh = d.d_head, I = d.I;
   L.status = L.take(256);
   if (d.dtype == AFF_BF16) {
-    L.I_pad = round_up(I, 128);
+    L.I_pad = round_up(I, 256);   // whole 256-neuron tiles for CTA pairs
     L.T_pad = round_up(T, 128);
     L.W16 = L.take((size_t)2 * L.I_pad * D * 2);
     L.n16 = L.take((size_t)T * D * 2);
@@ -218,10 +219,22 @@ aff_status map2(CUtensorMap* m, const void* p, uint64_t inner, uint64_t rows) {
   return make_map(m, p, 2, d, s, 128, 1);
 }
 
-int pick_stages(int mode, int H) {
-  for (int s = 4; s >= 2; --s)
-    if (tile_smem_bytes(mode, s, H) <= (size_t)kMaxDynSmem) return s;
+int pick_stages(int mode, int H, bool pair) {
+  for (int s = 6; s >= 2; --s)
+    if (tile_smem_bytes(mode, s, H, pair) <= (size_t)kMaxDynSmem) return s;
   return 0;
+}
+
+// FO / ADD run one CTA per SM by default; AFFINITY_PAIR=1 selects CTA pairs
+// (256-row cta_group::2 MMAs, each CTA loading half of every token tile).
+// Both give identical results; on the Qwen3-0.6B-shaped layer the single-CTA
+// form measured faster (2.36 vs 2.70 ms for the FO kernel).
+bool use_pairs() {
+  static bool v = [] {
+    const char* e = std::getenv("AFFINITY_PAIR");
+    return e && e[0] == '1';
+  }();
+  return v;
 }
 
 TileParams base_params(const aff_dims& d, const Layout& L, uint8_t* ws, int mode) {
@@ -241,18 +254,42 @@ TileParams base_params(const aff_dims& d, const Layout& L, uint8_t* ws, int mode
   p.nkb_D = (int)ceil_div(d.D, 64);
   p.nkb_dh = (int)ceil_div(d.d_head, 64);
   p.nkb_I = (int)(L.I_pad / 64);
-  p.stages = pick_stages(mode, p.H);
+  p.ls_D = (int)(((d.D - 1) % 64) / 16 + 1);          // 16-wide K slices in the last block of D
+  p.ls_dh = (int)(((d.d_head - 1) % 64) / 16 + 1);    // ... and of d_head
+  p.stages = pick_stages(mode, p.H, false);
   p.status = reinterpret_cast<uint32_t*>(ws + L.status);
   p.eps = d.eps;
   return p;
 }
 
-aff_status run_tile(const CUtensorMap* maps, TileParams& p, int sm_count, cudaStream_t s, bool dominant = false) {
+aff_status run_tile(const CUtensorMap* maps, TileParams& p, cudaStream_t s, bool dominant = false) {
   if (p.n_units <= 0) return AFF_OK;
-  const int grid = p.n_units < sm_count ? p.n_units : sm_count;
+  // CTAs (or CTA pairs) resident at once, cached per device and configuration
+  static std::mutex mu;
+  static std::vector<std::pair<std::vector<int>, int>> cache;
+  int dev = 0;
+  AFF_CUDA(cudaGetDevice(&dev));
+  const std::vector<int> key = {dev, p.mode, p.pair, p.stages, p.H};
+  int fit = 0;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (auto& kv : cache)
+      if (kv.first == key) fit = kv.second;
+  }
+  if (fit <= 0) {
+    cudaError_t e = launch_tile_kernel(maps, p, &fit, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tile kernel occupancy query");
+    if (fit <= 0) {
+      g_last_cuda_error = "the tile kernel does not fit on this device";
+      return AFF_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    cache.push_back({key, fit});
+  }
+  int grid = p.n_units < fit ? p.n_units : fit;
   const bool timed = dominant && g_timing_start && g_timing_stop;
   if (timed) AFF_CUDA(cudaEventRecord(g_timing_start, s));
-  cudaError_t e = launch_tile_kernel(maps, p, grid, s);
+  cudaError_t e = launch_tile_kernel(maps, p, &grid, s);
   if (e != cudaSuccess) return cuda_fail(e, "affinity_tile_kernel");
   if (timed) AFF_CUDA(cudaEventRecord(g_timing_stop, s));
   return AFF_OK;
@@ -378,13 +415,17 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     p.n_ntiles = (int)ceil_div((int64_t)H * dh, 128);
     p.n_units = p.n_ktiles * p.n_ntiles;
     p.M16 = M16;
-    if ((st = run_tile(maps, p, sm_count, s)) != AFF_OK) return st;
+    if ((st = run_tile(maps, p, s)) != AFF_OK) return st;
   }
-  // FO / ADD: per token tile, operating point (FO) then every head
+  // FO / ADD: per token tile, operating point (FO) then every head.  With CTA
+  // pairs each CTA loads half (64 rows) of every token tile.
   {
+    const bool pair = use_pairs();
+    const uint32_t brows = pair ? 64u : 128u;
+    uint64_t dx[2] = {(uint64_t)D, (uint64_t)T}, sx[1] = {(uint64_t)D * 2};
     if ((st = map2(&maps[0], W16, (uint64_t)D, (uint64_t)2 * I_pad)) != AFF_OK) return st;
     if (fo) {
-      if ((st = map2(&maps[1], n16, (uint64_t)D, (uint64_t)T)) != AFF_OK) return st;
+      if ((st = make_map(&maps[1], n16, 2, dx, sx, brows, 1)) != AFF_OK) return st;
     } else {
       maps[1] = maps[0];
     }
@@ -393,11 +434,13 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     if ((st = make_map(&maps[2], M16, 3, dm, sd, 128, 1)) != AFF_OK) return st;
     uint64_t da[3] = {(uint64_t)dh, (uint64_t)H, (uint64_t)T};
     uint64_t sa[2] = {(uint64_t)dh * 2, (uint64_t)H * dh * 2};
-    if ((st = make_map(&maps[3], a16, 3, da, sa, 128, 2)) != AFF_OK) return st;
+    if ((st = make_map(&maps[3], a16, 3, da, sa, brows, 2)) != AFF_OK) return st;
     TileParams p = base_params(d, L, ws, fo ? kModeFO : kModeADD);
-    p.n_units = (int)(L.n_chunks * p.n_ktiles);
+    p.pair = pair ? 1 : 0;
+    p.stages = pick_stages(p.mode, p.H, pair);
+    p.n_units = (int)(L.n_chunks * (pair ? p.n_ktiles / 2 : p.n_ktiles));
     p.partial = partial;
-    if ((st = run_tile(maps, p, sm_count, s, true)) != AFF_OK) return st;
+    if ((st = run_tile(maps, p, s, true)) != AFF_OK) return st;
   }
   AFF_CUDA(launch_reduce_partials(partial, headsum, (int)L.n_chunks, 2, H, I_pad, s));
   AFF_CUDA(launch_finalize_up(headsum, wdn, fo, T, H, G, I, I_pad, S_out, S_head_out, s));
@@ -469,7 +512,7 @@ aff_status affinity_down(const void* x, const void* gamma, const void* Wg, const
     TileParams p = base_params(d, L, ws, kModeAlpha);
     p.n_units = (int)(ceil_div(p.n_ttiles, kTilesPerUnit) * p.n_ktiles);
     p.alpha16 = alpha16;
-    if ((st = run_tile(maps, p, sm_count, s, true)) != AFF_OK) return st;
+    if ((st = run_tile(maps, p, s, true)) != AFF_OK) return st;
   }
   // x' = x + alpha Wd^T and sum_d x'^2 per token
   {
@@ -482,7 +525,7 @@ aff_status affinity_down(const void* x, const void* gamma, const void* Wg, const
     p.n_units = (int)ceil_div(T_pad, 256);
     p.partial = ssx;
     p.x_bf16 = (const uint16_t*)x;
-    if ((st = run_tile(maps, p, sm_count, s)) != AFF_OK) return st;
+    if ((st = run_tile(maps, p, s)) != AFF_OK) return st;
   }
   AFF_CUDA(launch_down_token_weights(alpha16, ssx, cpart, T, T_pad, D, I_pad, kDownTokenChunk, d.eps, s));
   // ||b_gk||^2 for every neuron and group
@@ -498,7 +541,7 @@ aff_status affinity_down(const void* x, const void* gamma, const void* Wg, const
     p.rows_per_group = (int)L.Rg;
     p.n_units = (int)ceil_div(I_pad, 256);
     p.bnorm = bnorm;
-    if ((st = run_tile(maps, p, sm_count, s)) != AFF_OK) return st;
+    if ((st = run_tile(maps, p, s)) != AFF_OK) return st;
   }
   AFF_CUDA(launch_finalize_down(cpart, bnorm, (int)L.n_tchunks, 2, T, I, I_pad, G, S_out, s));
   return AFF_OK;

@@ -161,18 +161,19 @@ __global__ void wd_colnorm_f32_kernel(const float* __restrict__ Wd, float* __res
 }
 
 // ---------------------------------------------------------------- reductions
-// S_head_d[h][k] = sum over chunks and halves of partial[c][hf][h][k], in fp64,
-// in a fixed order (8 interleaved chunk phases, then phases in order).
+// S_head_d[h][k] = sum over chunks and halves of partial[c][hf][h][k] in a fixed
+// order: fp32 sums over 8 interleaved chunk phases, then the phases in fp64
+// (fp64 arithmetic is slow on this part, so it is kept to the last level).
 __global__ void reduce_partials_kernel(const float* __restrict__ partial, double* __restrict__ out, int n_chunks,
                                        int halves, int H, int I_pad) {
   __shared__ double part[8][33];
   const int k = blockIdx.x * 32 + threadIdx.x;
   const int h = blockIdx.y;
-  double s = 0.0;
+  float s = 0.f;   // fp32 within a phase (at most n_chunks/8 terms), fp64 across the 8 phases
   if (k < I_pad)
     for (int c = threadIdx.y; c < n_chunks; c += 8)
-      for (int hf = 0; hf < halves; ++hf) s += (double)partial[((size_t)(c * halves + hf) * H + h) * I_pad + k];
-  part[threadIdx.y][threadIdx.x] = s;
+      for (int hf = 0; hf < halves; ++hf) s += partial[((size_t)(c * halves + hf) * H + h) * I_pad + k];
+  part[threadIdx.y][threadIdx.x] = (double)s;
   __syncthreads();
   if (threadIdx.y == 0 && k < I_pad) {
     double t = 0.0;

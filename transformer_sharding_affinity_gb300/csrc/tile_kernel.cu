@@ -30,14 +30,14 @@ enum JobKind : int { kJobGateUp = 0, kJobHead = 1, kJobFold = 2, kJobXPrime = 3,
 
 struct Job {
   int kind;
-  int nkb;      // K blocks of 64
-  int klen;     // valid K extent (for the last block's K-slice count)
-  int head;     // head index (kJobHead)
-  int part;     // fold: 0 = hi, 1 = lo half of gamma*Wo (selected per K block)
-  int t0;       // first token (row of the B tile, or of A1 for x')
-  int kt;       // neuron tile
-  int nt;       // column / row tile
-  int g;        // KV group (qnorm)
+  int nkb;       // K blocks of 64 in the job
+  int nkb_part;  // K blocks per part (fold / qnorm run the K range twice: hi then lo)
+  int last_nks;  // 16-wide K slices in the last block of a part
+  int head;      // head index (kJobHead)
+  int t0;        // first token (row of the B tile, or of A1 for x')
+  int kt;        // neuron tile
+  int nt;        // column / row tile
+  int g;         // KV group (qnorm)
 };
 
 struct Unit {
@@ -48,8 +48,20 @@ struct Unit {
   int base;     // x': first token; qnorm: first neuron
 };
 
-__device__ __forceinline__ Unit unit_info(const TileParams& p, int u) {
+// Unit u of the schedule.  With CTA pairs (FO / ADD) a unit covers 256 neurons:
+// the CTA of cluster rank `rank` owns neuron tile 2 * (u % (n_ktiles / 2)) + rank.
+template <bool PAIR>
+__device__ __forceinline__ Unit unit_info(const TileParams& p, int u, int rank) {
   Unit U{};
+  if (PAIR) {
+    const int npair = p.n_ktiles >> 1;
+    U.kt = 2 * (u % npair) + rank;
+    U.chunk = u / npair;
+    U.tile0 = U.chunk * p.tiles_per_unit;
+    const int nt = min(p.tiles_per_unit, p.n_ttiles - U.tile0);
+    U.njobs = nt * (p.mode == kModeFO ? 1 + p.H : p.H);
+    return U;
+  }
   switch (p.mode) {
     case kModeFold:
       U.kt = u % p.n_ktiles;
@@ -79,55 +91,45 @@ __device__ __forceinline__ Unit unit_info(const TileParams& p, int u) {
   return U;
 }
 
-__device__ __forceinline__ Job job_info(const TileParams& p, const Unit& U, int j) {
+// Position within a unit's job list, advanced without divisions: FO / ADD:
+// a = token tile of the unit, b = job within the tile; qnorm: a = group,
+// b = row tile; the other modes count jobs in b.
+struct JobIter {
+  int a, b;
+};
+
+// The next job of unit U (every role walks the same sequence).
+template <int MODE>
+__device__ __forceinline__ Job job_next(const TileParams& p, const Unit& U, JobIter& it) {
   Job J{};
   J.kt = U.kt;
-  switch (p.mode) {
-    case kModeFold:
-      J.kind = kJobFold;
-      J.nkb = 2 * p.nkb_D;
-      J.klen = p.D;
-      J.nt = U.base;
-      break;
-    case kModeFO: {
-      int per = 1 + p.H;
-      int tile = U.tile0 + j / per, r = j % per;
-      J.t0 = tile * kBlockN;
-      if (r == 0) {
-        J.kind = kJobGateUp; J.nkb = p.nkb_D; J.klen = p.D;
-      } else {
-        J.kind = kJobHead; J.head = r - 1; J.nkb = p.nkb_dh; J.klen = p.dh;
-      }
-      break;
+  if constexpr (MODE == kModeFold) {
+    J.kind = kJobFold; J.nkb = 2 * p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D; J.nt = U.base;
+  } else if constexpr (MODE == kModeFO) {
+    J.t0 = (U.tile0 + it.a) * kBlockN;
+    if (it.b == 0) {
+      J.kind = kJobGateUp; J.nkb = p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D;
+    } else {
+      J.kind = kJobHead; J.head = it.b - 1; J.nkb = p.nkb_dh; J.nkb_part = p.nkb_dh; J.last_nks = p.ls_dh;
     }
-    case kModeADD: {
-      int tile = U.tile0 + j / p.H;
-      J.t0 = tile * kBlockN;
-      J.kind = kJobHead; J.head = j % p.H; J.nkb = p.nkb_dh; J.klen = p.dh;
-      break;
-    }
-    case kModeAlpha:
-      J.t0 = (U.tile0 + j) * kBlockN;
-      J.kind = kJobGateUp; J.nkb = p.nkb_D; J.klen = p.D;
-      break;
-    case kModeXPrime:
-      J.kind = kJobXPrime; J.nkb = p.nkb_I; J.klen = p.I_pad;
-      J.t0 = U.base; J.nt = j;
-      break;
-    case kModeQNorm:
-      J.kind = kJobQNorm; J.nkb = 2 * p.nkb_D; J.klen = p.D;
-      J.g = j / p.n_ntiles; J.nt = j % p.n_ntiles;
-      break;
+    if (++it.b == 1 + p.H) { it.b = 0; ++it.a; }
+  } else if constexpr (MODE == kModeADD) {
+    J.t0 = (U.tile0 + it.a) * kBlockN;
+    J.kind = kJobHead; J.head = it.b; J.nkb = p.nkb_dh; J.nkb_part = p.nkb_dh; J.last_nks = p.ls_dh;
+    if (++it.b == p.H) { it.b = 0; ++it.a; }
+  } else if constexpr (MODE == kModeAlpha) {
+    J.t0 = (U.tile0 + it.b) * kBlockN;
+    J.kind = kJobGateUp; J.nkb = p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D;
+    ++it.b;
+  } else if constexpr (MODE == kModeXPrime) {
+    J.kind = kJobXPrime; J.nkb = p.nkb_I; J.nkb_part = p.nkb_I; J.last_nks = 4;
+    J.t0 = U.base; J.nt = it.b++;
+  } else {   // kModeQNorm
+    J.kind = kJobQNorm; J.nkb = 2 * p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D;
+    J.g = it.a; J.nt = it.b;
+    if (++it.b == p.n_ntiles) { it.b = 0; ++it.a; }
   }
   return J;
-}
-
-// Number of 16-wide K slices in K block kb of a job.
-__device__ __forceinline__ int kslices(const Job& J, int kb, int nkb_D) {
-  int k_in = (J.kind == kJobFold || J.kind == kJobQNorm) ? (kb % nkb_D) : kb;
-  int rem = J.klen - k_in * kBlockK;
-  int n = (rem + 15) >> 4;
-  return n < 4 ? n : 4;
 }
 
 struct Smem {
@@ -149,7 +151,7 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     affinity_tile_kernel(const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
                          const __grid_constant__ CUtensorMap map2, const __grid_constant__ CUtensorMap map3,
@@ -159,9 +161,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
 
   const int S = p.stages;
+  constexpr int kSB = PAIR ? kPairStageBytes : kStageBytes;   // bytes of one pipeline stage
+  constexpr int kBOff = 2 * kTileBytes;                         // B tile offset within a stage
   Smem sm;
   sm.stage0 = base;
-  uint8_t* cur = base + (size_t)S * kStageBytes;
+  uint8_t* cur = base + (size_t)S * kSB;
   sm.sacc = reinterpret_cast<float*>(cur);
   int sacc_floats = (MODE == kModeFO || MODE == kModeADD) ? 2 * p.H * kBlockM : 0;
   cur += (size_t)sacc_floats * 4;
@@ -175,6 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int crank = PAIR ? (int)cluster_ctarank() : 0;   // 0 = leader (issues the MMAs), 1 = peer
+  const int cid = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ncl = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -183,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.tfull[b], 1);
-      mbar_init(&sm.tempty[b], kEpiWarps);
+      mbar_init(&sm.tempty[b], PAIR ? 2 * kEpiWarps : kEpiWarps);   // pairs: both CTAs' epilogues
     }
     mbar_init(sm.drain, 1);
     *sm.abort_flag = 0;
@@ -196,116 +203,174 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&map3);
   }
   if (warp == 1) {
-    tmem_alloc(sm.tmem_slot, kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(sm.tmem_slot, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(sm.tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
   }
   if (warp >= 2) {
     for (int i = threadIdx.x - 64; i < sacc_floats; i += kEpiWarps * 32) sm.sacc[i] = 0.f;
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync_all();   // both CTAs' barriers and tensor memory exist before either uses the other's
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_slot;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int it = 0;
+      int s = 0, issued = 0;
+      uint32_t ph = 0;                 // phase parity of the current use of stage s
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        Unit U = unit_info(p, u);
+      for (int u = cid; ok && u < p.n_units; u += ncl) {
+        const Unit U = unit_info<PAIR>(p, u, crank);
+        JobIter jt{0, 0};
         for (int j = 0; ok && j < U.njobs; ++j) {
-          Job J = job_info(p, U, j);
-          for (int kb = 0; kb < J.nkb; ++kb, ++it) {
-            const int s = it % S;
-            const uint32_t k = (uint32_t)(it / S);
-            if (!mbar_wait(&sm.empty[s], (k & 1u) ^ 1u, sm.abort_flag, p.status)) { ok = false; break; }
-            uint8_t* st = sm.stage0 + (size_t)s * kStageBytes;
+          const Job J = job_next<MODE>(p, U, jt);
+          for (int kb = 0, kb_in = 0, part = 0; kb < J.nkb; ++kb) {
+            const bool w = PAIR ? mbar_wait_cluster(&sm.empty[s], ph ^ 1u, sm.abort_flag, p.status)
+                                : mbar_wait(&sm.empty[s], ph ^ 1u, sm.abort_flag, p.status);
+            if (!w) { ok = false; break; }
+            uint8_t* st = sm.stage0 + s * kSB;
             uint64_t* fb = &sm.full[s];
-            mbar_arrive_expect_tx(fb, kStageBytes);
-            const int kx = kb * kBlockK;
-            switch (J.kind) {
-              case kJobGateUp:   // A = W16 gate / up rows, B = n16 token rows
-                tma_load_2d(st, &map0, fb, kx, J.kt * kBlockM);
-                tma_load_2d(st + kTileBytes, &map0, fb, kx, p.I_pad + J.kt * kBlockM);
-                tma_load_2d(st + 2 * kTileBytes, &map1, fb, kx, J.t0);
-                break;
-              case kJobHead:     // A = M16 (gate, up) of head h, B = a16 head h
-                tma_load_3d(st, &map2, fb, kx, J.kt * kBlockM, 2 * J.head);
-                tma_load_3d(st + kTileBytes, &map2, fb, kx, J.kt * kBlockM, 2 * J.head + 1);
-                tma_load_3d(st + 2 * kTileBytes, &map3, fb, kx, J.head, J.t0);
-                break;
-              case kJobFold: {   // A = W16 rows, B = gamma*Wo^T (hi or lo part)
-                const int part = kb / p.nkb_D, kxp = (kb % p.nkb_D) * kBlockK;
-                tma_load_2d(st, &map0, fb, kxp, J.kt * kBlockM);
-                tma_load_2d(st + kTileBytes, &map0, fb, kxp, p.I_pad + J.kt * kBlockM);
-                tma_load_3d(st + 2 * kTileBytes, &map1, fb, kxp, part, J.nt * kBlockN);
-                break;
+            const int kx = kb_in * kBlockK;
+            if (PAIR) {
+              // Both CTAs' loads land on the leader's full barrier, which expects both stages' bytes.
+              const uint32_t fb_leader = mapa_shared(smem_u32(fb), 0);
+              const int tb = J.t0 + crank * kPairBRows;   // this CTA's half of the token tile
+              if (crank == 0) mbar_arrive_expect_tx(fb, 2 * kPairStageBytes);
+              if (J.kind == kJobGateUp) {
+                tma_load_2d_pair(st, &map0, fb_leader, kx, J.kt * kBlockM);
+                tma_load_2d_pair(st + kTileBytes, &map0, fb_leader, kx, p.I_pad + J.kt * kBlockM);
+                tma_load_2d_pair(st + kBOff, &map1, fb_leader, kx, tb);
+              } else {
+                tma_load_3d_pair(st, &map2, fb_leader, kx, J.kt * kBlockM, 2 * J.head);
+                tma_load_3d_pair(st + kTileBytes, &map2, fb_leader, kx, J.kt * kBlockM, 2 * J.head + 1);
+                tma_load_3d_pair(st + kBOff, &map3, fb_leader, kx, J.head, tb);
               }
-              case kJobXPrime:   // A = alpha16 token rows (two tiles), B = Wd16 rows d
-                tma_load_2d(st, &map0, fb, kx, J.t0);
-                tma_load_2d(st + kTileBytes, &map0, fb, kx, J.t0 + kBlockM);
-                tma_load_2d(st + 2 * kTileBytes, &map1, fb, kx, J.nt * kBlockN);
-                break;
-              case kJobQNorm: {  // A = Wd^T neuron rows (two tiles), B = group g's gamma'-scaled q/k/v rows (hi | lo)
-                const int part = kb / p.nkb_D, kxp = (kb % p.nkb_D) * kBlockK;
-                tma_load_2d(st, &map0, fb, kxp, U.base);
-                tma_load_2d(st + kTileBytes, &map0, fb, kxp, U.base + kBlockM);
-                tma_load_4d(st + 2 * kTileBytes, &map1, fb, kxp, part, J.nt * kBlockN, J.g);
-                break;
+            } else {
+              mbar_arrive_expect_tx(fb, kStageBytes);
+              switch (J.kind) {
+                case kJobGateUp:   // A = W16 gate / up rows, B = n16 token rows
+                  tma_load_2d(st, &map0, fb, kx, J.kt * kBlockM);
+                  tma_load_2d(st + kTileBytes, &map0, fb, kx, p.I_pad + J.kt * kBlockM);
+                  tma_load_2d(st + kBOff, &map1, fb, kx, J.t0);
+                  break;
+                case kJobHead:     // A = M16 (gate, up) of head h, B = a16 head h
+                  tma_load_3d(st, &map2, fb, kx, J.kt * kBlockM, 2 * J.head);
+                  tma_load_3d(st + kTileBytes, &map2, fb, kx, J.kt * kBlockM, 2 * J.head + 1);
+                  tma_load_3d(st + kBOff, &map3, fb, kx, J.head, J.t0);
+                  break;
+                case kJobFold:     // A = W16 rows, B = gamma*Wo^T (hi part, then lo part)
+                  tma_load_2d(st, &map0, fb, kx, J.kt * kBlockM);
+                  tma_load_2d(st + kTileBytes, &map0, fb, kx, p.I_pad + J.kt * kBlockM);
+                  tma_load_3d(st + kBOff, &map1, fb, kx, part, J.nt * kBlockN);
+                  break;
+                case kJobXPrime:   // A = alpha16 token rows (two tiles), B = Wd16 rows d
+                  tma_load_2d(st, &map0, fb, kx, J.t0);
+                  tma_load_2d(st + kTileBytes, &map0, fb, kx, J.t0 + kBlockM);
+                  tma_load_2d(st + kBOff, &map1, fb, kx, J.nt * kBlockN);
+                  break;
+                case kJobQNorm:    // A = Wd^T neuron rows (two tiles), B = group g's gamma'-scaled q/k/v rows (hi | lo)
+                  tma_load_2d(st, &map0, fb, kx, U.base);
+                  tma_load_2d(st + kTileBytes, &map0, fb, kx, U.base + kBlockM);
+                  tma_load_4d(st + kBOff, &map1, fb, kx, part, J.nt * kBlockN, J.g);
+                  break;
               }
             }
+            ++issued;
+            if (++s == S) { s = 0; ph ^= 1u; }
+            if (++kb_in == J.nkb_part) { kb_in = 0; ++part; }
           }
         }
       }
       if (!ok) {
         // Let every copy already issued land before shared memory is released.
-        const int n = it < S ? it : S;
-        for (int i = 1; i <= n; ++i) {
-          const int q = it - i;
-          volatile int dummy = 0;
-          mbar_wait(&sm.full[q % S], (uint32_t)((q / S) & 1), &dummy, p.status, 100000000ull);
+        if (PAIR && crank == 1) {
+          // the peer's copies signal the leader's barriers: give them a bounded grace period
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 2000000ull) __nanosleep(1000);
+        } else {
+          const int n = issued < S ? issued : S;
+          for (int i = 1; i <= n; ++i) {
+            const int q = issued - i;
+            volatile int dummy = 0;
+            mbar_wait(&sm.full[q % S], (uint32_t)((q / S) & 1), &dummy, p.status, 100000000ull);
+          }
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16(kBlockM, kBlockN, 0);
-      int it = 0, jc = 0;
+    // A lean loop: this one thread must issue MMAs as fast as the tensor pipe
+    // retires them, so no divisions, and descriptors advance by constants.
+    if (lane == 0 && crank == 0) {   // in a pair only the leader issues (for both CTAs)
+      const uint32_t idesc = idesc_f16(PAIR ? 2 * kBlockM : kBlockM, kBlockN, 0);
+      const uint64_t dbase = smem_desc_k_sw128(smem_u32(sm.stage0));   // A1 of stage 0
+      constexpr uint64_t kStageDesc = (uint64_t)(kSB >> 4);             // descriptor step per stage
+      constexpr uint64_t kA2 = (uint64_t)(kTileBytes >> 4), kB = (uint64_t)(kBOff >> 4);
+      int s = 0, b = 0;
+      uint32_t ph = 0, tph = 0;        // stage phase; TMEM buffer phase (flips every second job)
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        Unit U = unit_info(p, u);
-        for (int j = 0; ok && j < U.njobs; ++j, ++jc) {
-          Job J = job_info(p, U, j);
-          const int b = jc & 1;
-          if (!mbar_wait(&sm.tempty[b], (uint32_t)(((jc >> 1) & 1) ^ 1), sm.abort_flag, p.status)) { ok = false; break; }
+      for (int u = cid; ok && u < p.n_units; u += ncl) {
+        const Unit U = unit_info<PAIR>(p, u, crank);
+        JobIter jt{0, 0};
+        for (int j = 0; ok && j < U.njobs; ++j) {
+          const Job J = job_next<MODE>(p, U, jt);
+          const bool w = PAIR ? mbar_wait_cluster(&sm.tempty[b], tph ^ 1u, sm.abort_flag, p.status)
+                              : mbar_wait(&sm.tempty[b], tph ^ 1u, sm.abort_flag, p.status);
+          if (!w) { ok = false; break; }
           tc_fence_after();
           const uint32_t d1 = tmem + (uint32_t)(b * 2 * kBlockN);
           const uint32_t d2 = d1 + kBlockN;
-          for (int kb = 0; kb < J.nkb; ++kb, ++it) {
-            const int s = it % S;
-            const uint32_t k = (uint32_t)(it / S);
-            if (!mbar_wait(&sm.full[s], k & 1u, sm.abort_flag, p.status)) { ok = false; break; }
+          uint32_t acc = 0u;
+          for (int kb = 0, kb_in = 0; kb < J.nkb; ++kb) {
+            const bool wf = PAIR ? mbar_wait_cluster(&sm.full[s], ph, sm.abort_flag, p.status)
+                                 : mbar_wait(&sm.full[s], ph, sm.abort_flag, p.status);
+            if (!wf) { ok = false; break; }
             tc_fence_after();
-            const uint32_t st = smem_u32(sm.stage0 + (size_t)s * kStageBytes);
-            const uint64_t da1 = smem_desc_k_sw128(st);
-            const uint64_t da2 = smem_desc_k_sw128(st + kTileBytes);
-            const uint64_t db = smem_desc_k_sw128(st + 2 * kTileBytes);
-            const int nks = kslices(J, kb, p.nkb_D);
-            for (int ks = 0; ks < nks; ++ks) {
-              const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
-              mma_f16_ss(d1, da1 + 2 * ks, db + 2 * ks, idesc, acc);
-              mma_f16_ss(d2, da2 + 2 * ks, db + 2 * ks, idesc, acc);
+            const uint64_t da1 = dbase + (uint64_t)s * kStageDesc;
+            const uint64_t da2 = da1 + kA2, db = da1 + kB;
+            const int nks = (kb_in == J.nkb_part - 1) ? J.last_nks : 4;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              if (ks < nks) {
+                if (PAIR) {
+                  mma_f16_ss_pair(d1, da1 + 2 * ks, db + 2 * ks, idesc, acc);
+                  mma_f16_ss_pair(d2, da2 + 2 * ks, db + 2 * ks, idesc, acc);
+                } else {
+                  mma_f16_ss(d1, da1 + 2 * ks, db + 2 * ks, idesc, acc);
+                  mma_f16_ss(d2, da2 + 2 * ks, db + 2 * ks, idesc, acc);
+                }
+                acc = 1u;
+              }
             }
-            mma_commit(&sm.empty[s]);
+            if (PAIR)
+              mma_commit_pair_mc(&sm.empty[s], 3);   // the stage is free again in both CTAs
+            else
+              mma_commit(&sm.empty[s]);
+            if (++s == S) { s = 0; ph ^= 1u; }
+            if (++kb_in == J.nkb_part) kb_in = 0;
           }
           if (!ok) break;
-          mma_commit(&sm.tfull[b]);
+          if (PAIR)
+            mma_commit_pair_mc(&sm.tfull[b], 3);
+          else
+            mma_commit(&sm.tfull[b]);
+          if (++b == 2) { b = 0; tph ^= 1u; }
         }
       }
       if (!ok) {
-        mma_commit(sm.drain);
+        if (PAIR)
+          mma_commit_pair_mc(sm.drain, 1);
+        else
+          mma_commit(sm.drain);
         volatile int dummy = 0;
         mbar_wait(sm.drain, 0, &dummy, p.status, 100000000ull);
       }
@@ -316,19 +381,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hf = (warp - 2) >> 2;    // which 64-column half of the tile
     const int row = q * 32 + lane;     // row of the A tile = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
+    // TMEM-empty arrivals go to the leader's barrier (its own when unpaired)
+    const uint32_t tempty_addr0 = PAIR ? mapa_shared(smem_u32(&sm.tempty[0]), 0) : 0u;
     uint32_t abA[32], abB[32];         // FO: fp16 pairs of silu'(g)u and silu(g), 64 tokens
 #pragma unroll
     for (int i = 0; i < 32; ++i) { abA[i] = 0u; abB[i] = 0u; }
     float ss1 = 0.f, ss2 = 0.f;        // x' / qnorm running sums
-    int jc = 0;
+    int b = 0;
+    uint32_t tph = 0;                  // TMEM buffer phase (flips every second job)
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-      Unit U = unit_info(p, u);
-      for (int j = 0; j < U.njobs; ++j, ++jc) {
-        Job J = job_info(p, U, j);
-        const int b = jc & 1;
+    for (int u = cid; ok && u < p.n_units; u += ncl) {
+      const Unit U = unit_info<PAIR>(p, u, crank);
+      JobIter jt{0, 0};
+      for (int j = 0; j < U.njobs; ++j, b ^= 1, tph ^= (uint32_t)(b == 0)) {
+        const Job J = job_next<MODE>(p, U, jt);
         int w_ok = 1;
-        if (lane == 0) w_ok = mbar_wait(&sm.tfull[b], (uint32_t)((jc >> 1) & 1), sm.abort_flag, p.status) ? 1 : 0;
+        if (lane == 0)
+          w_ok = (PAIR ? mbar_wait_cluster(&sm.tfull[b], tph, sm.abort_flag, p.status)
+                       : mbar_wait(&sm.tfull[b], tph, sm.abort_flag, p.status))
+                     ? 1
+                     : 0;
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
         if (!w_ok) { ok = false; break; }
         tc_fence_after();
@@ -346,7 +418,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (c == 3) {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.tempty[b]);
+                if (lane == 0) {
+                  if (PAIR)
+                    mbar_arrive_cluster(tempty_addr0 + (uint32_t)(b * 8));
+                  else
+                    mbar_arrive(&sm.tempty[b]);
+                }
               }
 #pragma unroll
               for (int i = 0; i < 16; i += 2) {
@@ -387,7 +464,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c == 3) {
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) mbar_arrive(&sm.tempty[b]);
+              if (lane == 0) {
+                  if (PAIR)
+                    mbar_arrive_cluster(tempty_addr0 + (uint32_t)(b * 8));
+                  else
+                    mbar_arrive(&sm.tempty[b]);
+                }
             }
 #pragma unroll
             for (int i = 0; i < 16; i += 2) {
@@ -421,7 +503,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c == 3) {
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) mbar_arrive(&sm.tempty[b]);
+              if (lane == 0) {
+                  if (PAIR)
+                    mbar_arrive_cluster(tempty_addr0 + (uint32_t)(b * 8));
+                  else
+                    mbar_arrive(&sm.tempty[b]);
+                }
             }
 #pragma unroll
             for (int i = 0; i < 16; i += 8) {
@@ -455,7 +542,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c == 3) {
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) mbar_arrive(&sm.tempty[b]);
+              if (lane == 0) {
+                  if (PAIR)
+                    mbar_arrive_cluster(tempty_addr0 + (uint32_t)(b * 8));
+                  else
+                    mbar_arrive(&sm.tempty[b]);
+                }
             }
             const int d0 = J.nt * kBlockN + hf * 64 + c * 16;
 #pragma unroll
@@ -487,7 +579,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c == 3) {
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) mbar_arrive(&sm.tempty[b]);
+              if (lane == 0) {
+                  if (PAIR)
+                    mbar_arrive_cluster(tempty_addr0 + (uint32_t)(b * 8));
+                  else
+                    mbar_arrive(&sm.tempty[b]);
+                }
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -527,36 +624,77 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync_all();   // neither CTA of a pair leaves while the other may still use its memory
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-size_t tile_smem_bytes(int mode, int stages, int H) {
+size_t tile_smem_bytes(int mode, int stages, int H, bool pair) {
   size_t sacc = (mode == kModeFO || mode == kModeADD) ? (size_t)2 * H * kBlockM * 4 : 0;
-  return 1024 + (size_t)stages * kStageBytes + sacc + (size_t)(2 * stages + 5) * 8 + 8;
+  return 1024 + (size_t)stages * (pair ? kPairStageBytes : kStageBytes) + sacc + (size_t)(2 * stages + 5) * 8 + 8;
 }
 
-template <int MODE>
-static cudaError_t launch_mode(const CUtensorMap* maps, const TileParams& p, int grid, cudaStream_t stream) {
-  const size_t smem = tile_smem_bytes(MODE, p.stages, p.H);
-  cudaError_t e = cudaFuncSetAttribute(affinity_tile_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+// Launches `grid` CTAs (pairs: 2 * grid as clusters of 2).  With grid == 0 it
+// only reports in *grid how many CTAs (pairs) fit on the device at once.
+template <int MODE, bool PAIR>
+static cudaError_t launch_mode(const CUtensorMap* maps, const TileParams& p, int* grid, cudaStream_t stream) {
+  const size_t smem = tile_smem_bytes(MODE, p.stages, p.H, PAIR);
+  auto* fn = affinity_tile_kernel<MODE, PAIR>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  affinity_tile_kernel<MODE><<<grid, kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
-  return cudaGetLastError();
+  if (!PAIR) {
+    if (*grid <= 0) {
+      int dev = 0, n = 0;
+      cudaGetDevice(&dev);
+      e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+      *grid = n;   // shared memory and TMEM allow one CTA per SM
+      return e;
+    }
+    fn<<<*grid, kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (*grid <= 0) {
+    int n = 0;
+    cfg.gridDim = dim3(2, 1, 1);
+    e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+    *grid = n;
+    return e;
+  }
+  cfg.gridDim = dim3(2 * *grid, 1, 1);
+  return cudaLaunchKernelEx(&cfg, fn, maps[0], maps[1], maps[2], maps[3], p);
 }
 
-cudaError_t launch_tile_kernel(const CUtensorMap* maps, const TileParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_tile_kernel(const CUtensorMap* maps, const TileParams& p, int* grid, cudaStream_t stream) {
   switch (p.mode) {
-    case kModeFold: return launch_mode<kModeFold>(maps, p, grid, stream);
-    case kModeFO: return launch_mode<kModeFO>(maps, p, grid, stream);
-    case kModeADD: return launch_mode<kModeADD>(maps, p, grid, stream);
-    case kModeAlpha: return launch_mode<kModeAlpha>(maps, p, grid, stream);
-    case kModeXPrime: return launch_mode<kModeXPrime>(maps, p, grid, stream);
-    case kModeQNorm: return launch_mode<kModeQNorm>(maps, p, grid, stream);
+    case kModeFold: return launch_mode<kModeFold, false>(maps, p, grid, stream);
+    case kModeFO:
+      return p.pair ? launch_mode<kModeFO, true>(maps, p, grid, stream)
+                    : launch_mode<kModeFO, false>(maps, p, grid, stream);
+    case kModeADD:
+      return p.pair ? launch_mode<kModeADD, true>(maps, p, grid, stream)
+                    : launch_mode<kModeADD, false>(maps, p, grid, stream);
+    case kModeAlpha: return launch_mode<kModeAlpha, false>(maps, p, grid, stream);
+    case kModeXPrime: return launch_mode<kModeXPrime, false>(maps, p, grid, stream);
+    case kModeQNorm: return launch_mode<kModeQNorm, false>(maps, p, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

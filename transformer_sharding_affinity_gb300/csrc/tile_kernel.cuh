@@ -15,6 +15,10 @@ constexpr int kBlockN = 128;      // rows per B tile  (TMEM columns per accumula
 constexpr int kBlockK = 64;       // fp16 elements per K block (one 128 B swizzle row)
 constexpr int kTileBytes = kBlockM * kBlockK * 2;     // 16 KB
 constexpr int kStageBytes = 3 * kTileBytes;           // A1 + A2 + B = 48 KB
+// CTA-pair (cta_group::2) variant of FO / ADD: each CTA holds its own 128 A rows
+// and half (64 rows) of the shared 128-row B tile, so a stage is 40 KB.
+constexpr int kPairBRows = kBlockN / 2;
+constexpr int kPairStageBytes = 2 * kTileBytes + kPairBRows * kBlockK * 2;
 constexpr int kThreads = 320;                         // TMA warp, MMA warp, 8 epilogue warps
 constexpr int kEpiWarps = 8;
 constexpr int kTmemCols = 512;                        // 2 buffers x (D1 128 + D2 128)
@@ -40,6 +44,8 @@ struct TileParams {
   int32_t n_ntiles;        // fold: column tiles of 128 over H*dh; x': over D; qnorm: row tiles per group
   int32_t rows_per_group;  // qnorm: (H/G + 2) * dh
   int32_t nkb_D, nkb_dh, nkb_I;
+  int32_t ls_D, ls_dh;     // 16-wide K slices in the last K block of D and of dh
+  int32_t pair;            // FO / ADD: 1 = CTA pairs with 256-row (cta_group::2) MMAs
   uint32_t* status;
   float* partial;          // FO/ADD: [n_chunks][2][H][I_pad]; x': [T_pad] sum x'^2 parts
   __half* M16;             // fold output

@@ -407,8 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t c1 = tl + (uint32_t)(b * 2 * kBlockN + hf * 64);
         const uint32_t c2 = c1 + kBlockN;
 
-        if constexpr (MODE == kModeFO || MODE == kModeAlpha) {
+        if constexpr (MODE == kModeFO) {
           if (J.kind == kJobGateUp) {
+            // Phase 1: stash g, u as fp16 pairs in the registers that will hold A', B'
+            // and hand the accumulator buffer back at once, so the MMAs of the next
+            // two head jobs run while phase 2 (exp + reciprocal per element) computes.
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               uint32_t gr[16], ur[16];
@@ -427,26 +430,49 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
 #pragma unroll
               for (int i = 0; i < 16; i += 2) {
-                float gA[2], gB[2], al[2];
+                abA[c * 8 + i / 2] = pack_h2(__uint_as_float(gr[i]), __uint_as_float(gr[i + 1]));
+                abB[c * 8 + i / 2] = pack_h2(__uint_as_float(ur[i]), __uint_as_float(ur[i + 1]));
+              }
+            }
+            // Phase 2: (g, u) -> (A', B') = (silu'(g) u, silu(g)) in place.
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  const float g = __uint_as_float(gr[i + e]);
-                  const float uu = __uint_as_float(ur[i + e]);
-                  const float sg = __frcp_rn(1.0f + __expf(-g));        // sigmoid(g)
-                  const float si = g * sg;                              // silu(g)
-                  gA[e] = sg * fmaf(g, 1.0f - sg, 1.0f) * uu;           // silu'(g) u
-                  gB[e] = si;
-                  al[e] = si * uu;                                      // alpha = silu(g) u
-                }
-                if constexpr (MODE == kModeFO) {
-                  abA[c * 8 + i / 2] = pack_h2(gA[0], gA[1]);
-                  abB[c * 8 + i / 2] = pack_h2(gB[0], gB[1]);
-                } else {
-                  const int t = J.t0 + hf * 64 + c * 16 + i;
-                  const int kk = J.kt * kBlockM + row;
-                  p.alpha16[(size_t)t * p.I_pad + kk] = __float2half_rn(al[0]);
-                  p.alpha16[(size_t)(t + 1) * p.I_pad + kk] = __float2half_rn(al[1]);
-                }
+            for (int i = 0; i < 32; ++i) {
+              float gA[2], gB[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float g = e ? h_hi(abA[i]) : h_lo(abA[i]);
+                const float uu = e ? h_hi(abB[i]) : h_lo(abB[i]);
+                const float sg = __fdividef(1.0f, 1.0f + __expf(-g));  // sigmoid(g)
+                gA[e] = sg * fmaf(g, 1.0f - sg, 1.0f) * uu;           // silu'(g) u
+                gB[e] = g * sg;                                       // silu(g)
+              }
+              abA[i] = pack_h2(gA[0], gA[1]);
+              abB[i] = pack_h2(gB[0], gB[1]);
+            }
+            continue;
+          }
+        }
+        if constexpr (MODE == kModeAlpha) {
+          {   // kJobGateUp: alpha = silu(g) u straight from the accumulators
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t gr[16], ur[16];
+              tmem_ld16(c1 + c * 16, gr);
+              tmem_ld16(c2 + c * 16, ur);
+              tmem_ld_wait();
+              if (c == 3) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.tempty[b]);
+              }
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float g = __uint_as_float(gr[i]);
+                const float uu = __uint_as_float(ur[i]);
+                const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
+                const int t = J.t0 + hf * 64 + c * 16 + i;
+                const int kk = J.kt * kBlockM + row;
+                p.alpha16[(size_t)t * p.I_pad + kk] = __float2half_rn(g * sg * uu);
               }
             }
             continue;

@@ -295,6 +295,36 @@ aff_status run_tile(const CUtensorMap* maps, TileParams& p, cudaStream_t s, bool
   return AFF_OK;
 }
 
+// A second stream (and two events) per host thread and device: the weight-side
+// preparation runs on it concurrently with the token-side preparation, forked
+// from and joined back into the caller's stream, so ordering relative to the
+// caller's other work is unchanged.  Created on first use, kept for the life
+// of the process (no device memory is involved).
+struct SideStream {
+  int dev = -1;
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+aff_status side_stream(SideStream** out) {
+  thread_local std::vector<SideStream> per_dev;
+  int dev = 0;
+  AFF_CUDA(cudaGetDevice(&dev));
+  for (auto& ss : per_dev)
+    if (ss.dev == dev) {
+      *out = &ss;
+      return AFF_OK;
+    }
+  SideStream ss;
+  ss.dev = dev;
+  AFF_CUDA(cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking));
+  AFF_CUDA(cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming));
+  AFF_CUDA(cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming));
+  per_dev.push_back(ss);
+  *out = &per_dev.back();
+  return AFF_OK;
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 aff_status check_ws(const Layout& L, void* ws, size_t bytes) {
@@ -397,9 +427,16 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   const uint16_t* x_b = static_cast<const uint16_t*>(x);
   const uint16_t* g_b = static_cast<const uint16_t*>(gamma);
 
-  AFF_CUDA(launch_prep_gate_up((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, status, s));
-  AFF_CUDA(launch_scaled_transpose_split((const uint16_t*)Wo, g_b, GWo16, D, H * dh, status, s));
-  if (fo) AFF_CUDA(launch_wd_colnorm((const uint16_t*)Wd, wdn, D, I, I_pad, s));
+  // weight side (fp16 gate/up rows, gamma*Wo^T, ||w^d||^2, the fold) on the side stream
+  SideStream* side = nullptr;
+  if ((st = side_stream(&side)) != AFF_OK) return st;
+  const cudaStream_t ws2 = side->stream;
+  AFF_CUDA(cudaEventRecord(side->fork, s));
+  AFF_CUDA(cudaStreamWaitEvent(ws2, side->fork, 0));
+  AFF_CUDA(launch_prep_gate_up((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, status, ws2));
+  AFF_CUDA(launch_scaled_transpose_split((const uint16_t*)Wo, g_b, GWo16, D, H * dh, status, ws2));
+  if (fo) AFF_CUDA(launch_wd_colnorm((const uint16_t*)Wd, wdn, D, I, I_pad, ws2));
+  // token side on the caller's stream meanwhile
   AFF_CUDA(launch_prep_tokens(x_b, a_b, g_b, fo ? n16 : nullptr, a16, nullptr, T, D, H * dh, d.eps, status, s));
 
   CUtensorMap maps[4];
@@ -415,8 +452,10 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     p.n_ntiles = (int)ceil_div((int64_t)H * dh, 128);
     p.n_units = p.n_ktiles * p.n_ntiles;
     p.M16 = M16;
-    if ((st = run_tile(maps, p, s)) != AFF_OK) return st;
+    if ((st = run_tile(maps, p, ws2)) != AFF_OK) return st;
   }
+  AFF_CUDA(cudaEventRecord(side->join, ws2));
+  AFF_CUDA(cudaStreamWaitEvent(s, side->join, 0));
   // FO / ADD: per token tile, operating point (FO) then every head.  With CTA
   // pairs each CTA loads half (64 rows) of every token tile.
   {

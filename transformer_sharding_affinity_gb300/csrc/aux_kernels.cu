@@ -182,6 +182,33 @@ __global__ void reduce_partials_kernel(const float* __restrict__ partial, double
   }
 }
 
+// Same reduction, four neurons per thread with 16-byte loads (I_pad % 128 == 0).
+__global__ void reduce_partials4_kernel(const float* __restrict__ partial, double* __restrict__ out, int n_chunks,
+                                        int halves, int H, int I_pad) {
+  __shared__ double part[8][32][4];
+  const int k = blockIdx.x * 128 + threadIdx.x * 4;
+  const int h = blockIdx.y;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int c = threadIdx.y; c < n_chunks; c += 8)
+    for (int hf = 0; hf < halves; ++hf) {
+      const float4 v = *reinterpret_cast<const float4*>(partial + ((size_t)(c * halves + hf) * H + h) * I_pad + k);
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+  part[threadIdx.y][threadIdx.x][0] = s.x;
+  part[threadIdx.y][threadIdx.x][1] = s.y;
+  part[threadIdx.y][threadIdx.x][2] = s.z;
+  part[threadIdx.y][threadIdx.x][3] = s.w;
+  __syncthreads();
+  if (threadIdx.y == 0) {
+    for (int e = 0; e < 4; ++e) {
+      double t = 0.0;
+      for (int i = 0; i < 8; ++i) t += part[i][threadIdx.x][e];
+      out[(size_t)h * I_pad + k + e] = t;
+    }
+  }
+}
+
 // S_head[h][k] = sum_t(...) / T (x ||w^d_k||^2 for FO); S_up[g][k] = sum_{h in g} S_head[h][k].
 __global__ void finalize_up_kernel(const double* __restrict__ sh, const float* __restrict__ wdn, int fo, int T,
                                    int H, int G, int I, int I_pad, float* __restrict__ S_out,
@@ -468,8 +495,13 @@ cudaError_t launch_wd_colnorm_f32(const float* Wd, float* wdn, int D, int I, cud
 
 cudaError_t launch_reduce_partials(const float* partial, double* out, int n_chunks, int halves, int H, int I_pad,
                                    cudaStream_t s) {
-  dim3 grid((I_pad + 31) / 32, H), block(32, 8);
-  reduce_partials_kernel<<<grid, block, 0, s>>>(partial, out, n_chunks, halves, H, I_pad);
+  if (I_pad % 128 == 0) {
+    dim3 grid(I_pad / 128, H), block(32, 8);
+    reduce_partials4_kernel<<<grid, block, 0, s>>>(partial, out, n_chunks, halves, H, I_pad);
+  } else {
+    dim3 grid((I_pad + 31) / 32, H), block(32, 8);
+    reduce_partials_kernel<<<grid, block, 0, s>>>(partial, out, n_chunks, halves, H, I_pad);
+  }
   return cudaGetLastError();
 }
 

@@ -223,6 +223,49 @@ AFF_API aff_status affinity_objective(const double* Shat_up, const double* Shat_
                               int32_t N, int32_t G, int64_t I, double* J);
 
 /*
+ * Host-only helper ("Objective", §3: each affinity matrix is normalised to
+ * unit mass before it enters J): out[i] = S[i] / sum_j S[j], summed in fp64
+ * in index order.  S: host fp32 [n] (an S_up [G, I] or S_down [I, G] as
+ * written by affinity_up / affinity_down); out: host fp64 [n].
+ * AFF_ERR_INVALID_ARG if n < 1 or the sum is not positive and finite.
+ */
+AFF_API aff_status affinity_unit_mass(const float* S, int64_t n, double* out);
+
+/*
+ * Host-only helper ("Optimiser", §3, the head step of the alternating
+ * search): with the neuron maps nu of all N layers fixed, choose for every
+ * layer i the balanced KV-group map h_i that maximises its gain
+ * C_i = affinity_group_gain(Shat_up_i, nu_i, Shat_down_{i-1}, nu_{i-1}), by
+ * scoring every balanced partition (affinity_score_partitions, first
+ * maximum on ties).  Because h_i enters J (equation (6)) only through layer
+ * i's up term and layer i-1's down term, the result maximises J over all h
+ * for the given nu.
+ *   Shat_up   host fp64, N contiguous [G, I] unit-mass blocks
+ *   Shat_down host fp64, N-1 contiguous [I, G] blocks (may be NULL if N == 1)
+ *   nu        host int32 N x [I], values in [0, L)
+ *   h_out     host int32 N x [G] (written)
+ *   J_out     host fp64: J of (h_out, nu), or NULL
+ * Same limits on (G, L) as affinity_score_partitions.
+ */
+AFF_API aff_status affinity_best_heads(const double* Shat_up, const double* Shat_down,
+                                       const int32_t* nu, int32_t N, int32_t G, int64_t I,
+                                       int32_t L, int32_t* h_out, double* J_out);
+
+/*
+ * Host-only helper for token-sharded calibration (one GPU per shard of the
+ * calibration tokens).  Every entry of S_up, S_head and S_down is a mean over
+ * tokens times a per-neuron factor (§3 "Affinity scores": E_t[...]), so the
+ * full-set value is the token-weighted mean of the shards' values:
+ *   out[j] = sum_r T_r * S_r[j] / sum_r T_r,
+ * accumulated in fp64 in shard order r = 0, 1, ... (deterministic).
+ *   S_shards  n_shards host pointers to fp32 [n] (may be NULL where T_r == 0)
+ *   T_shards  host int64 [n_shards], tokens of each shard, >= 0, sum > 0
+ *   out       host fp32 [n]; may alias none of the inputs
+ */
+AFF_API aff_status affinity_combine_shards(const float* const* S_shards, const int64_t* T_shards,
+                                           int32_t n_shards, int64_t n, float* out);
+
+/*
  * Profiling hook (no effect on results): register two caller-created CUDA
  * events (cudaEvent_t handles) that later affinity_up / affinity_down calls
  * made from this host thread record on their stream immediately before and

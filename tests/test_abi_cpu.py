@@ -175,3 +175,46 @@ def test_group_gain_and_objective_match_oracle(lib):
     bad[0] = L
     with pytest.raises(B.AffinityError):
         B.group_gain(ups[0], bad, L)
+
+
+def test_unit_mass_matches_oracle(lib):
+    rng = np.random.default_rng(4)
+    S = rng.random((8, 96)).astype(np.float32)
+    np.testing.assert_allclose(B.unit_mass(S), P.unit_mass(S.astype(np.float64)), rtol=1e-14)
+    assert abs(B.unit_mass(S).sum() - 1.0) < 1e-12
+    for bad in (np.zeros((2, 3), np.float32), np.full((2, 2), np.inf, np.float32)):
+        with pytest.raises(B.AffinityError):
+            B.unit_mass(bad)
+
+
+def test_best_heads_is_the_brute_force_optimum(lib):
+    """With nu fixed, the per-layer partition choice maximises J over every
+    combination of balanced head maps (brute force over all N-tuples)."""
+    import itertools
+    rng = np.random.default_rng(6)
+    N, G, I, L = 3, 4, 12, 2
+    ups = [P.unit_mass(rng.random((G, I))) for _ in range(N)]
+    downs = [P.unit_mass(rng.random((I, G))) for _ in range(N - 1)]
+    ns = [rng.permutation(P.contiguous_neurons(I, L)) for _ in range(N)]
+    h, J = B.best_heads(ups, downs, ns, L)
+    maps = P.balanced_partitions(G, L)
+    best = max(P.objective_J(ups, downs, list(hs), ns) for hs in itertools.product(maps, repeat=N))
+    np.testing.assert_allclose(J, best, rtol=1e-13)
+    np.testing.assert_allclose(J, P.objective_J(ups, downs, list(h), ns), rtol=1e-13)
+    # per layer it is the oracle's partition choice on the oracle's gain
+    for i in range(N):
+        C = P.group_gain(ups[i], L, ns[i], downs[i - 1] if i else None, ns[i - 1] if i else None)
+        assert tuple(h[i]) == tuple(P.score_partitions(C)[2])
+
+
+def test_combine_shards_is_the_token_weighted_mean(lib):
+    rng = np.random.default_rng(8)
+    S = [rng.random((4, 10)).astype(np.float32) for _ in range(3)]
+    T = [100, 0, 37]
+    got = B.combine_shards(S, T)
+    ref = (100 * S[0].astype(np.float64) + 37 * S[2]) / 137
+    np.testing.assert_allclose(got, ref, rtol=1e-7)
+    np.testing.assert_array_equal(B.combine_shards([S[0]], [5]), S[0])
+    for bad_T in ([0, 0, 0], [1, -1, 1]):
+        with pytest.raises(B.AffinityError):
+            B.combine_shards(S, bad_T)

@@ -1,0 +1,105 @@
+"""The 28-layer Qwen3-shaped stack: S_up (FO) of every layer and S_down of
+every layer but the last on the GPU, then unit mass, contiguous neuron maps,
+the best of the 2520 balanced KV-group partitions per layer and the objective
+J ("Affinity-Aware Sharding for Delayed Tensor Parallelism", §3 "Objective",
+equation (6), "Optimiser").  The host sequence is checked against the oracle
+on CPU; the GPU run adds sampled parity on the first and last layers."""
+import numpy as np
+import pytest
+
+from oracle import affinity_oracle as O
+from oracle import partitions as P
+from transformer_sharding_affinity_gb300 import stack as ST
+
+from parity_util import TOL, rel_err, topk_agrees
+
+
+def _check_host_sequence(res, L):
+    """Every number of place_heads against the oracle's partition functions."""
+    N = len(res.S_up)
+    G, I = res.S_up[0].shape
+    ups = [P.unit_mass(s.astype(np.float64)) for s in res.S_up]
+    downs = [P.unit_mass(s.astype(np.float64)) for s in res.S_down]
+    for a, b in zip(res.Shat_up + res.Shat_down, ups + downs):
+        np.testing.assert_allclose(a, b, rtol=1e-13)
+    nu = [P.contiguous_neurons(I, L)] * N
+    hc = [P.contiguous_heads(G, L)] * N
+    np.testing.assert_array_equal(res.nu, np.stack(nu))
+    np.testing.assert_array_equal(res.h_contiguous, np.stack(hc))
+    np.testing.assert_allclose(res.J_contiguous, P.objective_J(ups, downs, hc, nu), rtol=1e-12)
+    for i in range(N):
+        C = P.group_gain(ups[i], L, nu[i], downs[i - 1] if i else None, nu[i - 1] if i else None)
+        _, _, best = P.score_partitions(C)
+        assert tuple(res.h_best[i]) == tuple(best), f"layer {i}"
+    np.testing.assert_allclose(res.J_best, P.objective_J(ups, downs, list(res.h_best), nu), rtol=1e-12)
+    assert 0.0 <= res.J_contiguous <= res.J_best <= 2 * N - 1
+
+
+def test_place_heads_host_sequence():
+    rng = np.random.default_rng(12)
+    N, G, I, L = 5, 8, 96, 4
+    S_up = [rng.gamma(0.5, size=(G, I)).astype(np.float32) for _ in range(N)]
+    S_down = [rng.gamma(0.5, size=(I, G)).astype(np.float32) for _ in range(N - 1)]
+    res = ST.place_heads(S_up, S_down, L)
+    _check_host_sequence(res, L)
+
+
+def test_place_heads_uniform_scores_give_the_expectation():
+    """Uniform S makes every layout score (2N-1)/L; the first partition wins."""
+    N, G, I, L = 4, 8, 64, 4
+    res = ST.place_heads([np.ones((G, I), np.float32)] * N, [np.ones((I, G), np.float32)] * (N - 1), L)
+    np.testing.assert_allclose([res.J_contiguous, res.J_best], (2 * N - 1) / L, rtol=1e-12)
+    np.testing.assert_array_equal(res.h_best, res.h_contiguous)
+
+
+@pytest.mark.gpu
+@pytest.mark.slow
+def test_qwen3_stack_28_layers():
+    torch = pytest.importorskip("torch")
+    from transformer_sharding_affinity_gb300 import binding as B
+    from transformer_sharding_affinity_gb300 import device as DV
+    from transformer_sharding_affinity_gb300 import workloads as W
+
+    shape0 = W.stack_layer(0)
+    d = B.dims(shape0.T, shape0.D, shape0.H, shape0.G, shape0.dh, shape0.I, shape0.eps, B.AFF_BF16)
+    N, L = W.STACK_LAYERS, 4
+    keep = {}
+
+    def layer_inputs(i):
+        layer = W.make_layer(W.stack_layer(i), with_next=i + 1 < N)
+        if i in (0, N - 1):
+            keep[i] = layer
+        return DV.to_device(layer, "bf16", keys=DV.ALL_KEYS if i + 1 < N else DV.UP_KEYS)
+
+    S_up, S_down = ST.calibrate_stack(layer_inputs, N, d)
+    assert len(S_up) == N and len(S_down) == N - 1
+    for S in S_up + S_down:
+        assert np.all(np.isfinite(S)) and S.min() >= 0.0 and S.max() > 0.0
+    torch.cuda.synchronize()
+
+    rng = np.random.default_rng(28)
+    for i in (0, N - 1):
+        shape, layer = W.stack_layer(i), keep[i]
+        S_gpu = S_up[i]
+        idx = set(rng.choice(shape.I, 48, replace=False).tolist())
+        for g in range(shape.G):
+            idx.update(np.argsort(-S_gpu[g], kind="stable")[:16].tolist())
+        idx = np.array(sorted(idx))
+        S_ref, _ = O.s_up(layer["a"], layer["x"], layer["Wo"], layer["gamma"], layer["Wg"], layer["Wu"],
+                          layer["Wd"], shape.H, shape.G, shape.dh, shape.eps, "fo", neurons=idx)
+        e = rel_err(S_gpu[:, idx], S_ref, floor_ref=float(S_gpu.max()))
+        assert e <= TOL, f"layer {i} S_up: max rel err {e:.3e}"
+        for g in range(shape.G):
+            assert topk_agrees(S_gpu[g, idx], S_ref[g]), f"layer {i}: top-8 of group {g} differs"
+    layer = keep[0]
+    shape = W.stack_layer(0)
+    idx = rng.choice(shape.I, 64, replace=False)
+    Sd_ref = O.s_down(layer["x"], layer["gamma"], layer["Wg"], layer["Wu"], layer["Wd"], layer["gamma_next"],
+                      layer["Wq_next"], layer["Wk_next"], layer["Wv_next"], shape.H, shape.G, shape.dh, shape.eps,
+                      neurons=idx)
+    e = rel_err(S_down[0][idx], Sd_ref, floor_ref=float(S_down[0].max()))
+    assert e <= TOL, f"layer 0 S_down: max rel err {e:.3e}"
+
+    res = ST.place_heads(S_up, S_down, L)
+    _check_host_sequence(res, L)
+    assert res.h_best.shape == (N, shape.G)

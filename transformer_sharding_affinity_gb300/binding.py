@@ -79,6 +79,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.affinity_group_gain.restype = st
     lib.affinity_objective.argtypes = [_P, _P, _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, _P]
     lib.affinity_objective.restype = st
+    lib.affinity_unit_mass.argtypes = [_P, ctypes.c_int64, _P]
+    lib.affinity_unit_mass.restype = st
+    lib.affinity_best_heads.argtypes = [_P, _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+                                        _P, _P]
+    lib.affinity_best_heads.restype = st
+    lib.affinity_combine_shards.argtypes = [_P, _P, ctypes.c_int32, ctypes.c_int64, _P]
+    lib.affinity_combine_shards.restype = st
     lib.affinity_strerror.argtypes = [ctypes.c_int32]
     lib.affinity_strerror.restype = ctypes.c_char_p
     lib.affinity_last_cuda_error.argtypes = []
@@ -211,6 +218,46 @@ def objective(Shat_up: Sequence[np.ndarray], Shat_down: Sequence[np.ndarray], h:
     _check(load().affinity_objective(up.ctypes.data, None if dn is None else dn.ctypes.data, hh.ctypes.data,
                                      nn.ctypes.data, N, G, I, ctypes.byref(J)), "affinity_objective")
     return J.value
+
+
+def unit_mass(S: np.ndarray) -> np.ndarray:
+    """S / sum(S) in fp64 (affinity_unit_mass); S is a host fp32 array of any shape."""
+    S = np.ascontiguousarray(S, dtype=np.float32)
+    out = np.empty(S.shape, np.float64)
+    _check(load().affinity_unit_mass(S.ctypes.data, S.size, out.ctypes.data), "affinity_unit_mass")
+    return out
+
+
+def best_heads(Shat_up: Sequence[np.ndarray], Shat_down: Sequence[np.ndarray], nu: Sequence, L: int):
+    """Best balanced KV-group map of every layer for fixed neuron maps (affinity_best_heads).
+
+    Returns (h [N, G] int32, J of (h, nu))."""
+    N = len(Shat_up)
+    G, I = np.asarray(Shat_up[0]).shape
+    up = np.ascontiguousarray(np.stack([np.asarray(s, np.float64) for s in Shat_up]))
+    dn = np.ascontiguousarray(np.stack([np.asarray(s, np.float64) for s in Shat_down])) if N > 1 else None
+    nn = np.ascontiguousarray(np.stack([np.asarray(v, np.int32) for v in nu]))
+    h = np.empty((N, G), np.int32)
+    J = ctypes.c_double(0.0)
+    _check(load().affinity_best_heads(up.ctypes.data, None if dn is None else dn.ctypes.data, nn.ctypes.data, N, G,
+                                      I, int(L), h.ctypes.data, ctypes.byref(J)), "affinity_best_heads")
+    return h, J.value
+
+
+def combine_shards(S_shards: Sequence[np.ndarray], T_shards: Sequence[int]) -> np.ndarray:
+    """Token-weighted merge of S matrices from disjoint token shards (affinity_combine_shards)."""
+    arrs = [np.ascontiguousarray(s, dtype=np.float32) for s in S_shards]
+    shape = arrs[0].shape
+    if any(a.shape != shape for a in arrs):
+        raise ValueError("all shards must have the same shape")
+    ptrs = (ctypes.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
+    T = np.ascontiguousarray(T_shards, dtype=np.int64)
+    if T.shape != (len(arrs),):
+        raise ValueError("one token count per shard")
+    out = np.empty(shape, np.float32)
+    _check(load().affinity_combine_shards(ctypes.cast(ptrs, ctypes.c_void_p), T.ctypes.data, len(arrs),
+                                          arrs[0].size, out.ctypes.data), "affinity_combine_shards")
+    return out
 
 
 def set_timing_events(start_event, stop_event) -> None:

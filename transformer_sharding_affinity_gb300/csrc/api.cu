@@ -1,7 +1,7 @@
 // api.cu -- the C ABI declared in include/affinity.h: argument validation,
 // workspace layout, TMA descriptor encoding and the launch sequence of the
 // affinity pass ("Affinity-Aware Sharding for Delayed Tensor Parallelism",
-// §3 "Affinity scores", "Objective", "Optimiser").
+// §3 "Affinity scores").  The host-only layout helpers live in layout.cu.
 #include "affinity.h"
 #include "aux_kernels.cuh"
 #include "tile_kernel.cuh"
@@ -594,103 +594,6 @@ aff_status affinity_device_status(void* workspace, aff_stream_t stream) {
   AFF_CUDA(cudaMemcpy(&v, workspace, 4, cudaMemcpyDeviceToHost));
   AFF_CUDA(cudaMemset(workspace, 0, 4));
   return static_cast<aff_status>(v);
-}
-
-// ---------------------------------------------------------------- host helpers
-aff_status affinity_score_partitions(const double* C, int32_t G, int32_t L, double* scores, int64_t* count,
-                                     int64_t* best_index, int32_t* best_assign) {
-  if (!C || !count || !best_index || G < 1 || L < 1 || G > 16 || L > G || G % L) return AFF_ERR_INVALID_ARG;
-  const int cap = G / L;
-  {
-    // G! / ((G/L)!)^L as a running product of binomials; refuse enumerations past 1e8.
-    double total = 1.0, rem = G;
-    for (int l = 0; l < L; ++l) {
-      double b = 1.0;
-      for (int i = 0; i < cap; ++i) b = b * (rem - i) / (i + 1);
-      total *= b;
-      rem -= cap;
-    }
-    if (total > 1e8) return AFF_ERR_UNSUPPORTED_SHAPE;
-  }
-  int h[16], used[16] = {0};
-  int64_t n = 0, best = -1;
-  double best_score = 0.0;
-  // depth-first, devices tried in increasing order: lexicographic order of (h(0), ..., h(G-1))
-  int g = 0;
-  for (int i = 0; i < G; ++i) h[i] = -1;
-  while (g >= 0) {
-    if (g == G) {
-      double sc = 0.0;
-      for (int i = 0; i < G; ++i) sc += C[(size_t)i * L + h[i]];
-      if (scores) scores[n] = sc;
-      if (best < 0 || sc > best_score) {
-        best = n;
-        best_score = sc;
-        if (best_assign)
-          for (int i = 0; i < G; ++i) best_assign[i] = h[i];
-      }
-      ++n;
-      --g;
-      continue;
-    }
-    if (h[g] >= 0) used[h[g]]--;
-    int l = h[g] + 1;
-    while (l < L && used[l] >= cap) ++l;
-    if (l < L) {
-      h[g] = l;
-      used[l]++;
-      ++g;
-      if (g < G) h[g] = -1;
-    } else {
-      h[g] = -1;
-      --g;
-    }
-  }
-  *count = n;
-  *best_index = best;
-  return AFF_OK;
-}
-
-aff_status affinity_group_gain(const double* Shat_up_i, const int32_t* nu_i, const double* Shat_down_prev,
-                               const int32_t* nu_prev, int32_t G, int64_t I, int32_t L, double* C) {
-  if (!Shat_up_i || !nu_i || !C || G < 1 || I < 1 || L < 1) return AFF_ERR_INVALID_ARG;
-  if ((Shat_down_prev == nullptr) != (nu_prev == nullptr)) return AFF_ERR_INVALID_ARG;
-  for (int64_t k = 0; k < I; ++k) {
-    if (nu_i[k] < 0 || nu_i[k] >= L) return AFF_ERR_INVALID_ARG;
-    if (nu_prev && (nu_prev[k] < 0 || nu_prev[k] >= L)) return AFF_ERR_INVALID_ARG;
-  }
-  for (int64_t i = 0; i < (int64_t)G * L; ++i) C[i] = 0.0;
-  for (int g = 0; g < G; ++g)
-    for (int64_t k = 0; k < I; ++k) C[(size_t)g * L + nu_i[k]] += Shat_up_i[(size_t)g * I + k];
-  if (Shat_down_prev)
-    for (int64_t k = 0; k < I; ++k)
-      for (int g = 0; g < G; ++g) C[(size_t)g * L + nu_prev[k]] += Shat_down_prev[(size_t)k * G + g];
-  return AFF_OK;
-}
-
-aff_status affinity_objective(const double* Shat_up, const double* Shat_down, const int32_t* h, const int32_t* nu,
-                              int32_t N, int32_t G, int64_t I, double* J) {
-  if (!Shat_up || !h || !nu || !J || N < 1 || G < 1 || I < 1) return AFF_ERR_INVALID_ARG;
-  if (N > 1 && !Shat_down) return AFF_ERR_INVALID_ARG;
-  double s = 0.0;
-  for (int i = 0; i < N; ++i) {
-    const double* S = Shat_up + (size_t)i * G * I;
-    const int32_t* hi = h + (size_t)i * G;
-    const int32_t* ni = nu + (size_t)i * I;
-    for (int g = 0; g < G; ++g)
-      for (int64_t k = 0; k < I; ++k)
-        if (hi[g] == ni[k]) s += S[(size_t)g * I + k];
-  }
-  for (int i = 0; i + 1 < N; ++i) {
-    const double* S = Shat_down + (size_t)i * I * G;
-    const int32_t* ni = nu + (size_t)i * I;
-    const int32_t* hn = h + (size_t)(i + 1) * G;
-    for (int64_t k = 0; k < I; ++k)
-      for (int g = 0; g < G; ++g)
-        if (ni[k] == hn[g]) s += S[(size_t)k * G + g];
-  }
-  *J = s;
-  return AFF_OK;
 }
 
 }  // extern "C"

@@ -11,6 +11,7 @@ import numpy as np
 
 UP_KEYS = ("a", "x", "Wo", "gamma", "Wg", "Wu", "Wd")
 DOWN_KEYS = ("x", "gamma", "Wg", "Wu", "Wd", "gamma_next", "Wq_next", "Wk_next", "Wv_next")
+ALL_KEYS = UP_KEYS + DOWN_KEYS[5:]
 
 
 def host_tensor(layer: Dict[str, np.ndarray], key: str, dtype: str):

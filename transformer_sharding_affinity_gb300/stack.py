@@ -1,0 +1,97 @@
+"""Calibration and head placement for a stack of N layers.
+
+For each layer i the GPU pass computes S_up_i [G, I] (FO or ADD) and, for
+every layer but the last, S_down_i [I, G] toward layer i+1's KV groups.  The
+host helpers of the library then normalise every matrix to unit mass, take
+the contiguous neuron maps, choose each layer's KV-group map by scoring every
+balanced partition, and evaluate the total co-located affinity J for the
+contiguous and the chosen layouts ("Affinity-Aware Sharding for Delayed Tensor
+Parallelism", §3 "Objective", equation (6), and "Optimiser").
+
+This module only sequences library calls; every number comes from
+``libaffinity``.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Callable, Dict, List, Optional
+
+import numpy as np
+
+from . import binding as B
+
+
+@dataclasses.dataclass
+class StackResult:
+    S_up: List[np.ndarray]        # N x [G, I] fp32
+    S_down: List[np.ndarray]      # N-1 x [I, G] fp32
+    Shat_up: List[np.ndarray]     # unit-mass fp64
+    Shat_down: List[np.ndarray]
+    nu: np.ndarray                # [N, I] neuron -> device
+    h_contiguous: np.ndarray      # [N, G]
+    h_best: np.ndarray            # [N, G]
+    J_contiguous: float
+    J_best: float
+
+
+def contiguous_map(n: int, L: int) -> np.ndarray:
+    """Item j -> device j // (n / L) (the unpermuted Megatron layout)."""
+    if n % L:
+        raise ValueError("n must be a multiple of L")
+    return (np.arange(n) // (n // L)).astype(np.int32)
+
+
+def calibrate_stack(layer_inputs: Callable[[int], Dict[str, object]], n_layers: int, d: "B.aff_dims",
+                    mode: int = B.AFF_MODE_FO, stream=None) -> tuple:
+    """Run S_up for layers 0..N-1 and S_down for layers 0..N-2 on the GPU.
+
+    ``layer_inputs(i)`` returns layer i's device tensors under the names of
+    ``affinity_up`` / ``affinity_down`` (a, x, Wo, gamma, Wg, Wu, Wd and, for
+    i < N-1, gamma_next, Wq_next, Wk_next, Wv_next: layer i+1's attention
+    pre-norm gain and q/k/v projections).  Returns (S_up list, S_down list) on
+    the host."""
+    import torch
+
+    G, I = int(d.G), int(d.I)
+    ws_bytes = max(B.workspace_size(d, mode), B.workspace_size(d, mode, down=True))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    S_up_dev = torch.empty(G, I, device="cuda")
+    S_dn_dev = torch.empty(I, G, device="cuda")
+    S_up, S_down = [], []
+    for i in range(n_layers):
+        t = layer_inputs(i)
+        B.affinity_up(t["a"], t["x"], t["Wo"], t["gamma"], t["Wg"], t["Wu"], t["Wd"], d, mode, S_up_dev, None, ws,
+                      stream=stream)
+        _status(ws, stream, f"layer {i} S_up")
+        S_up.append(S_up_dev.cpu().numpy().copy())
+        if i + 1 < n_layers:
+            B.affinity_down(t["x"], t["gamma"], t["Wg"], t["Wu"], t["Wd"], t["gamma_next"], t["Wq_next"],
+                            t["Wk_next"], t["Wv_next"], d, S_dn_dev, ws, stream=stream)
+            _status(ws, stream, f"layer {i} S_down")
+            S_down.append(S_dn_dev.cpu().numpy().copy())
+    return S_up, S_down
+
+
+def _status(ws, stream, where: str) -> None:
+    st = B.device_status(ws, stream)
+    if st != B.AFF_OK:
+        raise B.AffinityError(st, where, B.strerror(st))
+
+
+def place_heads(S_up: List[np.ndarray], S_down: List[np.ndarray], L: int,
+                nu: Optional[np.ndarray] = None) -> StackResult:
+    """Unit-mass normalisation, contiguous neuron maps (unless given), the best
+    KV-group map of every layer and J for the contiguous and chosen layouts."""
+    N = len(S_up)
+    if len(S_down) != N - 1:
+        raise ValueError("need one S_down per layer but the last")
+    G, I = S_up[0].shape
+    Shat_up = [B.unit_mass(s) for s in S_up]
+    Shat_down = [B.unit_mass(s) for s in S_down]
+    if nu is None:
+        nu = np.stack([contiguous_map(I, L)] * N)
+    h_contig = np.stack([contiguous_map(G, L)] * N)
+    J_contig = B.objective(Shat_up, Shat_down, h_contig, nu)
+    h_best, J_best = B.best_heads(Shat_up, Shat_down, nu, L)
+    return StackResult(S_up, S_down, Shat_up, Shat_down, np.asarray(nu, np.int32), h_contig, h_best, J_contig,
+                       J_best)

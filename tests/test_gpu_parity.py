@@ -33,13 +33,15 @@ MEDIUM = S("qwen_slice", T=4096, D=1024, H=16, G=8, dh=128, I=512, dtype="bf16",
            x_dist="normal_outliers", seed=21)
 
 
-def _assert_up(shape, mode, tol=TOL):
+def _assert_up(shape, mode, tol=TOL, record=None):
     layer = W.make_layer(shape)
     (S_gpu, Sh_gpu), = run_up(B, DV, shape, layer, mode)
     S_ref, Sh_ref = oracle_up(O, shape, layer, mode)
     err = rowmax_err if shape.T < FEW_TOKENS else rel_err
     e = err(S_gpu, S_ref)
     eh = err(Sh_gpu, Sh_ref)
+    if record:
+        record(f"{shape.name}_{mode}_max_rel_err", e)
     assert e <= tol and eh <= tol, f"{shape.name} {mode}: max rel err S {e:.3e}, S_head {eh:.3e}"
     for g in range(shape.G):
         assert topk_agrees(S_gpu[g], S_ref[g]), f"{shape.name} {mode}: top-8 of group {g} differs"
@@ -56,13 +58,13 @@ def test_up_small(shape, mode):
 
 
 @pytest.mark.parametrize("mode", ["fo", "add"])
-def test_up_tiny_fp32(mode):
-    _assert_up(W.CONFIGS["tiny"], mode, tol=TOL_F32)
+def test_up_tiny_fp32(mode, record_property):
+    _assert_up(W.CONFIGS["tiny"], mode, tol=TOL_F32, record=record_property)
 
 
 @pytest.mark.parametrize("mode", ["fo", "add"])
-def test_up_medium(mode):
-    _assert_up(MEDIUM, mode)
+def test_up_medium(mode, record_property):
+    _assert_up(MEDIUM, mode, record=record_property)
 
 
 def test_up_deterministic():
@@ -107,12 +109,13 @@ def test_up_permutation_equivariance():
 
 
 @pytest.mark.parametrize("shape", SMALL[:4] + [W.CONFIGS["tiny"]], ids=[s.name for s in SMALL[:4]] + ["tiny"])
-def test_down_small(shape):
+def test_down_small(shape, record_property):
     layer = W.make_layer(shape, with_next=True)
     S_gpu, = run_down(B, DV, shape, layer)
     S_ref = oracle_down(O, shape, layer)
     tol = TOL_F32 if shape.dtype == "fp32" else TOL
     e = rel_err(S_gpu, S_ref)
+    record_property(f"{shape.name}_down_max_rel_err", e)
     assert e <= tol, f"{shape.name} down: max rel err {e:.3e}"
 
 
@@ -140,7 +143,7 @@ FULL = ["qwen3_0p6b_layer", "danube3_500m_layer", "llama3_8b_layer"]
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", FULL)
-def test_up_full_size_sampled(name):
+def test_up_full_size_sampled(name, record_property):
     """Full-size layer, FO (and ADD for the Danube3 shape): relative error on the
     sampled neurons, and the oracle's order of the sampled set reproduces the
     GPU's top-8 per group."""
@@ -153,17 +156,20 @@ def test_up_full_size_sampled(name):
         idx = _candidates(S_gpu, rng)
         S_ref, _ = oracle_up(O, shape, layer, mode, neurons=idx)
         e = rel_err(S_gpu[:, idx], S_ref, floor_ref=float(S_gpu.max()))
+        record_property(f"{name}_{mode}_max_rel_err", e)
+        record_property(f"{name}_{mode}_sampled_neurons", len(idx))
         assert e <= TOL, f"{name} {mode}: max rel err {e:.3e} on {len(idx)} sampled neurons"
         for g in range(shape.G):
             assert topk_agrees(S_gpu[g, idx], S_ref[g]), f"{name} {mode}: top-8 of group {g} differs"
 
 
 @pytest.mark.slow
-def test_down_full_size_sampled():
+def test_down_full_size_sampled(record_property):
     shape = W.CONFIGS["qwen3_0p6b_layer"]
     layer = W.make_layer(shape, with_next=True)
     S_gpu, = run_down(B, DV, shape, layer)
     idx = np.random.default_rng(5).choice(shape.I, size=64, replace=False)
     S_ref = oracle_down(O, shape, layer, neurons=idx)
     e = rel_err(S_gpu[idx], S_ref, floor_ref=float(S_gpu.max()))
+    record_property("qwen3_0p6b_layer_down_max_rel_err", e)
     assert e <= TOL, f"down full size: max rel err {e:.3e}"

@@ -54,7 +54,7 @@ def test_place_heads_uniform_scores_give_the_expectation():
 
 @pytest.mark.gpu
 @pytest.mark.slow
-def test_qwen3_stack_28_layers():
+def test_qwen3_stack_28_layers(record_property):
     torch = pytest.importorskip("torch")
     from transformer_sharding_affinity_gb300 import binding as B
     from transformer_sharding_affinity_gb300 import device as DV
@@ -88,6 +88,7 @@ def test_qwen3_stack_28_layers():
         S_ref, _ = O.s_up(layer["a"], layer["x"], layer["Wo"], layer["gamma"], layer["Wg"], layer["Wu"],
                           layer["Wd"], shape.H, shape.G, shape.dh, shape.eps, "fo", neurons=idx)
         e = rel_err(S_gpu[:, idx], S_ref, floor_ref=float(S_gpu.max()))
+        record_property(f"layer{i}_fo_max_rel_err", e)
         assert e <= TOL, f"layer {i} S_up: max rel err {e:.3e}"
         for g in range(shape.G):
             assert topk_agrees(S_gpu[g, idx], S_ref[g]), f"layer {i}: top-8 of group {g} differs"
@@ -98,8 +99,11 @@ def test_qwen3_stack_28_layers():
                       layer["Wq_next"], layer["Wk_next"], layer["Wv_next"], shape.H, shape.G, shape.dh, shape.eps,
                       neurons=idx)
     e = rel_err(S_down[0][idx], Sd_ref, floor_ref=float(S_down[0].max()))
+    record_property("layer0_down_max_rel_err", e)
     assert e <= TOL, f"layer 0 S_down: max rel err {e:.3e}"
 
     res = ST.place_heads(S_up, S_down, L)
     _check_host_sequence(res, L)
     assert res.h_best.shape == (N, shape.G)
+    record_property("J_contiguous", res.J_contiguous)
+    record_property("J_best_heads", res.J_best)

@@ -144,8 +144,6 @@ struct Smem {
   uint8_t* stage0;
 };
 
-__device__ __forceinline__ float h_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu))); }
-__device__ __forceinline__ float h_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -383,9 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
     // TMEM-empty arrivals go to the leader's barrier (its own when unpaired)
     const uint32_t tempty_addr0 = PAIR ? mapa_shared(smem_u32(&sm.tempty[0]), 0) : 0u;
-    uint32_t abA[32], abB[32];         // FO: fp16 pairs of silu'(g)u and silu(g), 64 tokens
+    uint64_t abA[32], abB[32];         // FO: f32x2 pairs of silu'(g)u and silu(g), 64 tokens
 #pragma unroll
-    for (int i = 0; i < 32; ++i) { abA[i] = 0u; abB[i] = 0u; }
+    for (int i = 0; i < 32; ++i) { abA[i] = 0ull; abB[i] = 0ull; }
     float ss1 = 0.f, ss2 = 0.f;        // x' / qnorm running sums
     int b = 0;
     uint32_t tph = 0;                  // TMEM buffer phase (flips every second job)
@@ -409,9 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if constexpr (MODE == kModeFO) {
           if (J.kind == kJobGateUp) {
-            // Phase 1: stash g, u as fp16 pairs in the registers that will hold A', B'
-            // and hand the accumulator buffer back at once, so the MMAs of the next
-            // two head jobs run while phase 2 (exp + reciprocal per element) computes.
+            // Phase 1: stash g, u in the registers that will hold A', B' and hand the
+            // accumulator buffer back at once, so the MMAs of the next two head
+            // jobs run while phase 2 (exp + reciprocal per element) computes.
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               uint32_t gr[16], ur[16];
@@ -430,24 +428,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
 #pragma unroll
               for (int i = 0; i < 16; i += 2) {
-                abA[c * 8 + i / 2] = pack_h2(__uint_as_float(gr[i]), __uint_as_float(gr[i + 1]));
-                abB[c * 8 + i / 2] = pack_h2(__uint_as_float(ur[i]), __uint_as_float(ur[i + 1]));
+                abA[c * 8 + i / 2] = pk_u(gr[i], gr[i + 1]);
+                abB[c * 8 + i / 2] = pk_u(ur[i], ur[i + 1]);
               }
             }
             // Phase 2: (g, u) -> (A', B') = (silu'(g) u, silu(g)) in place.
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
+              const float2 g2 = unpk(abA[i]), u2 = unpk(abB[i]);
               float gA[2], gB[2];
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
-                const float g = e ? h_hi(abA[i]) : h_lo(abA[i]);
-                const float uu = e ? h_hi(abB[i]) : h_lo(abB[i]);
+                const float g = e ? g2.y : g2.x;
+                const float uu = e ? u2.y : u2.x;
                 const float sg = __fdividef(1.0f, 1.0f + __expf(-g));  // sigmoid(g)
                 gA[e] = sg * fmaf(g, 1.0f - sg, 1.0f) * uu;           // silu'(g) u
                 gB[e] = g * sg;                                       // silu(g)
               }
-              abA[i] = pack_h2(gA[0], gA[1]);
-              abB[i] = pack_h2(gB[0], gB[1]);
+              abA[i] = pk(gA[0], gA[1]);
+              abB[i] = pk(gB[0], gB[1]);
             }
             continue;
           }
@@ -482,31 +481,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           // kJobHead: per token Delta = A' pg + B' pu (FO) or pg^2 + pu^2 (ADD), summed over tokens
           uint64_t acc = pk(0.f, 0.f);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t pg[16], pu[16];
-            tmem_ld16(c1 + c * 16, pg);
-            tmem_ld16(c2 + c * 16, pu);
+          for (int c = 0; c < 8; ++c) {
+            uint32_t pg[8], pu[8];
+            tmem_ld8(c1 + c * 8, pg);
+            tmem_ld8(c2 + c * 8, pu);
             tmem_ld_wait();
-            if (c == 3) {
+            if (c == 7) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) {
-                  if (PAIR)
-                    mbar_arrive_cluster(tempty_addr0 + (uint32_t)(b * 8));
-                  else
-                    mbar_arrive(&sm.tempty[b]);
-                }
+                if (PAIR)
+                  mbar_arrive_cluster(tempty_addr0 + (uint32_t)(b * 8));
+                else
+                  mbar_arrive(&sm.tempty[b]);
+              }
             }
 #pragma unroll
-            for (int i = 0; i < 16; i += 2) {
+            for (int i = 0; i < 8; i += 2) {
               const uint64_t vg = pk_u(pg[i], pg[i + 1]);
               const uint64_t vu = pk_u(pu[i], pu[i + 1]);
               if constexpr (MODE == kModeFO) {
-                const uint32_t wa = abA[c * 8 + i / 2], wb = abB[c * 8 + i / 2];
-                const uint64_t va = pk(h_lo(wa), h_hi(wa));
-                const uint64_t vb = pk(h_lo(wb), h_hi(wb));
-                uint64_t d = mul2(va, vg);
-                d = fma2(vb, vu, d);
+                uint64_t d = mul2(abA[c * 4 + i / 2], vg);
+                d = fma2(abB[c * 4 + i / 2], vu, d);
                 acc = fma2(d, d, acc);
               } else {
                 acc = fma2(vg, vg, acc);

@@ -17,7 +17,7 @@ every token before it is dotted with a neuron's gate/up row.  The only
 liberty taken is that the token average E_t is accumulated over blocks of
 tokens (a loop over t), which changes the rounding order and nothing else.
 
-Readings of points the paper leaves open (each is listed in the design doc):
+Readings of points the paper leaves open:
   * r = rms(x) = sqrt(mean_d x_d^2 + eps) with eps an explicit argument.
   * Head h belongs to KV group floor(h / (H/G)) (contiguous, the usual
     grouped-query order); both FO and ADD are summed over a group's heads.

@@ -10,7 +10,7 @@ co-located affinity J, eq. 6) and "Optimiser" (scoring every labelled
 balanced partition of the KV groups, G!/((G/L)!)^L of them, given the
 neighbouring neuron assignments).
 
-Readings (listed in DESIGN.md):
+Readings of points the paper leaves open:
   * Partitions are enumerated lexicographically over (h(0), ..., h(G-1)) and
     the first maximum wins ties.
   * The gain of placing group g of layer i on device l, given nu_{i-1} and

@@ -45,7 +45,11 @@ def fo_flops(s) -> dict:
 # the FO tile kernel, from an ncu capture of this bench's workload; valid only
 # while the kernel sources hash to the recorded value (otherwise null).
 KERNEL_SOURCES = ("tile_kernel.cu", "tile_kernel.cuh", "sm103_primitives.cuh")
-TRAFFIC = {}
+TRAFFIC = {
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass), third FO launch of
+    # `python bench.py --steps 2 --warmup 3 --no-cpu-baseline --e2e-steps 0`: 453.52 + 96.26 MB
+    ("qwen3_0p6b_layer", "fo", 65536): {"bytes": 549.78e6, "src": "53801c51cb698a3c"},
+}
 
 
 def kernel_source_hash() -> str:

@@ -39,10 +39,10 @@
  *  For fixed inputs, shapes and library build the outputs are bit-identical
  *  from run to run (fixed reduction orders, no floating-point atomics).
  *
- *  bf16 path numerics: operands are staged as fp16 (the normalised FFN
- *  input gamma*x/r, a/r, the folded per-head matrices, the SwiGLU operating
- *  point) and contracted on the tensor cores with fp32 accumulation; token
- *  sums are finished in fp64.  Intermediates must fit fp16's range
+ *  bf16 path numerics: tensor-core operands are staged as fp16 (the
+ *  normalised FFN input gamma*x/r, a/r, the folded per-head matrices) and
+ *  contracted with fp32 accumulation; the SwiGLU operating point stays fp32;
+ *  token sums are finished in fp64.  Intermediates must fit fp16's range
  *  (|value| < 65504); an overflow latches AFF_ERR_RANGE.  fp32 path: fp32
  *  arithmetic on the CUDA cores (meant for small shapes).
  */
@@ -75,7 +75,8 @@ typedef enum {
   AFF_ERR_CUDA = 6,               /* a CUDA call failed; see affinity_last_cuda_error() */
   AFF_ERR_DEVICE_TIMEOUT = 7,     /* a kernel's bounded wait expired (device-latched) */
   AFF_ERR_RANGE = 8,              /* an fp16 intermediate overflowed (device-latched) */
-  AFF_ERR_ALIGNMENT = 9           /* a pointer is not 16-byte aligned */
+  AFF_ERR_ALIGNMENT = 9,          /* a pointer is not 16-byte aligned */
+  AFF_ERR_NO_CONVERGENCE = 10     /* an iterative solver hit its iteration cap (device-latched) */
 } aff_status;
 
 typedef enum {
@@ -264,6 +265,92 @@ AFF_API aff_status affinity_best_heads(const double* Shat_up, const double* Shat
  */
 AFF_API aff_status affinity_combine_shards(const float* const* S_shards, const int64_t* T_shards,
                                            int32_t n_shards, int64_t n, float* out);
+
+/* ------------------------------------------------------------------------
+ * Layout search ("Optimiser", §3).  Unit-mass matrices are fp64.
+ * ---------------------------------------------------------------------- */
+
+/* Options of the neuron solver; zero fields take the defaults. */
+typedef struct {
+  int32_t dual_iters;   /* dual-ascent iterations on the device offsets (default 300) */
+  double dual_decay;    /* step decay per iteration, in (0, 1] (default 0.98) */
+  int64_t max_cycles;   /* cap on applied exchange cycles (default 64 * I) */
+} aff_assign_opts;
+
+/*
+ * The gain of putting neuron k of layer i on device l, on the GPU:
+ *   M[k, l] = sum_{g: h_i(g) = l} Shat_up_i[g, k]
+ *           + sum_{g: h_next(g) = l} Shat_down_i[k, g]
+ * (the second sum only when Shat_down_i is given; the last layer of a stack
+ * has none).  Groups are added in ascending order, up term first.
+ *   Shat_up_i   device fp64 [G, I];  Shat_down_i device fp64 [I, G] or NULL
+ *   h_i, h_next host int32 [G], devices in [0, L) (h_next NULL iff Shat_down_i is)
+ *   M_out       device fp64 [I, L]
+ * 1 <= G <= 16, 1 <= L <= 8; 8-byte aligned device pointers.  Enqueued on
+ * `stream`; nothing is synchronised.
+ */
+AFF_API aff_status affinity_neuron_gain(const double* Shat_up_i, const double* Shat_down_i,
+                                        const int32_t* h_i, const int32_t* h_next, int32_t G, int64_t I,
+                                        int32_t L, double* M_out, aff_stream_t stream);
+
+/*
+ * Best balanced neuron map of each of `n_layers` independent problems: nu
+ * maximises sum_k M[k, nu(k)] with exactly I/L neurons per device.  One CTA
+ * per problem runs dual ascent on the L device offsets, a fix-up that makes
+ * single cheapest moves from over- to under-full devices, and then applies
+ * the best exchange cycle of devices (one neuron moved out of each device on
+ * the cycle, the best neuron per ordered device pair) while one gains more
+ * than rounding.  When none gains, the map is optimal, so the value equals
+ * the Hungarian solution up to rounding; ties between equally good maps are
+ * broken by the fixed search order.
+ *   M          device fp64 [n_layers][I][L]
+ *   nu_out     device int32 [n_layers][I]
+ *   value_out  device fp64 [n_layers]: sum_k M[k, nu(k)]
+ *   workspace  device, >= 256 B, 256-byte aligned (status word; read it with
+ *              affinity_device_status: AFF_ERR_NO_CONVERGENCE if max_cycles
+ *              was reached, the map then being balanced but not proven best)
+ * Requires 1 <= L <= 8, I % L == 0, L <= I <= 49152.  Deterministic.
+ */
+AFF_API aff_status affinity_assign_neurons(const double* M, int32_t n_layers, int64_t I, int32_t L,
+                                           const aff_assign_opts* opts, int32_t* nu_out,
+                                           double* value_out, void* workspace, size_t workspace_bytes,
+                                           aff_stream_t stream);
+
+/* Options of the alternating search; zero fields take the defaults. */
+typedef struct {
+  int32_t max_sweeps;          /* sweeps of (neuron step, head step) at most (default 16) */
+  int32_t freeze_heads;        /* nonzero: keep every h_i as given */
+  int32_t freeze_neurons;      /* nonzero: keep every nu_i as given */
+  int32_t minimise;            /* nonzero: minimise J instead of maximising it */
+  const uint8_t* layer_mask;   /* host [N]: 0 keeps layer i's maps as given; NULL: all move */
+  aff_assign_opts assign;      /* neuron-solver options */
+} aff_layout_opts;
+
+/* Device workspace bytes for affinity_optimise_layout. */
+AFF_API aff_status affinity_layout_workspace_size(int32_t N, int32_t G, int64_t I, int32_t L,
+                                                  size_t* bytes);
+
+/*
+ * Alternating maximisation of J (equation (6)) over balanced layouts of an
+ * N-layer stack ("Optimiser", §3).  From the given maps, each sweep first
+ * sets every layer's neuron map to the best one given h_i and h_{i+1} (GPU,
+ * affinity_neuron_gain + affinity_assign_neurons over all layers at once),
+ * then every layer's KV-group map to the best balanced partition given
+ * nu_{i-1} and nu_i (host, affinity_group_gain + affinity_score_partitions).
+ * Each step is optimal given the rest, so J never decreases; the search
+ * stops when a sweep gains less than 1e-12 relative, or after max_sweeps.
+ *   Shat_up   host fp64, N contiguous [G, I] unit-mass blocks
+ *   Shat_down host fp64, N-1 contiguous [I, G] blocks (NULL if N == 1)
+ *   h, nu     host int32 N x [G] and N x [I]: the balanced starting maps on
+ *             entry (e.g. contiguous), the result on return
+ *   J_out     host fp64: J of the result;  sweeps_out: sweeps run (may be NULL)
+ * G % L == 0, G <= 16 and the limits of affinity_assign_neurons.
+ * Synchronises `stream` once per sweep (the head step runs on the host).
+ */
+AFF_API aff_status affinity_optimise_layout(const double* Shat_up, const double* Shat_down, int32_t N,
+                                            int32_t G, int64_t I, int32_t L, const aff_layout_opts* opts,
+                                            int32_t* h, int32_t* nu, double* J_out, int32_t* sweeps_out,
+                                            void* workspace, size_t workspace_bytes, aff_stream_t stream);
 
 /*
  * Profiling hook (no effect on results): register two caller-created CUDA

@@ -218,3 +218,51 @@ def test_combine_shards_is_the_token_weighted_mean(lib):
     for bad_T in ([0, 0, 0], [1, -1, 1]):
         with pytest.raises(B.AffinityError):
             B.combine_shards(S, bad_T)
+
+
+# ---------------------------------------------------------------- layout search: validation before any device use
+
+def test_layout_search_argument_checks(lib):
+    P_ = ctypes.c_void_p
+    fake = P_(1 << 20)          # never dereferenced: every check below fails before a device is touched
+    h = np.zeros(8, np.int32)
+    h4 = (np.arange(8) // 2).astype(np.int32)
+    assert lib.affinity_neuron_gain(fake, None, h4.ctypes.data, None, 8, 64, 9, fake, None) == \
+        B.AFF_ERR_UNSUPPORTED_SHAPE
+    assert lib.affinity_neuron_gain(fake, None, h4.ctypes.data, None, 17, 64, 4, fake, None) == B.AFF_ERR_INVALID_ARG
+    bad = h4.copy()
+    bad[0] = 4
+    assert lib.affinity_neuron_gain(fake, None, bad.ctypes.data, None, 8, 64, 4, fake, None) == B.AFF_ERR_INVALID_ARG
+    assert lib.affinity_neuron_gain(fake, fake, h4.ctypes.data, None, 8, 64, 4, fake, None) == B.AFF_ERR_INVALID_ARG
+    assert lib.affinity_neuron_gain(fake, None, h4.ctypes.data, None, 8, 64, 4, fake, None) == B.AFF_ERR_ARCH
+
+    def assign(I, L, ws=fake, nbytes=256):
+        return lib.affinity_assign_neurons(fake, 1, I, L, None, fake, fake, ws, nbytes, None)
+    assert assign(66, 4) == B.AFF_ERR_UNSUPPORTED_SHAPE
+    assert assign(49152 + 4, 4) == B.AFF_ERR_UNSUPPORTED_SHAPE
+    assert assign(64, 9) == B.AFF_ERR_UNSUPPORTED_SHAPE
+    assert assign(64, 4, nbytes=128) == B.AFF_ERR_WORKSPACE
+    assert assign(64, 4, ws=P_((1 << 20) + 8)) == B.AFF_ERR_WORKSPACE
+    assert assign(64, 4) == B.AFF_ERR_ARCH
+
+    n = B.layout_workspace_size(28, 8, 3072, 4)
+    assert n >= 28 * 8 * 3072 * 8 * 2 + 28 * 3072 * 4 * 8
+    with pytest.raises(B.AffinityError):
+        B.layout_workspace_size(2, 6, 64, 4)      # G % L != 0
+    N, G, I, L = 2, 8, 64, 4
+    up = np.full((N, G, I), 1.0 / (G * I))
+    dn = np.full((N - 1, I, G), 1.0 / (G * I))
+    hh = np.stack([h4] * N).astype(np.int32)
+    nn = np.stack([(np.arange(I) // (I // L)).astype(np.int32)] * N)
+    J, sw = ctypes.c_double(0), ctypes.c_int32(0)
+    ws_n = B.layout_workspace_size(N, G, I, L)
+
+    def opt(hmap, numap, nbytes=ws_n):
+        return lib.affinity_optimise_layout(up.ctypes.data, dn.ctypes.data, N, G, I, L, None, hmap.ctypes.data,
+                                            numap.ctypes.data, ctypes.byref(J), ctypes.byref(sw), fake, nbytes, None)
+    unbalanced = hh.copy()
+    unbalanced[0, 0] = 1
+    assert opt(unbalanced, nn) == B.AFF_ERR_INVALID_ARG
+    assert opt(hh, nn, nbytes=ws_n - 1) == B.AFF_ERR_WORKSPACE
+    assert opt(hh, nn) == B.AFF_ERR_ARCH
+    assert h.sum() == 0

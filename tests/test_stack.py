@@ -107,3 +107,17 @@ def test_qwen3_stack_28_layers(record_property):
     assert res.h_best.shape == (N, shape.G)
     record_property("J_contiguous", res.J_contiguous)
     record_property("J_best_heads", res.J_best)
+
+    # the alternating search from the contiguous layout: J never falls below
+    # the head-only optimum, and the first layer's neuron map is the exact
+    # best balanced map given the result's head maps
+    from oracle import assignment as A
+    lay = ST.optimise(res.Shat_up, res.Shat_down, L)
+    record_property("J_optimised", lay.J)
+    record_property("sweeps", lay.sweeps)
+    np.testing.assert_allclose(lay.J, P.objective_J(res.Shat_up, res.Shat_down, list(lay.h), list(lay.nu)),
+                               rtol=1e-12)
+    assert lay.J >= res.J_best - 1e-12 and lay.J <= 2 * N - 1
+    M0 = A.neuron_gain(res.Shat_up[0], lay.h[0], L, res.Shat_down[0], lay.h[1])
+    _, best0 = A.best_balanced_neurons(M0)
+    np.testing.assert_allclose(A.assignment_value(M0, lay.nu[0]), best0, rtol=1e-12)

@@ -28,6 +28,7 @@ AFF_ERR_CUDA = 6
 AFF_ERR_DEVICE_TIMEOUT = 7
 AFF_ERR_RANGE = 8
 AFF_ERR_ALIGNMENT = 9
+AFF_ERR_NO_CONVERGENCE = 10
 
 AFF_MODE_FO = 0
 AFF_MODE_ADD = 1
@@ -40,6 +41,16 @@ class aff_dims(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("D", ctypes.c_int64), ("H", ctypes.c_int64), ("G", ctypes.c_int64),
                 ("d_head", ctypes.c_int64), ("I", ctypes.c_int64), ("eps", ctypes.c_float),
                 ("dtype", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+class aff_assign_opts(ctypes.Structure):
+    _fields_ = [("dual_iters", ctypes.c_int32), ("dual_decay", ctypes.c_double), ("max_cycles", ctypes.c_int64)]
+
+
+class aff_layout_opts(ctypes.Structure):
+    _fields_ = [("max_sweeps", ctypes.c_int32), ("freeze_heads", ctypes.c_int32),
+                ("freeze_neurons", ctypes.c_int32), ("minimise", ctypes.c_int32),
+                ("layer_mask", ctypes.c_void_p), ("assign", aff_assign_opts)]
 
 
 class AffinityError(RuntimeError):
@@ -86,6 +97,18 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.affinity_best_heads.restype = st
     lib.affinity_combine_shards.argtypes = [_P, _P, ctypes.c_int32, ctypes.c_int64, _P]
     lib.affinity_combine_shards.restype = st
+    lib.affinity_neuron_gain.argtypes = [_P, _P, _P, _P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, _P, _P]
+    lib.affinity_neuron_gain.restype = st
+    lib.affinity_assign_neurons.argtypes = [_P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+                                            ctypes.POINTER(aff_assign_opts), _P, _P, _P, ctypes.c_size_t, _P]
+    lib.affinity_assign_neurons.restype = st
+    lib.affinity_layout_workspace_size.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+                                                   ctypes.POINTER(ctypes.c_size_t)]
+    lib.affinity_layout_workspace_size.restype = st
+    lib.affinity_optimise_layout.argtypes = [_P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+                                             ctypes.POINTER(aff_layout_opts), _P, _P, ctypes.POINTER(ctypes.c_double),
+                                             ctypes.POINTER(ctypes.c_int32), _P, ctypes.c_size_t, _P]
+    lib.affinity_optimise_layout.restype = st
     lib.affinity_strerror.argtypes = [ctypes.c_int32]
     lib.affinity_strerror.restype = ctypes.c_char_p
     lib.affinity_last_cuda_error.argtypes = []
@@ -258,6 +281,61 @@ def combine_shards(S_shards: Sequence[np.ndarray], T_shards: Sequence[int]) -> n
     _check(load().affinity_combine_shards(ctypes.cast(ptrs, ctypes.c_void_p), T.ctypes.data, len(arrs),
                                           arrs[0].size, out.ctypes.data), "affinity_combine_shards")
     return out
+
+
+def neuron_gain(Shat_up_i, Shat_down_i, h_i, h_next, L: int, M_out, stream=None) -> None:
+    """Enqueue M [I, L] (affinity_neuron_gain); Shat_* and M_out are CUDA fp64 tensors."""
+    G, I = Shat_up_i.shape
+    h = np.ascontiguousarray(h_i, dtype=np.int32)
+    hn = None if h_next is None else np.ascontiguousarray(h_next, dtype=np.int32)
+    _check(load().affinity_neuron_gain(_ptr(Shat_up_i), _ptr(Shat_down_i), h.ctypes.data,
+                                       None if hn is None else hn.ctypes.data, G, I, int(L), _ptr(M_out),
+                                       _stream(stream)), "affinity_neuron_gain")
+
+
+def assign_opts(dual_iters: int = 0, dual_decay: float = 0.0, max_cycles: int = 0) -> aff_assign_opts:
+    return aff_assign_opts(int(dual_iters), float(dual_decay), int(max_cycles))
+
+
+def assign_neurons(M, L: int, nu_out, value_out, workspace, opts: Optional[aff_assign_opts] = None,
+                   stream=None, workspace_bytes=None) -> None:
+    """Enqueue the balanced neuron solver on M [n, I, L] (CUDA fp64) -> nu_out [n, I] int32, value_out [n] fp64."""
+    n, I = (1, M.shape[0]) if M.dim() == 2 else (M.shape[0], M.shape[1])
+    _check(load().affinity_assign_neurons(_ptr(M), n, I, int(L), None if opts is None else ctypes.byref(opts),
+                                          _ptr(nu_out), _ptr(value_out), _ptr(workspace),
+                                          _ws_bytes(workspace, workspace_bytes), _stream(stream)),
+           "affinity_assign_neurons")
+
+
+def layout_workspace_size(N: int, G: int, I: int, L: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().affinity_layout_workspace_size(int(N), int(G), int(I), int(L), ctypes.byref(n)),
+           "affinity_layout_workspace_size")
+    return n.value
+
+
+def optimise_layout(Shat_up: Sequence[np.ndarray], Shat_down: Sequence[np.ndarray], L: int, h0, nu0, workspace,
+                    max_sweeps: int = 0, freeze_heads: bool = False, freeze_neurons: bool = False,
+                    minimise: bool = False, layer_mask=None, assign: Optional[aff_assign_opts] = None,
+                    stream=None, workspace_bytes=None):
+    """Alternating layout search (affinity_optimise_layout). Returns (h [N, G], nu [N, I], J, sweeps)."""
+    N = len(Shat_up)
+    G, I = np.asarray(Shat_up[0]).shape
+    up = np.ascontiguousarray(np.stack([np.asarray(s, np.float64) for s in Shat_up]))
+    dn = np.ascontiguousarray(np.stack([np.asarray(s, np.float64) for s in Shat_down])) if N > 1 else None
+    h = np.ascontiguousarray(np.array(h0, dtype=np.int32).reshape(N, G))
+    nu = np.ascontiguousarray(np.array(nu0, dtype=np.int32).reshape(N, I))
+    mask = None if layer_mask is None else np.ascontiguousarray(layer_mask, dtype=np.uint8)
+    opts = aff_layout_opts(int(max_sweeps), int(bool(freeze_heads)), int(bool(freeze_neurons)), int(bool(minimise)),
+                           None if mask is None else mask.ctypes.data, assign or aff_assign_opts())
+    J = ctypes.c_double(0.0)
+    sweeps = ctypes.c_int32(0)
+    _check(load().affinity_optimise_layout(up.ctypes.data, None if dn is None else dn.ctypes.data, N, G, I, int(L),
+                                           ctypes.byref(opts), h.ctypes.data, nu.ctypes.data, ctypes.byref(J),
+                                           ctypes.byref(sweeps), _ptr(workspace),
+                                           _ws_bytes(workspace, workspace_bytes), _stream(stream)),
+           "affinity_optimise_layout")
+    return h, nu, J.value, sweeps.value
 
 
 def set_timing_events(start_event, stop_event) -> None:

@@ -4,6 +4,7 @@
 // §3 "Affinity scores").  The host-only layout helpers live in layout.cu.
 #include "affinity.h"
 #include "aux_kernels.cuh"
+#include "internal.h"
 #include "tile_kernel.cuh"
 
 #include <cuda.h>
@@ -25,21 +26,44 @@ size_t tile_smem_bytes(int mode, int stages, int H, bool pair);
 using namespace aff;
 
 namespace {
-
 thread_local std::string g_last_cuda_error;
 thread_local cudaEvent_t g_timing_start = nullptr;  // see affinity_set_timing_events
 thread_local cudaEvent_t g_timing_stop = nullptr;
+}  // namespace
 
-aff_status cuda_fail(cudaError_t e, const char* where) {
+aff_status aff::cuda_fail(cudaError_t e, const char* where) {
   g_last_cuda_error = std::string(where) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
   return AFF_ERR_CUDA;
 }
 
-#define AFF_CUDA(call)                                   \
-  do {                                                   \
-    cudaError_t e_ = (call);                             \
-    if (e_ != cudaSuccess) return cuda_fail(e_, #call);  \
-  } while (0)
+// ---------------------------------------------------------------- device checks
+aff_status aff::check_device(int* sm_count) {
+  static std::mutex mu;
+  static std::vector<int> sms;  // per device: 0 unknown, -1 wrong arch, >0 SM count
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return AFF_ERR_ARCH;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if ((int)sms.size() <= dev) sms.resize(dev + 1, 0);
+  if (sms[dev] == 0) {
+    int maj = 0, min = 0, n = 0;
+    if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return AFF_ERR_ARCH;
+    }
+    sms[dev] = (maj == 10 && min == 3) ? n : -1;
+  }
+  if (sms[dev] < 0) return AFF_ERR_ARCH;
+  *sm_count = sms[dev];
+  return AFF_OK;
+}
+
+namespace {
 
 constexpr int64_t kMaxDim = (int64_t)1 << 30;
 constexpr int kTilesPerUnit = 2;      // token tiles (of 128) per FO / ADD unit
@@ -135,33 +159,6 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
   }
   L.total = (size_t)round_up((int64_t)L.total, 1024);
   return L;
-}
-
-// ---------------------------------------------------------------- device checks
-aff_status check_device(int* sm_count) {
-  static std::mutex mu;
-  static std::vector<int> sms;  // per device: 0 unknown, -1 wrong arch, >0 SM count
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return AFF_ERR_ARCH;
-  }
-  std::lock_guard<std::mutex> lk(mu);
-  if ((int)sms.size() <= dev) sms.resize(dev + 1, 0);
-  if (sms[dev] == 0) {
-    int maj = 0, min = 0, n = 0;
-    if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-      cudaGetLastError();
-      return AFF_ERR_ARCH;
-    }
-    sms[dev] = (maj == 10 && min == 3) ? n : -1;
-  }
-  if (sms[dev] < 0) return AFF_ERR_ARCH;
-  *sm_count = sms[dev];
-  return AFF_OK;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -359,6 +356,7 @@ const char* affinity_strerror(aff_status s) {
     case AFF_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait expired";
     case AFF_ERR_RANGE: return "an fp16 intermediate overflowed (|value| >= 65504)";
     case AFF_ERR_ALIGNMENT: return "a device pointer is not 16-byte aligned";
+    case AFF_ERR_NO_CONVERGENCE: return "an iterative solver reached its iteration cap";
   }
   return "unknown status";
 }

@@ -95,3 +95,30 @@ def place_heads(S_up: List[np.ndarray], S_down: List[np.ndarray], L: int,
     h_best, J_best = B.best_heads(Shat_up, Shat_down, nu, L)
     return StackResult(S_up, S_down, Shat_up, Shat_down, np.asarray(nu, np.int32), h_contig, h_best, J_contig,
                        J_best)
+
+
+@dataclasses.dataclass
+class LayoutResult:
+    h: np.ndarray        # [N, G]
+    nu: np.ndarray       # [N, I]
+    J: float
+    sweeps: int
+
+
+def optimise(Shat_up: List[np.ndarray], Shat_down: List[np.ndarray], L: int, h0: Optional[np.ndarray] = None,
+             nu0: Optional[np.ndarray] = None, stream=None, **opts) -> LayoutResult:
+    """Alternate the neuron step (GPU) and the head step (host) from the given
+    maps -- contiguous by default -- until J stops increasing
+    (``affinity_optimise_layout``).  Keyword options: max_sweeps,
+    freeze_heads, freeze_neurons, minimise, layer_mask, assign."""
+    import torch
+
+    N = len(Shat_up)
+    G, I = np.asarray(Shat_up[0]).shape
+    if h0 is None:
+        h0 = np.stack([contiguous_map(G, L)] * N)
+    if nu0 is None:
+        nu0 = np.stack([contiguous_map(I, L)] * N)
+    ws = torch.empty(B.layout_workspace_size(N, G, I, L), dtype=torch.uint8, device="cuda")
+    h, nu, J, sweeps = B.optimise_layout(Shat_up, Shat_down, L, h0, nu0, ws, stream=stream, **opts)
+    return LayoutResult(h, nu, J, sweeps)

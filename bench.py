@@ -190,6 +190,78 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def run_layout(args) -> None:
+    """Layout search on a 28-layer Qwen3-shaped stack of seeded unit-mass
+    affinity matrices: the GPU neuron step for all layers in one launch
+    (CUDA events) and the whole alternating search from the contiguous layout
+    (wall clock, including the host head steps)."""
+    import torch
+    from transformer_sharding_affinity_gb300 import binding as B
+    from transformer_sharding_affinity_gb300 import stack as ST
+    from transformer_sharding_affinity_gb300 import workloads as W
+
+    B.load()
+    shape = W.CONFIGS["qwen3_0p6b_stack"]
+    N, G, I, L = W.STACK_LAYERS, shape.G, shape.I, 4
+    rng = np.random.Generator(np.random.PCG64(shape.seed))
+    S_up = [rng.gamma(0.5, size=(G, I)).astype(np.float32) for _ in range(N)]
+    S_dn = [rng.gamma(0.5, size=(I, G)).astype(np.float32) for _ in range(N - 1)]
+    up = [B.unit_mass(s) for s in S_up]
+    dn = [B.unit_mass(s) for s in S_dn]
+    hc = np.stack([ST.contiguous_map(G, L)] * N)
+    # neuron step of every layer at once on M built by the gain kernel
+    d_up = torch.from_numpy(np.stack(up)).cuda()
+    d_dn = torch.from_numpy(np.stack(dn)).cuda()
+    M = torch.empty(N, I, L, dtype=torch.float64, device="cuda")
+    nu = torch.empty(N, I, dtype=torch.int32, device="cuda")
+    val = torch.empty(N, dtype=torch.float64, device="cuda")
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+
+    def neuron_step():
+        for i in range(N):
+            B.neuron_gain(d_up[i], d_dn[i] if i + 1 < N else None, hc[i], hc[i + 1] if i + 1 < N else None, L, M[i])
+        B.assign_neurons(M, L, nu, val, ws)
+
+    for _ in range(args.warmup):
+        neuron_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        neuron_step()
+    e1.record()
+    torch.cuda.synchronize()
+    step_ms = e0.elapsed_time(e1) / args.steps
+    st = B.device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {B.strerror(st)}")
+    ST.optimise(up, dn, L)    # warm
+    t0 = time.perf_counter()
+    res = ST.optimise(up, dn, L)
+    opt_s = time.perf_counter() - t0
+    J0 = B.objective(up, dn, hc, np.stack([ST.contiguous_map(I, L)] * N))
+    line = {"metric": "layout search: balanced neuron step for every layer of a 28-layer stack",
+            "value": N / (step_ms * 1e-3), "unit": "layers/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "none",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "qwen3_0p6b_stack unit-mass affinities (gamma(0.5) draws)", "N": N, "G": G,
+                       "I": I, "L": L},
+            "roofline": {"bound": "latency", "note": "one 1024-thread CTA per layer; M (I*L*8 B) re-read "
+                                                     "from L1 on every dual-ascent iteration"},
+            "optimise": {"seconds": opt_s, "sweeps": res.sweeps, "J_contiguous": J0, "J": res.J},
+            "gpu_launches": N + 1}
+    if not args.no_cpu_baseline:
+        from oracle import assignment as A
+        M0 = A.neuron_gain(up[0], hc[0], L, dn[0], hc[1])
+        t0 = time.perf_counter()
+        A.best_balanced_neurons(M0)
+        t = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": 1.0 / t, "unit": "layers/s", "cores": 1, "kind": "oracle",
+                                "sample": f"scipy linear_sum_assignment on the {I}x{I} replicated-slot matrix of "
+                                          f"layer 0 ({t:.2f} s)"}
+    print(json.dumps(line), flush=True)
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -203,11 +275,16 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling runs on a smaller case)")
+    ap.add_argument("--path", default="scores", choices=["scores", "layout"],
+                    help="scores: the S_up calibration pass (default); layout: the layout search")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.path == "layout":
+        run_layout(args)
         return
 
     import torch

@@ -352,6 +352,48 @@ AFF_API aff_status affinity_optimise_layout(const double* Shat_up, const double*
                                             int32_t* h, int32_t* nu, double* J_out, int32_t* sweeps_out,
                                             void* workspace, size_t workspace_bytes, aff_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Layout realisation ("The layout as a free variable", §3).
+ * ---------------------------------------------------------------------- */
+
+/*
+ * Host-only: the storage orders that realise a balanced layout.  KV groups
+ * and neurons are sorted by device, stably (ascending index within a
+ * device); every group brings its H/G query heads in ascending order.
+ *   h [G], nu [I]: devices in [0, L), G/L groups and I/L neurons per device
+ *   group_order [G], head_order [H], neuron_order [I]: written; position p
+ *   of the permuted storage holds original group / head / neuron order[p],
+ *   and device l's shard is positions [l*n/L, (l+1)*n/L).
+ * The permuted weights are then (rows of a matrix stored out x in):
+ *   Wq rows by head_order (blocks of d_head rows), Wk/Wv rows by
+ *   group_order (blocks of d_head rows), Wo columns by head_order (blocks of
+ *   d_head columns), Wg/Wu rows by neuron_order, Wd columns by neuron_order;
+ *   see affinity_gather_blocks.
+ */
+AFF_API aff_status affinity_layout_orders(const int32_t* h, const int32_t* nu, int32_t G, int64_t H,
+                                          int64_t I, int32_t L, int32_t* group_order, int32_t* head_order,
+                                          int32_t* neuron_order);
+
+/*
+ * Device gather of fixed-size blocks: out[r][j] = in[r][order[j]] for
+ * r < rows, j < n_blocks, each block `block_bytes` bytes and each row
+ * n_blocks * block_bytes bytes (contiguous).  A row permutation of a matrix
+ * is rows = 1 with one or more matrix rows per block; a column permutation
+ * is rows = the matrix's row count with one or more columns per block.
+ *   in, out    device, non-overlapping; any alignment (wider words are used
+ *              when pointers and block size allow)
+ *   order      HOST int32 [n_blocks], a permutation of 0..n_blocks-1
+ *              (AFF_ERR_INVALID_ARG otherwise; checked before any launch)
+ *   workspace  device, >= 4 * n_blocks bytes, 256-byte aligned: the order
+ *              is copied there on `stream`.  From pageable memory the copy is
+ *              staged before the call returns; a pinned `order` must stay
+ *              valid until the stream has run the copy.
+ * Bit-exact data movement; enqueued on `stream`.
+ */
+AFF_API aff_status affinity_gather_blocks(const void* in, void* out, int64_t rows, int64_t n_blocks,
+                                          int64_t block_bytes, const int32_t* order, void* workspace,
+                                          size_t workspace_bytes, aff_stream_t stream);
+
 /*
  * Profiling hook (no effect on results): register two caller-created CUDA
  * events (cudaEvent_t handles) that later affinity_up / affinity_down calls

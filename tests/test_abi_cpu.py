@@ -266,3 +266,35 @@ def test_layout_search_argument_checks(lib):
     assert opt(hh, nn, nbytes=ws_n - 1) == B.AFF_ERR_WORKSPACE
     assert opt(hh, nn) == B.AFF_ERR_ARCH
     assert h.sum() == 0
+
+
+def test_layout_orders_match_the_oracle_and_gather_checks(lib):
+    from oracle import layer_forward as LF
+    rng = np.random.default_rng(13)
+    G, H, I, L, dh = 8, 16, 96, 4, 4
+    h = rng.permutation(P.contiguous_heads(G, L)).astype(np.int32)
+    nu = rng.permutation(P.contiguous_neurons(I, L)).astype(np.int32)
+    go, ho, no = B.layout_orders(h, nu, H, L)
+    w = {k: np.zeros((1, 1)) for k in ()}
+    shapes = {"Wq": (H * dh, 8), "Wk": (G * dh, 8), "Wv": (G * dh, 8), "Wo": (8, H * dh), "Wg": (I, 8),
+              "Wu": (I, 8), "Wd": (8, I)}
+    w = {k: rng.standard_normal(s) for k, s in shapes.items()}
+    _, rgo, rho, rno = LF.realise(w, h, nu, H, G, dh, L)
+    np.testing.assert_array_equal(go, rgo)
+    np.testing.assert_array_equal(ho, rho)
+    np.testing.assert_array_equal(no, rno)
+    bad = h.copy()
+    bad[0] = (bad[0] + 1) % L
+    with pytest.raises(B.AffinityError):
+        B.layout_orders(bad, nu, H, L)
+    fake = ctypes.c_void_p(1 << 20)
+    other = ctypes.c_void_p(1 << 24)
+    o = np.array([0, 2, 2, 1], np.int32)       # not a permutation
+    assert lib.affinity_gather_blocks(fake, other, 1, 4, 16, o.ctypes.data, fake, 256, None) == \
+        B.AFF_ERR_INVALID_ARG
+    o = np.array([0, 2, 3, 1], np.int32)
+    assert lib.affinity_gather_blocks(fake, fake, 1, 4, 16, o.ctypes.data, other, 256, None) == \
+        B.AFF_ERR_INVALID_ARG                   # in and out overlap
+    assert lib.affinity_gather_blocks(fake, other, 1, 4, 16, o.ctypes.data, other, 8, None) == B.AFF_ERR_WORKSPACE
+    assert lib.affinity_gather_blocks(fake, other, 1, 4, 16, o.ctypes.data, ctypes.c_void_p(1 << 28), 256,
+                                      None) == B.AFF_ERR_ARCH

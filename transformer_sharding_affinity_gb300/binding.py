@@ -109,6 +109,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                              ctypes.POINTER(aff_layout_opts), _P, _P, ctypes.POINTER(ctypes.c_double),
                                              ctypes.POINTER(ctypes.c_int32), _P, ctypes.c_size_t, _P]
     lib.affinity_optimise_layout.restype = st
+    lib.affinity_layout_orders.argtypes = [_P, _P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                           _P, _P, _P]
+    lib.affinity_layout_orders.restype = st
+    lib.affinity_gather_blocks.argtypes = [_P, _P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _P, _P,
+                                           ctypes.c_size_t, _P]
+    lib.affinity_gather_blocks.restype = st
     lib.affinity_strerror.argtypes = [ctypes.c_int32]
     lib.affinity_strerror.restype = ctypes.c_char_p
     lib.affinity_last_cuda_error.argtypes = []
@@ -336,6 +342,27 @@ def optimise_layout(Shat_up: Sequence[np.ndarray], Shat_down: Sequence[np.ndarra
                                            _ws_bytes(workspace, workspace_bytes), _stream(stream)),
            "affinity_optimise_layout")
     return h, nu, J.value, sweeps.value
+
+
+def layout_orders(h, nu, H: int, L: int):
+    """(group_order [G], head_order [H], neuron_order [I]) realising a balanced layout (affinity_layout_orders)."""
+    hh = np.ascontiguousarray(h, dtype=np.int32)
+    nn = np.ascontiguousarray(nu, dtype=np.int32)
+    go = np.empty(hh.size, np.int32)
+    ho = np.empty(int(H), np.int32)
+    no = np.empty(nn.size, np.int32)
+    _check(load().affinity_layout_orders(hh.ctypes.data, nn.ctypes.data, hh.size, int(H), nn.size, int(L),
+                                         go.ctypes.data, ho.ctypes.data, no.ctypes.data), "affinity_layout_orders")
+    return go, ho, no
+
+
+def gather_blocks(src, dst, rows: int, n_blocks: int, block_bytes: int, order, workspace, stream=None,
+                  workspace_bytes=None) -> None:
+    """Enqueue dst[r][j] = src[r][order[j]] over byte blocks (affinity_gather_blocks); order is a host array."""
+    o = np.ascontiguousarray(order, dtype=np.int32)
+    _check(load().affinity_gather_blocks(_ptr(src), _ptr(dst), int(rows), int(n_blocks), int(block_bytes),
+                                         o.ctypes.data, _ptr(workspace), _ws_bytes(workspace, workspace_bytes),
+                                         _stream(stream)), "affinity_gather_blocks")
 
 
 def set_timing_events(start_event, stop_event) -> None:

@@ -122,3 +122,30 @@ def optimise(Shat_up: List[np.ndarray], Shat_down: List[np.ndarray], L: int, h0:
     ws = torch.empty(B.layout_workspace_size(N, G, I, L), dtype=torch.uint8, device="cuda")
     h, nu, J, sweeps = B.optimise_layout(Shat_up, Shat_down, L, h0, nu0, ws, stream=stream, **opts)
     return LayoutResult(h, nu, J, sweeps)
+
+
+def realise_layout(w: Dict[str, object], h, nu, H: int, G: int, d_head: int, L: int, stream=None):
+    """Permuted copies of one layer's weights for a balanced layout (device
+    tensors, nn.Linear storage): Wq/Wk/Wv rows by KV group with their query
+    heads, Wo columns by query head, Wg/Wu rows and Wd columns by neuron, all
+    in order of device; device l's shard is the l-th contiguous slice.
+    Returns (permuted dict, group_order, head_order, neuron_order)."""
+    import torch
+
+    go, ho, no = B.layout_orders(h, nu, H, L)
+    I = int(w["Wg"].shape[0])
+    D = int(w["Wg"].shape[1])
+    es = w["Wg"].element_size()
+    ws = torch.empty(max(256, 4 * max(H, G, I)), dtype=torch.uint8, device=w["Wg"].device)
+    out = {}
+    for name, order, n in (("Wq", ho, H), ("Wk", go, G), ("Wv", go, G)):
+        out[name] = torch.empty_like(w[name])
+        B.gather_blocks(w[name], out[name], 1, n, d_head * D * es, order, ws, stream)
+    out["Wo"] = torch.empty_like(w["Wo"])
+    B.gather_blocks(w["Wo"], out["Wo"], D, H, d_head * es, ho, ws, stream)
+    for name in ("Wg", "Wu"):
+        out[name] = torch.empty_like(w[name])
+        B.gather_blocks(w[name], out[name], 1, I, D * es, no, ws, stream)
+    out["Wd"] = torch.empty_like(w["Wd"])
+    B.gather_blocks(w["Wd"], out["Wd"], D, I, es, no, ws, stream)
+    return out, go, ho, no

@@ -133,16 +133,21 @@ def sum_over_groups(S_head: np.ndarray, H: int, G: int) -> np.ndarray:
 
 def s_up(a, x, Wo, gamma, Wg, Wu, Wd, H, G, dh, eps, mode="fo", neurons=None,
          token_block=512):
-    """S_up for one layer, FO or ADD ("Affinity scores" paragraph of §3).
+    """S_up for one layer, FO, ADD or LOO ("Affinity scores" paragraph of §3).
 
     FO:  S_hk = E_t[Delta_hk^2] * ||w^d_k||^2 (eq. 5 for Delta; w^d_k the
          down-projection column), then summed over each KV group's heads.
     ADD: S_hk = E_t[(p_h . w^g_k)^2 + (p_h . w^u_k)^2], summed likewise.
+    LOO: the exact leave-one-out change of the pre-activations,
+         S_hk = E_t[(g_k - g_k^(-h))^2 + (u_k - u_k^(-h))^2], where g^(-h),
+         u^(-h) are recomputed from the residual with head h's write
+         c_h = a_h W_o^(h) removed, x - c_h, including its new rms (the
+         paper's ablation score that differs from ADD only by the rms change).
 
     ``neurons`` restricts the columns (the definition evaluated for those k
     only).  Returns (S_up [G, K], S_head [H, K]).
     """
-    if mode not in ("fo", "add"):
+    if mode not in ("fo", "add", "loo"):
         raise ValueError(mode)
     a = np.asarray(a, F)
     x = np.asarray(x, F)
@@ -154,9 +159,21 @@ def s_up(a, x, Wo, gamma, Wg, Wu, Wd, H, G, dh, eps, mode="fo", neurons=None,
     T = x.shape[0]
     K = Wg.shape[0]
     acc = np.zeros((H, K), F)
+    Wo_ = np.asarray(Wo, F)
     for t0 in range(0, T, token_block):
         ts = slice(t0, min(T, t0 + token_block))
         n, r = normalised_input(x[ts], gamma, eps)
+        if mode == "loo":
+            g = n @ Wg.T
+            u = n @ Wu.T
+            for h in range(H):
+                cols = slice(h * dh, (h + 1) * dh)
+                c = a[ts, cols] @ Wo_[:, cols].T              # head h's write into the residual
+                n_rm, _ = normalised_input(x[ts] - c, gamma, eps)
+                dg = g - n_rm @ Wg.T
+                du = u - n_rm @ Wu.T
+                acc[h] += np.sum(dg * dg + du * du, axis=0)
+            continue
         p = head_pieces(a[ts], Wo, gamma, r, H, dh)       # [Tb, H, D]
         pg = p @ Wg.T                                      # [Tb, H, K]
         pu = p @ Wu.T

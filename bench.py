@@ -269,7 +269,7 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_0p6b_layer")
-    ap.add_argument("--mode", default="fo", choices=["fo", "add"])
+    ap.add_argument("--mode", default="fo", choices=["fo", "add", "loo"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -393,8 +393,14 @@ def main() -> None:
         return
     pk = peaks()
     fl = fo_flops(shape)
-    flops_per_step = fl["total"] if args.mode == "fo" else fl["fold"] + 2 * shape.T * shape.H * shape.dh * 2 * shape.I
-    tile_flops = fl["tile_kernel"] if args.mode == "fo" else 2 * shape.T * shape.H * shape.dh * 2 * shape.I
+    heads = 2 * shape.T * shape.H * shape.dh * 2 * shape.I
+    if args.mode == "fo":
+        flops_per_step, tile_flops = fl["total"], fl["tile_kernel"]
+    elif args.mode == "add":
+        flops_per_step, tile_flops = fl["fold"] + heads, heads
+    else:   # loo: the FO-shaped pass plus c_h / r = (a_h / r) Wo^(h)^T for the rms of x - c_h
+        flops_per_step = fl["total"] + 2 * shape.T * shape.H * shape.dh * shape.D
+        tile_flops = fl["tile_kernel"]
     achieved = tile_flops / (kern_ms * 1e-3) / 1e12
     tokens = shape.T * ws
     line = {
@@ -409,14 +415,15 @@ def main() -> None:
         "step_flops": flops_per_step,
         "step_tflops": flops_per_step / (ms_step * 1e-3) / 1e12,
         "step_frac_of_peak": flops_per_step / (ms_step * 1e-3) / 1e12 / pk["bf16_tflops"],
-        "roofline": {"bound": "tensor", "kernel": "affinity_tile_kernel<FO> (operating point + per-head contraction)",
+        "roofline": {"bound": "tensor", "kernel": f"affinity_tile_kernel<{args.mode.upper()}> "
+                                                  "(operating point + per-head contraction)",
                      "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / pk["bf16_tflops"],
                      "frac_sustained": achieved / pk["bf16_tflops_sustained"] if pk["bf16_tflops_sustained"] else None,
                      "peak_source": pk["source"] + " bf16 dense (fp16 runs at the bf16 rate)",
                      "kernel_ms": kern_ms, "algorithmic_flops_per_launch": tile_flops,
                      "traffic": measured_traffic(args.workload, args.mode, shape.T)},
-        "gpu_launches": 8 * args.steps,
+        "gpu_launches": {"fo": 8, "add": 7, "loo": 10}[args.mode] * args.steps,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": shape.G * shape.I * 4, "ms_per_step": e2e_ms},
         "clocks": clocks.summary(),

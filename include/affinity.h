@@ -81,7 +81,10 @@ typedef enum {
 
 typedef enum {
   AFF_MODE_FO = 0,   /* S_hk = E_t[Delta_hk^2] * ||w^d_k||^2, Delta from eq. (5) */
-  AFF_MODE_ADD = 1   /* S_hk = E_t[(p_h.w^g_k)^2 + (p_h.w^u_k)^2] */
+  AFF_MODE_ADD = 1,  /* S_hk = E_t[(p_h.w^g_k)^2 + (p_h.w^u_k)^2] */
+  AFF_MODE_LOO = 2   /* S_hk = E_t[(g_k - g_k^(-h))^2 + (u_k - u_k^(-h))^2]: exact leave-one-out,
+                        the pre-activations recomputed from x - a_h W_o^(h) with its own rms
+                        (AFF_BF16 only) */
 } aff_mode;
 
 typedef enum { AFF_BF16 = 0, AFF_FP32 = 1 } aff_dtype;
@@ -118,6 +121,12 @@ AFF_API aff_status affinity_workspace_size(const aff_dims* dims, int32_t mode, i
  *        p_h = gamma * (a_h W_o^(h)) / r,  r = rms(x),
  *        g_k = (gamma*x/r).w^g_k,  u_k = (gamma*x/r).w^u_k.
  *   ADD: S_up[g, k] = sum_{h in g} E_t[(p_h.w^g_k)^2 + (p_h.w^u_k)^2].
+ *   LOO: S_up[g, k] = sum_{h in g} E_t[(g_k - g_k^(-h))^2 + (u_k - u_k^(-h))^2] with
+ *        g_k^(-h) = (gamma*(x - c_h)/rms(x - c_h)).w^g_k, c_h = a_h W_o^(h) (likewise u):
+ *        the exact leave-one-out change ("Affinity scores": it differs from ADD
+ *        only by the rms change).  Computed as g (1 - rho) + rho (p_h.w^g) with
+ *        rho = r / rms(x - c_h) from a tensor-core pass over c_h / r.  AFF_BF16
+ *        only (AFF_ERR_UNSUPPORTED_DTYPE for AFF_FP32).
  * E_t is the mean over the T tokens.  Wd is read only in FO mode (it may be
  * NULL in ADD mode).
  * Outputs (device, fp32): S_out [G, I] row-major; S_head_out [H, I] (the

@@ -298,3 +298,12 @@ def test_layout_orders_match_the_oracle_and_gather_checks(lib):
     assert lib.affinity_gather_blocks(fake, other, 1, 4, 16, o.ctypes.data, other, 8, None) == B.AFF_ERR_WORKSPACE
     assert lib.affinity_gather_blocks(fake, other, 1, 4, 16, o.ctypes.data, ctypes.c_void_p(1 << 28), 256,
                                       None) == B.AFF_ERR_ARCH
+
+
+def test_loo_mode_is_bf16_only(lib):
+    d = B.dims(256, 64, 4, 2, 16, 128, 1e-6, B.AFF_FP32)
+    n = ctypes.c_size_t(0)
+    assert lib.affinity_workspace_size(ctypes.byref(d), B.AFF_MODE_LOO, 0, ctypes.byref(n)) == \
+        B.AFF_ERR_UNSUPPORTED_DTYPE
+    db = B.dims(256, 64, 4, 2, 16, 128, 1e-6, B.AFF_BF16)
+    assert B.workspace_size(db, B.AFF_MODE_LOO) > B.workspace_size(db, B.AFF_MODE_ADD)

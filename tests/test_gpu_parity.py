@@ -51,7 +51,7 @@ def _assert_up(shape, mode, tol=TOL, record=None):
     return e
 
 
-@pytest.mark.parametrize("mode", ["fo", "add"])
+@pytest.mark.parametrize("mode", ["fo", "add", "loo"])
 @pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
 def test_up_small(shape, mode):
     _assert_up(shape, mode)
@@ -62,9 +62,18 @@ def test_up_tiny_fp32(mode, record_property):
     _assert_up(W.CONFIGS["tiny"], mode, tol=TOL_F32, record=record_property)
 
 
-@pytest.mark.parametrize("mode", ["fo", "add"])
+@pytest.mark.parametrize("mode", ["fo", "add", "loo"])
 def test_up_medium(mode, record_property):
     _assert_up(MEDIUM, mode, record=record_property)
+
+
+def test_loo_is_deterministic_and_differs_from_add():
+    shape = MEDIUM.scaled(T=2048)
+    layer = W.make_layer(shape)
+    outs = run_up(B, DV, shape, layer, "loo", runs=2)
+    assert np.array_equal(outs[0][0].view(np.uint32), outs[1][0].view(np.uint32))
+    (S_add, _), = run_up(B, DV, shape, layer, "add")
+    assert np.max(np.abs(outs[0][0] / S_add - 1)) > 1e-2
 
 
 def test_up_deterministic():
@@ -144,12 +153,12 @@ FULL = ["qwen3_0p6b_layer", "danube3_500m_layer", "llama3_8b_layer"]
 @pytest.mark.slow
 @pytest.mark.parametrize("name", FULL)
 def test_up_full_size_sampled(name, record_property):
-    """Full-size layer, FO (and ADD for the Danube3 shape): relative error on the
+    """Full-size layer, FO (ADD for the Danube3 shape, LOO for the Qwen3 shape): relative error on the
     sampled neurons, and the oracle's order of the sampled set reproduces the
     GPU's top-8 per group."""
     shape = W.CONFIGS[name]
     layer = W.make_layer(shape)
-    modes = ["fo", "add"] if name == "danube3_500m_layer" else ["fo"]
+    modes = {"danube3_500m_layer": ["fo", "add"], "qwen3_0p6b_layer": ["fo", "loo"]}.get(name, ["fo"])
     rng = np.random.default_rng(99)
     for mode in modes:
         (S_gpu, _), = run_up(B, DV, shape, layer, mode, per_head=False)

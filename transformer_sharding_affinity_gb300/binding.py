@@ -32,9 +32,10 @@ AFF_ERR_NO_CONVERGENCE = 10
 
 AFF_MODE_FO = 0
 AFF_MODE_ADD = 1
+AFF_MODE_LOO = 2
 AFF_BF16 = 0
 AFF_FP32 = 1
-MODES = {"fo": AFF_MODE_FO, "add": AFF_MODE_ADD}
+MODES = {"fo": AFF_MODE_FO, "add": AFF_MODE_ADD, "loo": AFF_MODE_LOO}
 
 
 class aff_dims(ctypes.Structure):

@@ -97,6 +97,7 @@ struct Layout {
   // bf16 path
   size_t W16 = 0, GWo16 = 0, M16 = 0, n16 = 0, a16 = 0, partial = 0, headsum = 0, wdn = 0;
   size_t alpha16 = 0, Wd16 = 0, WdT16 = 0, Wqkv16 = 0, ssx = 0, cpart = 0, bnorm = 0;
+  size_t Wo16 = 0, cn = 0, rho = 0, inv_r = 0;   // leave-one-out score
   // fp32 path
   size_t n32 = 0, a32 = 0, M32 = 0, ab = 0, alpha32 = 0;
   int64_t I_pad = 0, T_pad = 0, n_chunks = 0, n_tchunks = 0, Rg = 0;
@@ -126,6 +127,12 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
       L.partial = L.take((size_t)L.n_chunks * 2 * H * L.I_pad * 4);
       L.headsum = L.take((size_t)H * L.I_pad * 8);
       if (mode == AFF_MODE_FO) L.wdn = L.take((size_t)L.I_pad * 4);
+      if (mode == AFF_MODE_LOO) {
+        L.Wo16 = L.take((size_t)D * H * dh * 2);
+        L.cn = L.take((size_t)4 * H * L.T_pad * 4);
+        L.rho = L.take((size_t)H * L.T_pad * 4);
+        L.inv_r = L.take((size_t)L.T_pad * 4);
+      }
     } else {
       L.Rg = (H / G + 2) * dh;
       L.n_tchunks = ceil_div(T, kDownTokenChunk);
@@ -367,7 +374,8 @@ aff_status affinity_workspace_size(const aff_dims* dims, int32_t mode, int32_t d
   if (!bytes) return AFF_ERR_INVALID_ARG;
   aff_status st = check_dims(dims);
   if (st != AFF_OK) return st;
-  if (!down && mode != AFF_MODE_FO && mode != AFF_MODE_ADD) return AFF_ERR_INVALID_ARG;
+  if (!down && mode != AFF_MODE_FO && mode != AFF_MODE_ADD && mode != AFF_MODE_LOO) return AFF_ERR_INVALID_ARG;
+  if (!down && mode == AFF_MODE_LOO && dims->dtype != AFF_BF16) return AFF_ERR_UNSUPPORTED_DTYPE;
   *bytes = make_layout(*dims, mode, down != 0).total;
   return AFF_OK;
 }
@@ -377,8 +385,10 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
                        float* S_head_out, void* workspace, size_t workspace_bytes, aff_stream_t stream) {
   aff_status st = check_dims(dims);
   if (st != AFF_OK) return st;
-  if (mode != AFF_MODE_FO && mode != AFF_MODE_ADD) return AFF_ERR_INVALID_ARG;
+  if (mode != AFF_MODE_FO && mode != AFF_MODE_ADD && mode != AFF_MODE_LOO) return AFF_ERR_INVALID_ARG;
   const bool fo = mode == AFF_MODE_FO;
+  const bool loo = mode == AFF_MODE_LOO;
+  if (loo && dims->dtype != AFF_BF16) return AFF_ERR_UNSUPPORTED_DTYPE;
   if (!a || !x || !Wo || !gamma || !Wg || !Wu || (fo && !Wd) || !S_out) return AFF_ERR_INVALID_ARG;
   const void* ptrs[] = {a, x, Wo, gamma, Wg, Wu, fo ? Wd : nullptr, S_out, S_head_out};
   for (const void* p : ptrs)
@@ -434,8 +444,12 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   AFF_CUDA(launch_prep_gate_up((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, status, ws2));
   AFF_CUDA(launch_scaled_transpose_split((const uint16_t*)Wo, g_b, GWo16, D, H * dh, status, ws2));
   if (fo) AFF_CUDA(launch_wd_colnorm((const uint16_t*)Wd, wdn, D, I, I_pad, ws2));
+  __half* Wo16 = loo ? reinterpret_cast<__half*>(ws + L.Wo16) : nullptr;
+  float* inv_r = loo ? reinterpret_cast<float*>(ws + L.inv_r) : nullptr;
+  if (loo) AFF_CUDA(launch_to_fp16((const uint16_t*)Wo, Wo16, (size_t)D * H * dh, status, ws2));
   // token side on the caller's stream meanwhile
-  AFF_CUDA(launch_prep_tokens(x_b, a_b, g_b, fo ? n16 : nullptr, a16, nullptr, T, D, H * dh, d.eps, status, s));
+  AFF_CUDA(launch_prep_tokens(x_b, a_b, g_b, (fo || loo) ? n16 : nullptr, a16, inv_r, T, D, H * dh, d.eps, status,
+                              s));
 
   CUtensorMap maps[4];
   std::memset(maps, 0, sizeof maps);
@@ -454,14 +468,33 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   }
   AFF_CUDA(cudaEventRecord(side->join, ws2));
   AFF_CUDA(cudaStreamWaitEvent(s, side->join, 0));
-  // FO / ADD: per token tile, operating point (FO) then every head.  With CTA
-  // pairs each CTA loads half (64 rows) of every token tile.
+  float* rho = loo ? reinterpret_cast<float*>(ws + L.rho) : nullptr;
+  if (loo) {
+    // rho[h][t] = r / rms(x - c_h): tensor-core pass over (a_h / r) Wo^(h)^T with the
+    // per-token sums over d in the epilogue, then a small kernel
+    float* cn = reinterpret_cast<float*>(ws + L.cn);
+    uint64_t da[3] = {(uint64_t)dh, (uint64_t)H, (uint64_t)T};
+    uint64_t sa[2] = {(uint64_t)dh * 2, (uint64_t)H * dh * 2};
+    if ((st = make_map(&maps[0], a16, 3, da, sa, 128, 2)) != AFF_OK) return st;
+    if ((st = map2(&maps[1], Wo16, (uint64_t)H * dh, (uint64_t)D)) != AFF_OK) return st;
+    maps[2] = maps[0];
+    maps[3] = maps[0];
+    TileParams p = base_params(d, L, ws, kModeCNorm);
+    p.n_ntiles = (int)ceil_div(D, 128);
+    p.n_units = (int)(ceil_div(L.T_pad, 256) * H);
+    p.partial = cn;
+    p.x_bf16 = x_b;
+    if ((st = run_tile(maps, p, s)) != AFF_OK) return st;
+    AFF_CUDA(launch_loo_rho(cn, inv_r, rho, T, (int)L.T_pad, H, D, s));
+  }
+  // FO / ADD / LOO: per token tile, operating point (FO, LOO) then every head.
+  // With CTA pairs (FO / ADD) each CTA loads half (64 rows) of every token tile.
   {
-    const bool pair = use_pairs();
+    const bool pair = use_pairs() && !loo;
     const uint32_t brows = pair ? 64u : 128u;
     uint64_t dx[2] = {(uint64_t)D, (uint64_t)T}, sx[1] = {(uint64_t)D * 2};
     if ((st = map2(&maps[0], W16, (uint64_t)D, (uint64_t)2 * I_pad)) != AFF_OK) return st;
-    if (fo) {
+    if (fo || loo) {
       if ((st = make_map(&maps[1], n16, 2, dx, sx, brows, 1)) != AFF_OK) return st;
     } else {
       maps[1] = maps[0];
@@ -472,8 +505,9 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     uint64_t da[3] = {(uint64_t)dh, (uint64_t)H, (uint64_t)T};
     uint64_t sa[2] = {(uint64_t)dh * 2, (uint64_t)H * dh * 2};
     if ((st = make_map(&maps[3], a16, 3, da, sa, brows, 2)) != AFF_OK) return st;
-    TileParams p = base_params(d, L, ws, fo ? kModeFO : kModeADD);
+    TileParams p = base_params(d, L, ws, fo ? kModeFO : (loo ? kModeLOO : kModeADD));
     p.pair = pair ? 1 : 0;
+    p.rho = rho;
     p.stages = pick_stages(p.mode, p.H, pair);
     p.n_units = (int)(L.n_chunks * (pair ? p.n_ktiles / 2 : p.n_ktiles));
     p.partial = partial;

@@ -227,6 +227,42 @@ __global__ void finalize_up_kernel(const double* __restrict__ sh, const float* _
   S_out[(size_t)g * I + k] = (float)s;
 }
 
+// ---------------------------------------------------------------- leave-one-out score
+// out = fp16 copy of n bf16 values (n % 8 == 0), 8 per thread.
+__global__ void to_fp16_kernel(const uint16_t* __restrict__ in, __half* __restrict__ out, size_t n,
+                               uint32_t* status) {
+  bool bad = false;
+  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n / 8; v += (size_t)gridDim.x * blockDim.x) {
+    uint4 q = *reinterpret_cast<const uint4*>(in + v * 8);
+    const uint16_t* e = reinterpret_cast<const uint16_t*>(&q);
+    __align__(16) __half o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = to_h(bf2f(e[i]), bad);
+    *reinterpret_cast<uint4*>(out + v * 8) = *reinterpret_cast<uint4*>(o);
+  }
+  if (bad) latch_status(status, kStatusRange);
+}
+
+// rho[h][t] = r_t / rms(x_t - c_th), from the two column halves of
+// CC = sum_d (c/r)^2 and XD = sum_d x (c/r):  since mean_d x^2 = r^2 - eps,
+//   rms(x - c)^2 / r^2 = 1 + (CC - 2 XD / r) / D.
+// Padding tokens (t >= T) get rho = 1; they carry no signal.
+__global__ void loo_rho_kernel(const float* __restrict__ cn, const float* __restrict__ inv_r, float* __restrict__ rho,
+                               int T, int T_pad, int H, int D) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  const int h = blockIdx.y;
+  if (t >= T_pad) return;
+  float v = 1.0f;
+  if (t < T) {
+    const size_t plane = (size_t)H * T_pad, at = (size_t)h * T_pad + t;
+    const float cc = cn[0 * plane + at] + cn[2 * plane + at];   // halves 0 and 1 of quantity 0
+    const float xd = cn[1 * plane + at] + cn[3 * plane + at];   // halves 0 and 1 of quantity 1
+    const float q = 1.0f + (cc - 2.0f * xd * inv_r[t]) / (float)D;
+    v = rsqrtf(fmaxf(q, 1e-30f));
+  }
+  rho[(size_t)h * T_pad + t] = v;
+}
+
 // ---------------------------------------------------------------- down edge
 // Wd16 [D][I_pad] and WdT16 [I_pad][D]: fp16 copies of Wd (zero padded).
 __global__ void prep_wd_kernel(const uint16_t* __restrict__ Wd, __half* __restrict__ Wd16,
@@ -509,6 +545,18 @@ cudaError_t launch_finalize_up(const double* sh, const float* wdn, int fo, int T
                                float* S_out, float* S_head_out, cudaStream_t s) {
   dim3 grid((I + 127) / 128, G);
   finalize_up_kernel<<<grid, 128, 0, s>>>(sh, wdn, fo, T, H, G, I, I_pad, S_out, S_head_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_fp16(const uint16_t* in, __half* out, size_t n, uint32_t* status, cudaStream_t s) {
+  const size_t blocks = (n / 8 + 255) / 256;
+  to_fp16_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(in, out, n, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_loo_rho(const float* cn, const float* inv_r, float* rho, int T, int T_pad, int H, int D,
+                           cudaStream_t s) {
+  loo_rho_kernel<<<dim3((T_pad + 255) / 256, H), 256, 0, s>>>(cn, inv_r, rho, T, T_pad, H, D);
   return cudaGetLastError();
 }
 

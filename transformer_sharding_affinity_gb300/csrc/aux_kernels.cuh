@@ -19,6 +19,9 @@ cudaError_t launch_reduce_partials(const float* partial, double* out, int n_chun
                                    cudaStream_t s);
 cudaError_t launch_finalize_up(const double* sh, const float* wdn, int fo, int T, int H, int G, int I, int I_pad,
                                float* S_out, float* S_head_out, cudaStream_t s);
+cudaError_t launch_to_fp16(const uint16_t* in, __half* out, size_t n, uint32_t* status, cudaStream_t s);
+cudaError_t launch_loo_rho(const float* cn, const float* inv_r, float* rho, int T, int T_pad, int H, int D,
+                           cudaStream_t s);
 cudaError_t launch_prep_wd(const uint16_t* Wd, __half* Wd16, __half* WdT16, int D, int I, int I_pad, uint32_t* status,
                            cudaStream_t s);
 cudaError_t launch_prep_qkv(const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* gamma_next,

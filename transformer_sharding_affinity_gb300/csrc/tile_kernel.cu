@@ -26,7 +26,7 @@
 
 namespace aff {
 
-enum JobKind : int { kJobGateUp = 0, kJobHead = 1, kJobFold = 2, kJobXPrime = 3, kJobQNorm = 4 };
+enum JobKind : int { kJobGateUp = 0, kJobHead = 1, kJobFold = 2, kJobXPrime = 3, kJobQNorm = 4, kJobCNorm = 5 };
 
 struct Job {
   int kind;
@@ -42,10 +42,11 @@ struct Job {
 
 struct Unit {
   int njobs;
-  int chunk;    // FO/ADD: token chunk index
+  int chunk;    // FO/ADD/LOO: token chunk index
   int kt;
-  int tile0;    // FO/ADD/alpha: first token tile
-  int base;     // x': first token; qnorm: first neuron
+  int tile0;    // FO/ADD/LOO/alpha: first token tile
+  int base;     // x', cnorm: first token; qnorm: first neuron
+  int head;     // cnorm: head
 };
 
 // Unit u of the schedule.  With CTA pairs (FO / ADD) a unit covers 256 neurons:
@@ -69,16 +70,22 @@ __device__ __forceinline__ Unit unit_info(const TileParams& p, int u, int rank) 
       U.base = u / p.n_ktiles;  // column tile
       break;
     case kModeFO:
+    case kModeLOO:
     case kModeADD:
     case kModeAlpha: {
       U.kt = u % p.n_ktiles;
       U.chunk = u / p.n_ktiles;
       U.tile0 = U.chunk * p.tiles_per_unit;
       int nt = min(p.tiles_per_unit, p.n_ttiles - U.tile0);
-      int per = p.mode == kModeFO ? 1 + p.H : (p.mode == kModeADD ? p.H : 1);
+      int per = (p.mode == kModeFO || p.mode == kModeLOO) ? 1 + p.H : (p.mode == kModeADD ? p.H : 1);
       U.njobs = nt * per;
       break;
     }
+    case kModeCNorm:   // consecutive units: the heads of one 256-token block
+      U.head = u % p.H;
+      U.base = (u / p.H) * 2 * kBlockM;
+      U.njobs = p.n_ntiles;
+      break;
     case kModeXPrime:
       U.base = u * 2 * kBlockM;
       U.njobs = p.n_ntiles;
@@ -105,7 +112,7 @@ __device__ __forceinline__ Job job_next(const TileParams& p, const Unit& U, JobI
   J.kt = U.kt;
   if constexpr (MODE == kModeFold) {
     J.kind = kJobFold; J.nkb = 2 * p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D; J.nt = U.base;
-  } else if constexpr (MODE == kModeFO) {
+  } else if constexpr (MODE == kModeFO || MODE == kModeLOO) {
     J.t0 = (U.tile0 + it.a) * kBlockN;
     if (it.b == 0) {
       J.kind = kJobGateUp; J.nkb = p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D;
@@ -124,6 +131,9 @@ __device__ __forceinline__ Job job_next(const TileParams& p, const Unit& U, JobI
   } else if constexpr (MODE == kModeXPrime) {
     J.kind = kJobXPrime; J.nkb = p.nkb_I; J.nkb_part = p.nkb_I; J.last_nks = 4;
     J.t0 = U.base; J.nt = it.b++;
+  } else if constexpr (MODE == kModeCNorm) {
+    J.kind = kJobCNorm; J.nkb = p.nkb_dh; J.nkb_part = p.nkb_dh; J.last_nks = p.ls_dh;
+    J.t0 = U.base; J.head = U.head; J.nt = it.b++;
   } else {   // kModeQNorm
     J.kind = kJobQNorm; J.nkb = 2 * p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D;
     J.g = it.a; J.nt = it.b;
@@ -165,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   sm.stage0 = base;
   uint8_t* cur = base + (size_t)S * kSB;
   sm.sacc = reinterpret_cast<float*>(cur);
-  int sacc_floats = (MODE == kModeFO || MODE == kModeADD) ? 2 * p.H * kBlockM : 0;
+  int sacc_floats = (MODE == kModeFO || MODE == kModeADD || MODE == kModeLOO) ? 2 * p.H * kBlockM : 0;
   cur += (size_t)sacc_floats * 4;
   sm.full = reinterpret_cast<uint64_t*>(cur);
   sm.empty = sm.full + S;
@@ -274,6 +284,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                   tma_load_2d(st, &map0, fb, kx, J.t0);
                   tma_load_2d(st + kTileBytes, &map0, fb, kx, J.t0 + kBlockM);
                   tma_load_2d(st + kBOff, &map1, fb, kx, J.nt * kBlockN);
+                  break;
+                case kJobCNorm:    // A = a16 head h token rows (two tiles), B = Wo16 rows d, head h's columns
+                  tma_load_3d(st, &map0, fb, kx, J.head, J.t0);
+                  tma_load_3d(st + kTileBytes, &map0, fb, kx, J.head, J.t0 + kBlockM);
+                  tma_load_2d(st + kBOff, &map1, fb, J.head * p.dh + kx, J.nt * kBlockN);
                   break;
                 case kJobQNorm:    // A = Wd^T neuron rows (two tiles), B = group g's gamma'-scaled q/k/v rows (hi | lo)
                   tma_load_2d(st, &map0, fb, kx, U.base);
@@ -384,7 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t abA[32], abB[32];         // FO: f32x2 pairs of silu'(g)u and silu(g), 64 tokens
 #pragma unroll
     for (int i = 0; i < 32; ++i) { abA[i] = 0ull; abB[i] = 0ull; }
-    float ss1 = 0.f, ss2 = 0.f;        // x' / qnorm running sums
+    float ss1 = 0.f, ss2 = 0.f;        // x' / qnorm / cnorm running sums
+    float xd1 = 0.f, xd2 = 0.f;        // cnorm: sum_d x (c/r)
     int b = 0;
     uint32_t tph = 0;                  // TMEM buffer phase (flips every second job)
     bool ok = true;
@@ -405,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t c1 = tl + (uint32_t)(b * 2 * kBlockN + hf * 64);
         const uint32_t c2 = c1 + kBlockN;
 
-        if constexpr (MODE == kModeFO) {
+        if constexpr (MODE == kModeFO || MODE == kModeLOO) {
           if (J.kind == kJobGateUp) {
             // Phase 1: stash g, u in the registers that will hold A', B' and hand the
             // accumulator buffer back at once, so the MMAs of the next two head
@@ -432,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 abB[c * 8 + i / 2] = pk_u(ur[i], ur[i + 1]);
               }
             }
+            if constexpr (MODE == kModeLOO) continue;   // LOO uses g and u themselves
             // Phase 2: (g, u) -> (A', B') = (silu'(g) u, silu(g)) in place.
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -477,16 +494,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             continue;
           }
         }
-        if constexpr (MODE == kModeFO || MODE == kModeADD) {
-          // kJobHead: per token Delta = A' pg + B' pu (FO) or pg^2 + pu^2 (ADD), summed over tokens
+        if constexpr (MODE == kModeFO || MODE == kModeADD || MODE == kModeLOO) {
+          // kJobHead: per token Delta = A' pg + B' pu (FO) or pg^2 + pu^2 (ADD), summed over tokens;
+          // LOO: g - g^(-h) = g (1 - rho) + rho pg with rho = r / rms(x - c_h), likewise for u
           uint64_t acc = pk(0.f, 0.f);
+          // columns per TMEM read: 8, or 4 in LOO mode (its arithmetic needs more registers)
+          constexpr int kW = MODE == kModeLOO ? 4 : 8;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t pg[8], pu[8];
-            tmem_ld8(c1 + c * 8, pg);
-            tmem_ld8(c2 + c * 8, pu);
+          for (int c = 0; c < 64 / kW; ++c) {
+            uint32_t pg[kW], pu[kW];
+            if constexpr (kW == 8) {
+              tmem_ld8(c1 + c * kW, pg);
+              tmem_ld8(c2 + c * kW, pu);
+            } else {
+              tmem_ld4(c1 + c * kW, pg);
+              tmem_ld4(c2 + c * kW, pu);
+            }
             tmem_ld_wait();
-            if (c == 7) {
+            if (c == 64 / kW - 1) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) {
@@ -496,14 +521,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                   mbar_arrive(&sm.tempty[b]);
               }
             }
+            float4 rq = make_float4(0.f, 0.f, 0.f, 0.f);   // LOO: rho of the chunk's 4 tokens
+            if constexpr (MODE == kModeLOO)   // the same address in every lane: a broadcast
+              rq = __ldg(reinterpret_cast<const float4*>(p.rho + (size_t)J.head * p.T_pad + J.t0 + hf * 64) + c);
 #pragma unroll
-            for (int i = 0; i < 8; i += 2) {
+            for (int i = 0; i < kW; i += 2) {
               const uint64_t vg = pk_u(pg[i], pg[i + 1]);
               const uint64_t vu = pk_u(pu[i], pu[i + 1]);
+              const int ai = (c * kW + i) / 2;   // token pair within the thread's 64 tokens
               if constexpr (MODE == kModeFO) {
-                uint64_t d = mul2(abA[c * 4 + i / 2], vg);
-                d = fma2(abB[c * 4 + i / 2], vu, d);
+                uint64_t d = mul2(abA[ai], vg);
+                d = fma2(abB[ai], vu, d);
                 acc = fma2(d, d, acc);
+              } else if constexpr (MODE == kModeLOO) {
+                const float r0 = i == 0 ? rq.x : rq.z, r1 = i == 0 ? rq.y : rq.w;
+                const uint64_t rr = pk(r0, r1), om = pk(1.0f - r0, 1.0f - r1);
+                const uint64_t dg = fma2(abA[ai], om, mul2(vg, rr));
+                const uint64_t du = fma2(abB[ai], om, mul2(vu, rr));
+                acc = fma2(dg, dg, acc);
+                acc = fma2(du, du, acc);
               } else {
                 acc = fma2(vg, vg, acc);
                 acc = fma2(vu, vu, acc);
@@ -590,6 +626,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if constexpr (MODE == kModeCNorm) {
+          // D1 = (c_h / r)[t1][d], D2 = ...[t2][d]: accumulate sum_d (c/r)^2 and sum_d x (c/r)
+          const int t1 = J.t0 + row, t2 = J.t0 + kBlockM + row;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v1[16], v2[16];
+            tmem_ld16(c1 + c * 16, v1);
+            tmem_ld16(c2 + c * 16, v2);
+            tmem_ld_wait();
+            if (c == 3) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&sm.tempty[b]);
+            }
+            // columns past D hold zeros (the B tile was zero-filled), so only x needs a guard;
+            // D % 8 == 0, so an 8-column group is either wholly inside or wholly past D
+            const int d0 = J.nt * kBlockN + hf * 64 + c * 16;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float a1 = __uint_as_float(v1[i]), a2 = __uint_as_float(v2[i]);
+              ss1 = fmaf(a1, a1, ss1);
+              ss2 = fmaf(a2, a2, ss2);
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const int d = d0 + q * 8;
+              if (d < p.D) {
+                if (t1 < p.T) {
+                  const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.x_bf16 + (size_t)t1 * p.D + d));
+                  const uint32_t e[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    xd1 = fmaf(__uint_as_float(e[i] << 16), __uint_as_float(v1[q * 8 + 2 * i]), xd1);
+                    xd1 = fmaf(__uint_as_float(e[i] & 0xFFFF0000u), __uint_as_float(v1[q * 8 + 2 * i + 1]), xd1);
+                  }
+                }
+                if (t2 < p.T) {
+                  const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.x_bf16 + (size_t)t2 * p.D + d));
+                  const uint32_t e[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    xd2 = fmaf(__uint_as_float(e[i] << 16), __uint_as_float(v2[q * 8 + 2 * i]), xd2);
+                    xd2 = fmaf(__uint_as_float(e[i] & 0xFFFF0000u), __uint_as_float(v2[q * 8 + 2 * i + 1]), xd2);
+                  }
+                }
+              }
+            }
+          }
+        }
         if constexpr (MODE == kModeQNorm) {
           // D1 = Q[k1][r], D2 = Q[k2][r] for the rows r of group J.g; sum Q^2 over the group's rows
 #pragma unroll
@@ -627,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---- end of unit
-      if constexpr (MODE == kModeFO || MODE == kModeADD) {
+      if constexpr (MODE == kModeFO || MODE == kModeADD || MODE == kModeLOO) {
         float* dst = p.partial + ((size_t)(U.chunk * 2 + hf) * p.H) * p.I_pad + U.kt * kBlockM + row;
         for (int h = 0; h < p.H; ++h) {
           float* sp = &sm.sacc[(hf * p.H + h) * kBlockM + row];
@@ -641,6 +726,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t2 < p.T_pad) p.partial[(size_t)hf * p.T_pad + t2] = ss2;
         ss1 = 0.f;
         ss2 = 0.f;
+      }
+      if constexpr (MODE == kModeCNorm) {
+        // [hf][quantity][H][T_pad]: quantity 0 = sum (c/r)^2, 1 = sum x (c/r)
+        const int t1 = U.base + row, t2 = U.base + kBlockM + row;
+        float* cc = p.partial + ((size_t)(hf * 2 + 0) * p.H + U.head) * p.T_pad;
+        float* xd = p.partial + ((size_t)(hf * 2 + 1) * p.H + U.head) * p.T_pad;
+        if (t1 < p.T_pad) { cc[t1] = ss1; xd[t1] = xd1; }
+        if (t2 < p.T_pad) { cc[t2] = ss2; xd[t2] = xd2; }
+        ss1 = ss2 = xd1 = xd2 = 0.f;
       }
     }
   }
@@ -660,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 size_t tile_smem_bytes(int mode, int stages, int H, bool pair) {
-  size_t sacc = (mode == kModeFO || mode == kModeADD) ? (size_t)2 * H * kBlockM * 4 : 0;
+  size_t sacc = (mode == kModeFO || mode == kModeADD || mode == kModeLOO) ? (size_t)2 * H * kBlockM * 4 : 0;
   return 1024 + (size_t)stages * (pair ? kPairStageBytes : kStageBytes) + sacc + (size_t)(2 * stages + 5) * 8 + 8;
 }
 
@@ -717,6 +811,8 @@ cudaError_t launch_tile_kernel(const CUtensorMap* maps, const TileParams& p, int
     case kModeAlpha: return launch_mode<kModeAlpha, false>(maps, p, grid, stream);
     case kModeXPrime: return launch_mode<kModeXPrime, false>(maps, p, grid, stream);
     case kModeQNorm: return launch_mode<kModeQNorm, false>(maps, p, grid, stream);
+    case kModeCNorm: return launch_mode<kModeCNorm, false>(maps, p, grid, stream);
+    case kModeLOO: return launch_mode<kModeLOO, false>(maps, p, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -30,7 +30,9 @@ enum TileMode : int {
   kModeADD = 2,    // per token tile: every head's (p.w^g)^2 + (p.w^u)^2
   kModeAlpha = 3,  // per token tile: alpha = silu(g) u  -> fp16 [T_pad][I_pad]
   kModeXPrime = 4, // x' = x + alpha Wd^T for 256 tokens, sum_d x'^2 -> 1/r'^2
-  kModeQNorm = 5   // ||b_gk||^2 = sum over group g's q/k/v rows r of ((Wqkv' diag(gamma'))_r . w^d_k)^2
+  kModeQNorm = 5,  // ||b_gk||^2 = sum over group g's q/k/v rows r of ((Wqkv' diag(gamma'))_r . w^d_k)^2
+  kModeCNorm = 6,  // per (256 tokens, head h): c_h/r = (a_h/r) Wo^(h)^T; sum_d (c/r)^2 and sum_d x (c/r)
+  kModeLOO = 7     // per token tile: operating point g, u, then every head's exact leave-one-out change
 };
 
 struct TileParams {
@@ -53,6 +55,7 @@ struct TileParams {
   const uint16_t* x_bf16;  // x' epilogue reads x (bf16 bits) [T][D]
   float* inv_rp2;          // x' output 1/r'^2 [T_pad]
   float* bnorm;            // qnorm output [I_pad][G]
+  const float* rho;        // LOO: r / rms(x - c_h), [H][T_pad]
   float eps;
 };
 

@@ -14,6 +14,7 @@
 #include <cstdlib>
 #include <cstdio>
 #include <cstring>
+#include <deque>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -311,7 +312,7 @@ struct SideStream {
 };
 
 aff_status side_stream(SideStream** out) {
-  thread_local std::vector<SideStream> per_dev;
+  thread_local std::deque<SideStream> per_dev;   // a deque keeps earlier entries in place
   int dev = 0;
   AFF_CUDA(cudaGetDevice(&dev));
   for (auto& ss : per_dev)

@@ -448,22 +448,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 abB[c * 8 + i / 2] = pk_u(ur[i], ur[i + 1]);
               }
             }
-            if constexpr (MODE == kModeLOO) continue;   // LOO uses g and u themselves
-            // Phase 2: (g, u) -> (A', B') = (silu'(g) u, silu(g)) in place.
+            // Phase 2 (FO): (g, u) -> (A', B') = (silu'(g) u, silu(g)) in place; LOO keeps g and u.
+            if constexpr (MODE == kModeFO) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float2 g2 = unpk(abA[i]), u2 = unpk(abB[i]);
-              float gA[2], gB[2];
+              for (int i = 0; i < 32; ++i) {
+                const float2 g2 = unpk(abA[i]), u2 = unpk(abB[i]);
+                float gA[2], gB[2];
 #pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const float g = e ? g2.y : g2.x;
-                const float uu = e ? u2.y : u2.x;
-                const float sg = __fdividef(1.0f, 1.0f + __expf(-g));  // sigmoid(g)
-                gA[e] = sg * fmaf(g, 1.0f - sg, 1.0f) * uu;           // silu'(g) u
-                gB[e] = g * sg;                                       // silu(g)
+                for (int e = 0; e < 2; ++e) {
+                  const float g = e ? g2.y : g2.x;
+                  const float uu = e ? u2.y : u2.x;
+                  const float sg = __fdividef(1.0f, 1.0f + __expf(-g));  // sigmoid(g)
+                  gA[e] = sg * fmaf(g, 1.0f - sg, 1.0f) * uu;           // silu'(g) u
+                  gB[e] = g * sg;                                       // silu(g)
+                }
+                abA[i] = pk(gA[0], gA[1]);
+                abB[i] = pk(gB[0], gB[1]);
               }
-              abA[i] = pk(gA[0], gA[1]);
-              abB[i] = pk(gB[0], gB[1]);
             }
             continue;
           }
@@ -496,9 +497,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if constexpr (MODE == kModeFO || MODE == kModeADD || MODE == kModeLOO) {
           // kJobHead: per token Delta = A' pg + B' pu (FO) or pg^2 + pu^2 (ADD), summed over tokens;
-          // LOO: g - g^(-h) = g (1 - rho) + rho pg with rho = r / rms(x - c_h), likewise for u
+          // LOO: g - g^(-h) = g (1 - rho) + rho pg = g + rho (pg - g) with rho = r / rms(x - c_h),
+          // likewise for u
           uint64_t acc = pk(0.f, 0.f);
-          // columns per TMEM read: 8, or 4 in LOO mode (its arithmetic needs more registers)
+          // TMEM columns per read: 8, or 4 in LOO mode (its arithmetic needs more registers)
           constexpr int kW = MODE == kModeLOO ? 4 : 8;
 #pragma unroll
           for (int c = 0; c < 64 / kW; ++c) {
@@ -534,10 +536,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 d = fma2(abB[ai], vu, d);
                 acc = fma2(d, d, acc);
               } else if constexpr (MODE == kModeLOO) {
-                const float r0 = i == 0 ? rq.x : rq.z, r1 = i == 0 ? rq.y : rq.w;
-                const uint64_t rr = pk(r0, r1), om = pk(1.0f - r0, 1.0f - r1);
-                const uint64_t dg = fma2(abA[ai], om, mul2(vg, rr));
-                const uint64_t du = fma2(abB[ai], om, mul2(vu, rr));
+                const uint64_t rr = i == 0 ? pk(rq.x, rq.y) : pk(rq.z, rq.w), neg1 = pk(-1.0f, -1.0f);
+                const uint64_t dg = fma2(rr, fma2(abA[ai], neg1, vg), abA[ai]);
+                const uint64_t du = fma2(rr, fma2(abB[ai], neg1, vu), abB[ai]);
                 acc = fma2(dg, dg, acc);
                 acc = fma2(du, du, acc);
               } else {

@@ -182,3 +182,23 @@ def test_down_full_size_sampled(record_property):
     e = rel_err(S_gpu[idx], S_ref, floor_ref=float(S_gpu.max()))
     record_property("qwen3_0p6b_layer_down_max_rel_err", e)
     assert e <= TOL, f"down full size: max rel err {e:.3e}"
+
+
+_SWEEP = [W.random_small_shape(np.random.default_rng(1000 + i), name=f"rand{i}") for i in range(12)]
+
+
+@pytest.mark.parametrize("shape", _SWEEP, ids=[s.name for s in _SWEEP])
+def test_up_random_shapes(shape):
+    """Seeded random small shapes (ragged T, D, d_head and I; 1-12 heads in
+    1-4 groups): every mode against the oracle."""
+    for mode in ("fo", "add", "loo"):
+        _assert_up(shape, mode)
+
+
+@pytest.mark.parametrize("shape", _SWEEP[:6], ids=[s.name for s in _SWEEP[:6]])
+def test_down_random_shapes(shape):
+    layer = W.make_layer(shape, with_next=True)
+    S_gpu, = run_down(B, DV, shape, layer)
+    S_ref = oracle_down(O, shape, layer)
+    err = rowmax_err(S_gpu.T, S_ref.T) if shape.T < FEW_TOKENS else rel_err(S_gpu, S_ref)
+    assert err <= TOL, f"{shape.name} down: {err:.3e}"

@@ -242,6 +242,17 @@ bool use_pairs() {
   return v;
 }
 
+// Heads whose width is a multiple of 16 but not of 64 (e.g. 96) leave the last
+// 64-wide K block of every head job partly empty.  Streaming all heads' K
+// ranges back to back fills every block; AFFINITY_STREAM_HEADS=0 turns it off.
+bool stream_heads(const aff_dims& d) {
+  static const bool allowed = [] {
+    const char* e = std::getenv("AFFINITY_STREAM_HEADS");
+    return !(e && e[0] == '0');
+  }();
+  return allowed && d.d_head % 16 == 0 && d.d_head % 64 != 0;
+}
+
 TileParams base_params(const aff_dims& d, const Layout& L, uint8_t* ws, int mode) {
   TileParams p{};
   p.mode = mode;
@@ -262,6 +273,13 @@ TileParams base_params(const aff_dims& d, const Layout& L, uint8_t* ws, int mode
   p.ls_D = (int)(((d.D - 1) % 64) / 16 + 1);          // 16-wide K slices in the last block of D
   p.ls_dh = (int)(((d.d_head - 1) % 64) / 16 + 1);    // ... and of d_head
   p.stages = pick_stages(mode, p.H, false);
+  if (stream_heads(d)) {
+    const int64_t slices = d.H * d.d_head / 16;
+    p.stream_heads = 1;
+    p.nkb_HD = (int)ceil_div(slices, 4);
+    p.ls_HD = (int)((slices - 1) % 4 + 1);
+    p.spp = (int)(d.d_head / 16);
+  }
   p.status = reinterpret_cast<uint32_t*>(ws + L.status);
   p.eps = d.eps;
   return p;
@@ -491,7 +509,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   // FO / ADD / LOO: per token tile, operating point (FO, LOO) then every head.
   // With CTA pairs (FO / ADD) each CTA loads half (64 rows) of every token tile.
   {
-    const bool pair = use_pairs() && !loo;
+    const bool pair = use_pairs() && !loo && !stream_heads(d);
     const uint32_t brows = pair ? 64u : 128u;
     uint64_t dx[2] = {(uint64_t)D, (uint64_t)T}, sx[1] = {(uint64_t)D * 2};
     if ((st = map2(&maps[0], W16, (uint64_t)D, (uint64_t)2 * I_pad)) != AFF_OK) return st;
@@ -500,12 +518,18 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     } else {
       maps[1] = maps[0];
     }
-    uint64_t dm[3] = {(uint64_t)dh, (uint64_t)I_pad, (uint64_t)2 * H};
-    uint64_t sd[2] = {(uint64_t)dh * 2, (uint64_t)I_pad * dh * 2};
-    if ((st = make_map(&maps[2], M16, 3, dm, sd, 128, 1)) != AFF_OK) return st;
-    uint64_t da[3] = {(uint64_t)dh, (uint64_t)H, (uint64_t)T};
-    uint64_t sa[2] = {(uint64_t)dh * 2, (uint64_t)H * dh * 2};
-    if ((st = make_map(&maps[3], a16, 3, da, sa, brows, 2)) != AFF_OK) return st;
+    if (stream_heads(d)) {
+      // M16 as [2 * I_pad][H*dh] and a16 as [T][H*dh]: K blocks run across head boundaries
+      if ((st = map2(&maps[2], M16, (uint64_t)H * dh, (uint64_t)2 * I_pad)) != AFF_OK) return st;
+      if ((st = map2(&maps[3], a16, (uint64_t)H * dh, (uint64_t)T)) != AFF_OK) return st;
+    } else {
+      uint64_t dm[3] = {(uint64_t)dh, (uint64_t)I_pad, (uint64_t)2 * H};
+      uint64_t sd[2] = {(uint64_t)dh * 2, (uint64_t)I_pad * dh * 2};
+      if ((st = make_map(&maps[2], M16, 3, dm, sd, 128, 1)) != AFF_OK) return st;
+      uint64_t da[3] = {(uint64_t)dh, (uint64_t)H, (uint64_t)T};
+      uint64_t sa[2] = {(uint64_t)dh * 2, (uint64_t)H * dh * 2};
+      if ((st = make_map(&maps[3], a16, 3, da, sa, brows, 2)) != AFF_OK) return st;
+    }
     TileParams p = base_params(d, L, ws, fo ? kModeFO : (loo ? kModeLOO : kModeADD));
     p.pair = pair ? 1 : 0;
     p.rho = rho;

@@ -26,7 +26,10 @@
 
 namespace aff {
 
-enum JobKind : int { kJobGateUp = 0, kJobHead = 1, kJobFold = 2, kJobXPrime = 3, kJobQNorm = 4, kJobCNorm = 5 };
+enum JobKind : int {
+  kJobGateUp = 0, kJobHead = 1, kJobFold = 2, kJobXPrime = 3, kJobQNorm = 4, kJobCNorm = 5,
+  kJobStream = 6   // producer / MMA view of all H head jobs of a token tile, K ranges back to back
+};
 
 struct Job {
   int kind;
@@ -41,7 +44,8 @@ struct Job {
 };
 
 struct Unit {
-  int njobs;
+  int njobs;     // jobs as the epilogue sees them
+  int njobs_pm;  // jobs as the producer and the MMA issuer see them (fewer when heads are streamed)
   int chunk;    // FO/ADD/LOO: token chunk index
   int kt;
   int tile0;    // FO/ADD/LOO/alpha: first token tile
@@ -61,6 +65,7 @@ __device__ __forceinline__ Unit unit_info(const TileParams& p, int u, int rank) 
     U.tile0 = U.chunk * p.tiles_per_unit;
     const int nt = min(p.tiles_per_unit, p.n_ttiles - U.tile0);
     U.njobs = nt * (p.mode == kModeFO ? 1 + p.H : p.H);
+    U.njobs_pm = U.njobs;
     return U;
   }
   switch (p.mode) {
@@ -77,9 +82,11 @@ __device__ __forceinline__ Unit unit_info(const TileParams& p, int u, int rank) 
       U.chunk = u / p.n_ktiles;
       U.tile0 = U.chunk * p.tiles_per_unit;
       int nt = min(p.tiles_per_unit, p.n_ttiles - U.tile0);
-      int per = (p.mode == kModeFO || p.mode == kModeLOO) ? 1 + p.H : (p.mode == kModeADD ? p.H : 1);
+      const bool op = p.mode == kModeFO || p.mode == kModeLOO;   // with an operating-point job
+      int per = op ? 1 + p.H : (p.mode == kModeADD ? p.H : 1);
       U.njobs = nt * per;
-      break;
+      U.njobs_pm = (p.stream_heads && p.mode != kModeAlpha) ? nt * (op ? 2 : 1) : U.njobs;
+      return U;
     }
     case kModeCNorm:   // consecutive units: the heads of one 256-token block
       U.head = u % p.H;
@@ -95,6 +102,7 @@ __device__ __forceinline__ Unit unit_info(const TileParams& p, int u, int rank) 
       U.njobs = p.G * p.n_ntiles;
       break;
   }
+  U.njobs_pm = U.njobs;
   return U;
 }
 
@@ -105,15 +113,26 @@ struct JobIter {
   int a, b;
 };
 
-// The next job of unit U (every role walks the same sequence).
+// The next job of unit U.  Every role walks the same sequence, except that
+// with streamed heads the producer and the MMA issuer (pm) see one kJobStream
+// where the epilogue sees the H head jobs of a token tile.
 template <int MODE>
-__device__ __forceinline__ Job job_next(const TileParams& p, const Unit& U, JobIter& it) {
+__device__ __forceinline__ Job job_next(const TileParams& p, const Unit& U, JobIter& it, bool pm = false) {
   Job J{};
   J.kt = U.kt;
   if constexpr (MODE == kModeFold) {
     J.kind = kJobFold; J.nkb = 2 * p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D; J.nt = U.base;
   } else if constexpr (MODE == kModeFO || MODE == kModeLOO) {
     J.t0 = (U.tile0 + it.a) * kBlockN;
+    if (pm && p.stream_heads) {
+      if (it.b == 0) {
+        J.kind = kJobGateUp; J.nkb = p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D;
+      } else {
+        J.kind = kJobStream; J.nkb = p.nkb_HD; J.nkb_part = p.nkb_HD; J.last_nks = p.ls_HD;
+      }
+      if (++it.b == 2) { it.b = 0; ++it.a; }
+      return J;
+    }
     if (it.b == 0) {
       J.kind = kJobGateUp; J.nkb = p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D;
     } else {
@@ -122,6 +141,11 @@ __device__ __forceinline__ Job job_next(const TileParams& p, const Unit& U, JobI
     if (++it.b == 1 + p.H) { it.b = 0; ++it.a; }
   } else if constexpr (MODE == kModeADD) {
     J.t0 = (U.tile0 + it.a) * kBlockN;
+    if (pm && p.stream_heads) {
+      J.kind = kJobStream; J.nkb = p.nkb_HD; J.nkb_part = p.nkb_HD; J.last_nks = p.ls_HD;
+      ++it.a;
+      return J;
+    }
     J.kind = kJobHead; J.head = it.b; J.nkb = p.nkb_dh; J.nkb_part = p.nkb_dh; J.last_nks = p.ls_dh;
     if (++it.b == p.H) { it.b = 0; ++it.a; }
   } else if constexpr (MODE == kModeAlpha) {
@@ -239,8 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = cid; ok && u < p.n_units; u += ncl) {
         const Unit U = unit_info<PAIR>(p, u, crank);
         JobIter jt{0, 0};
-        for (int j = 0; ok && j < U.njobs; ++j) {
-          const Job J = job_next<MODE>(p, U, jt);
+        for (int j = 0; ok && j < U.njobs_pm; ++j) {
+          const Job J = job_next<MODE>(p, U, jt, true);
           for (int kb = 0, kb_in = 0, part = 0; kb < J.nkb; ++kb) {
             const bool w = PAIR ? mbar_wait_cluster(&sm.empty[s], ph ^ 1u, sm.abort_flag, p.status)
                                 : mbar_wait(&sm.empty[s], ph ^ 1u, sm.abort_flag, p.status);
@@ -269,6 +293,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                   tma_load_2d(st, &map0, fb, kx, J.kt * kBlockM);
                   tma_load_2d(st + kTileBytes, &map0, fb, kx, p.I_pad + J.kt * kBlockM);
                   tma_load_2d(st + kBOff, &map1, fb, kx, J.t0);
+                  break;
+                case kJobStream:   // A = M16 gate / up planes, B = a16; K runs over all heads' columns
+                  tma_load_2d(st, &map2, fb, kx, J.kt * kBlockM);
+                  tma_load_2d(st + kTileBytes, &map2, fb, kx, p.I_pad + J.kt * kBlockM);
+                  tma_load_2d(st + kBOff, &map3, fb, kx, J.t0);
                   break;
                 case kJobHead:     // A = M16 (gate, up) of head h, B = a16 head h
                   tma_load_3d(st, &map2, fb, kx, J.kt * kBlockM, 2 * J.head);
@@ -334,12 +363,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = cid; ok && u < p.n_units; u += ncl) {
         const Unit U = unit_info<PAIR>(p, u, crank);
         JobIter jt{0, 0};
-        for (int j = 0; ok && j < U.njobs; ++j) {
-          const Job J = job_next<MODE>(p, U, jt);
+        for (int j = 0; ok && j < U.njobs_pm; ++j) {
+          const Job J = job_next<MODE>(p, U, jt, true);
           const bool w = PAIR ? mbar_wait_cluster(&sm.tempty[b], tph ^ 1u, sm.abort_flag, p.status)
                               : mbar_wait(&sm.tempty[b], tph ^ 1u, sm.abort_flag, p.status);
           if (!w) { ok = false; break; }
           tc_fence_after();
+          if (!PAIR && J.kind == kJobStream) {
+            // The H heads' K slices arrive back to back; a stage may hold the end of one
+            // head and the start of the next.  When a head's last slice is issued its
+            // accumulator is committed and the next head moves to the other buffer.
+            int sih = 0, heads_left = p.H;
+            for (int kb = 0; ok && kb < J.nkb; ++kb) {
+              if (!mbar_wait(&sm.full[s], ph, sm.abort_flag, p.status)) { ok = false; break; }
+              tc_fence_after();
+              const uint64_t da1 = dbase + (uint64_t)s * kStageDesc;
+              const uint64_t da2 = da1 + kA2, db = da1 + kB;
+              const int nks = (kb == J.nkb - 1) ? J.last_nks : 4;
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                if (ks < nks && heads_left > 0) {
+                  const uint32_t d1 = tmem + (uint32_t)(b * 2 * kBlockN);
+                  const uint32_t acc = sih > 0 ? 1u : 0u;
+                  mma_f16_ss(d1, da1 + 2 * ks, db + 2 * ks, idesc, acc);
+                  mma_f16_ss(d1 + kBlockN, da2 + 2 * ks, db + 2 * ks, idesc, acc);
+                  if (++sih == p.spp) {
+                    mma_commit(&sm.tfull[b]);
+                    if (++b == 2) { b = 0; tph ^= 1u; }
+                    sih = 0;
+                    if (--heads_left > 0) {
+                      if (!mbar_wait(&sm.tempty[b], tph ^ 1u, sm.abort_flag, p.status)) { ok = false; break; }
+                      tc_fence_after();
+                    }
+                  }
+                }
+              }
+              mma_commit(&sm.empty[s]);   // also on the way out, so the producer can drain
+              if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            continue;
+          }
           const uint32_t d1 = tmem + (uint32_t)(b * 2 * kBlockN);
           const uint32_t d2 = d1 + kBlockN;
           uint32_t acc = 0u;
@@ -583,8 +646,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 vu.y = pack_h2(__uint_as_float(mu[i + 2]), __uint_as_float(mu[i + 3]));
                 vu.z = pack_h2(__uint_as_float(mu[i + 4]), __uint_as_float(mu[i + 5]));
                 vu.w = pack_h2(__uint_as_float(mu[i + 6]), __uint_as_float(mu[i + 7]));
-                *reinterpret_cast<uint4*>(p.M16 + ((size_t)(2 * h) * p.I_pad + kk) * p.dh + jj) = vg;
-                *reinterpret_cast<uint4*>(p.M16 + ((size_t)(2 * h + 1) * p.I_pad + kk) * p.dh + jj) = vu;
+                if (p.stream_heads) {   // [2][I_pad][H*dh]: heads back to back along K
+                  const size_t HD = (size_t)p.H * p.dh;
+                  *reinterpret_cast<uint4*>(p.M16 + (size_t)kk * HD + n) = vg;
+                  *reinterpret_cast<uint4*>(p.M16 + ((size_t)p.I_pad + kk) * HD + n) = vu;
+                } else {                // [2H][I_pad][dh]
+                  *reinterpret_cast<uint4*>(p.M16 + ((size_t)(2 * h) * p.I_pad + kk) * p.dh + jj) = vg;
+                  *reinterpret_cast<uint4*>(p.M16 + ((size_t)(2 * h + 1) * p.I_pad + kk) * p.dh + jj) = vu;
+                }
               }
             }
           }

@@ -48,6 +48,10 @@ struct TileParams {
   int32_t nkb_D, nkb_dh, nkb_I;
   int32_t ls_D, ls_dh;     // 16-wide K slices in the last K block of D and of dh
   int32_t pair;            // FO / ADD: 1 = CTA pairs with 256-row (cta_group::2) MMAs
+  int32_t stream_heads;    // FO / ADD / LOO: 1 = the heads' K ranges are streamed back to back
+                           // (d_head % 16 == 0 but not % 64): M16 is [2][I_pad][H*dh], a16 read as [T][H*dh]
+  int32_t nkb_HD, ls_HD;   // streaming: K blocks over H*dh, 16-wide slices in the last one
+  int32_t spp;             // streaming: 16-wide K slices per head (d_head / 16)
   uint32_t* status;
   float* partial;          // FO/ADD: [n_chunks][2][H][I_pad]; x': [T_pad] sum x'^2 parts
   __half* M16;             // fold output

@@ -238,6 +238,12 @@ def run_layout(args) -> None:
     ST.optimise(up, dn, L)    # warm
     t0 = time.perf_counter()
     res = ST.optimise(up, dn, L)
+    # the paper's run also scores eight random balanced layouts (seeds 1000..1007)
+    J_random = []
+    for seed in range(1000, 1008):
+        r = np.random.default_rng(seed)
+        J_random.append(B.objective(up, dn, [r.permutation(ST.contiguous_map(G, L)) for _ in range(N)],
+                                    [r.permutation(ST.contiguous_map(I, L)) for _ in range(N)]))
     opt_s = time.perf_counter() - t0
     J0 = B.objective(up, dn, hc, np.stack([ST.contiguous_map(I, L)] * N))
     line = {"metric": "layout search: balanced neuron step for every layer of a 28-layer stack",
@@ -248,7 +254,9 @@ def run_layout(args) -> None:
                        "I": I, "L": L},
             "roofline": {"bound": "latency", "note": "one 1024-thread CTA per layer; M (I*L*8 B) re-read "
                                                      "from L1 on every dual-ascent iteration"},
-            "optimise": {"seconds": opt_s, "sweeps": res.sweeps, "J_contiguous": J0, "J": res.J},
+            "optimise": {"seconds": opt_s, "sweeps": res.sweeps, "J_contiguous": J0, "J": res.J,
+                         "J_random_mean": float(np.mean(J_random)),
+                         "note": "seconds include scoring eight random layouts"},
             "gpu_launches": N + 1}
     if not args.no_cpu_baseline:
         from oracle import assignment as A

@@ -191,6 +191,21 @@ AFF_API aff_status affinity_down(const void* x, const void* gamma, const void* W
 AFF_API aff_status affinity_device_status(void* workspace, aff_stream_t stream);
 
 /*
+ * Self-test of the device-side failure path (no counterpart in the paper).
+ * Every pipeline wait inside the library's kernels is bounded: past its time
+ * limit it latches AFF_ERR_DEVICE_TIMEOUT in the workspace status word and
+ * returns instead of spinning, so the context stays usable.  This call
+ * launches one kernel whose single wait can never be satisfied, with the
+ * given limit; afterwards affinity_device_status(workspace) must report
+ * AFF_ERR_DEVICE_TIMEOUT.  Nothing faults, traps or hangs.
+ *   workspace  device, >= 256 bytes, 256-byte aligned (its status word is
+ *              cleared first)
+ *   limit_ns   1e3 .. 1e10
+ */
+AFF_API aff_status affinity_selftest_timeout(void* workspace, size_t workspace_bytes, int64_t limit_ns,
+                                             aff_stream_t stream);
+
+/*
  * Host-only helper ("Optimiser", §3): score every labelled balanced
  * partition h of G KV groups onto L devices (G/L groups per device) by
  * sum_g C[g, h(g)], where C [G, L] (host, row-major, fp64) is the gain of

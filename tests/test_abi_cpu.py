@@ -307,3 +307,11 @@ def test_loo_mode_is_bf16_only(lib):
         B.AFF_ERR_UNSUPPORTED_DTYPE
     db = B.dims(256, 64, 4, 2, 16, 128, 1e-6, B.AFF_BF16)
     assert B.workspace_size(db, B.AFF_MODE_LOO) > B.workspace_size(db, B.AFF_MODE_ADD)
+
+
+def test_selftest_timeout_argument_checks(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.affinity_selftest_timeout(fake, 128, 5_000_000, None) == B.AFF_ERR_WORKSPACE
+    assert lib.affinity_selftest_timeout(ctypes.c_void_p((1 << 20) + 16), 256, 5_000_000, None) == B.AFF_ERR_WORKSPACE
+    assert lib.affinity_selftest_timeout(fake, 256, 10, None) == B.AFF_ERR_INVALID_ARG
+    assert lib.affinity_selftest_timeout(fake, 256, 5_000_000, None) == B.AFF_ERR_ARCH

@@ -54,7 +54,7 @@ def test_place_heads_uniform_scores_give_the_expectation():
 
 @pytest.mark.gpu
 @pytest.mark.slow
-def test_qwen3_stack_28_layers(record_property):
+def test_qwen3_stack_28_layers(record_property, tmp_path):
     torch = pytest.importorskip("torch")
     from transformer_sharding_affinity_gb300 import binding as B
     from transformer_sharding_affinity_gb300 import device as DV
@@ -71,7 +71,7 @@ def test_qwen3_stack_28_layers(record_property):
             keep[i] = layer
         return DV.to_device(layer, "bf16", keys=DV.ALL_KEYS if i + 1 < N else DV.UP_KEYS)
 
-    S_up, S_down = ST.calibrate_stack(layer_inputs, N, d)
+    S_up, S_down = ST.calibrate_stack(layer_inputs, N, d, checkpoint_dir=str(tmp_path))
     assert len(S_up) == N and len(S_down) == N - 1
     for S in S_up + S_down:
         assert np.all(np.isfinite(S)) and S.min() >= 0.0 and S.max() > 0.0
@@ -102,9 +102,28 @@ def test_qwen3_stack_28_layers(record_property):
     record_property("layer0_down_max_rel_err", e)
     assert e <= TOL, f"layer 0 S_down: max rel err {e:.3e}"
 
+    # resume: only the layers whose checkpoints are gone are recomputed, bit for bit
+    for i in (0, N - 1):
+        (tmp_path / f"layer_{i:03d}.npz").unlink()
+    recomputed = []
+
+    def counted(i):
+        recomputed.append(i)
+        return layer_inputs(i)
+    up2, dn2 = ST.calibrate_stack(counted, N, d, checkpoint_dir=str(tmp_path))
+    assert recomputed == [0, N - 1]
+    for a, b in zip(up2 + dn2, S_up + S_down):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
     res = ST.place_heads(S_up, S_down, L)
     _check_host_sequence(res, L)
     assert res.h_best.shape == (N, shape.G)
+    # a uniformly random balanced layout scores (2N - 1) / L in expectation ("Objective")
+    from transformer_sharding_affinity_gb300 import binding as Bb
+    J = [Bb.objective(res.Shat_up, res.Shat_down, [rng.permutation(P.contiguous_heads(shape.G, L)) for _ in range(N)],
+                      [rng.permutation(P.contiguous_neurons(shape.I, L)) for _ in range(N)]) for _ in range(200)]
+    record_property("J_random_mean", float(np.mean(J)))
+    assert abs(np.mean(J) - (2 * N - 1) / L) < 4 * np.std(J) / np.sqrt(len(J)) + 1e-9
     record_property("J_contiguous", res.J_contiguous)
     record_property("J_best_heads", res.J_best)
 
@@ -121,3 +140,24 @@ def test_qwen3_stack_28_layers(record_property):
     M0 = A.neuron_gain(res.Shat_up[0], lay.h[0], L, res.Shat_down[0], lay.h[1])
     _, best0 = A.best_balanced_neurons(M0)
     np.testing.assert_allclose(A.assignment_value(M0, lay.nu[0]), best0, rtol=1e-12)
+
+
+def test_calibrate_stack_resumes_from_checkpoints(tmp_path):
+    """Layers already on disk are loaded, not recomputed: with every layer
+    saved, the call needs no GPU and never asks for inputs."""
+    from transformer_sharding_affinity_gb300 import binding as B
+    rng = np.random.default_rng(21)
+    N, G, I = 3, 4, 16
+    saved_up = [rng.random((G, I)).astype(np.float32) for _ in range(N)]
+    saved_dn = [rng.random((I, G)).astype(np.float32) for _ in range(N - 1)]
+    for i in range(N):
+        arrays = {"S_up": saved_up[i]} if i == N - 1 else {"S_up": saved_up[i], "S_down": saved_dn[i]}
+        np.savez(tmp_path / f"layer_{i:03d}.npz", **arrays)
+
+    def no_inputs(i):
+        raise AssertionError(f"layer {i} was recomputed")
+
+    d = B.dims(64, 32, 4, G, 8, I)
+    up, dn = ST.calibrate_stack(no_inputs, N, d, checkpoint_dir=str(tmp_path))
+    for a, b in zip(up + dn, saved_up + saved_dn):
+        assert np.array_equal(a, b)

@@ -110,6 +110,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                              ctypes.POINTER(aff_layout_opts), _P, _P, ctypes.POINTER(ctypes.c_double),
                                              ctypes.POINTER(ctypes.c_int32), _P, ctypes.c_size_t, _P]
     lib.affinity_optimise_layout.restype = st
+    lib.affinity_selftest_timeout.argtypes = [_P, ctypes.c_size_t, ctypes.c_int64, _P]
+    lib.affinity_selftest_timeout.restype = st
     lib.affinity_layout_orders.argtypes = [_P, _P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                            _P, _P, _P]
     lib.affinity_layout_orders.restype = st
@@ -201,6 +203,12 @@ def affinity_down(x, gamma, Wg, Wu, Wd, gamma_next, Wq_next, Wk_next, Wv_next, d
     _check(load().affinity_down(_ptr(x), _ptr(gamma), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(gamma_next),
                                 _ptr(Wq_next), _ptr(Wk_next), _ptr(Wv_next), ctypes.byref(d), _ptr(S_out),
                                 _ptr(workspace), nbytes, _stream(stream)), "affinity_down")
+
+
+def selftest_timeout(workspace, limit_ns: int = 5_000_000, stream=None, workspace_bytes=None) -> None:
+    """Enqueue a kernel whose one bounded wait must time out (affinity_selftest_timeout)."""
+    _check(load().affinity_selftest_timeout(_ptr(workspace), _ws_bytes(workspace, workspace_bytes), int(limit_ns),
+                                            _stream(stream)), "affinity_selftest_timeout")
 
 
 def device_status(workspace, stream=None) -> int:

@@ -643,6 +643,19 @@ aff_status affinity_down(const void* x, const void* gamma, const void* Wg, const
   return AFF_OK;
 }
 
+aff_status affinity_selftest_timeout(void* workspace, size_t workspace_bytes, int64_t limit_ns, aff_stream_t stream) {
+  if (!workspace || workspace_bytes < 256 || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return AFF_ERR_WORKSPACE;
+  if (limit_ns < 1000 || limit_ns > 10000000000LL) return AFF_ERR_INVALID_ARG;
+  int sm_count = 0;
+  aff_status st = check_device(&sm_count);
+  if (st != AFF_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t* status = static_cast<uint32_t*>(workspace);
+  AFF_CUDA(cudaMemsetAsync(status, 0, 4, s));
+  AFF_CUDA(launch_wait_selftest(status, (unsigned long long)limit_ns, s));
+  return AFF_OK;
+}
+
 aff_status affinity_device_status(void* workspace, aff_stream_t stream) {
   if (!workspace) return AFF_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -227,6 +227,27 @@ __global__ void finalize_up_kernel(const double* __restrict__ sh, const float* _
   S_out[(size_t)g * I + k] = (float)s;
 }
 
+// ---------------------------------------------------------------- self-test of the bounded waits
+// One thread waits on an mbarrier that nothing arrives at.  The wait must give
+// up after limit_ns, latch the timeout status and return, leaving the context
+// usable -- the path every pipeline wait of the tile kernel takes on a stall.
+__global__ void wait_selftest_kernel(uint32_t* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, status, limit_ns);
+}
+
+cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- leave-one-out score
 // out = fp16 copy of n bf16 values (n % 8 == 0), 8 per thread.
 __global__ void to_fp16_kernel(const uint16_t* __restrict__ in, __half* __restrict__ out, size_t n,

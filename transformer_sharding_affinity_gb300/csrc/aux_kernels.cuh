@@ -19,6 +19,7 @@ cudaError_t launch_reduce_partials(const float* partial, double* out, int n_chun
                                    cudaStream_t s);
 cudaError_t launch_finalize_up(const double* sh, const float* wdn, int fo, int T, int H, int G, int I, int I_pad,
                                float* S_out, float* S_head_out, cudaStream_t s);
+cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, cudaStream_t s);
 cudaError_t launch_to_fp16(const uint16_t* in, __half* out, size_t n, uint32_t* status, cudaStream_t s);
 cudaError_t launch_loo_rho(const float* cn, const float* inv_r, float* rho, int T, int T_pad, int H, int D,
                            cudaStream_t s);

@@ -55,7 +55,7 @@ struct Unit {
 
 // Unit u of the schedule.  With CTA pairs (FO / ADD) a unit covers 256 neurons:
 // the CTA of cluster rank `rank` owns neuron tile 2 * (u % (n_ktiles / 2)) + rank.
-template <bool PAIR>
+template <bool PAIR, bool STREAM = false>
 __device__ __forceinline__ Unit unit_info(const TileParams& p, int u, int rank) {
   Unit U{};
   if (PAIR) {
@@ -85,7 +85,7 @@ __device__ __forceinline__ Unit unit_info(const TileParams& p, int u, int rank) 
       const bool op = p.mode == kModeFO || p.mode == kModeLOO;   // with an operating-point job
       int per = op ? 1 + p.H : (p.mode == kModeADD ? p.H : 1);
       U.njobs = nt * per;
-      U.njobs_pm = (p.stream_heads && p.mode != kModeAlpha) ? nt * (op ? 2 : 1) : U.njobs;
+      U.njobs_pm = (STREAM && p.mode != kModeAlpha) ? nt * (op ? 2 : 1) : U.njobs;
       return U;
     }
     case kModeCNorm:   // consecutive units: the heads of one 256-token block
@@ -116,7 +116,7 @@ struct JobIter {
 // The next job of unit U.  Every role walks the same sequence, except that
 // with streamed heads the producer and the MMA issuer (pm) see one kJobStream
 // where the epilogue sees the H head jobs of a token tile.
-template <int MODE>
+template <int MODE, bool STREAM = false>
 __device__ __forceinline__ Job job_next(const TileParams& p, const Unit& U, JobIter& it, bool pm = false) {
   Job J{};
   J.kt = U.kt;
@@ -124,7 +124,7 @@ __device__ __forceinline__ Job job_next(const TileParams& p, const Unit& U, JobI
     J.kind = kJobFold; J.nkb = 2 * p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D; J.nt = U.base;
   } else if constexpr (MODE == kModeFO || MODE == kModeLOO) {
     J.t0 = (U.tile0 + it.a) * kBlockN;
-    if (pm && p.stream_heads) {
+    if (STREAM && pm) {
       if (it.b == 0) {
         J.kind = kJobGateUp; J.nkb = p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D;
       } else {
@@ -141,7 +141,7 @@ __device__ __forceinline__ Job job_next(const TileParams& p, const Unit& U, JobI
     if (++it.b == 1 + p.H) { it.b = 0; ++it.a; }
   } else if constexpr (MODE == kModeADD) {
     J.t0 = (U.tile0 + it.a) * kBlockN;
-    if (pm && p.stream_heads) {
+    if (STREAM && pm) {
       J.kind = kJobStream; J.nkb = p.nkb_HD; J.nkb_part = p.nkb_HD; J.last_nks = p.ls_HD;
       ++it.a;
       return J;
@@ -183,7 +183,10 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int MODE, bool PAIR>
+// STREAM: the producer and MMA issuer walk the heads' K ranges back to back
+// (FO / ADD / LOO with p.stream_heads); a separate instantiation, so the
+// issue loop of the other shapes carries no extra branch.
+template <int MODE, bool PAIR, bool STREAM>
 __global__ void __launch_bounds__(kThreads, 1)
     affinity_tile_kernel(const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
                          const __grid_constant__ CUtensorMap map2, const __grid_constant__ CUtensorMap map3,
@@ -261,10 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;                 // phase parity of the current use of stage s
       bool ok = true;
       for (int u = cid; ok && u < p.n_units; u += ncl) {
-        const Unit U = unit_info<PAIR>(p, u, crank);
+        const Unit U = unit_info<PAIR, STREAM>(p, u, crank);
         JobIter jt{0, 0};
         for (int j = 0; ok && j < U.njobs_pm; ++j) {
-          const Job J = job_next<MODE>(p, U, jt, true);
+          const Job J = job_next<MODE, STREAM>(p, U, jt, true);
           for (int kb = 0, kb_in = 0, part = 0; kb < J.nkb; ++kb) {
             const bool w = PAIR ? mbar_wait_cluster(&sm.empty[s], ph ^ 1u, sm.abort_flag, p.status)
                                 : mbar_wait(&sm.empty[s], ph ^ 1u, sm.abort_flag, p.status);
@@ -361,15 +364,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0, tph = 0;        // stage phase; TMEM buffer phase (flips every second job)
       bool ok = true;
       for (int u = cid; ok && u < p.n_units; u += ncl) {
-        const Unit U = unit_info<PAIR>(p, u, crank);
+        const Unit U = unit_info<PAIR, STREAM>(p, u, crank);
         JobIter jt{0, 0};
         for (int j = 0; ok && j < U.njobs_pm; ++j) {
-          const Job J = job_next<MODE>(p, U, jt, true);
+          const Job J = job_next<MODE, STREAM>(p, U, jt, true);
           const bool w = PAIR ? mbar_wait_cluster(&sm.tempty[b], tph ^ 1u, sm.abort_flag, p.status)
                               : mbar_wait(&sm.tempty[b], tph ^ 1u, sm.abort_flag, p.status);
           if (!w) { ok = false; break; }
           tc_fence_after();
-          if (!PAIR && J.kind == kJobStream) {
+          if constexpr (STREAM) {
+           if (J.kind == kJobStream) {
             // The H heads' K slices arrive back to back; a stage may hold the end of one
             // head and the start of the next.  When a head's last slice is issued its
             // accumulator is committed and the next head moves to the other buffer.
@@ -402,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (++s == S) { s = 0; ph ^= 1u; }
             }
             continue;
+           }
           }
           const uint32_t d1 = tmem + (uint32_t)(b * 2 * kBlockN);
           const uint32_t d2 = d1 + kBlockN;
@@ -468,10 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tph = 0;                  // TMEM buffer phase (flips every second job)
     bool ok = true;
     for (int u = cid; ok && u < p.n_units; u += ncl) {
-      const Unit U = unit_info<PAIR>(p, u, crank);
+      const Unit U = unit_info<PAIR, STREAM>(p, u, crank);
       JobIter jt{0, 0};
       for (int j = 0; j < U.njobs; ++j, b ^= 1, tph ^= (uint32_t)(b == 0)) {
-        const Job J = job_next<MODE>(p, U, jt);
+        const Job J = job_next<MODE, STREAM>(p, U, jt);
         int w_ok = 1;
         if (lane == 0)
           w_ok = (PAIR ? mbar_wait_cluster(&sm.tfull[b], tph, sm.abort_flag, p.status)
@@ -830,10 +835,10 @@ size_t tile_smem_bytes(int mode, int stages, int H, bool pair) {
 
 // Launches `grid` CTAs (pairs: 2 * grid as clusters of 2).  With grid == 0 it
 // only reports in *grid how many CTAs (pairs) fit on the device at once.
-template <int MODE, bool PAIR>
+template <int MODE, bool PAIR, bool STREAM = false>
 static cudaError_t launch_mode(const CUtensorMap* maps, const TileParams& p, int* grid, cudaStream_t stream) {
   const size_t smem = tile_smem_bytes(MODE, p.stages, p.H, PAIR);
-  auto* fn = affinity_tile_kernel<MODE, PAIR>;
+  auto* fn = affinity_tile_kernel<MODE, PAIR, STREAM>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (!PAIR) {
@@ -873,16 +878,20 @@ cudaError_t launch_tile_kernel(const CUtensorMap* maps, const TileParams& p, int
   switch (p.mode) {
     case kModeFold: return launch_mode<kModeFold, false>(maps, p, grid, stream);
     case kModeFO:
+      if (p.stream_heads) return launch_mode<kModeFO, false, true>(maps, p, grid, stream);
       return p.pair ? launch_mode<kModeFO, true>(maps, p, grid, stream)
                     : launch_mode<kModeFO, false>(maps, p, grid, stream);
     case kModeADD:
+      if (p.stream_heads) return launch_mode<kModeADD, false, true>(maps, p, grid, stream);
       return p.pair ? launch_mode<kModeADD, true>(maps, p, grid, stream)
                     : launch_mode<kModeADD, false>(maps, p, grid, stream);
     case kModeAlpha: return launch_mode<kModeAlpha, false>(maps, p, grid, stream);
     case kModeXPrime: return launch_mode<kModeXPrime, false>(maps, p, grid, stream);
     case kModeQNorm: return launch_mode<kModeQNorm, false>(maps, p, grid, stream);
     case kModeCNorm: return launch_mode<kModeCNorm, false>(maps, p, grid, stream);
-    case kModeLOO: return launch_mode<kModeLOO, false>(maps, p, grid, stream);
+    case kModeLOO:
+      return p.stream_heads ? launch_mode<kModeLOO, false, true>(maps, p, grid, stream)
+                            : launch_mode<kModeLOO, false>(maps, p, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -14,6 +14,7 @@ This module only sequences library calls; every number comes from
 from __future__ import annotations
 
 import dataclasses
+import os
 from typing import Callable, Dict, List, Optional
 
 import numpy as np
@@ -42,33 +43,59 @@ def contiguous_map(n: int, L: int) -> np.ndarray:
 
 
 def calibrate_stack(layer_inputs: Callable[[int], Dict[str, object]], n_layers: int, d: "B.aff_dims",
-                    mode: int = B.AFF_MODE_FO, stream=None) -> tuple:
+                    mode: int = B.AFF_MODE_FO, stream=None, checkpoint_dir: Optional[str] = None) -> tuple:
     """Run S_up for layers 0..N-1 and S_down for layers 0..N-2 on the GPU.
 
     ``layer_inputs(i)`` returns layer i's device tensors under the names of
     ``affinity_up`` / ``affinity_down`` (a, x, Wo, gamma, Wg, Wu, Wd and, for
     i < N-1, gamma_next, Wq_next, Wk_next, Wv_next: layer i+1's attention
     pre-norm gain and q/k/v projections).  Returns (S_up list, S_down list) on
-    the host."""
-    import torch
+    the host.
 
+    With ``checkpoint_dir`` every finished layer is saved as
+    ``layer_<i>.npz`` (written to a temporary name, then renamed), and a
+    layer whose file is already there is loaded instead of recomputed, so an
+    interrupted run resumes where it stopped."""
     G, I = int(d.G), int(d.I)
-    ws_bytes = max(B.workspace_size(d, mode), B.workspace_size(d, mode, down=True))
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
-    S_up_dev = torch.empty(G, I, device="cuda")
-    S_dn_dev = torch.empty(I, G, device="cuda")
+    state = {}
+
+    def buffers():
+        if not state:
+            import torch
+            ws_bytes = max(B.workspace_size(d, mode), B.workspace_size(d, mode, down=True))
+            state["ws"] = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+            state["up"] = torch.empty(G, I, device="cuda")
+            state["dn"] = torch.empty(I, G, device="cuda")
+        return state["ws"], state["up"], state["dn"]
+
     S_up, S_down = [], []
     for i in range(n_layers):
+        last = i + 1 == n_layers
+        path = None if checkpoint_dir is None else os.path.join(checkpoint_dir, f"layer_{i:03d}.npz")
+        if path is not None and os.path.exists(path):
+            with np.load(path) as f:
+                if f["S_up"].shape == (G, I) and (last or f["S_down"].shape == (I, G)):
+                    S_up.append(f["S_up"].copy())
+                    if not last:
+                        S_down.append(f["S_down"].copy())
+                    continue
+        ws, up_dev, dn_dev = buffers()
         t = layer_inputs(i)
-        B.affinity_up(t["a"], t["x"], t["Wo"], t["gamma"], t["Wg"], t["Wu"], t["Wd"], d, mode, S_up_dev, None, ws,
+        B.affinity_up(t["a"], t["x"], t["Wo"], t["gamma"], t["Wg"], t["Wu"], t["Wd"], d, mode, up_dev, None, ws,
                       stream=stream)
         _status(ws, stream, f"layer {i} S_up")
-        S_up.append(S_up_dev.cpu().numpy().copy())
-        if i + 1 < n_layers:
+        S_up.append(up_dev.cpu().numpy().copy())
+        if not last:
             B.affinity_down(t["x"], t["gamma"], t["Wg"], t["Wu"], t["Wd"], t["gamma_next"], t["Wq_next"],
-                            t["Wk_next"], t["Wv_next"], d, S_dn_dev, ws, stream=stream)
+                            t["Wk_next"], t["Wv_next"], d, dn_dev, ws, stream=stream)
             _status(ws, stream, f"layer {i} S_down")
-            S_down.append(S_dn_dev.cpu().numpy().copy())
+            S_down.append(dn_dev.cpu().numpy().copy())
+        if path is not None:
+            os.makedirs(checkpoint_dir, exist_ok=True)
+            tmp = path + ".tmp.npz"
+            arrays = {"S_up": S_up[-1]} if last else {"S_up": S_up[-1], "S_down": S_down[-1]}
+            np.savez(tmp, **arrays)
+            os.replace(tmp, path)
     return S_up, S_down
 
 

@@ -125,7 +125,9 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
       L.GWo16 = L.take((size_t)H * dh * 2 * D * 2);
       L.M16 = L.take((size_t)2 * H * L.I_pad * dh * 2);
       L.a16 = L.take((size_t)T * H * dh * 2);
-      L.partial = L.take((size_t)L.n_chunks * 2 * H * L.I_pad * 4);
+      // one slot per (chunk, column group of the epilogue, head, neuron)
+      const int tile_mode = mode == AFF_MODE_LOO ? kModeLOO : (mode == AFF_MODE_ADD ? kModeADD : kModeFO);
+      L.partial = L.take((size_t)L.n_chunks * epi_warps(tile_mode, false) / 4 * H * L.I_pad * 4);
       L.headsum = L.take((size_t)H * L.I_pad * 8);
       if (mode == AFF_MODE_FO) L.wdn = L.take((size_t)L.I_pad * 4);
       if (mode == AFF_MODE_LOO) {
@@ -506,6 +508,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     if ((st = run_tile(maps, p, s)) != AFF_OK) return st;
     AFF_CUDA(launch_loo_rho(cn, inv_r, rho, T, (int)L.T_pad, H, D, s));
   }
+  int epi_groups = 2;   // column groups per token tile in the partial sums (set below)
   // FO / ADD / LOO: per token tile, operating point (FO, LOO) then every head.
   // With CTA pairs (FO / ADD) each CTA loads half (64 rows) of every token tile.
   {
@@ -536,9 +539,10 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     p.stages = pick_stages(p.mode, p.H, pair);
     p.n_units = (int)(L.n_chunks * (pair ? p.n_ktiles / 2 : p.n_ktiles));
     p.partial = partial;
+    epi_groups = epi_warps(p.mode, pair) / 4;
     if ((st = run_tile(maps, p, s, true)) != AFF_OK) return st;
   }
-  AFF_CUDA(launch_reduce_partials(partial, headsum, (int)L.n_chunks, 2, H, I_pad, s));
+  AFF_CUDA(launch_reduce_partials(partial, headsum, (int)L.n_chunks, epi_groups, H, I_pad, s));
   AFF_CUDA(launch_finalize_up(headsum, wdn, fo, T, H, G, I, I_pad, S_out, S_head_out, s));
   return AFF_OK;
 }

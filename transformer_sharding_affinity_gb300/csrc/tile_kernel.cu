@@ -187,7 +187,7 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 // (FO / ADD / LOO with p.stream_heads); a separate instantiation, so the
 // issue loop of the other shapes carries no extra branch.
 template <int MODE, bool PAIR, bool STREAM>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
     affinity_tile_kernel(const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
                          const __grid_constant__ CUtensorMap map2, const __grid_constant__ CUtensorMap map3,
                          const TileParams p) {
@@ -195,6 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
 
+  constexpr int EW = epi_warps(MODE, PAIR);   // epilogue warps
+  constexpr int NG = EW / 4;                    // column groups of a 128-column accumulator
+  constexpr int CW = kBlockN / NG;              // columns (tokens) per epilogue thread
   const int S = p.stages;
   constexpr int kSB = PAIR ? kPairStageBytes : kStageBytes;   // bytes of one pipeline stage
   constexpr int kBOff = 2 * kTileBytes;                         // B tile offset within a stage
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   sm.stage0 = base;
   uint8_t* cur = base + (size_t)S * kSB;
   sm.sacc = reinterpret_cast<float*>(cur);
-  int sacc_floats = (MODE == kModeFO || MODE == kModeADD || MODE == kModeLOO) ? 2 * p.H * kBlockM : 0;
+  int sacc_floats = (MODE == kModeFO || MODE == kModeADD || MODE == kModeLOO) ? NG * p.H * kBlockM : 0;
   cur += (size_t)sacc_floats * 4;
   sm.full = reinterpret_cast<uint64_t*>(cur);
   sm.empty = sm.full + S;
@@ -225,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.tfull[b], 1);
-      mbar_init(&sm.tempty[b], PAIR ? 2 * kEpiWarps : kEpiWarps);   // pairs: both CTAs' epilogues
+      mbar_init(&sm.tempty[b], PAIR ? 2 * EW : EW);   // pairs: both CTAs' epilogues
     }
     mbar_init(sm.drain, 1);
     *sm.abort_flag = 0;
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (warp >= 2) {
-    for (int i = threadIdx.x - 64; i < sacc_floats; i += kEpiWarps * 32) sm.sacc[i] = 0.f;
+    for (int i = threadIdx.x - 64; i < sacc_floats; i += EW * 32) sm.sacc[i] = 0.f;
   }
   tc_fence_before();
   if (PAIR)
@@ -459,14 +462,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // TMEM lane quarter this warp may read
-    const int hf = (warp - 2) >> 2;    // which 64-column half of the tile
+    const int hf = (warp - 2) >> 2;    // which group of CW columns of the tile
     const int row = q * 32 + lane;     // row of the A tile = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
     // TMEM-empty arrivals go to the leader's barrier (its own when unpaired)
     const uint32_t tempty_addr0 = PAIR ? mapa_shared(smem_u32(&sm.tempty[0]), 0) : 0u;
-    uint64_t abA[32], abB[32];         // FO: f32x2 pairs of silu'(g)u and silu(g), 64 tokens
+    uint64_t abA[CW / 2], abB[CW / 2];   // FO: f32x2 pairs of silu'(g)u and silu(g), CW tokens
 #pragma unroll
-    for (int i = 0; i < 32; ++i) { abA[i] = 0ull; abB[i] = 0ull; }
+    for (int i = 0; i < CW / 2; ++i) { abA[i] = 0ull; abB[i] = 0ull; }
     float ss1 = 0.f, ss2 = 0.f;        // x' / qnorm / cnorm running sums
     float xd1 = 0.f, xd2 = 0.f;        // cnorm: sum_d x (c/r)
     int b = 0;
@@ -486,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
         if (!w_ok) { ok = false; break; }
         tc_fence_after();
-        const uint32_t c1 = tl + (uint32_t)(b * 2 * kBlockN + hf * 64);
+        const uint32_t c1 = tl + (uint32_t)(b * 2 * kBlockN + hf * CW);
         const uint32_t c2 = c1 + kBlockN;
 
         if constexpr (MODE == kModeFO || MODE == kModeLOO) {
@@ -494,13 +497,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Phase 1: stash g, u in the registers that will hold A', B' and hand the
             // accumulator buffer back at once, so the MMAs of the next two head
             // jobs run while phase 2 (exp + reciprocal per element) computes.
+            constexpr int kG = CW == 64 ? 16 : 8;   // TMEM columns per read
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint32_t gr[16], ur[16];
-              tmem_ld16(c1 + c * 16, gr);
-              tmem_ld16(c2 + c * 16, ur);
+            for (int c = 0; c < CW / kG; ++c) {
+              uint32_t gr[kG], ur[kG];
+              if constexpr (kG == 16) {
+                tmem_ld16(c1 + c * kG, gr);
+                tmem_ld16(c2 + c * kG, ur);
+              } else {
+                tmem_ld8(c1 + c * kG, gr);
+                tmem_ld8(c2 + c * kG, ur);
+              }
               tmem_ld_wait();
-              if (c == 3) {
+              if (c == CW / kG - 1) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
@@ -511,15 +520,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
 #pragma unroll
-              for (int i = 0; i < 16; i += 2) {
-                abA[c * 8 + i / 2] = pk_u(gr[i], gr[i + 1]);
-                abB[c * 8 + i / 2] = pk_u(ur[i], ur[i + 1]);
+              for (int i = 0; i < kG; i += 2) {
+                abA[(c * kG + i) / 2] = pk_u(gr[i], gr[i + 1]);
+                abB[(c * kG + i) / 2] = pk_u(ur[i], ur[i + 1]);
               }
             }
             // Phase 2 (FO): (g, u) -> (A', B') = (silu'(g) u, silu(g)) in place; LOO keeps g and u.
             if constexpr (MODE == kModeFO) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
+              for (int i = 0; i < CW / 2; ++i) {
                 const float2 g2 = unpk(abA[i]), u2 = unpk(abB[i]);
                 float gA[2], gB[2];
 #pragma unroll
@@ -571,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // TMEM columns per read: 8, or 4 in LOO mode (its arithmetic needs more registers)
           constexpr int kW = MODE == kModeLOO ? 4 : 8;
 #pragma unroll
-          for (int c = 0; c < 64 / kW; ++c) {
+          for (int c = 0; c < CW / kW; ++c) {
             uint32_t pg[kW], pu[kW];
             if constexpr (kW == 8) {
               tmem_ld8(c1 + c * kW, pg);
@@ -581,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_ld4(c2 + c * kW, pu);
             }
             tmem_ld_wait();
-            if (c == 64 / kW - 1) {
+            if (c == CW / kW - 1) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) {
@@ -593,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float4 rq = make_float4(0.f, 0.f, 0.f, 0.f);   // LOO: rho of the chunk's 4 tokens
             if constexpr (MODE == kModeLOO)   // the same address in every lane: a broadcast
-              rq = __ldg(reinterpret_cast<const float4*>(p.rho + (size_t)J.head * p.T_pad + J.t0 + hf * 64) + c);
+              rq = __ldg(reinterpret_cast<const float4*>(p.rho + (size_t)J.head * p.T_pad + J.t0 + hf * CW) + c);
 #pragma unroll
             for (int i = 0; i < kW; i += 2) {
               const uint64_t vg = pk_u(pg[i], pg[i + 1]);
@@ -618,6 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 s2 = unpk(acc);
           sm.sacc[(hf * p.H + J.head) * kBlockM + row] += s2.x + s2.y;
         }
+        static_assert(EW == kWideEpiWarps || CW == 64, "the 8-warp epilogues read 64 columns per thread");
         if constexpr (MODE == kModeFold) {
           // D1 = Mg[k][n], D2 = Mu[k][n] for neuron k = kt*128 + row, columns n = nt*128 + hf*64 + ...
           const int kk = J.kt * kBlockM + row;
@@ -788,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // ---- end of unit
       if constexpr (MODE == kModeFO || MODE == kModeADD || MODE == kModeLOO) {
-        float* dst = p.partial + ((size_t)(U.chunk * 2 + hf) * p.H) * p.I_pad + U.kt * kBlockM + row;
+        float* dst = p.partial + ((size_t)(U.chunk * NG + hf) * p.H) * p.I_pad + U.kt * kBlockM + row;
         for (int h = 0; h < p.H; ++h) {
           float* sp = &sm.sacc[(hf * p.H + h) * kBlockM + row];
           dst[(size_t)h * p.I_pad] = *sp;
@@ -829,7 +839,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 size_t tile_smem_bytes(int mode, int stages, int H, bool pair) {
-  size_t sacc = (mode == kModeFO || mode == kModeADD || mode == kModeLOO) ? (size_t)2 * H * kBlockM * 4 : 0;
+  const size_t groups = (size_t)epi_warps(mode, pair) / 4;
+  size_t sacc = (mode == kModeFO || mode == kModeADD || mode == kModeLOO) ? groups * H * kBlockM * 4 : 0;
   return 1024 + (size_t)stages * (pair ? kPairStageBytes : kStageBytes) + sacc + (size_t)(2 * stages + 5) * 8 + 8;
 }
 
@@ -849,7 +860,7 @@ static cudaError_t launch_mode(const CUtensorMap* maps, const TileParams& p, int
       *grid = n;   // shared memory and TMEM allow one CTA per SM
       return e;
     }
-    fn<<<*grid, kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+    fn<<<*grid, block_threads(MODE, PAIR), smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -858,7 +869,7 @@ static cudaError_t launch_mode(const CUtensorMap* maps, const TileParams& p, int
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(block_threads(MODE, PAIR), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;

@@ -67,3 +67,19 @@ def test_nothing_is_written_past_the_workspace_or_the_outputs(mode):
     if not down:
         assert torch.all(head[SHAPE.H * SHAPE.I:] == -7.0).item(), "floats past S_head_out were written"
     assert torch.isfinite(out[:out_n]).all().item()
+
+
+def test_one_call_helpers_match_the_abi():
+    from transformer_sharding_affinity_gb300 import scores
+    layer = W.make_layer(SHAPE, with_next=True)
+    dev = DV.to_device(layer, "bf16", keys=DV.ALL_KEYS)
+    S, Sh = scores.s_up(dev["a"], dev["x"], dev["Wo"], dev["gamma"], dev["Wg"], dev["Wu"], dev["Wd"], SHAPE.H,
+                        SHAPE.G, "fo", SHAPE.eps, per_head=True)
+    S_ref, _ = oracle_up(O, SHAPE, layer, "fo")
+    assert rel_err(S.cpu().numpy(), S_ref) <= TOL
+    np.testing.assert_allclose(Sh.cpu().numpy().reshape(SHAPE.G, -1, SHAPE.I).sum(1), S.cpu().numpy(), rtol=2e-6)
+    Sd = scores.s_down(dev["x"], dev["gamma"], dev["Wg"], dev["Wu"], dev["Wd"], dev["gamma_next"], dev["Wq_next"],
+                       dev["Wk_next"], dev["Wv_next"], SHAPE.H, SHAPE.G, SHAPE.eps)
+    Sd_ref = O.s_down(layer["x"], layer["gamma"], layer["Wg"], layer["Wu"], layer["Wd"], layer["gamma_next"],
+                      layer["Wq_next"], layer["Wk_next"], layer["Wv_next"], SHAPE.H, SHAPE.G, SHAPE.dh, SHAPE.eps)
+    assert rel_err(Sd.cpu().numpy(), Sd_ref) <= TOL

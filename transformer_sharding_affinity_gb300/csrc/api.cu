@@ -132,7 +132,7 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
       if (mode == AFF_MODE_FO) L.wdn = L.take((size_t)L.I_pad * 4);
       if (mode == AFF_MODE_LOO) {
         L.Wo16 = L.take((size_t)D * H * dh * 2);
-        L.cn = L.take((size_t)4 * H * L.T_pad * 4);
+        L.cn = L.take((size_t)2 * (epi_warps(kModeCNorm, false) / 4) * H * L.T_pad * 4);
         L.rho = L.take((size_t)H * L.T_pad * 4);
         L.inv_r = L.take((size_t)L.T_pad * 4);
       }
@@ -506,7 +506,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     p.partial = cn;
     p.x_bf16 = x_b;
     if ((st = run_tile(maps, p, s)) != AFF_OK) return st;
-    AFF_CUDA(launch_loo_rho(cn, inv_r, rho, T, (int)L.T_pad, H, D, s));
+    AFF_CUDA(launch_loo_rho(cn, inv_r, rho, T, (int)L.T_pad, H, D, epi_warps(kModeCNorm, false) / 4, s));
   }
   int epi_groups = 2;   // column groups per token tile in the partial sums (set below)
   // FO / ADD / LOO: per token tile, operating point (FO, LOO) then every head.

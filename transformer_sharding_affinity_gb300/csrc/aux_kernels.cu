@@ -269,15 +269,18 @@ __global__ void to_fp16_kernel(const uint16_t* __restrict__ in, __half* __restri
 //   rms(x - c)^2 / r^2 = 1 + (CC - 2 XD / r) / D.
 // Padding tokens (t >= T) get rho = 1; they carry no signal.
 __global__ void loo_rho_kernel(const float* __restrict__ cn, const float* __restrict__ inv_r, float* __restrict__ rho,
-                               int T, int T_pad, int H, int D) {
+                               int T, int T_pad, int H, int D, int groups) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   const int h = blockIdx.y;
   if (t >= T_pad) return;
   float v = 1.0f;
   if (t < T) {
     const size_t plane = (size_t)H * T_pad, at = (size_t)h * T_pad + t;
-    const float cc = cn[0 * plane + at] + cn[2 * plane + at];   // halves 0 and 1 of quantity 0
-    const float xd = cn[1 * plane + at] + cn[3 * plane + at];   // halves 0 and 1 of quantity 1
+    float cc = 0.f, xd = 0.f;   // column groups in order: [group][quantity][H][T_pad]
+    for (int g = 0; g < groups; ++g) {
+      cc += cn[(size_t)(2 * g) * plane + at];
+      xd += cn[(size_t)(2 * g + 1) * plane + at];
+    }
     const float q = 1.0f + (cc - 2.0f * xd * inv_r[t]) / (float)D;
     v = rsqrtf(fmaxf(q, 1e-30f));
   }
@@ -576,8 +579,8 @@ cudaError_t launch_to_fp16(const uint16_t* in, __half* out, size_t n, uint32_t* 
 }
 
 cudaError_t launch_loo_rho(const float* cn, const float* inv_r, float* rho, int T, int T_pad, int H, int D,
-                           cudaStream_t s) {
-  loo_rho_kernel<<<dim3((T_pad + 255) / 256, H), 256, 0, s>>>(cn, inv_r, rho, T, T_pad, H, D);
+                           int groups, cudaStream_t s) {
+  loo_rho_kernel<<<dim3((T_pad + 255) / 256, H), 256, 0, s>>>(cn, inv_r, rho, T, T_pad, H, D, groups);
   return cudaGetLastError();
 }
 

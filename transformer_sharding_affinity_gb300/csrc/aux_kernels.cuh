@@ -22,7 +22,7 @@ cudaError_t launch_finalize_up(const double* sh, const float* wdn, int fo, int T
 cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, cudaStream_t s);
 cudaError_t launch_to_fp16(const uint16_t* in, __half* out, size_t n, uint32_t* status, cudaStream_t s);
 cudaError_t launch_loo_rho(const float* cn, const float* inv_r, float* rho, int T, int T_pad, int H, int D,
-                           cudaStream_t s);
+                           int groups, cudaStream_t s);
 cudaError_t launch_prep_wd(const uint16_t* Wd, __half* Wd16, __half* WdT16, int D, int I, int I_pad, uint32_t* status,
                            cudaStream_t s);
 cudaError_t launch_prep_qkv(const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* gamma_next,

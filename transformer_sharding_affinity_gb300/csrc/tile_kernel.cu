@@ -715,19 +715,19 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
           // D1 = (c_h / r)[t1][d], D2 = ...[t2][d]: accumulate sum_d (c/r)^2 and sum_d x (c/r)
           const int t1 = J.t0 + row, t2 = J.t0 + kBlockM + row;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < CW / 16; ++c) {
             uint32_t v1[16], v2[16];
             tmem_ld16(c1 + c * 16, v1);
             tmem_ld16(c2 + c * 16, v2);
             tmem_ld_wait();
-            if (c == 3) {
+            if (c == CW / 16 - 1) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(&sm.tempty[b]);
             }
             // columns past D hold zeros (the B tile was zero-filled), so only x needs a guard;
             // D % 8 == 0, so an 8-column group is either wholly inside or wholly past D
-            const int d0 = J.nt * kBlockN + hf * 64 + c * 16;
+            const int d0 = J.nt * kBlockN + hf * CW + c * 16;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const float a1 = __uint_as_float(v1[i]), a2 = __uint_as_float(v2[i]);
@@ -813,7 +813,7 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
         ss2 = 0.f;
       }
       if constexpr (MODE == kModeCNorm) {
-        // [hf][quantity][H][T_pad]: quantity 0 = sum (c/r)^2, 1 = sum x (c/r)
+        // [column group][quantity][H][T_pad]: quantity 0 = sum (c/r)^2, 1 = sum x (c/r)
         const int t1 = U.base + row, t2 = U.base + kBlockM + row;
         float* cc = p.partial + ((size_t)(hf * 2 + 0) * p.H + U.head) * p.T_pad;
         float* xd = p.partial + ((size_t)(hf * 2 + 1) * p.H + U.head) * p.T_pad;

@@ -283,6 +283,8 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling runs on a smaller case)")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step in a CUDA graph and time its replays")
     ap.add_argument("--path", default="scores", choices=["scores", "layout"],
                     help="scores: the S_up calibration pass (default); layout: the layout search")
     args = ap.parse_args()
@@ -340,6 +342,21 @@ def main() -> None:
     st = B.device_status(work)
     if st != 0:
         raise RuntimeError(f"device status {st}: {B.strerror(st)}")
+    graph = None
+    kern_direct = []
+    if args.graph:
+        # the dominant kernel's time comes from direct calls (events recorded inside a
+        # graph are not timing events); the timed loop then replays one captured step
+        for i in range(min(args.steps, 20)):
+            step(i)
+        torch.cuda.synchronize()
+        kern_direct = [ev_k0[i].elapsed_time(ev_k1[i]) for i in range(min(args.steps, 20))]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            B.affinity_up(dev["a"], dev["x"], dev["Wo"], dev["gamma"], dev["Wg"], dev["Wu"], dev["Wd"], d, mode, S,
+                          None, work, torch.cuda.current_stream())
+        for _ in range(args.warmup):
+            graph.replay()
 
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
@@ -348,13 +365,18 @@ def main() -> None:
     with ClockSampler(local) as clocks:
         t0.record()
         for i in range(args.steps):
-            step(i)
+            if graph is None:
+                step(i)
+            else:
+                graph.replay()
         t1.record()
         torch.cuda.synchronize()
+
     if ws > 1:
         torch.distributed.barrier()
     ms = t0.elapsed_time(t1)
-    kern_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(ev_k0, ev_k1)]))
+    kern_ms = float(np.mean(kern_direct if graph is not None else
+                            [a.elapsed_time(b) for a, b in zip(ev_k0, ev_k1)]))
     st = B.device_status(work)
     if st != 0:
         raise RuntimeError(f"device status {st}: {B.strerror(st)}")
@@ -418,6 +440,7 @@ def main() -> None:
         "data": "synthetic",
         "config": {"workload": args.workload, "T": shape.T, "D": shape.D, "H": shape.H, "G": shape.G,
                    "d_head": shape.dh, "I": shape.I, "mode": args.mode, "parallelism": f"dp{ws} (token shards)",
+                   "launch": "CUDA graph replay of one step" if graph is not None else "direct calls",
                    "l2": "inputs larger than L2 (a + x = %.0f MB per step); no flush" %
                          ((shape.T * (shape.H * shape.dh + shape.D) * 2) / 2**20)},
         "step_flops": flops_per_step,

@@ -83,3 +83,43 @@ def test_one_call_helpers_match_the_abi():
     Sd_ref = O.s_down(layer["x"], layer["gamma"], layer["Wg"], layer["Wu"], layer["Wd"], layer["gamma_next"],
                       layer["Wq_next"], layer["Wk_next"], layer["Wv_next"], SHAPE.H, SHAPE.G, SHAPE.dh, SHAPE.eps)
     assert rel_err(Sd.cpu().numpy(), Sd_ref) <= TOL
+
+
+def test_the_pass_can_be_captured_in_a_cuda_graph():
+    """affinity_up is stream-ordered with no host synchronisation, so it can be
+    captured (including its side-stream fork / join) and replayed; replays
+    are bit-identical to direct calls and follow new inputs written in place."""
+    layer = W.make_layer(SHAPE)
+    dev = DV.to_device(layer, "bf16")
+    d = dims_of(B, SHAPE)
+    ws = torch.empty(B.workspace_size(d, B.AFF_MODE_FO), dtype=torch.uint8, device="cuda")
+    S = torch.empty(SHAPE.G, SHAPE.I, device="cuda")
+
+    def call():
+        B.affinity_up(dev["a"], dev["x"], dev["Wo"], dev["gamma"], dev["Wg"], dev["Wu"], dev["Wd"], d,
+                      B.AFF_MODE_FO, S, None, ws)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()                                    # warm-up outside capture (first-use setup)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    direct = S.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    S.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert B.device_status(ws) == B.AFF_OK
+    assert torch.equal(S, direct)
+    # new activations in the same buffers: the replay computes them
+    other = W.make_layer(SHAPE.scaled(seed=SHAPE.seed + 1))
+    dev["a"].copy_(DV.host_tensor(other, "a", "bf16").cuda())
+    dev["x"].copy_(DV.host_tensor(other, "x", "bf16").cuda())
+    g.replay()
+    torch.cuda.synchronize()
+    ref = dict(layer)
+    ref["a"], ref["x"] = other["a"], other["x"]
+    S_ref, _ = oracle_up(O, SHAPE, ref, "fo")
+    assert rel_err(S.cpu().numpy(), S_ref) <= TOL

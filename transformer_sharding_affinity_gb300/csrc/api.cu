@@ -470,7 +470,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   if (loo) AFF_CUDA(launch_to_fp16((const uint16_t*)Wo, Wo16, (size_t)D * H * dh, status, ws2));
   // token side on the caller's stream meanwhile
   AFF_CUDA(launch_prep_tokens(x_b, a_b, g_b, (fo || loo) ? n16 : nullptr, a16, inv_r, T, D, H * dh, d.eps, status,
-                              s));
+                              sm_count, s));
 
   CUtensorMap maps[4];
   std::memset(maps, 0, sizeof maps);
@@ -597,7 +597,7 @@ aff_status affinity_down(const void* x, const void* gamma, const void* Wg, const
 
   AFF_CUDA(launch_prep_gate_up((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, status, s));
   AFF_CUDA(launch_prep_tokens((const uint16_t*)x, nullptr, (const uint16_t*)gamma, n16, nullptr, nullptr, T, D, 0,
-                              d.eps, status, s));
+                              d.eps, status, sm_count, s));
   AFF_CUDA(launch_prep_wd((const uint16_t*)Wd, Wd16, WdT16, D, I, I_pad, status, s));
   AFF_CUDA(launch_prep_qkv((const uint16_t*)Wq_next, (const uint16_t*)Wk_next, (const uint16_t*)Wv_next,
                            (const uint16_t*)gamma_next, Wqkv16, G, H / G, dh, D, status, s));

@@ -25,9 +25,10 @@ __global__ void prep_tokens_kernel(const uint16_t* __restrict__ x, const uint16_
                                    const uint16_t* __restrict__ gamma, __half* __restrict__ n16,
                                    __half* __restrict__ a16, float* __restrict__ inv_r, int T, int D, int HD,
                                    float eps, uint32_t* status) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp >= T) return;
+  const int n_warps = (gridDim.x * blockDim.x) >> 5;
+  bool bad = false;
+  for (int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; warp < T; warp += n_warps) {
   const size_t t = (size_t)warp;
   const uint4* xr = reinterpret_cast<const uint4*>(x + t * D);
   float ss = 0.f;
@@ -44,7 +45,6 @@ __global__ void prep_tokens_kernel(const uint16_t* __restrict__ x, const uint16_
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   const float ir = rsqrtf(ss / (float)D + eps);
   if (lane == 0 && inv_r) inv_r[t] = ir;
-  bool bad = false;
   if (n16) {
     const uint4* gr = reinterpret_cast<const uint4*>(gamma);
     uint4* nr = reinterpret_cast<uint4*>(n16 + t * D);
@@ -69,6 +69,7 @@ __global__ void prep_tokens_kernel(const uint16_t* __restrict__ x, const uint16_
       for (int i = 0; i < 8; ++i) o[i] = to_h(bf2f(e[i]) * ir, bad);
       orow[v] = *reinterpret_cast<uint4*>(o);
     }
+  }
   }
   if (bad) latch_status(status, kStatusRange);
 }
@@ -520,11 +521,26 @@ static inline int blocks_for(size_t n, int threads, int cap = 8192) {
   return (int)(b < (size_t)cap ? (b > 0 ? b : 1) : cap);
 }
 
+// At most 3 blocks of 8 warps per SM (a grid-stride loop over tokens): enough
+// loads in flight to run near HBM speed, while leaving registers for the fold
+// (one 320-thread CTA per SM), which runs concurrently on the side stream; at
+// 4 blocks the two no longer fit one SM's register file together.  Measured on
+// the Qwen3-shaped layer, the whole call: 8 blocks 2.406 ms, 4 blocks 2.388,
+// 3 blocks 2.365, 2 blocks 2.374.  The
+// kernel asks for the largest shared-memory carve-out although it uses none:
+// an SM configured for a small carve-out could not take the fold's 214 KB CTA
+// until it drained, which serialised the two.
 cudaError_t launch_prep_tokens(const uint16_t* x, const uint16_t* a, const uint16_t* gamma, __half* n16, __half* a16,
-                               float* inv_r, int T, int D, int HD, float eps, uint32_t* status, cudaStream_t s) {
+                               float* inv_r, int T, int D, int HD, float eps, uint32_t* status, int sm_count,
+                               cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(prep_tokens_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   const int warps_per_block = 8;
-  prep_tokens_kernel<<<(T + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0, s>>>(
-      x, a, gamma, n16, a16, inv_r, T, D, HD, eps, status);
+  const int want = (T + warps_per_block - 1) / warps_per_block;
+  const int cap = 3 * (sm_count > 0 ? sm_count : 1);
+  prep_tokens_kernel<<<want < cap ? want : cap, 32 * warps_per_block, 0, s>>>(x, a, gamma, n16, a16, inv_r, T, D,
+                                                                               HD, eps, status);
   return cudaGetLastError();
 }
 

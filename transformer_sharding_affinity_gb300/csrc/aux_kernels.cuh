@@ -8,7 +8,8 @@
 namespace aff {
 
 cudaError_t launch_prep_tokens(const uint16_t* x, const uint16_t* a, const uint16_t* gamma, __half* n16, __half* a16,
-                               float* inv_r, int T, int D, int HD, float eps, uint32_t* status, cudaStream_t s);
+                               float* inv_r, int T, int D, int HD, float eps, uint32_t* status, int sm_count,
+                               cudaStream_t s);
 cudaError_t launch_prep_gate_up(const uint16_t* Wg, const uint16_t* Wu, __half* W16, int I, int I_pad, int D,
                                 uint32_t* status, cudaStream_t s);
 cudaError_t launch_scaled_transpose_split(const uint16_t* W, const uint16_t* scale, __half* out, int Drows, int Ncols,

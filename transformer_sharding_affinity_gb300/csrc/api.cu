@@ -328,7 +328,7 @@ aff_status run_tile(const CUtensorMap* maps, TileParams& p, cudaStream_t s, bool
 struct SideStream {
   int dev = -1;
   cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, join_late = nullptr;
 };
 
 aff_status side_stream(SideStream** out) {
@@ -345,6 +345,7 @@ aff_status side_stream(SideStream** out) {
   AFF_CUDA(cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking));
   AFF_CUDA(cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming));
   AFF_CUDA(cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming));
+  AFF_CUDA(cudaEventCreateWithFlags(&ss.join_late, cudaEventDisableTiming));
   per_dev.push_back(ss);
   *out = &per_dev.back();
   return AFF_OK;
@@ -464,7 +465,6 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   AFF_CUDA(cudaStreamWaitEvent(ws2, side->fork, 0));
   AFF_CUDA(launch_prep_gate_up((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, status, ws2));
   AFF_CUDA(launch_scaled_transpose_split((const uint16_t*)Wo, g_b, GWo16, D, H * dh, status, ws2));
-  if (fo) AFF_CUDA(launch_wd_colnorm((const uint16_t*)Wd, wdn, D, I, I_pad, ws2));
   __half* Wo16 = loo ? reinterpret_cast<__half*>(ws + L.Wo16) : nullptr;
   float* inv_r = loo ? reinterpret_cast<float*>(ws + L.inv_r) : nullptr;
   if (loo) AFF_CUDA(launch_to_fp16((const uint16_t*)Wo, Wo16, (size_t)D * H * dh, status, ws2));
@@ -489,6 +489,9 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   }
   AFF_CUDA(cudaEventRecord(side->join, ws2));
   AFF_CUDA(cudaStreamWaitEvent(s, side->join, 0));
+  // ||w^d||^2 is needed only by the last kernel: computed after the fold, joined late
+  if (fo) AFF_CUDA(launch_wd_colnorm((const uint16_t*)Wd, wdn, D, I, I_pad, ws2));
+  AFF_CUDA(cudaEventRecord(side->join_late, ws2));
   float* rho = loo ? reinterpret_cast<float*>(ws + L.rho) : nullptr;
   if (loo) {
     // rho[h][t] = r / rms(x - c_h): tensor-core pass over (a_h / r) Wo^(h)^T with the
@@ -543,6 +546,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     if ((st = run_tile(maps, p, s, true)) != AFF_OK) return st;
   }
   AFF_CUDA(launch_reduce_partials(partial, headsum, (int)L.n_chunks, epi_groups, H, I_pad, s));
+  AFF_CUDA(cudaStreamWaitEvent(s, side->join_late, 0));
   AFF_CUDA(launch_finalize_up(headsum, wdn, fo, T, H, G, I, I_pad, S_out, S_head_out, s));
   return AFF_OK;
 }

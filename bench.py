@@ -454,7 +454,7 @@ def main() -> None:
                      "peak_source": pk["source"] + " bf16 dense (fp16 runs at the bf16 rate)",
                      "kernel_ms": kern_ms, "algorithmic_flops_per_launch": tile_flops,
                      "traffic": measured_traffic(args.workload, args.mode, shape.T)},
-        "gpu_launches": {"fo": 8, "add": 7, "loo": 10}[args.mode] * args.steps,
+        "gpu_launches": {"fo": 7, "add": 6, "loo": 9}[args.mode] * args.steps,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": shape.G * shape.I * 4, "ms_per_step": e2e_ms},
         "clocks": clocks.summary(),

@@ -128,7 +128,6 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
       // one slot per (chunk, column group of the epilogue, head, neuron)
       const int tile_mode = mode == AFF_MODE_LOO ? kModeLOO : (mode == AFF_MODE_ADD ? kModeADD : kModeFO);
       L.partial = L.take((size_t)L.n_chunks * epi_warps(tile_mode, false) / 4 * H * L.I_pad * 4);
-      L.headsum = L.take((size_t)H * L.I_pad * 8);
       if (mode == AFF_MODE_FO) L.wdn = L.take((size_t)L.I_pad * 4);
       if (mode == AFF_MODE_LOO) {
         L.Wo16 = L.take((size_t)D * H * dh * 2);
@@ -545,9 +544,9 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     epi_groups = epi_warps(p.mode, pair) / 4;
     if ((st = run_tile(maps, p, s, true)) != AFF_OK) return st;
   }
-  AFF_CUDA(launch_reduce_partials(partial, headsum, (int)L.n_chunks, epi_groups, H, I_pad, s));
   AFF_CUDA(cudaStreamWaitEvent(s, side->join_late, 0));
-  AFF_CUDA(launch_finalize_up(headsum, wdn, fo, T, H, G, I, I_pad, S_out, S_head_out, s));
+  AFF_CUDA(launch_reduce_finalize(partial, wdn, fo, (int)L.n_chunks, epi_groups, T, H, G, I, I_pad, S_out,
+                                  S_head_out, s));
   return AFF_OK;
 }
 

@@ -210,6 +210,53 @@ __global__ void reduce_partials4_kernel(const float* __restrict__ partial, doubl
   }
 }
 
+// The chunk partial sums of one KV group's heads, reduced and finalised in one
+// pass: block = 128 neurons (32 threads x 4, 16-byte loads) x 16 chunk phases,
+// one group.  For every head of the group, each thread sums its chunks in fp32
+// (at most n_chunks / 16 chunks times the column groups), the 16 phases are
+// added in fp64 in order, and
+//   S_head[h][k] = sum / T (x ||w^d_k||^2 for FO),  S_up[g][k] = sum_{h in g} S_head[h][k].
+// Needs I_pad % 128 == 0.
+__global__ void __launch_bounds__(512) reduce_finalize_kernel(const float* __restrict__ partial,
+                                                              const float* __restrict__ wdn, int fo, int n_chunks,
+                                                              int groups, int T, int H, int G, int I, int I_pad,
+                                                              float* __restrict__ S_out, float* __restrict__ S_head_out) {
+  __shared__ double part[16][32][4];
+  const int k0 = blockIdx.x * 128 + threadIdx.x * 4;
+  const int g = blockIdx.y;
+  const int hpg = H / G;
+  double total[4] = {0.0, 0.0, 0.0, 0.0};
+  for (int h = g * hpg; h < (g + 1) * hpg; ++h) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int c = threadIdx.y; c < n_chunks; c += 16)
+      for (int q = 0; q < groups; ++q) {
+        const float4 v = *reinterpret_cast<const float4*>(partial + ((size_t)(c * groups + q) * H + h) * I_pad + k0);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+    part[threadIdx.y][threadIdx.x][0] = acc.x;
+    part[threadIdx.y][threadIdx.x][1] = acc.y;
+    part[threadIdx.y][threadIdx.x][2] = acc.z;
+    part[threadIdx.y][threadIdx.x][3] = acc.w;
+    __syncthreads();
+    if (threadIdx.y == 0) {
+      for (int e = 0; e < 4; ++e) {
+        const int k = k0 + e;
+        if (k >= I) continue;
+        double t = 0.0;
+        for (int i = 0; i < 16; ++i) t += part[i][threadIdx.x][e];
+        const double v = t * ((fo ? (double)wdn[k] : 1.0) / (double)T);
+        if (S_head_out) S_head_out[(size_t)h * I + k] = (float)v;
+        total[e] += v;
+      }
+    }
+    __syncthreads();
+  }
+  if (threadIdx.y == 0)
+    for (int e = 0; e < 4; ++e)
+      if (k0 + e < I) S_out[(size_t)g * I + k0 + e] = (float)total[e];
+}
+
 // S_head[h][k] = sum_t(...) / T (x ||w^d_k||^2 for FO); S_up[g][k] = sum_{h in g} S_head[h][k].
 __global__ void finalize_up_kernel(const double* __restrict__ sh, const float* __restrict__ wdn, int fo, int T,
                                    int H, int G, int I, int I_pad, float* __restrict__ S_out,
@@ -578,6 +625,14 @@ cudaError_t launch_reduce_partials(const float* partial, double* out, int n_chun
     dim3 grid((I_pad + 31) / 32, H), block(32, 8);
     reduce_partials_kernel<<<grid, block, 0, s>>>(partial, out, n_chunks, halves, H, I_pad);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_finalize(const float* partial, const float* wdn, int fo, int n_chunks, int groups, int T,
+                                   int H, int G, int I, int I_pad, float* S_out, float* S_head_out, cudaStream_t s) {
+  dim3 grid(I_pad / 128, G), block(32, 16);
+  reduce_finalize_kernel<<<grid, block, 0, s>>>(partial, wdn, fo, n_chunks, groups, T, H, G, I, I_pad, S_out,
+                                                S_head_out);
   return cudaGetLastError();
 }
 

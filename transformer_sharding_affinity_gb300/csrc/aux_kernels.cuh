@@ -18,6 +18,8 @@ cudaError_t launch_wd_colnorm(const uint16_t* Wd, float* wdn, int D, int I, int 
 cudaError_t launch_wd_colnorm_f32(const float* Wd, float* wdn, int D, int I, cudaStream_t s);
 cudaError_t launch_reduce_partials(const float* partial, double* out, int n_chunks, int halves, int H, int I_pad,
                                    cudaStream_t s);
+cudaError_t launch_reduce_finalize(const float* partial, const float* wdn, int fo, int n_chunks, int groups, int T,
+                                   int H, int G, int I, int I_pad, float* S_out, float* S_head_out, cudaStream_t s);
 cudaError_t launch_finalize_up(const double* sh, const float* wdn, int fo, int T, int H, int G, int I, int I_pad,
                                float* S_out, float* S_head_out, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, cudaStream_t s);

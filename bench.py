@@ -277,7 +277,7 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_0p6b_layer")
-    ap.add_argument("--mode", default="fo", choices=["fo", "add", "loo"])
+    ap.add_argument("--mode", default="fo", choices=["fo", "add", "loo", "down"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -313,14 +313,24 @@ def main() -> None:
     if args.tokens:
         base = base.scaled(T=args.tokens)
     shape = base.scaled(seed=base.seed + 1000 * rank)     # each rank: its own token batch
-    layer = W.make_layer(shape)
-    host = {k: DV.host_tensor(layer, k, shape.dtype).pin_memory() for k in DV.UP_KEYS}
+    down = args.mode == "down"
+    keys = DV.DOWN_KEYS if down else DV.UP_KEYS
+    layer = W.make_layer(shape, with_next=down)
+    host = {k: DV.host_tensor(layer, k, shape.dtype).pin_memory() for k in keys}
     dev = {k: v.to("cuda") for k, v in host.items()}
     d = B.dims(shape.T, shape.D, shape.H, shape.G, shape.dh, shape.I, shape.eps)
-    mode = B.MODES[args.mode]
-    work = torch.empty(B.workspace_size(d, mode), dtype=torch.uint8, device="cuda")
-    S = torch.empty(shape.G, shape.I, device="cuda")
+    mode = 0 if down else B.MODES[args.mode]
+    work = torch.empty(B.workspace_size(d, mode, down=down), dtype=torch.uint8, device="cuda")
+    S = torch.empty((shape.I, shape.G) if down else (shape.G, shape.I), device="cuda")
     stream = torch.cuda.current_stream()
+
+    def call(t):
+        if down:
+            B.affinity_down(t["x"], t["gamma"], t["Wg"], t["Wu"], t["Wd"], t["gamma_next"], t["Wq_next"],
+                            t["Wk_next"], t["Wv_next"], d, S, work, stream)
+        else:
+            B.affinity_up(t["a"], t["x"], t["Wo"], t["gamma"], t["Wg"], t["Wu"], t["Wd"], d, mode, S, None, work,
+                          stream)
 
     ev_k0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev_k1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -331,9 +341,7 @@ def main() -> None:
     def step(i=None, bufs=dev):
         if i is not None:
             B.set_timing_events(ev_k0[i], ev_k1[i])
-        t = bufs
-        B.affinity_up(t["a"], t["x"], t["Wo"], t["gamma"], t["Wg"], t["Wu"], t["Wd"], d, mode, S, None, work,
-                      stream)
+        call(bufs)
         if i is not None:
             B.set_timing_events(None, None)
 
@@ -353,8 +361,9 @@ def main() -> None:
         kern_direct = [ev_k0[i].elapsed_time(ev_k1[i]) for i in range(min(args.steps, 20))]
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            B.affinity_up(dev["a"], dev["x"], dev["Wo"], dev["gamma"], dev["Wg"], dev["Wu"], dev["Wd"], d, mode, S,
-                          None, work, torch.cuda.current_stream())
+            stream = torch.cuda.current_stream()
+            call(dev)
+        stream = torch.cuda.current_stream()
         for _ in range(args.warmup):
             graph.replay()
 
@@ -392,7 +401,7 @@ def main() -> None:
     # compute of step i; a buffer set is refilled only after the step that
     # read it has finished.
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    S_host = torch.empty(shape.G, shape.I, pin_memory=True)
+    S_host = torch.empty(tuple(S.shape), pin_memory=True)
     bufs = [dev, {k: torch.empty_like(v) for k, v in dev.items()}]
     copy_stream = torch.cuda.Stream()
     ready = [torch.cuda.Event() for _ in range(2)]
@@ -406,7 +415,7 @@ def main() -> None:
         with torch.cuda.stream(copy_stream):
             if i >= 2:
                 copy_stream.wait_event(free[j])
-            for k in DV.UP_KEYS:
+            for k in keys:
                 bufs[j][k].copy_(host[k], non_blocking=True)
             ready[j].record(copy_stream)
         stream.wait_event(ready[j])
@@ -428,9 +437,13 @@ def main() -> None:
         flops_per_step, tile_flops = fl["total"], fl["tile_kernel"]
     elif args.mode == "add":
         flops_per_step, tile_flops = fl["fold"] + heads, heads
-    else:   # loo: the FO-shaped pass plus c_h / r = (a_h / r) Wo^(h)^T for the rms of x - c_h
+    elif args.mode == "loo":   # the FO-shaped pass plus c_h / r = (a_h / r) Wo^(h)^T for the rms of x - c_h
         flops_per_step = fl["total"] + 2 * shape.T * shape.H * shape.dh * shape.D
         tile_flops = fl["tile_kernel"]
+    else:   # down: gate/up GEMM for alpha, x' = x + alpha Wd^T, ||W^qkv_g (gamma' * w^d_k)||^2 (hi + lo)
+        tile_flops = fl["gate_up"]
+        flops_per_step = tile_flops + 2 * shape.T * shape.I * shape.D + \
+            2 * 2 * (shape.H + 2 * shape.G) * shape.dh * shape.D * shape.I
     achieved = tile_flops / (kern_ms * 1e-3) / 1e12
     tokens = shape.T * ws
     line = {
@@ -446,20 +459,23 @@ def main() -> None:
         "step_flops": flops_per_step,
         "step_tflops": flops_per_step / (ms_step * 1e-3) / 1e12,
         "step_frac_of_peak": flops_per_step / (ms_step * 1e-3) / 1e12 / pk["bf16_tflops"],
-        "roofline": {"bound": "tensor", "kernel": f"affinity_tile_kernel<{args.mode.upper()}> "
-                                                  "(operating point + per-head contraction)",
+        "roofline": {"bound": "tensor",
+                     "kernel": ("affinity_tile_kernel<ALPHA> (gate/up GEMM, alpha = silu(g) u)" if down else
+                                f"affinity_tile_kernel<{args.mode.upper()}> (operating point + per-head contraction)"),
                      "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / pk["bf16_tflops"],
                      "frac_sustained": achieved / pk["bf16_tflops_sustained"] if pk["bf16_tflops_sustained"] else None,
                      "peak_source": pk["source"] + " bf16 dense (fp16 runs at the bf16 rate)",
                      "kernel_ms": kern_ms, "algorithmic_flops_per_launch": tile_flops,
                      "traffic": measured_traffic(args.workload, args.mode, shape.T)},
-        "gpu_launches": {"fo": 7, "add": 6, "loo": 9}[args.mode] * args.steps,
+        "gpu_launches": {"fo": 7, "add": 6, "loo": 9, "down": 9}[args.mode] * args.steps,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": shape.G * shape.I * 4, "ms_per_step": e2e_ms},
         "clocks": clocks.summary(),
     }
-    if not args.no_cpu_baseline and ws == 1:
+    if down:
+        line["metric"] = "calibration tokens/sec for S^down affinity per layer; % of GB300 bf16 tensor peak"
+    if not args.no_cpu_baseline and ws == 1 and not down:
         line["cpu_baseline"] = cpu_oracle_rate(shape, layer, args.cpu_budget)
     print(json.dumps(line), flush=True)
     if ws > 1:

@@ -642,7 +642,7 @@ aff_status affinity_down(const void* x, const void* gamma, const void* Wg, const
     TileParams p = base_params(d, L, ws, kModeQNorm);
     p.n_ntiles = (int)ceil_div(L.Rg, 128);
     p.rows_per_group = (int)L.Rg;
-    p.n_units = (int)ceil_div(I_pad, 256);
+    p.n_units = (int)(ceil_div(I_pad, 256) * G);
     p.bnorm = bnorm;
     if ((st = run_tile(maps, p, s)) != AFF_OK) return st;
   }

@@ -383,21 +383,39 @@ __global__ void prep_qkv_kernel(const uint16_t* __restrict__ Wq, const uint16_t*
 
 // cpart[c][k] = sum over the tokens t of chunk c of alpha_tk^2 / r'_t^2, with
 // 1/r'^2 = 1 / ((ss0 + ss1)/D + eps) from the two halves of sum_d x'^2.
+// cpart[c][k] = sum over the tokens t of chunk c of alpha_tk^2 / r'_t^2, with
+// 1/r'_t^2 = 1 / (sum_d x'_td^2 / D + eps) from the two column halves of ssx.
+// Block = one chunk of tokens x 1024 neurons (8 per thread, 16-byte loads of
+// alpha); the chunk's token weights are formed once, in shared memory.
 __global__ void down_token_weights_kernel(const __half* __restrict__ alpha16, const float* __restrict__ ssx,
                                           float* __restrict__ cpart, int T, int T_pad, int D, int I_pad,
                                           int chunk, float eps) {
-  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  extern __shared__ float w_tok[];   // [chunk]
   const int c = blockIdx.y;
-  if (k >= I_pad) return;
-  const int t0 = c * chunk, t1 = min(T, t0 + chunk);
-  float s = 0.f;
-  for (int t = t0; t < t1; ++t) {
-    const float ssum = ssx[t] + ssx[(size_t)T_pad + t];
-    const float w = 1.0f / (ssum / (float)D + eps);
-    const float al = __half2float(alpha16[(size_t)t * I_pad + k]);
-    s = fmaf(al * al, w, s);
+  const int t0 = c * chunk, n = min(T, t0 + chunk) - t0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const float ssum = ssx[t0 + i] + ssx[(size_t)T_pad + t0 + i];
+    w_tok[i] = 1.0f / (ssum / (float)D + eps);
   }
-  cpart[(size_t)c * I_pad + k] = s;
+  __syncthreads();
+  const int k0 = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (k0 >= I_pad) return;
+  float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int i = 0; i < n; ++i) {
+    const uint4 q = __ldg(reinterpret_cast<const uint4*>(alpha16 + (size_t)(t0 + i) * I_pad + k0));
+    const __half2* h = reinterpret_cast<const __half2*>(&q);
+    const float w = w_tok[i];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __half22float2(h[e]);
+      s[2 * e] = fmaf(f.x * f.x, w, s[2 * e]);
+      s[2 * e + 1] = fmaf(f.y * f.y, w, s[2 * e + 1]);
+    }
+  }
+  float4* dst = reinterpret_cast<float4*>(cpart + (size_t)c * I_pad + k0);
+  dst[0] = make_float4(s[0], s[1], s[2], s[3]);
+  dst[1] = make_float4(s[4], s[5], s[6], s[7]);
 }
 
 // S_down[k][g] = (sum_c cpart[c][k] / T) * (bn[0][k][g] + bn[1][k][g])  (fp64 sums, fixed order)
@@ -671,8 +689,9 @@ cudaError_t launch_prep_qkv(const uint16_t* Wq, const uint16_t* Wk, const uint16
 
 cudaError_t launch_down_token_weights(const __half* alpha16, const float* ssx, float* cpart, int T, int T_pad, int D,
                                       int I_pad, int chunk, float eps, cudaStream_t s) {
-  dim3 grid((I_pad + 127) / 128, (T + chunk - 1) / chunk);
-  down_token_weights_kernel<<<grid, 128, 0, s>>>(alpha16, ssx, cpart, T, T_pad, D, I_pad, chunk, eps);
+  dim3 grid((I_pad / 8 + 127) / 128, (T + chunk - 1) / chunk);
+  down_token_weights_kernel<<<grid, 128, (size_t)chunk * sizeof(float), s>>>(alpha16, ssx, cpart, T, T_pad, D,
+                                                                             I_pad, chunk, eps);
   return cudaGetLastError();
 }
 

@@ -50,7 +50,7 @@ struct Unit {
   int kt;
   int tile0;    // FO/ADD/LOO/alpha: first token tile
   int base;     // x', cnorm: first token; qnorm: first neuron
-  int head;     // cnorm: head
+  int head;     // cnorm: head; qnorm: KV group
 };
 
 // Unit u of the schedule.  With CTA pairs (FO / ADD) a unit covers 256 neurons:
@@ -97,9 +97,10 @@ __device__ __forceinline__ Unit unit_info(const TileParams& p, int u, int rank) 
       U.base = u * 2 * kBlockM;
       U.njobs = p.n_ntiles;
       break;
-    case kModeQNorm:
-      U.base = u * 2 * kBlockM;
-      U.njobs = p.G * p.n_ntiles;
+    case kModeQNorm:   // one unit per (256 neurons, KV group): the group's row tiles
+      U.base = (u / p.G) * 2 * kBlockM;
+      U.head = u % p.G;
+      U.njobs = p.n_ntiles;
       break;
   }
   U.njobs_pm = U.njobs;
@@ -160,8 +161,7 @@ __device__ __forceinline__ Job job_next(const TileParams& p, const Unit& U, JobI
     J.t0 = U.base; J.head = U.head; J.nt = it.b++;
   } else {   // kModeQNorm
     J.kind = kJobQNorm; J.nkb = 2 * p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D;
-    J.g = it.a; J.nt = it.b;
-    if (++it.b == p.n_ntiles) { it.b = 0; ++it.a; }
+    J.g = U.head; J.nt = it.b++;
   }
   return J;
 }
@@ -692,20 +692,33 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
                     mbar_arrive(&sm.tempty[b]);
                 }
             }
+            // D % 8 == 0: an 8-column group is wholly inside or wholly past D; x is read 16 B at a time
             const int d0 = J.nt * kBlockN + hf * 64 + c * 16;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int d = d0 + i;
+            for (int q = 0; q < 2; ++q) {
+              const int d = d0 + q * 8;
               if (d < p.D) {
                 if (t1 < p.T) {
-                  const float xv = __uint_as_float((uint32_t)p.x_bf16[(size_t)t1 * p.D + d] << 16);
-                  const float v = xv + __uint_as_float(v1[i]);
-                  ss1 = fmaf(v, v, ss1);
+                  const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.x_bf16 + (size_t)t1 * p.D + d));
+                  const uint32_t e[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    const float v0 = __uint_as_float(e[i] << 16) + __uint_as_float(v1[q * 8 + 2 * i]);
+                    const float v1_ = __uint_as_float(e[i] & 0xFFFF0000u) + __uint_as_float(v1[q * 8 + 2 * i + 1]);
+                    ss1 = fmaf(v0, v0, ss1);
+                    ss1 = fmaf(v1_, v1_, ss1);
+                  }
                 }
                 if (t2 < p.T) {
-                  const float xv = __uint_as_float((uint32_t)p.x_bf16[(size_t)t2 * p.D + d] << 16);
-                  const float v = xv + __uint_as_float(v2[i]);
-                  ss2 = fmaf(v, v, ss2);
+                  const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.x_bf16 + (size_t)t2 * p.D + d));
+                  const uint32_t e[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    const float v0 = __uint_as_float(e[i] << 16) + __uint_as_float(v2[q * 8 + 2 * i]);
+                    const float v1_ = __uint_as_float(e[i] & 0xFFFF0000u) + __uint_as_float(v2[q * 8 + 2 * i + 1]);
+                    ss2 = fmaf(v0, v0, ss2);
+                    ss2 = fmaf(v1_, v1_, ss2);
+                  }
                 }
               }
             }

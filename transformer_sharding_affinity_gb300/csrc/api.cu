@@ -142,7 +142,7 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
       L.Wd16 = L.take((size_t)D * L.I_pad * 2);
       L.WdT16 = L.take((size_t)L.I_pad * D * 2);
       L.Wqkv16 = L.take((size_t)G * L.Rg * 2 * D * 2);
-      L.ssx = L.take((size_t)2 * L.T_pad * 4);
+      L.ssx = L.take((size_t)(epi_warps(kModeXPrime, false) / 4) * L.T_pad * 4);
       L.cpart = L.take((size_t)L.n_tchunks * L.I_pad * 4);
       L.bnorm = L.take((size_t)2 * L.I_pad * G * 4);
     }
@@ -630,7 +630,8 @@ aff_status affinity_down(const void* x, const void* gamma, const void* Wg, const
     p.x_bf16 = (const uint16_t*)x;
     if ((st = run_tile(maps, p, s)) != AFF_OK) return st;
   }
-  AFF_CUDA(launch_down_token_weights(alpha16, ssx, cpart, T, T_pad, D, I_pad, kDownTokenChunk, d.eps, s));
+  AFF_CUDA(launch_down_token_weights(alpha16, ssx, cpart, T, T_pad, D, I_pad, kDownTokenChunk, d.eps,
+                                     epi_warps(kModeXPrime, false) / 4, s));
   // ||b_gk||^2 for every neuron and group
   {
     if ((st = map2(&maps[0], WdT16, (uint64_t)D, (uint64_t)I_pad)) != AFF_OK) return st;

@@ -384,17 +384,18 @@ __global__ void prep_qkv_kernel(const uint16_t* __restrict__ Wq, const uint16_t*
 // cpart[c][k] = sum over the tokens t of chunk c of alpha_tk^2 / r'_t^2, with
 // 1/r'^2 = 1 / ((ss0 + ss1)/D + eps) from the two halves of sum_d x'^2.
 // cpart[c][k] = sum over the tokens t of chunk c of alpha_tk^2 / r'_t^2, with
-// 1/r'_t^2 = 1 / (sum_d x'_td^2 / D + eps) from the two column halves of ssx.
+// 1/r'_t^2 = 1 / (sum_d x'_td^2 / D + eps) from the column groups of ssx.
 // Block = one chunk of tokens x 1024 neurons (8 per thread, 16-byte loads of
 // alpha); the chunk's token weights are formed once, in shared memory.
 __global__ void down_token_weights_kernel(const __half* __restrict__ alpha16, const float* __restrict__ ssx,
                                           float* __restrict__ cpart, int T, int T_pad, int D, int I_pad,
-                                          int chunk, float eps) {
+                                          int chunk, float eps, int groups) {
   extern __shared__ float w_tok[];   // [chunk]
   const int c = blockIdx.y;
   const int t0 = c * chunk, n = min(T, t0 + chunk) - t0;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const float ssum = ssx[t0 + i] + ssx[(size_t)T_pad + t0 + i];
+    float ssum = 0.f;   // the x' pass's column groups, in order
+    for (int g = 0; g < groups; ++g) ssum += ssx[(size_t)g * T_pad + t0 + i];
     w_tok[i] = 1.0f / (ssum / (float)D + eps);
   }
   __syncthreads();
@@ -688,10 +689,10 @@ cudaError_t launch_prep_qkv(const uint16_t* Wq, const uint16_t* Wk, const uint16
 }
 
 cudaError_t launch_down_token_weights(const __half* alpha16, const float* ssx, float* cpart, int T, int T_pad, int D,
-                                      int I_pad, int chunk, float eps, cudaStream_t s) {
+                                      int I_pad, int chunk, float eps, int groups, cudaStream_t s) {
   dim3 grid((I_pad / 8 + 127) / 128, (T + chunk - 1) / chunk);
   down_token_weights_kernel<<<grid, 128, (size_t)chunk * sizeof(float), s>>>(alpha16, ssx, cpart, T, T_pad, D,
-                                                                             I_pad, chunk, eps);
+                                                                             I_pad, chunk, eps, groups);
   return cudaGetLastError();
 }
 

@@ -31,7 +31,7 @@ cudaError_t launch_prep_wd(const uint16_t* Wd, __half* Wd16, __half* WdT16, int 
 cudaError_t launch_prep_qkv(const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* gamma_next,
                             __half* out, int G, int hpg, int dh, int D, uint32_t* status, cudaStream_t s);
 cudaError_t launch_down_token_weights(const __half* alpha16, const float* ssx, float* cpart, int T, int T_pad, int D,
-                                      int I_pad, int chunk, float eps, cudaStream_t s);
+                                      int I_pad, int chunk, float eps, int groups, cudaStream_t s);
 cudaError_t launch_finalize_down(const float* cpart, const float* bnorm, int n_chunks, int bhalves, int T, int I,
                                  int I_pad, int G, float* S_out, cudaStream_t s);
 

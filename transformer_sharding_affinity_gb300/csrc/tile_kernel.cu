@@ -677,12 +677,12 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
           // D1 = (alpha Wd^T)[t1][d], D2 = ...[t2][d]; x' = x + D; accumulate x'^2 over d
           const int t1 = J.t0 + row, t2 = J.t0 + kBlockM + row;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < CW / 16; ++c) {
             uint32_t v1[16], v2[16];
             tmem_ld16(c1 + c * 16, v1);
             tmem_ld16(c2 + c * 16, v2);
             tmem_ld_wait();
-            if (c == 3) {
+            if (c == CW / 16 - 1) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) {
@@ -693,7 +693,7 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
                 }
             }
             // D % 8 == 0: an 8-column group is wholly inside or wholly past D; x is read 16 B at a time
-            const int d0 = J.nt * kBlockN + hf * 64 + c * 16;
+            const int d0 = J.nt * kBlockN + hf * CW + c * 16;
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
               const int d = d0 + q * 8;
@@ -820,7 +820,7 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
       }
       if constexpr (MODE == kModeXPrime) {
         const int t1 = U.base + row, t2 = U.base + kBlockM + row;
-        if (t1 < p.T_pad) p.partial[(size_t)hf * p.T_pad + t1] = ss1;
+        if (t1 < p.T_pad) p.partial[(size_t)hf * p.T_pad + t1] = ss1;   // [column group][T_pad]
         if (t2 < p.T_pad) p.partial[(size_t)hf * p.T_pad + t2] = ss2;
         ss1 = 0.f;
         ss2 = 0.f;

@@ -20,16 +20,16 @@ constexpr int kStageBytes = 3 * kTileBytes;           // A1 + A2 + B = 48 KB
 constexpr int kPairBRows = kBlockN / 2;
 constexpr int kPairStageBytes = 2 * kTileBytes + kPairBRows * kBlockK * 2;
 // Epilogue warps: 8 (two per TMEM lane quarter, 64 columns each), or 16 for
-// the leave-one-out passes (four per lane quarter, 32 columns each): the c_h
-// pass waits on x loads and the LOO pass on its heavier per-token arithmetic,
-// both latency-bound with 8 (3.20 -> 2.47 ms on
+// the x' pass of the down edge and the leave-one-out passes (four per lane
+// quarter, 32 columns each): the x' and c_h passes wait on x loads and the
+// LOO pass on its heavier per-token arithmetic, all latency-bound with 8 (3.20 -> 2.47 ms on
 // the Qwen3-shaped layer; FO and ADD measured slower with 16: 2.17 -> 2.34 ms
 // for FO, 96 registers a thread then).  The block is one TMA warp, one MMA
 // warp and the epilogue warps.
 constexpr int kWideEpiWarps = 16;
 constexpr int kEpiWarps = 8;
 constexpr __host__ __device__ int epi_warps(int mode, bool pair) {
-  return (!pair && (mode == 6 || mode == 7)) ? kWideEpiWarps : kEpiWarps;
+  return (!pair && (mode == 4 || mode == 6 || mode == 7)) ? kWideEpiWarps : kEpiWarps;
 }
 constexpr __host__ __device__ int block_threads(int mode, bool pair) { return 64 + 32 * epi_warps(mode, pair); }
 constexpr int kTmemCols = 512;                        // 2 buffers x (D1 128 + D2 128)

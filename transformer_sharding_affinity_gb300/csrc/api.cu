@@ -21,7 +21,7 @@
 
 namespace aff {
 cudaError_t launch_tile_kernel(const CUtensorMap* maps, const TileParams& p, int* grid, cudaStream_t stream);
-size_t tile_smem_bytes(int mode, int stages, int H, bool pair);
+size_t tile_smem_bytes(int mode, int stages, int H);
 }  // namespace aff
 
 using namespace aff;
@@ -71,6 +71,10 @@ constexpr int kTilesPerUnit = 2;      // token tiles (of 128) per FO / ADD unit
 constexpr int kDownTokenChunk = 256;  // tokens per partial sum of E_t[alpha^2 / r'^2]
 
 inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+// Partial sums of x'^2 per token that the x' pass writes: one per column tile
+// of 256 and column group of its epilogue.
+inline int xprime_groups(int64_t D) { return (int)((D + 255) / 256) * (epi_warps(kModeXPrime) / 4); }
 inline int64_t ceil_div(int64_t v, int64_t m) { return (v + m - 1) / m; }
 
 aff_status check_dims(const aff_dims* d) {
@@ -85,7 +89,7 @@ aff_status check_dims(const aff_dims* d) {
   if (d->dtype == AFF_BF16) {
     if (d->D % 8 || d->d_head % 8 || d->I % 8) return AFF_ERR_UNSUPPORTED_SHAPE;
     // per-thread head sums live in shared memory next to 2+ pipeline stages
-    if (tile_smem_bytes(kModeFO, 2, (int)d->H, false) > (size_t)kMaxDynSmem) return AFF_ERR_UNSUPPORTED_SHAPE;
+    if (tile_smem_bytes(kModeFO, 2, (int)d->H) > (size_t)kMaxDynSmem) return AFF_ERR_UNSUPPORTED_SHAPE;
     if (d->H * d->d_head > kMaxDim) return AFF_ERR_UNSUPPORTED_SHAPE;
   }
   return AFF_OK;
@@ -116,7 +120,7 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
   const int64_t T = d.T, D = d.D, H = d.H, G = d.G, dh = d.d_head, I = d.I;
   L.status = L.take(256);
   if (d.dtype == AFF_BF16) {
-    L.I_pad = round_up(I, 256);   // whole 256-neuron tiles for CTA pairs
+    L.I_pad = round_up(I, 256);
     L.T_pad = round_up(T, 128);
     L.W16 = L.take((size_t)2 * L.I_pad * D * 2);
     L.n16 = L.take((size_t)T * D * 2);
@@ -127,11 +131,11 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
       L.a16 = L.take((size_t)T * H * dh * 2);
       // one slot per (chunk, column group of the epilogue, head, neuron)
       const int tile_mode = mode == AFF_MODE_LOO ? kModeLOO : (mode == AFF_MODE_ADD ? kModeADD : kModeFO);
-      L.partial = L.take((size_t)L.n_chunks * epi_warps(tile_mode, false) / 4 * H * L.I_pad * 4);
+      L.partial = L.take((size_t)L.n_chunks * (epi_warps(tile_mode) / 4) * H * L.I_pad * 4);
       if (mode == AFF_MODE_FO) L.wdn = L.take((size_t)L.I_pad * 4);
       if (mode == AFF_MODE_LOO) {
         L.Wo16 = L.take((size_t)D * H * dh * 2);
-        L.cn = L.take((size_t)2 * (epi_warps(kModeCNorm, false) / 4) * H * L.T_pad * 4);
+        L.cn = L.take((size_t)2 * (epi_warps(kModeCNorm) / 4) * H * L.T_pad * 4);
         L.rho = L.take((size_t)H * L.T_pad * 4);
         L.inv_r = L.take((size_t)L.T_pad * 4);
       }
@@ -142,7 +146,7 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
       L.Wd16 = L.take((size_t)D * L.I_pad * 2);
       L.WdT16 = L.take((size_t)L.I_pad * D * 2);
       L.Wqkv16 = L.take((size_t)G * L.Rg * 2 * D * 2);
-      L.ssx = L.take((size_t)(epi_warps(kModeXPrime, false) / 4) * L.T_pad * 4);
+      L.ssx = L.take((size_t)xprime_groups(D) * L.T_pad * 4);
       L.cpart = L.take((size_t)L.n_tchunks * L.I_pad * 4);
       L.bnorm = L.take((size_t)2 * L.I_pad * G * 4);
     }
@@ -225,22 +229,10 @@ aff_status map2(CUtensorMap* m, const void* p, uint64_t inner, uint64_t rows) {
   return make_map(m, p, 2, d, s, 128, 1);
 }
 
-int pick_stages(int mode, int H, bool pair) {
+int pick_stages(int mode, int H) {
   for (int s = 6; s >= 2; --s)
-    if (tile_smem_bytes(mode, s, H, pair) <= (size_t)kMaxDynSmem) return s;
+    if (tile_smem_bytes(mode, s, H) <= (size_t)kMaxDynSmem) return s;
   return 0;
-}
-
-// FO / ADD run one CTA per SM by default; AFFINITY_PAIR=1 selects CTA pairs
-// (256-row cta_group::2 MMAs, each CTA loading half of every token tile).
-// Both give identical results; on the Qwen3-0.6B-shaped layer the single-CTA
-// form measured faster (2.36 vs 2.70 ms for the FO kernel).
-bool use_pairs() {
-  static bool v = [] {
-    const char* e = std::getenv("AFFINITY_PAIR");
-    return e && e[0] == '1';
-  }();
-  return v;
 }
 
 // Heads whose width is a multiple of 16 but not of 64 (e.g. 96) leave the last
@@ -273,7 +265,7 @@ TileParams base_params(const aff_dims& d, const Layout& L, uint8_t* ws, int mode
   p.nkb_I = (int)(L.I_pad / 64);
   p.ls_D = (int)(((d.D - 1) % 64) / 16 + 1);          // 16-wide K slices in the last block of D
   p.ls_dh = (int)(((d.d_head - 1) % 64) / 16 + 1);    // ... and of d_head
-  p.stages = pick_stages(mode, p.H, false);
+  p.stages = pick_stages(mode, p.H);
   if (stream_heads(d)) {
     const int64_t slices = d.H * d.d_head / 16;
     p.stream_heads = 1;
@@ -288,12 +280,12 @@ TileParams base_params(const aff_dims& d, const Layout& L, uint8_t* ws, int mode
 
 aff_status run_tile(const CUtensorMap* maps, TileParams& p, cudaStream_t s, bool dominant = false) {
   if (p.n_units <= 0) return AFF_OK;
-  // CTAs (or CTA pairs) resident at once, cached per device and configuration
+  // CTAs resident at once, cached per device and configuration
   static std::mutex mu;
   static std::vector<std::pair<std::vector<int>, int>> cache;
   int dev = 0;
   AFF_CUDA(cudaGetDevice(&dev));
-  const std::vector<int> key = {dev, p.mode, p.pair, p.stages, p.H};
+  const std::vector<int> key = {dev, p.mode, p.stages, p.H};
   int fit = 0;
   {
     std::lock_guard<std::mutex> lk(mu);
@@ -503,19 +495,17 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     maps[2] = maps[0];
     maps[3] = maps[0];
     TileParams p = base_params(d, L, ws, kModeCNorm);
-    p.n_ntiles = (int)ceil_div(D, 128);
-    p.n_units = (int)(ceil_div(L.T_pad, 256) * H);
+    p.n_ntiles = (int)ceil_div(D, 256);
+    p.n_units = (int)(L.T_pad / 128 * H);
     p.partial = cn;
     p.x_bf16 = x_b;
     if ((st = run_tile(maps, p, s)) != AFF_OK) return st;
-    AFF_CUDA(launch_loo_rho(cn, inv_r, rho, T, (int)L.T_pad, H, D, epi_warps(kModeCNorm, false) / 4, s));
+    AFF_CUDA(launch_loo_rho(cn, inv_r, rho, T, (int)L.T_pad, H, D, epi_warps(kModeCNorm) / 4, s));
   }
   int epi_groups = 2;   // column groups per token tile in the partial sums (set below)
-  // FO / ADD / LOO: per token tile, operating point (FO, LOO) then every head.
-  // With CTA pairs (FO / ADD) each CTA loads half (64 rows) of every token tile.
+  // FO / ADD / LOO: per token tile, operating point (FO, LOO) then every head
   {
-    const bool pair = use_pairs() && !loo && !stream_heads(d);
-    const uint32_t brows = pair ? 64u : 128u;
+    const uint32_t brows = 128u;
     uint64_t dx[2] = {(uint64_t)D, (uint64_t)T}, sx[1] = {(uint64_t)D * 2};
     if ((st = map2(&maps[0], W16, (uint64_t)D, (uint64_t)2 * I_pad)) != AFF_OK) return st;
     if (fo || loo) {
@@ -536,12 +526,10 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
       if ((st = make_map(&maps[3], a16, 3, da, sa, brows, 2)) != AFF_OK) return st;
     }
     TileParams p = base_params(d, L, ws, fo ? kModeFO : (loo ? kModeLOO : kModeADD));
-    p.pair = pair ? 1 : 0;
     p.rho = rho;
-    p.stages = pick_stages(p.mode, p.H, pair);
-    p.n_units = (int)(L.n_chunks * (pair ? p.n_ktiles / 2 : p.n_ktiles));
+    p.n_units = (int)(L.n_chunks * p.n_ktiles);
     p.partial = partial;
-    epi_groups = epi_warps(p.mode, pair) / 4;
+    epi_groups = epi_warps(p.mode) / 4;
     if ((st = run_tile(maps, p, s, true)) != AFF_OK) return st;
   }
   AFF_CUDA(cudaStreamWaitEvent(s, side->join_late, 0));
@@ -598,12 +586,22 @@ aff_status affinity_down(const void* x, const void* gamma, const void* Wg, const
   __half* WdT16 = reinterpret_cast<__half*>(ws + L.WdT16);
   __half* Wqkv16 = reinterpret_cast<__half*>(ws + L.Wqkv16);
 
-  AFF_CUDA(launch_prep_gate_up((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, status, s));
+  // The weight side is staged on a side stream while the tokens are normalised on
+  // the caller's stream; the side stream later runs the ||b_gk||^2 pass, which
+  // needs only weights, beside the token-weight pass.
+  SideStream* side = nullptr;
+  if ((st = side_stream(&side)) != AFF_OK) return st;
+  const cudaStream_t ws2 = side->stream;
+  AFF_CUDA(cudaEventRecord(side->fork, s));
+  AFF_CUDA(cudaStreamWaitEvent(ws2, side->fork, 0));
+  AFF_CUDA(launch_prep_gate_up((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, status, ws2));
+  AFF_CUDA(launch_prep_wd((const uint16_t*)Wd, Wd16, WdT16, D, I, I_pad, status, ws2));
+  AFF_CUDA(launch_prep_qkv((const uint16_t*)Wq_next, (const uint16_t*)Wk_next, (const uint16_t*)Wv_next,
+                           (const uint16_t*)gamma_next, Wqkv16, G, H / G, dh, D, status, ws2));
+  AFF_CUDA(cudaEventRecord(side->join, ws2));
   AFF_CUDA(launch_prep_tokens((const uint16_t*)x, nullptr, (const uint16_t*)gamma, n16, nullptr, nullptr, T, D, 0,
                               d.eps, status, sm_count, s));
-  AFF_CUDA(launch_prep_wd((const uint16_t*)Wd, Wd16, WdT16, D, I, I_pad, status, s));
-  AFF_CUDA(launch_prep_qkv((const uint16_t*)Wq_next, (const uint16_t*)Wk_next, (const uint16_t*)Wv_next,
-                           (const uint16_t*)gamma_next, Wqkv16, G, H / G, dh, D, status, s));
+  AFF_CUDA(cudaStreamWaitEvent(s, side->join, 0));
   CUtensorMap maps[4];
   std::memset(maps, 0, sizeof maps);
   // alpha = silu(g) u for every (token, neuron)
@@ -624,15 +622,16 @@ aff_status affinity_down(const void* x, const void* gamma, const void* Wg, const
     maps[2] = maps[0];
     maps[3] = maps[0];
     TileParams p = base_params(d, L, ws, kModeXPrime);
-    p.n_ntiles = (int)ceil_div(D, 128);
-    p.n_units = (int)ceil_div(T_pad, 256);
+    p.n_ntiles = (int)ceil_div(D, 256);
+    p.n_units = (int)(T_pad / 128 * p.n_ntiles);
     p.partial = ssx;
     p.x_bf16 = (const uint16_t*)x;
     if ((st = run_tile(maps, p, s)) != AFF_OK) return st;
   }
-  AFF_CUDA(launch_down_token_weights(alpha16, ssx, cpart, T, T_pad, D, I_pad, kDownTokenChunk, d.eps,
-                                     epi_warps(kModeXPrime, false) / 4, s));
-  // ||b_gk||^2 for every neuron and group
+  // ||b_gk||^2 for every neuron and group, on the side stream once the tensor-core
+  // passes before it are done
+  AFF_CUDA(cudaEventRecord(side->fork, s));
+  AFF_CUDA(cudaStreamWaitEvent(ws2, side->fork, 0));
   {
     if ((st = map2(&maps[0], WdT16, (uint64_t)D, (uint64_t)I_pad)) != AFF_OK) return st;
     uint64_t dm[4] = {(uint64_t)D, 2, (uint64_t)L.Rg, (uint64_t)G};
@@ -641,12 +640,16 @@ aff_status affinity_down(const void* x, const void* gamma, const void* Wg, const
     maps[2] = maps[0];
     maps[3] = maps[0];
     TileParams p = base_params(d, L, ws, kModeQNorm);
-    p.n_ntiles = (int)ceil_div(L.Rg, 128);
+    p.n_ntiles = (int)ceil_div(L.Rg, 256);
     p.rows_per_group = (int)L.Rg;
-    p.n_units = (int)(ceil_div(I_pad, 256) * G);
+    p.n_units = (int)(I_pad / 128 * G);
     p.bnorm = bnorm;
-    if ((st = run_tile(maps, p, s)) != AFF_OK) return st;
+    if ((st = run_tile(maps, p, ws2)) != AFF_OK) return st;
   }
+  AFF_CUDA(cudaEventRecord(side->join_late, ws2));
+  AFF_CUDA(launch_down_token_weights(alpha16, ssx, cpart, T, T_pad, D, I_pad, kDownTokenChunk, d.eps,
+                                     xprime_groups(D), s));
+  AFF_CUDA(cudaStreamWaitEvent(s, side->join_late, 0));
   AFF_CUDA(launch_finalize_down(cpart, bnorm, (int)L.n_tchunks, 2, T, I, I_pad, G, S_out, s));
   return AFF_OK;
 }

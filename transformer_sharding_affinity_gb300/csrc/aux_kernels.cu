@@ -212,9 +212,9 @@ __global__ void reduce_partials4_kernel(const float* __restrict__ partial, doubl
 
 // The chunk partial sums of one KV group's heads, reduced and finalised in one
 // pass: block = 128 neurons (32 threads x 4, 16-byte loads) x 16 chunk phases,
-// one group.  For every head of the group, each thread sums its chunks in fp32
-// (at most n_chunks / 16 chunks times the column groups), the 16 phases are
-// added in fp64 in order, and
+// one group.  For every head of the group, each thread sums its chunks of the
+// [n_chunks][groups][H][I_pad] partials in fp32 (at most n_chunks / 16 chunks
+// times the column groups), the 16 phases are added in fp64 in order, and
 //   S_head[h][k] = sum / T (x ||w^d_k||^2 for FO),  S_up[g][k] = sum_{h in g} S_head[h][k].
 // Needs I_pad % 128 == 0.
 __global__ void __launch_bounds__(512) reduce_finalize_kernel(const float* __restrict__ partial,
@@ -382,9 +382,8 @@ __global__ void prep_qkv_kernel(const uint16_t* __restrict__ Wq, const uint16_t*
 }
 
 // cpart[c][k] = sum over the tokens t of chunk c of alpha_tk^2 / r'_t^2, with
-// 1/r'^2 = 1 / ((ss0 + ss1)/D + eps) from the two halves of sum_d x'^2.
-// cpart[c][k] = sum over the tokens t of chunk c of alpha_tk^2 / r'_t^2, with
-// 1/r'_t^2 = 1 / (sum_d x'_td^2 / D + eps) from the column groups of ssx.
+// 1/r'_t^2 = 1 / (sum_d x'_td^2 / D + eps) from the partial sums of ssx (one per
+// column tile and column group of the x' pass).
 // Block = one chunk of tokens x 1024 neurons (8 per thread, 16-byte loads of
 // alpha); the chunk's token weights are formed once, in shared memory.
 __global__ void down_token_weights_kernel(const __half* __restrict__ alpha16, const float* __restrict__ ssx,
@@ -393,10 +392,19 @@ __global__ void down_token_weights_kernel(const __half* __restrict__ alpha16, co
   extern __shared__ float w_tok[];   // [chunk]
   const int c = blockIdx.y;
   const int t0 = c * chunk, n = min(T, t0 + chunk) - t0;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    float ssum = 0.f;   // the x' pass's column groups, in order
-    for (int g = 0; g < groups; ++g) ssum += ssx[(size_t)g * T_pad + t0 + i];
-    w_tok[i] = 1.0f / (ssum / (float)D + eps);
+  // two tokens per thread, their loads interleaved; the partial sums in their order
+  for (int i = threadIdx.x; i < n; i += 2 * blockDim.x) {
+    const int i2 = i + blockDim.x;
+    const bool two = i2 < n;
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll 8
+    for (int g = 0; g < groups; ++g) {
+      const float* row = ssx + (size_t)g * T_pad + t0;
+      s0 += row[i];
+      if (two) s1 += row[i2];
+    }
+    w_tok[i] = 1.0f / (s0 / (float)D + eps);
+    if (two) w_tok[i2] = 1.0f / (s1 / (float)D + eps);
   }
   __syncthreads();
   const int k0 = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
@@ -420,12 +428,26 @@ __global__ void down_token_weights_kernel(const __half* __restrict__ alpha16, co
 }
 
 // S_down[k][g] = (sum_c cpart[c][k] / T) * (bn[0][k][g] + bn[1][k][g])  (fp64 sums, fixed order)
-__global__ void finalize_down_kernel(const float* __restrict__ cpart, const float* __restrict__ bnorm, int n_chunks,
-                                     int bhalves, int T, int I, int I_pad, int G, float* __restrict__ S_out) {
-  const int k = blockIdx.x * blockDim.x + threadIdx.x;
-  if (k >= I) return;
+// Block = 32 neurons x 8 warps; warp w sums chunks w, w + 8, ... and the eight
+// partial sums are added in warp order.
+__global__ void __launch_bounds__(256) finalize_down_kernel(const float* __restrict__ cpart,
+                                                            const float* __restrict__ bnorm, int n_chunks,
+                                                            int bhalves, int T, int I, int I_pad, int G,
+                                                            float* __restrict__ S_out) {
+  __shared__ double part[8][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int k = blockIdx.x * 32 + lane;
+  double cw = 0.0;
+  if (k < I) {
+#pragma unroll 8
+    for (int i = w; i < n_chunks; i += 8) cw += (double)cpart[(size_t)i * I_pad + k];
+  }
+  part[w][lane] = cw;
+  __syncthreads();
+  if (w != 0 || k >= I) return;
   double c = 0.0;
-  for (int i = 0; i < n_chunks; ++i) c += (double)cpart[(size_t)i * I_pad + k];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) c += part[q][lane];
   c /= (double)T;
   for (int g = 0; g < G; ++g) {
     double b = 0.0;
@@ -698,7 +720,7 @@ cudaError_t launch_down_token_weights(const __half* alpha16, const float* ssx, f
 
 cudaError_t launch_finalize_down(const float* cpart, const float* bnorm, int n_chunks, int bhalves, int T, int I,
                                  int I_pad, int G, float* S_out, cudaStream_t s) {
-  finalize_down_kernel<<<(I + 127) / 128, 128, 0, s>>>(cpart, bnorm, n_chunks, bhalves, T, I, I_pad, G, S_out);
+  finalize_down_kernel<<<(I + 31) / 32, 256, 0, s>>>(cpart, bnorm, n_chunks, bhalves, T, I, I_pad, G, S_out);
   return cudaGetLastError();
 }
 

@@ -5,16 +5,16 @@
 // One CTA per SM (227 KB of shared memory, all 512 TMEM columns).  Warp
 // roles:
 //   warp 0       TMA producer: a ring of `stages` 48 KB stages, each holding
-//                two 128 x 64 A tiles and one 128 x 64 B tile (fp16, 128 B
-//                swizzle);
-//   warp 1       MMA issuer (one thread): for every K slice of 16, two
-//                tcgen05.mma (M=128, N=128) into a pair of fp32 accumulators
-//                D1 = A1 B^T, D2 = A2 B^T in tensor memory; two such pairs
-//                (buffers) alternate so the epilogue of one job overlaps the
-//                MMAs of the next;
-//   warps 2..9   epilogue: TMEM -> registers with tcgen05.ld; warp w reads
-//                TMEM lanes 32*(w%4)..+31 (one row of A each) and half
-//                (w-2)/4 of the 128 columns.
+//                three 128 x 64 tiles (fp16, 128 B swizzle);
+//   warp 1       MMA issuer (one thread).  Most passes: for every K slice
+//                of 16, two tcgen05.mma (M = 128, N = 128) into a pair of fp32
+//                accumulators D1 = A1 B^T, D2 = A2 B^T.  The alpha pass: one
+//                MMA with M = 128 tokens (the third tile) and N = 256 (the
+//                gate and up tiles back to back), so its TMEM lanes are
+//                tokens.  Two accumulator buffers of 256 columns alternate so
+//                the epilogue of one job overlaps the MMAs of the next;
+//   warps 2..    epilogue: TMEM -> registers with tcgen05.ld; warp w reads
+//                TMEM lanes 32*(w%4)..+31 and one column group (w-2)/4.
 // Work is a fixed list of units, each a short list of jobs; CTAs take units
 // round-robin.  Which CTA computes a unit never changes its result, and
 // every unit writes its own partial sums, so the outputs do not depend on
@@ -53,21 +53,10 @@ struct Unit {
   int head;     // cnorm: head; qnorm: KV group
 };
 
-// Unit u of the schedule.  With CTA pairs (FO / ADD) a unit covers 256 neurons:
-// the CTA of cluster rank `rank` owns neuron tile 2 * (u % (n_ktiles / 2)) + rank.
-template <bool PAIR, bool STREAM = false>
-__device__ __forceinline__ Unit unit_info(const TileParams& p, int u, int rank) {
+// Unit u of the schedule.
+template <bool STREAM = false>
+__device__ __forceinline__ Unit unit_info(const TileParams& p, int u) {
   Unit U{};
-  if (PAIR) {
-    const int npair = p.n_ktiles >> 1;
-    U.kt = 2 * (u % npair) + rank;
-    U.chunk = u / npair;
-    U.tile0 = U.chunk * p.tiles_per_unit;
-    const int nt = min(p.tiles_per_unit, p.n_ttiles - U.tile0);
-    U.njobs = nt * (p.mode == kModeFO ? 1 + p.H : p.H);
-    U.njobs_pm = U.njobs;
-    return U;
-  }
   switch (p.mode) {
     case kModeFold:
       U.kt = u % p.n_ktiles;
@@ -88,17 +77,18 @@ __device__ __forceinline__ Unit unit_info(const TileParams& p, int u, int rank) 
       U.njobs_pm = (STREAM && p.mode != kModeAlpha) ? nt * (op ? 2 : 1) : U.njobs;
       return U;
     }
-    case kModeCNorm:   // consecutive units: the heads of one 256-token block
+    case kModeCNorm:   // consecutive units: the heads of one token tile; jobs: column tiles of 256
       U.head = u % p.H;
-      U.base = (u / p.H) * 2 * kBlockM;
+      U.base = (u / p.H) * kBlockM;
       U.njobs = p.n_ntiles;
       break;
-    case kModeXPrime:
-      U.base = u * 2 * kBlockM;
-      U.njobs = p.n_ntiles;
+    case kModeXPrime:   // one unit per (token tile, 256 columns d)
+      U.base = (u / p.n_ntiles) * kBlockM;
+      U.head = u % p.n_ntiles;   // the column tile
+      U.njobs = 1;
       break;
-    case kModeQNorm:   // one unit per (256 neurons, KV group): the group's row tiles
-      U.base = (u / p.G) * 2 * kBlockM;
+    case kModeQNorm:   // one unit per (128 neurons, KV group); jobs: the group's row tiles of 256
+      U.base = (u / p.G) * kBlockM;
       U.head = u % p.G;
       U.njobs = p.n_ntiles;
       break;
@@ -155,7 +145,7 @@ __device__ __forceinline__ Job job_next(const TileParams& p, const Unit& U, JobI
     ++it.b;
   } else if constexpr (MODE == kModeXPrime) {
     J.kind = kJobXPrime; J.nkb = p.nkb_I; J.nkb_part = p.nkb_I; J.last_nks = 4;
-    J.t0 = U.base; J.nt = it.b++;
+    J.t0 = U.base; J.nt = U.head;
   } else if constexpr (MODE == kModeCNorm) {
     J.kind = kJobCNorm; J.nkb = p.nkb_dh; J.nkb_part = p.nkb_dh; J.last_nks = p.ls_dh;
     J.t0 = U.base; J.head = U.head; J.nt = it.b++;
@@ -174,7 +164,7 @@ struct Smem {
   uint64_t* drain;
   uint32_t* tmem_slot;
   volatile int* abort_flag;
-  float* sacc;
+  float* sacc;     // FO / ADD / LOO: the unit's sums [column group][H][128 neurons]
   uint8_t* stage0;
 };
 
@@ -186,8 +176,8 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 // STREAM: the producer and MMA issuer walk the heads' K ranges back to back
 // (FO / ADD / LOO with p.stream_heads); a separate instantiation, so the
 // issue loop of the other shapes carries no extra branch.
-template <int MODE, bool PAIR, bool STREAM>
-__global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
+template <int MODE, bool STREAM>
+__global__ void __launch_bounds__(block_threads(MODE), 1)
     affinity_tile_kernel(const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
                          const __grid_constant__ CUtensorMap map2, const __grid_constant__ CUtensorMap map3,
                          const TileParams p) {
@@ -195,17 +185,21 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
 
-  constexpr int EW = epi_warps(MODE, PAIR);   // epilogue warps
-  constexpr int NG = EW / 4;                    // column groups of a 128-column accumulator
-  constexpr int CW = kBlockN / NG;              // columns (tokens) per epilogue thread
+  constexpr int EW = epi_warps(MODE);   // epilogue warps
+  constexpr int NG = EW / 4;              // column groups of a 128-column accumulator
+  constexpr int CW = kBlockN / NG;        // columns per epilogue thread (of each accumulator)
+  constexpr bool kHeads = MODE == kModeFO || MODE == kModeADD || MODE == kModeLOO;
+  // one N = 256 MMA per K slice (see the file comment)
+  constexpr bool kWide = MODE == kModeAlpha || MODE == kModeXPrime || MODE == kModeCNorm || MODE == kModeQNorm;
+  constexpr int CWW = 2 * kBlockN / NG;   // wide passes: columns of the 256 per epilogue thread
   const int S = p.stages;
-  constexpr int kSB = PAIR ? kPairStageBytes : kStageBytes;   // bytes of one pipeline stage
-  constexpr int kBOff = 2 * kTileBytes;                         // B tile offset within a stage
+  constexpr int kSB = kStageBytes;        // bytes of one pipeline stage
+  constexpr int kBOff = 2 * kTileBytes;   // offset of the third tile within a stage
   Smem sm;
   sm.stage0 = base;
   uint8_t* cur = base + (size_t)S * kSB;
   sm.sacc = reinterpret_cast<float*>(cur);
-  int sacc_floats = (MODE == kModeFO || MODE == kModeADD || MODE == kModeLOO) ? NG * p.H * kBlockM : 0;
+  const int sacc_floats = kHeads ? NG * p.H * kBlockM : 0;
   cur += (size_t)sacc_floats * 4;
   sm.full = reinterpret_cast<uint64_t*>(cur);
   sm.empty = sm.full + S;
@@ -217,9 +211,8 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int crank = PAIR ? (int)cluster_ctarank() : 0;   // 0 = leader (issues the MMAs), 1 = peer
-  const int cid = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int ncl = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int cid = (int)blockIdx.x;
+  const int ncl = (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -228,7 +221,7 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.tfull[b], 1);
-      mbar_init(&sm.tempty[b], PAIR ? 2 * EW : EW);   // pairs: both CTAs' epilogues
+      mbar_init(&sm.tempty[b], EW);
     }
     mbar_init(sm.drain, 1);
     *sm.abort_flag = 0;
@@ -241,22 +234,14 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
     prefetch_tmap(&map3);
   }
   if (warp == 1) {
-    if (PAIR) {
-      tmem_alloc_pair(sm.tmem_slot, kTmemCols);
-      tmem_relinquish_pair();
-    } else {
-      tmem_alloc(sm.tmem_slot, kTmemCols);
-      tmem_relinquish();
-    }
+    tmem_alloc(sm.tmem_slot, kTmemCols);
+    tmem_relinquish();
   }
   if (warp >= 2) {
     for (int i = threadIdx.x - 64; i < sacc_floats; i += EW * 32) sm.sacc[i] = 0.f;
   }
   tc_fence_before();
-  if (PAIR)
-    cluster_sync_all();   // both CTAs' barriers and tensor memory exist before either uses the other's
-  else
-    __syncthreads();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_slot;
 
@@ -267,70 +252,52 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
       uint32_t ph = 0;                 // phase parity of the current use of stage s
       bool ok = true;
       for (int u = cid; ok && u < p.n_units; u += ncl) {
-        const Unit U = unit_info<PAIR, STREAM>(p, u, crank);
+        const Unit U = unit_info<STREAM>(p, u);
         JobIter jt{0, 0};
         for (int j = 0; ok && j < U.njobs_pm; ++j) {
           const Job J = job_next<MODE, STREAM>(p, U, jt, true);
           for (int kb = 0, kb_in = 0, part = 0; kb < J.nkb; ++kb) {
-            const bool w = PAIR ? mbar_wait_cluster(&sm.empty[s], ph ^ 1u, sm.abort_flag, p.status)
-                                : mbar_wait(&sm.empty[s], ph ^ 1u, sm.abort_flag, p.status);
-            if (!w) { ok = false; break; }
+            if (!mbar_wait(&sm.empty[s], ph ^ 1u, sm.abort_flag, p.status)) { ok = false; break; }
             uint8_t* st = sm.stage0 + s * kSB;
             uint64_t* fb = &sm.full[s];
             const int kx = kb_in * kBlockK;
-            if (PAIR) {
-              // Both CTAs' loads land on the leader's full barrier, which expects both stages' bytes.
-              const uint32_t fb_leader = mapa_shared(smem_u32(fb), 0);
-              const int tb = J.t0 + crank * kPairBRows;   // this CTA's half of the token tile
-              if (crank == 0) mbar_arrive_expect_tx(fb, 2 * kPairStageBytes);
-              if (J.kind == kJobGateUp) {
-                tma_load_2d_pair(st, &map0, fb_leader, kx, J.kt * kBlockM);
-                tma_load_2d_pair(st + kTileBytes, &map0, fb_leader, kx, p.I_pad + J.kt * kBlockM);
-                tma_load_2d_pair(st + kBOff, &map1, fb_leader, kx, tb);
-              } else {
-                tma_load_3d_pair(st, &map2, fb_leader, kx, J.kt * kBlockM, 2 * J.head);
-                tma_load_3d_pair(st + kTileBytes, &map2, fb_leader, kx, J.kt * kBlockM, 2 * J.head + 1);
-                tma_load_3d_pair(st + kBOff, &map3, fb_leader, kx, J.head, tb);
-              }
-            } else {
-              mbar_arrive_expect_tx(fb, kStageBytes);
-              switch (J.kind) {
-                case kJobGateUp:   // A = W16 gate / up rows, B = n16 token rows
-                  tma_load_2d(st, &map0, fb, kx, J.kt * kBlockM);
-                  tma_load_2d(st + kTileBytes, &map0, fb, kx, p.I_pad + J.kt * kBlockM);
-                  tma_load_2d(st + kBOff, &map1, fb, kx, J.t0);
-                  break;
-                case kJobStream:   // A = M16 gate / up planes, B = a16; K runs over all heads' columns
-                  tma_load_2d(st, &map2, fb, kx, J.kt * kBlockM);
-                  tma_load_2d(st + kTileBytes, &map2, fb, kx, p.I_pad + J.kt * kBlockM);
-                  tma_load_2d(st + kBOff, &map3, fb, kx, J.t0);
-                  break;
-                case kJobHead:     // A = M16 (gate, up) of head h, B = a16 head h
-                  tma_load_3d(st, &map2, fb, kx, J.kt * kBlockM, 2 * J.head);
-                  tma_load_3d(st + kTileBytes, &map2, fb, kx, J.kt * kBlockM, 2 * J.head + 1);
-                  tma_load_3d(st + kBOff, &map3, fb, kx, J.head, J.t0);
-                  break;
-                case kJobFold:     // A = W16 rows, B = gamma*Wo^T (hi part, then lo part)
-                  tma_load_2d(st, &map0, fb, kx, J.kt * kBlockM);
-                  tma_load_2d(st + kTileBytes, &map0, fb, kx, p.I_pad + J.kt * kBlockM);
-                  tma_load_3d(st + kBOff, &map1, fb, kx, part, J.nt * kBlockN);
-                  break;
-                case kJobXPrime:   // A = alpha16 token rows (two tiles), B = Wd16 rows d
-                  tma_load_2d(st, &map0, fb, kx, J.t0);
-                  tma_load_2d(st + kTileBytes, &map0, fb, kx, J.t0 + kBlockM);
-                  tma_load_2d(st + kBOff, &map1, fb, kx, J.nt * kBlockN);
-                  break;
-                case kJobCNorm:    // A = a16 head h token rows (two tiles), B = Wo16 rows d, head h's columns
-                  tma_load_3d(st, &map0, fb, kx, J.head, J.t0);
-                  tma_load_3d(st + kTileBytes, &map0, fb, kx, J.head, J.t0 + kBlockM);
-                  tma_load_2d(st + kBOff, &map1, fb, J.head * p.dh + kx, J.nt * kBlockN);
-                  break;
-                case kJobQNorm:    // A = Wd^T neuron rows (two tiles), B = group g's gamma'-scaled q/k/v rows (hi | lo)
-                  tma_load_2d(st, &map0, fb, kx, U.base);
-                  tma_load_2d(st + kTileBytes, &map0, fb, kx, U.base + kBlockM);
-                  tma_load_4d(st + kBOff, &map1, fb, kx, part, J.nt * kBlockN, J.g);
-                  break;
-              }
+            mbar_arrive_expect_tx(fb, kStageBytes);
+            switch (J.kind) {
+              case kJobGateUp:   // W16 gate / up rows (the MMA's B), n16 token rows (its A)
+                tma_load_2d(st, &map0, fb, kx, J.kt * kBlockM);
+                tma_load_2d(st + kTileBytes, &map0, fb, kx, p.I_pad + J.kt * kBlockM);
+                tma_load_2d(st + kBOff, &map1, fb, kx, J.t0);
+                break;
+              case kJobStream:   // M16 gate / up planes, a16 tokens; K runs over all heads' columns
+                tma_load_2d(st, &map2, fb, kx, J.kt * kBlockM);
+                tma_load_2d(st + kTileBytes, &map2, fb, kx, p.I_pad + J.kt * kBlockM);
+                tma_load_2d(st + kBOff, &map3, fb, kx, J.t0);
+                break;
+              case kJobHead:     // M16 (gate, up) of head h, a16 head h tokens
+                tma_load_3d(st, &map2, fb, kx, J.kt * kBlockM, 2 * J.head);
+                tma_load_3d(st + kTileBytes, &map2, fb, kx, J.kt * kBlockM, 2 * J.head + 1);
+                tma_load_3d(st + kBOff, &map3, fb, kx, J.head, J.t0);
+                break;
+              case kJobFold:     // A = W16 rows, B = gamma*Wo^T (hi part, then lo part)
+                tma_load_2d(st, &map0, fb, kx, J.kt * kBlockM);
+                tma_load_2d(st + kTileBytes, &map0, fb, kx, p.I_pad + J.kt * kBlockM);
+                tma_load_3d(st + kBOff, &map1, fb, kx, part, J.nt * kBlockN);
+                break;
+              case kJobXPrime:   // Wd16 rows d (256, the MMA's B), alpha16 token rows (its A)
+                tma_load_2d(st, &map1, fb, kx, J.nt * 2 * kBlockN);
+                tma_load_2d(st + kTileBytes, &map1, fb, kx, J.nt * 2 * kBlockN + kBlockN);
+                tma_load_2d(st + kBOff, &map0, fb, kx, J.t0);
+                break;
+              case kJobCNorm:    // Wo16 rows d (256), head h's columns (B); a16 head h token rows (A)
+                tma_load_2d(st, &map1, fb, J.head * p.dh + kx, J.nt * 2 * kBlockN);
+                tma_load_2d(st + kTileBytes, &map1, fb, J.head * p.dh + kx, J.nt * 2 * kBlockN + kBlockN);
+                tma_load_3d(st + kBOff, &map0, fb, kx, J.head, J.t0);
+                break;
+              case kJobQNorm:    // group g's gamma'-scaled q/k/v rows, hi | lo along K (256, B); Wd^T neuron rows (A)
+                tma_load_4d(st, &map1, fb, kx, part, J.nt * 2 * kBlockN, J.g);
+                tma_load_4d(st + kTileBytes, &map1, fb, kx, part, J.nt * 2 * kBlockN + kBlockN, J.g);
+                tma_load_2d(st + kBOff, &map0, fb, kx, U.base);
+                break;
             }
             ++issued;
             if (++s == S) { s = 0; ph ^= 1u; }
@@ -340,17 +307,11 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
       }
       if (!ok) {
         // Let every copy already issued land before shared memory is released.
-        if (PAIR && crank == 1) {
-          // the peer's copies signal the leader's barriers: give them a bounded grace period
-          const uint64_t t0 = global_timer_ns();
-          while (global_timer_ns() - t0 < 2000000ull) __nanosleep(1000);
-        } else {
-          const int n = issued < S ? issued : S;
-          for (int i = 1; i <= n; ++i) {
-            const int q = issued - i;
-            volatile int dummy = 0;
-            mbar_wait(&sm.full[q % S], (uint32_t)((q / S) & 1), &dummy, p.status, 100000000ull);
-          }
+        const int n = issued < S ? issued : S;
+        for (int i = 1; i <= n; ++i) {
+          const int q = issued - i;
+          volatile int dummy = 0;
+          mbar_wait(&sm.full[q % S], (uint32_t)((q / S) & 1), &dummy, p.status, 100000000ull);
         }
       }
     }
@@ -358,22 +319,22 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
     // ------------------------------------------------------------ MMA issuer
     // A lean loop: this one thread must issue MMAs as fast as the tensor pipe
     // retires them, so no divisions, and descriptors advance by constants.
-    if (lane == 0 && crank == 0) {   // in a pair only the leader issues (for both CTAs)
-      const uint32_t idesc = idesc_f16(PAIR ? 2 * kBlockM : kBlockM, kBlockN, 0);
-      const uint64_t dbase = smem_desc_k_sw128(smem_u32(sm.stage0));   // A1 of stage 0
+    if (lane == 0) {
+      // wide passes: M = 128 (the third tile), N = 256 (the first two); one such
+      // MMA reads 12 KB of shared memory where a D1 / D2 pair reads 16 KB
+      constexpr uint32_t idesc = kWide ? idesc_f16(kBlockM, 2 * kBlockN, 0) : idesc_f16(kBlockM, kBlockN, 0);
+      const uint64_t dbase = smem_desc_k_sw128(smem_u32(sm.stage0));   // first tile of stage 0
       constexpr uint64_t kStageDesc = (uint64_t)(kSB >> 4);             // descriptor step per stage
       constexpr uint64_t kA2 = (uint64_t)(kTileBytes >> 4), kB = (uint64_t)(kBOff >> 4);
       int s = 0, b = 0;
       uint32_t ph = 0, tph = 0;        // stage phase; TMEM buffer phase (flips every second job)
       bool ok = true;
       for (int u = cid; ok && u < p.n_units; u += ncl) {
-        const Unit U = unit_info<PAIR, STREAM>(p, u, crank);
+        const Unit U = unit_info<STREAM>(p, u);
         JobIter jt{0, 0};
         for (int j = 0; ok && j < U.njobs_pm; ++j) {
           const Job J = job_next<MODE, STREAM>(p, U, jt, true);
-          const bool w = PAIR ? mbar_wait_cluster(&sm.tempty[b], tph ^ 1u, sm.abort_flag, p.status)
-                              : mbar_wait(&sm.tempty[b], tph ^ 1u, sm.abort_flag, p.status);
-          if (!w) { ok = false; break; }
+          if (!mbar_wait(&sm.tempty[b], tph ^ 1u, sm.abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           if constexpr (STREAM) {
            if (J.kind == kJobStream) {
@@ -415,9 +376,7 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
           const uint32_t d2 = d1 + kBlockN;
           uint32_t acc = 0u;
           for (int kb = 0, kb_in = 0; kb < J.nkb; ++kb) {
-            const bool wf = PAIR ? mbar_wait_cluster(&sm.full[s], ph, sm.abort_flag, p.status)
-                                 : mbar_wait(&sm.full[s], ph, sm.abort_flag, p.status);
-            if (!wf) { ok = false; break; }
+            if (!mbar_wait(&sm.full[s], ph, sm.abort_flag, p.status)) { ok = false; break; }
             tc_fence_after();
             const uint64_t da1 = dbase + (uint64_t)s * kStageDesc;
             const uint64_t da2 = da1 + kA2, db = da1 + kB;
@@ -425,9 +384,8 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               if (ks < nks) {
-                if (PAIR) {
-                  mma_f16_ss_pair(d1, da1 + 2 * ks, db + 2 * ks, idesc, acc);
-                  mma_f16_ss_pair(d2, da2 + 2 * ks, db + 2 * ks, idesc, acc);
+                if constexpr (kWide) {
+                  mma_f16_ss(d1, db + 2 * ks, da1 + 2 * ks, idesc, acc);
                 } else {
                   mma_f16_ss(d1, da1 + 2 * ks, db + 2 * ks, idesc, acc);
                   mma_f16_ss(d2, da2 + 2 * ks, db + 2 * ks, idesc, acc);
@@ -435,26 +393,17 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
                 acc = 1u;
               }
             }
-            if (PAIR)
-              mma_commit_pair_mc(&sm.empty[s], 3);   // the stage is free again in both CTAs
-            else
-              mma_commit(&sm.empty[s]);
+            mma_commit(&sm.empty[s]);
             if (++s == S) { s = 0; ph ^= 1u; }
             if (++kb_in == J.nkb_part) kb_in = 0;
           }
           if (!ok) break;
-          if (PAIR)
-            mma_commit_pair_mc(&sm.tfull[b], 3);
-          else
-            mma_commit(&sm.tfull[b]);
+          mma_commit(&sm.tfull[b]);
           if (++b == 2) { b = 0; tph ^= 1u; }
         }
       }
       if (!ok) {
-        if (PAIR)
-          mma_commit_pair_mc(sm.drain, 1);
-        else
-          mma_commit(sm.drain);
+        mma_commit(sm.drain);
         volatile int dummy = 0;
         mbar_wait(sm.drain, 0, &dummy, p.status, 100000000ull);
       }
@@ -463,29 +412,24 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // TMEM lane quarter this warp may read
     const int hf = (warp - 2) >> 2;    // which group of CW columns of the tile
-    const int row = q * 32 + lane;     // row of the A tile = TMEM lane
+    const int row = q * 32 + lane;     // TMEM lane = row of the MMA's A: an A1 row, or a token (alpha)
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
-    // TMEM-empty arrivals go to the leader's barrier (its own when unpaired)
-    const uint32_t tempty_addr0 = PAIR ? mapa_shared(smem_u32(&sm.tempty[0]), 0) : 0u;
-    uint64_t abA[CW / 2], abB[CW / 2];   // FO: f32x2 pairs of silu'(g)u and silu(g), CW tokens
+    // FO: f32x2 pairs of silu'(g)u and silu(g) of this neuron, CW tokens; LOO: g and u
+    uint64_t abA[CW / 2], abB[CW / 2];
 #pragma unroll
     for (int i = 0; i < CW / 2; ++i) { abA[i] = 0ull; abB[i] = 0ull; }
-    float ss1 = 0.f, ss2 = 0.f;        // x' / qnorm / cnorm running sums
-    float xd1 = 0.f, xd2 = 0.f;        // cnorm: sum_d x (c/r)
+    float ss1 = 0.f;                   // x' / qnorm / cnorm running sums
+    float xd1 = 0.f;                   // cnorm: sum_d x (c/r)
     int b = 0;
     uint32_t tph = 0;                  // TMEM buffer phase (flips every second job)
     bool ok = true;
     for (int u = cid; ok && u < p.n_units; u += ncl) {
-      const Unit U = unit_info<PAIR, STREAM>(p, u, crank);
+      const Unit U = unit_info<STREAM>(p, u);
       JobIter jt{0, 0};
       for (int j = 0; j < U.njobs; ++j, b ^= 1, tph ^= (uint32_t)(b == 0)) {
         const Job J = job_next<MODE, STREAM>(p, U, jt);
         int w_ok = 1;
-        if (lane == 0)
-          w_ok = (PAIR ? mbar_wait_cluster(&sm.tfull[b], tph, sm.abort_flag, p.status)
-                       : mbar_wait(&sm.tfull[b], tph, sm.abort_flag, p.status))
-                     ? 1
-                     : 0;
+        if (lane == 0) w_ok = mbar_wait(&sm.tfull[b], tph, sm.abort_flag, p.status) ? 1 : 0;
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
         if (!w_ok) { ok = false; break; }
         tc_fence_after();
@@ -512,12 +456,7 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
               if (c == CW / kG - 1) {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                  if (PAIR)
-                    mbar_arrive_cluster(tempty_addr0 + (uint32_t)(b * 8));
-                  else
-                    mbar_arrive(&sm.tempty[b]);
-                }
+                if (lane == 0) mbar_arrive(&sm.tempty[b]);
               }
 #pragma unroll
               for (int i = 0; i < kG; i += 2) {
@@ -547,32 +486,40 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
           }
         }
         if constexpr (MODE == kModeAlpha) {
-          {   // kJobGateUp: alpha = silu(g) u straight from the accumulators
+          {   // kJobGateUp: TMEM lane = token J.t0 + row, columns = g (first 128) and u of
+              // the neuron tile; alpha = silu(g) u, 16 neurons (32 B) stored at a time
+            __half* dst = p.alpha16 + (size_t)(J.t0 + row) * p.I_pad + J.kt * kBlockM + hf * CW;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < CW / 16; ++c) {
               uint32_t gr[16], ur[16];
               tmem_ld16(c1 + c * 16, gr);
               tmem_ld16(c2 + c * 16, ur);
               tmem_ld_wait();
-              if (c == 3) {
+              if (c == CW / 16 - 1) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.tempty[b]);
               }
+              uint32_t hv[8];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float g = __uint_as_float(gr[i]);
-                const float uu = __uint_as_float(ur[i]);
-                const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
-                const int t = J.t0 + hf * 64 + c * 16 + i;
-                const int kk = J.kt * kBlockM + row;
-                p.alpha16[(size_t)t * p.I_pad + kk] = __float2half_rn(g * sg * uu);
+              for (int i = 0; i < 16; i += 2) {
+                float a2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const float g = __uint_as_float(gr[i + e]);
+                  const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
+                  a2[e] = g * sg * __uint_as_float(ur[i + e]);
+                }
+                hv[i / 2] = pack_h2(a2[0], a2[1]);
               }
+              uint4* d4 = reinterpret_cast<uint4*>(dst + c * 16);
+              d4[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+              d4[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
             }
             continue;
           }
         }
-        if constexpr (MODE == kModeFO || MODE == kModeADD || MODE == kModeLOO) {
+        if constexpr (kHeads) {
           // kJobHead: per token Delta = A' pg + B' pu (FO) or pg^2 + pu^2 (ADD), summed over tokens;
           // LOO: g - g^(-h) = g (1 - rho) + rho pg = g + rho (pg - g) with rho = r / rms(x - c_h),
           // likewise for u
@@ -593,12 +540,7 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
             if (c == CW / kW - 1) {
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) {
-                if (PAIR)
-                  mbar_arrive_cluster(tempty_addr0 + (uint32_t)(b * 8));
-                else
-                  mbar_arrive(&sm.tempty[b]);
-              }
+              if (lane == 0) mbar_arrive(&sm.tempty[b]);
             }
             float4 rq = make_float4(0.f, 0.f, 0.f, 0.f);   // LOO: rho of the chunk's 4 tokens
             if constexpr (MODE == kModeLOO)   // the same address in every lane: a broadcast
@@ -607,7 +549,7 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
             for (int i = 0; i < kW; i += 2) {
               const uint64_t vg = pk_u(pg[i], pg[i + 1]);
               const uint64_t vu = pk_u(pu[i], pu[i + 1]);
-              const int ai = (c * kW + i) / 2;   // token pair within the thread's 64 tokens
+              const int ai = (c * kW + i) / 2;   // token pair within the thread's CW tokens
               if constexpr (MODE == kModeFO) {
                 uint64_t d = mul2(abA[ai], vg);
                 d = fma2(abB[ai], vu, d);
@@ -628,6 +570,7 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
           sm.sacc[(hf * p.H + J.head) * kBlockM + row] += s2.x + s2.y;
         }
         static_assert(EW == kWideEpiWarps || CW == 64, "the 8-warp epilogues read 64 columns per thread");
+
         if constexpr (MODE == kModeFold) {
           // D1 = Mg[k][n], D2 = Mu[k][n] for neuron k = kt*128 + row, columns n = nt*128 + hf*64 + ...
           const int kk = J.kt * kBlockM + row;
@@ -640,12 +583,7 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
             if (c == 3) {
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) {
-                  if (PAIR)
-                    mbar_arrive_cluster(tempty_addr0 + (uint32_t)(b * 8));
-                  else
-                    mbar_arrive(&sm.tempty[b]);
-                }
+              if (lane == 0) mbar_arrive(&sm.tempty[b]);
             }
 #pragma unroll
             for (int i = 0; i < 16; i += 8) {
@@ -673,100 +611,45 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
             }
           }
         }
-        if constexpr (MODE == kModeXPrime) {
-          // D1 = (alpha Wd^T)[t1][d], D2 = ...[t2][d]; x' = x + D; accumulate x'^2 over d
-          const int t1 = J.t0 + row, t2 = J.t0 + kBlockM + row;
+        if constexpr (MODE == kModeXPrime || MODE == kModeCNorm) {
+          // lane = token t; columns d = J.nt * 256 + hf * CWW + ...: x' pass: (alpha Wd^T)[t][d],
+          // x' = x + that, accumulate x'^2 over d; c_h pass: (c_h / r)[t][d], accumulate (c/r)^2
+          // and x (c/r) over d.  Columns past D hold zeros (the B tiles were zero-filled), so
+          // only x needs a guard; D % 8 == 0, so an 8-column group is wholly inside or past D.
+          const int t = J.t0 + row;
+          const uint32_t c0 = tl + (uint32_t)(b * 2 * kBlockN + hf * CWW);
 #pragma unroll
-          for (int c = 0; c < CW / 16; ++c) {
-            uint32_t v1[16], v2[16];
-            tmem_ld16(c1 + c * 16, v1);
-            tmem_ld16(c2 + c * 16, v2);
+          for (int c = 0; c < CWW / 16; ++c) {
+            uint32_t v[16];
+            tmem_ld16(c0 + c * 16, v);
             tmem_ld_wait();
-            if (c == CW / 16 - 1) {
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) {
-                  if (PAIR)
-                    mbar_arrive_cluster(tempty_addr0 + (uint32_t)(b * 8));
-                  else
-                    mbar_arrive(&sm.tempty[b]);
-                }
-            }
-            // D % 8 == 0: an 8-column group is wholly inside or wholly past D; x is read 16 B at a time
-            const int d0 = J.nt * kBlockN + hf * CW + c * 16;
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              const int d = d0 + q * 8;
-              if (d < p.D) {
-                if (t1 < p.T) {
-                  const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.x_bf16 + (size_t)t1 * p.D + d));
-                  const uint32_t e[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) {
-                    const float v0 = __uint_as_float(e[i] << 16) + __uint_as_float(v1[q * 8 + 2 * i]);
-                    const float v1_ = __uint_as_float(e[i] & 0xFFFF0000u) + __uint_as_float(v1[q * 8 + 2 * i + 1]);
-                    ss1 = fmaf(v0, v0, ss1);
-                    ss1 = fmaf(v1_, v1_, ss1);
-                  }
-                }
-                if (t2 < p.T) {
-                  const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.x_bf16 + (size_t)t2 * p.D + d));
-                  const uint32_t e[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) {
-                    const float v0 = __uint_as_float(e[i] << 16) + __uint_as_float(v2[q * 8 + 2 * i]);
-                    const float v1_ = __uint_as_float(e[i] & 0xFFFF0000u) + __uint_as_float(v2[q * 8 + 2 * i + 1]);
-                    ss2 = fmaf(v0, v0, ss2);
-                    ss2 = fmaf(v1_, v1_, ss2);
-                  }
-                }
-              }
-            }
-          }
-        }
-        if constexpr (MODE == kModeCNorm) {
-          // D1 = (c_h / r)[t1][d], D2 = ...[t2][d]: accumulate sum_d (c/r)^2 and sum_d x (c/r)
-          const int t1 = J.t0 + row, t2 = J.t0 + kBlockM + row;
-#pragma unroll
-          for (int c = 0; c < CW / 16; ++c) {
-            uint32_t v1[16], v2[16];
-            tmem_ld16(c1 + c * 16, v1);
-            tmem_ld16(c2 + c * 16, v2);
-            tmem_ld_wait();
-            if (c == CW / 16 - 1) {
+            if (c == CWW / 16 - 1) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(&sm.tempty[b]);
             }
-            // columns past D hold zeros (the B tile was zero-filled), so only x needs a guard;
-            // D % 8 == 0, so an 8-column group is either wholly inside or wholly past D
-            const int d0 = J.nt * kBlockN + hf * CW + c * 16;
+            if constexpr (MODE == kModeCNorm) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float a1 = __uint_as_float(v1[i]), a2 = __uint_as_float(v2[i]);
-              ss1 = fmaf(a1, a1, ss1);
-              ss2 = fmaf(a2, a2, ss2);
+              for (int i = 0; i < 16; ++i) ss1 = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), ss1);
             }
+            const int d0 = J.nt * 2 * kBlockN + hf * CWW + c * 16;
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              const int d = d0 + q * 8;
-              if (d < p.D) {
-                if (t1 < p.T) {
-                  const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.x_bf16 + (size_t)t1 * p.D + d));
-                  const uint32_t e[4] = {w.x, w.y, w.z, w.w};
+            for (int q8 = 0; q8 < 2; ++q8) {
+              const int d = d0 + q8 * 8;
+              if (d < p.D && t < p.T) {
+                const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.x_bf16 + (size_t)t * p.D + d));
+                const uint32_t e[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                  for (int i = 0; i < 4; ++i) {
-                    xd1 = fmaf(__uint_as_float(e[i] << 16), __uint_as_float(v1[q * 8 + 2 * i]), xd1);
-                    xd1 = fmaf(__uint_as_float(e[i] & 0xFFFF0000u), __uint_as_float(v1[q * 8 + 2 * i + 1]), xd1);
-                  }
-                }
-                if (t2 < p.T) {
-                  const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.x_bf16 + (size_t)t2 * p.D + d));
-                  const uint32_t e[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) {
-                    xd2 = fmaf(__uint_as_float(e[i] << 16), __uint_as_float(v2[q * 8 + 2 * i]), xd2);
-                    xd2 = fmaf(__uint_as_float(e[i] & 0xFFFF0000u), __uint_as_float(v2[q * 8 + 2 * i + 1]), xd2);
+                for (int i = 0; i < 4; ++i) {
+                  const float xa = __uint_as_float(e[i] << 16), xb = __uint_as_float(e[i] & 0xFFFF0000u);
+                  const float va = __uint_as_float(v[q8 * 8 + 2 * i]), vb = __uint_as_float(v[q8 * 8 + 2 * i + 1]);
+                  if constexpr (MODE == kModeXPrime) {
+                    const float ya = xa + va, yb = xb + vb;
+                    ss1 = fmaf(ya, ya, ss1);
+                    ss1 = fmaf(yb, yb, ss1);
+                  } else {
+                    xd1 = fmaf(xa, va, xd1);
+                    xd1 = fmaf(xb, vb, xd1);
                   }
                 }
               }
@@ -774,43 +657,34 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
           }
         }
         if constexpr (MODE == kModeQNorm) {
-          // D1 = Q[k1][r], D2 = Q[k2][r] for the rows r of group J.g; sum Q^2 over the group's rows
+          // lane = neuron k = U.base + row; columns = 256 rows r of group J.g (hi and lo
+          // parts already summed along K): accumulate Q[k][r]^2 over the group's rows
+          const uint32_t c0 = tl + (uint32_t)(b * 2 * kBlockN + hf * CWW);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v1[16], v2[16];
-            tmem_ld16(c1 + c * 16, v1);
-            tmem_ld16(c2 + c * 16, v2);
+          for (int c = 0; c < CWW / 16; ++c) {
+            uint32_t v[16];
+            tmem_ld16(c0 + c * 16, v);
             tmem_ld_wait();
-            if (c == 3) {
+            if (c == CWW / 16 - 1) {
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) {
-                  if (PAIR)
-                    mbar_arrive_cluster(tempty_addr0 + (uint32_t)(b * 8));
-                  else
-                    mbar_arrive(&sm.tempty[b]);
-                }
+              if (lane == 0) mbar_arrive(&sm.tempty[b]);
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float a1 = __uint_as_float(v1[i]), a2 = __uint_as_float(v2[i]);
-              ss1 = fmaf(a1, a1, ss1);
-              ss2 = fmaf(a2, a2, ss2);
-            }
+            for (int i = 0; i < 16; ++i) ss1 = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), ss1);
           }
           if (J.nt == p.n_ntiles - 1) {
-            // rows past the group's end were zero-filled, so the sum is the group's ||b_gk||^2 half
-            const int k1 = U.base + row, k2 = U.base + kBlockM + row;
-            if (k1 < p.I_pad) p.bnorm[((size_t)hf * p.I_pad + k1) * p.G + J.g] = ss1;
-            if (k2 < p.I_pad) p.bnorm[((size_t)hf * p.I_pad + k2) * p.G + J.g] = ss2;
+            // rows past the group's end were zero-filled, so the sum is this column group's share
+            const int k = U.base + row;
+            if (k < p.I_pad) p.bnorm[((size_t)hf * p.I_pad + k) * p.G + J.g] = ss1;
             ss1 = 0.f;
-            ss2 = 0.f;
           }
         }
       }
       if (!ok) break;
       // ---- end of unit
-      if constexpr (MODE == kModeFO || MODE == kModeADD || MODE == kModeLOO) {
+      if constexpr (kHeads) {
+        // [chunk][column group][H][I_pad]
         float* dst = p.partial + ((size_t)(U.chunk * NG + hf) * p.H) * p.I_pad + U.kt * kBlockM + row;
         for (int h = 0; h < p.H; ++h) {
           float* sp = &sm.sacc[(hf * p.H + h) * kBlockM + row];
@@ -819,103 +693,69 @@ __global__ void __launch_bounds__(block_threads(MODE, PAIR), 1)
         }
       }
       if constexpr (MODE == kModeXPrime) {
-        const int t1 = U.base + row, t2 = U.base + kBlockM + row;
-        if (t1 < p.T_pad) p.partial[(size_t)hf * p.T_pad + t1] = ss1;   // [column group][T_pad]
-        if (t2 < p.T_pad) p.partial[(size_t)hf * p.T_pad + t2] = ss2;
+        // [column tile][column group][T_pad]; token tiles are whole, so t < T_pad
+        p.partial[(size_t)(U.head * NG + hf) * p.T_pad + U.base + row] = ss1;
         ss1 = 0.f;
-        ss2 = 0.f;
       }
       if constexpr (MODE == kModeCNorm) {
         // [column group][quantity][H][T_pad]: quantity 0 = sum (c/r)^2, 1 = sum x (c/r)
-        const int t1 = U.base + row, t2 = U.base + kBlockM + row;
-        float* cc = p.partial + ((size_t)(hf * 2 + 0) * p.H + U.head) * p.T_pad;
-        float* xd = p.partial + ((size_t)(hf * 2 + 1) * p.H + U.head) * p.T_pad;
-        if (t1 < p.T_pad) { cc[t1] = ss1; xd[t1] = xd1; }
-        if (t2 < p.T_pad) { cc[t2] = ss2; xd[t2] = xd2; }
-        ss1 = ss2 = xd1 = xd2 = 0.f;
+        const int t = U.base + row;
+        p.partial[((size_t)(hf * 2 + 0) * p.H + U.head) * p.T_pad + t] = ss1;
+        p.partial[((size_t)(hf * 2 + 1) * p.H + U.head) * p.T_pad + t] = xd1;
+        ss1 = xd1 = 0.f;
       }
     }
   }
 
   tc_fence_before();
-  if (PAIR)
-    cluster_sync_all();   // neither CTA of a pair leaves while the other may still use its memory
-  else
-    __syncthreads();
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    if (PAIR)
-      tmem_dealloc_pair(tmem, kTmemCols);
-    else
-      tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-size_t tile_smem_bytes(int mode, int stages, int H, bool pair) {
-  const size_t groups = (size_t)epi_warps(mode, pair) / 4;
-  size_t sacc = (mode == kModeFO || mode == kModeADD || mode == kModeLOO) ? groups * H * kBlockM * 4 : 0;
-  return 1024 + (size_t)stages * (pair ? kPairStageBytes : kStageBytes) + sacc + (size_t)(2 * stages + 5) * 8 + 8;
+size_t tile_smem_bytes(int mode, int stages, int H) {
+  const bool heads = mode == kModeFO || mode == kModeADD || mode == kModeLOO;
+  const size_t sacc = heads ? (size_t)(epi_warps(mode) / 4) * H * kBlockM * 4 : 0;
+  return 1024 + (size_t)stages * kStageBytes + sacc + (size_t)(2 * stages + 5) * 8 + 8;
 }
 
-// Launches `grid` CTAs (pairs: 2 * grid as clusters of 2).  With grid == 0 it
-// only reports in *grid how many CTAs (pairs) fit on the device at once.
-template <int MODE, bool PAIR, bool STREAM = false>
+// Launches `grid` CTAs.  With grid == 0 it only reports in *grid how many CTAs
+// fit on the device at once.
+template <int MODE, bool STREAM = false>
 static cudaError_t launch_mode(const CUtensorMap* maps, const TileParams& p, int* grid, cudaStream_t stream) {
-  const size_t smem = tile_smem_bytes(MODE, p.stages, p.H, PAIR);
-  auto* fn = affinity_tile_kernel<MODE, PAIR, STREAM>;
+  const size_t smem = tile_smem_bytes(MODE, p.stages, p.H);
+  auto* fn = affinity_tile_kernel<MODE, STREAM>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  if (!PAIR) {
-    if (*grid <= 0) {
-      int dev = 0, n = 0;
-      cudaGetDevice(&dev);
-      e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-      *grid = n;   // shared memory and TMEM allow one CTA per SM
-      return e;
-    }
-    fn<<<*grid, block_threads(MODE, PAIR), smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
-    return cudaGetLastError();
-  }
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(block_threads(MODE, PAIR), 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   if (*grid <= 0) {
-    int n = 0;
-    cfg.gridDim = dim3(2, 1, 1);
-    e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
-    *grid = n;
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    *grid = n;   // shared memory and TMEM allow one CTA per SM
     return e;
   }
-  cfg.gridDim = dim3(2 * *grid, 1, 1);
-  return cudaLaunchKernelEx(&cfg, fn, maps[0], maps[1], maps[2], maps[3], p);
+  fn<<<*grid, block_threads(MODE), smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_tile_kernel(const CUtensorMap* maps, const TileParams& p, int* grid, cudaStream_t stream) {
   switch (p.mode) {
-    case kModeFold: return launch_mode<kModeFold, false>(maps, p, grid, stream);
+    case kModeFold: return launch_mode<kModeFold>(maps, p, grid, stream);
     case kModeFO:
-      if (p.stream_heads) return launch_mode<kModeFO, false, true>(maps, p, grid, stream);
-      return p.pair ? launch_mode<kModeFO, true>(maps, p, grid, stream)
-                    : launch_mode<kModeFO, false>(maps, p, grid, stream);
+      return p.stream_heads ? launch_mode<kModeFO, true>(maps, p, grid, stream)
+                            : launch_mode<kModeFO>(maps, p, grid, stream);
     case kModeADD:
-      if (p.stream_heads) return launch_mode<kModeADD, false, true>(maps, p, grid, stream);
-      return p.pair ? launch_mode<kModeADD, true>(maps, p, grid, stream)
-                    : launch_mode<kModeADD, false>(maps, p, grid, stream);
-    case kModeAlpha: return launch_mode<kModeAlpha, false>(maps, p, grid, stream);
-    case kModeXPrime: return launch_mode<kModeXPrime, false>(maps, p, grid, stream);
-    case kModeQNorm: return launch_mode<kModeQNorm, false>(maps, p, grid, stream);
-    case kModeCNorm: return launch_mode<kModeCNorm, false>(maps, p, grid, stream);
+      return p.stream_heads ? launch_mode<kModeADD, true>(maps, p, grid, stream)
+                            : launch_mode<kModeADD>(maps, p, grid, stream);
+    case kModeAlpha: return launch_mode<kModeAlpha>(maps, p, grid, stream);
+    case kModeXPrime: return launch_mode<kModeXPrime>(maps, p, grid, stream);
+    case kModeQNorm: return launch_mode<kModeQNorm>(maps, p, grid, stream);
+    case kModeCNorm: return launch_mode<kModeCNorm>(maps, p, grid, stream);
     case kModeLOO:
-      return p.stream_heads ? launch_mode<kModeLOO, false, true>(maps, p, grid, stream)
-                            : launch_mode<kModeLOO, false>(maps, p, grid, stream);
+      return p.stream_heads ? launch_mode<kModeLOO, true>(maps, p, grid, stream)
+                            : launch_mode<kModeLOO>(maps, p, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

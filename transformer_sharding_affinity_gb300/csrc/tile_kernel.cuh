@@ -7,32 +7,29 @@
 
 namespace aff {
 
-// Every job of the tile kernel is "two 128-row A tiles against one shared
-// 128-row B tile": D1 = A1 * B^T and D2 = A2 * B^T accumulate in tensor
-// memory over K in blocks of 64 fp16 elements (128-byte rows).
-constexpr int kBlockM = 128;      // rows per A tile  (TMEM lanes)
-constexpr int kBlockN = 128;      // rows per B tile  (TMEM columns per accumulator)
+// A job of the tile kernel stages, per K block of 64 fp16 elements (128-byte
+// rows), three 128-row tiles.  The FO / ADD / LOO passes and the fold run two
+// N = 128 MMAs per K slice, D1 = A1 * B^T and D2 = A2 * B^T, sharing the third
+// tile as B: TMEM lanes are A rows (neurons).  The other passes run one
+// N = 256 MMA: A = the third tile, B = the first two back to back, so their
+// lanes are the third tile's rows (tokens; neurons for ||b_gk||^2).
+constexpr int kBlockM = 128;      // rows per tile (TMEM lanes)
+constexpr int kBlockN = 128;      // TMEM columns per tile of the accumulator
 constexpr int kBlockK = 64;       // fp16 elements per K block (one 128 B swizzle row)
 constexpr int kTileBytes = kBlockM * kBlockK * 2;     // 16 KB
-constexpr int kStageBytes = 3 * kTileBytes;           // A1 + A2 + B = 48 KB
-// CTA-pair (cta_group::2) variant of FO / ADD: each CTA holds its own 128 A rows
-// and half (64 rows) of the shared 128-row B tile, so a stage is 40 KB.
-constexpr int kPairBRows = kBlockN / 2;
-constexpr int kPairStageBytes = 2 * kTileBytes + kPairBRows * kBlockK * 2;
-// Epilogue warps: 8 (two per TMEM lane quarter, 64 columns each), or 16 for
-// the x' pass of the down edge and the leave-one-out passes (four per lane
-// quarter, 32 columns each): the x' and c_h passes wait on x loads and the
-// LOO pass on its heavier per-token arithmetic, all latency-bound with 8 (3.20 -> 2.47 ms on
-// the Qwen3-shaped layer; FO and ADD measured slower with 16: 2.17 -> 2.34 ms
-// for FO, 96 registers a thread then).  The block is one TMA warp, one MMA
+constexpr int kStageBytes = 3 * kTileBytes;           // three tiles = 48 KB
+// Epilogue warps: 8 (two per TMEM lane quarter), or 16 for the x' pass of the
+// down edge and the leave-one-out passes (four per lane quarter): the x' and
+// c_h passes wait on x loads and the LOO pass on its heavier per-token
+// arithmetic, all latency-bound with 8.  The block is one TMA warp, one MMA
 // warp and the epilogue warps.
 constexpr int kWideEpiWarps = 16;
 constexpr int kEpiWarps = 8;
-constexpr __host__ __device__ int epi_warps(int mode, bool pair) {
-  return (!pair && (mode == 4 || mode == 6 || mode == 7)) ? kWideEpiWarps : kEpiWarps;
+constexpr __host__ __device__ int epi_warps(int mode) {
+  return (mode == 4 || mode == 6 || mode == 7) ? kWideEpiWarps : kEpiWarps;
 }
-constexpr __host__ __device__ int block_threads(int mode, bool pair) { return 64 + 32 * epi_warps(mode, pair); }
-constexpr int kTmemCols = 512;                        // 2 buffers x (D1 128 + D2 128)
+constexpr __host__ __device__ int block_threads(int mode) { return 64 + 32 * epi_warps(mode); }
+constexpr int kTmemCols = 512;                        // 2 accumulator buffers x 256 columns
 constexpr int kMaxDynSmem = 232448;                   // 227 KB opt-in limit per block
 
 enum TileMode : int {
@@ -40,9 +37,9 @@ enum TileMode : int {
   kModeFO = 1,     // per token tile: operating point, then every head's Delta^2
   kModeADD = 2,    // per token tile: every head's (p.w^g)^2 + (p.w^u)^2
   kModeAlpha = 3,  // per token tile: alpha = silu(g) u  -> fp16 [T_pad][I_pad]
-  kModeXPrime = 4, // x' = x + alpha Wd^T for 256 tokens, sum_d x'^2 -> 1/r'^2
+  kModeXPrime = 4, // x' = x + alpha Wd^T per (token tile, 256 columns d): partial sums of x'^2
   kModeQNorm = 5,  // ||b_gk||^2 = sum over group g's q/k/v rows r of ((Wqkv' diag(gamma'))_r . w^d_k)^2
-  kModeCNorm = 6,  // per (256 tokens, head h): c_h/r = (a_h/r) Wo^(h)^T; sum_d (c/r)^2 and sum_d x (c/r)
+  kModeCNorm = 6,  // per (token tile, head h): c_h/r = (a_h/r) Wo^(h)^T; sum_d (c/r)^2 and sum_d x (c/r)
   kModeLOO = 7     // per token tile: operating point g, u, then every head's exact leave-one-out change
 };
 
@@ -54,17 +51,16 @@ struct TileParams {
   int32_t n_ktiles;        // neuron tiles of 128 (I_pad / 128)
   int32_t n_ttiles;        // token tiles of 128 (T_pad / 128)
   int32_t tiles_per_unit;  // token tiles per FO/ADD/alpha unit
-  int32_t n_ntiles;        // fold: column tiles of 128 over H*dh; x': over D; qnorm: row tiles per group
+  int32_t n_ntiles;        // fold: column tiles of 128 over H*dh; x', c_h: tiles of 256 over D; qnorm: row tiles of 256 per group
   int32_t rows_per_group;  // qnorm: (H/G + 2) * dh
   int32_t nkb_D, nkb_dh, nkb_I;
   int32_t ls_D, ls_dh;     // 16-wide K slices in the last K block of D and of dh
-  int32_t pair;            // FO / ADD: 1 = CTA pairs with 256-row (cta_group::2) MMAs
   int32_t stream_heads;    // FO / ADD / LOO: 1 = the heads' K ranges are streamed back to back
                            // (d_head % 16 == 0 but not % 64): M16 is [2][I_pad][H*dh], a16 read as [T][H*dh]
   int32_t nkb_HD, ls_HD;   // streaming: K blocks over H*dh, 16-wide slices in the last one
   int32_t spp;             // streaming: 16-wide K slices per head (d_head / 16)
   uint32_t* status;
-  float* partial;          // FO/ADD: [n_chunks][2][H][I_pad]; x': [T_pad] sum x'^2 parts
+  float* partial;          // FO/ADD/LOO: [n_chunks][column group][H][I_pad]; x': [column tile][group][T_pad]
   __half* M16;             // fold output
   __half* alpha16;         // alpha output
   const uint16_t* x_bf16;  // x' epilogue reads x (bf16 bits) [T][D]

@@ -121,7 +121,7 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
   L.status = L.take(256);
   if (d.dtype == AFF_BF16) {
     L.I_pad = round_up(I, 256);
-    L.T_pad = round_up(T, 128);
+    L.T_pad = round_up(T, down ? 128 : 256);   // head passes take 256 tokens at a time
     L.W16 = L.take((size_t)2 * L.I_pad * D * 2);
     L.n16 = L.take((size_t)T * D * 2);
     if (!down) {
@@ -196,7 +196,7 @@ EncodeTiledFn encode_fn() {
 // fp16 tensor of `rank` dims (dims[0] innermost, contiguous), 128 B swizzle,
 // box = 64 innermost elements x box1 (x 1 in the other dims); OOB reads zero.
 aff_status make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, const uint64_t* strides,
-                    uint32_t box1, int box1_dim) {
+                    uint32_t box1, int box1_dim, uint32_t box2 = 1, int box2_dim = -1) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     g_last_cuda_error = "cuTensorMapEncodeTiled unavailable";
@@ -212,6 +212,7 @@ aff_status make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* d
   for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
   bx[0] = 64;
   bx[box1_dim] = box1;
+  if (box2_dim > 0) bx[box2_dim] = box2;
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), gd, gs, bx, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -222,6 +223,13 @@ aff_status make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* d
     return AFF_ERR_CUDA;
   }
   return AFF_OK;
+}
+
+// The gate (part 0) or up (part 1) rows of 128 consecutive neurons of W16
+// ([I_pad / 16][2][16][D]) as one box: dims (D, 16, 2, I_pad / 16), box (64, 16, 1, 8).
+aff_status map_gate_up(CUtensorMap* m, const void* W16, uint64_t D, uint64_t I_pad) {
+  uint64_t d[4] = {D, 16, 2, I_pad / 16}, s[3] = {D * 2, 16 * D * 2, 32 * D * 2};
+  return make_map(m, W16, 4, d, s, 16, 1, 8, 3);
 }
 
 aff_status map2(CUtensorMap* m, const void* p, uint64_t inner, uint64_t rows) {
@@ -467,7 +475,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   std::memset(maps, 0, sizeof maps);
   // fold: M_h = [Wg; Wu] diag(gamma) Wo^(h)
   {
-    if ((st = map2(&maps[0], W16, (uint64_t)D, (uint64_t)2 * I_pad)) != AFF_OK) return st;
+    if ((st = map_gate_up(&maps[0], W16, (uint64_t)D, (uint64_t)I_pad)) != AFF_OK) return st;
     uint64_t dm[3] = {(uint64_t)D, 2, (uint64_t)H * dh}, sd[2] = {(uint64_t)D * 2, (uint64_t)D * 4};
     if ((st = make_map(&maps[1], GWo16, 3, dm, sd, 128, 2)) != AFF_OK) return st;
     maps[2] = maps[0];
@@ -503,7 +511,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     AFF_CUDA(launch_loo_rho(cn, inv_r, rho, T, (int)L.T_pad, H, D, epi_warps(kModeCNorm) / 4, s));
   }
   int epi_groups = 2;   // column groups per token tile in the partial sums (set below)
-  // FO / ADD / LOO: per token tile, operating point (FO, LOO) then every head
+  // FO / ADD / LOO: per (256 tokens, 64 neurons), operating point (FO, LOO) then every head
   {
     const uint32_t brows = 128u;
     uint64_t dx[2] = {(uint64_t)D, (uint64_t)T}, sx[1] = {(uint64_t)D * 2};
@@ -514,12 +522,12 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
       maps[1] = maps[0];
     }
     if (stream_heads(d)) {
-      // M16 as [2 * I_pad][H*dh] and a16 as [T][H*dh]: K blocks run across head boundaries
+      // M16 as [2 I_pad][H*dh] and a16 as [T][H*dh]: K blocks run across head boundaries
       if ((st = map2(&maps[2], M16, (uint64_t)H * dh, (uint64_t)2 * I_pad)) != AFF_OK) return st;
       if ((st = map2(&maps[3], a16, (uint64_t)H * dh, (uint64_t)T)) != AFF_OK) return st;
     } else {
-      uint64_t dm[3] = {(uint64_t)dh, (uint64_t)I_pad, (uint64_t)2 * H};
-      uint64_t sd[2] = {(uint64_t)dh * 2, (uint64_t)I_pad * dh * 2};
+      uint64_t dm[3] = {(uint64_t)dh, (uint64_t)2 * I_pad, (uint64_t)H};
+      uint64_t sd[2] = {(uint64_t)dh * 2, (uint64_t)2 * I_pad * dh * 2};
       if ((st = make_map(&maps[2], M16, 3, dm, sd, 128, 1)) != AFF_OK) return st;
       uint64_t da[3] = {(uint64_t)dh, (uint64_t)H, (uint64_t)T};
       uint64_t sa[2] = {(uint64_t)dh * 2, (uint64_t)H * dh * 2};
@@ -527,7 +535,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     }
     TileParams p = base_params(d, L, ws, fo ? kModeFO : (loo ? kModeLOO : kModeADD));
     p.rho = rho;
-    p.n_units = (int)(L.n_chunks * p.n_ktiles);
+    p.n_units = (int)(L.n_chunks * 2 * p.n_ktiles);   // (256 tokens, 64 neurons)
     p.partial = partial;
     epi_groups = epi_warps(p.mode) / 4;
     if ((st = run_tile(maps, p, s, true)) != AFF_OK) return st;
@@ -606,7 +614,7 @@ aff_status affinity_down(const void* x, const void* gamma, const void* Wg, const
   std::memset(maps, 0, sizeof maps);
   // alpha = silu(g) u for every (token, neuron)
   {
-    if ((st = map2(&maps[0], W16, (uint64_t)D, (uint64_t)2 * I_pad)) != AFF_OK) return st;
+    if ((st = map_gate_up(&maps[0], W16, (uint64_t)D, (uint64_t)I_pad)) != AFF_OK) return st;
     if ((st = map2(&maps[1], n16, (uint64_t)D, (uint64_t)T)) != AFF_OK) return st;
     maps[2] = maps[0];
     maps[3] = maps[0];

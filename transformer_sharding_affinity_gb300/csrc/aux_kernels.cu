@@ -75,7 +75,8 @@ __global__ void prep_tokens_kernel(const uint16_t* __restrict__ x, const uint16_
 }
 
 // ---------------------------------------------------------------- weights
-// W16 = fp16 copy of [Wg; Wu] with each block padded to I_pad rows of zeros.
+// W16 = fp16 copy of Wg and Wu, I_pad neurons (zero rows past I), in groups of 16
+// neurons: their 16 gate rows, then their 16 up rows ([I_pad / 16][2][16][D]).
 __global__ void prep_gate_up_kernel(const uint16_t* __restrict__ Wg, const uint16_t* __restrict__ Wu,
                                     __half* __restrict__ W16, int I, int I_pad, int D, uint32_t* status) {
   const size_t n8 = (size_t)2 * I_pad * D / 8;
@@ -83,7 +84,8 @@ __global__ void prep_gate_up_kernel(const uint16_t* __restrict__ Wg, const uint1
   for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8; v += (size_t)gridDim.x * blockDim.x) {
     const size_t e0 = v * 8;
     const int r = (int)(e0 / D), d = (int)(e0 % D);
-    const int blk = r / I_pad, k = r % I_pad;
+    // row r: neuron group r / 32, gate (0) or up (1) row, neuron 16 * (r / 32) + r % 16
+    const int blk = (r >> 4) & 1, k = (r >> 5) * 16 + (r & 15);
     __align__(16) __half o[8];
     if (k < I) {
       const uint16_t* src = (blk == 0 ? Wg : Wu) + (size_t)k * D + d;

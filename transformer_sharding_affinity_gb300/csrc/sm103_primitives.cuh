@@ -187,6 +187,22 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(taddr));
 }
+// 16 lanes x 8 consecutive 32-bit columns, read twice: threads 0..15 get lanes
+// taddr.lane + i at columns taddr.col .. +7, threads 16..31 the same lanes at
+// columns taddr.col + kSplit .. +7 (the .16x32bx2 shape).
+template <int kSplit>
+__device__ __forceinline__ void tmem_ld8_x2(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr), "n"(kSplit));
+}
+// As tmem_ld8_x2 with 4 columns.
+template <int kSplit>
+__device__ __forceinline__ void tmem_ld4_x2(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x4.b32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr), "n"(kSplit));
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA

@@ -6,15 +6,22 @@
 // roles:
 //   warp 0       TMA producer: a ring of `stages` 48 KB stages, each holding
 //                three 128 x 64 tiles (fp16, 128 B swizzle);
-//   warp 1       MMA issuer (one thread).  Most passes: for every K slice
-//                of 16, two tcgen05.mma (M = 128, N = 128) into a pair of fp32
-//                accumulators D1 = A1 B^T, D2 = A2 B^T.  The alpha pass: one
-//                MMA with M = 128 tokens (the third tile) and N = 256 (the
-//                gate and up tiles back to back), so its TMEM lanes are
-//                tokens.  Two accumulator buffers of 256 columns alternate so
-//                the epilogue of one job overlaps the MMAs of the next;
+//   warp 1       MMA issuer (one thread): for every K slice of 16 one
+//                tcgen05.mma with M = 128 and N = 256 (two of the tiles back
+//                to back) into an fp32 accumulator of 256 TMEM columns; the
+//                fold issues two with N = 128 (D1 = A1 B^T, D2 = A2 B^T).
+//                Two accumulator buffers alternate so the epilogue of one job
+//                overlaps the MMAs of the next;
 //   warps 2..    epilogue: TMEM -> registers with tcgen05.ld; warp w reads
 //                TMEM lanes 32*(w%4)..+31 and one column group (w-2)/4.
+// FO / ADD / LOO: A = 128 weight rows of 64 neurons, in groups of 16 per lane
+// quarter: lanes 32q..32q+15 hold the gate rows (g, or p.w^g) of neurons
+// 16q..16q+15 and lanes 32q+16..32q+31 their up rows; B = 256 tokens.  The
+// epilogue reads them with the 16x32bx2 TMEM shape: thread l and thread l + 16
+// of a warp both get neuron 16q + l's gate and up values, for the first and
+// the second half of the warp's columns, so the sum over tokens stays within
+// a thread.  The alpha, x', c_h and ||b_gk||^2
+// passes: A = the third tile (tokens, or neurons), B = the first two.
 // Work is a fixed list of units, each a short list of jobs; CTAs take units
 // round-robin.  Which CTA computes a unit never changes its result, and
 // every unit writes its own partial sums, so the outputs do not depend on
@@ -65,16 +72,22 @@ __device__ __forceinline__ Unit unit_info(const TileParams& p, int u) {
       break;
     case kModeFO:
     case kModeLOO:
-    case kModeADD:
+    case kModeADD: {   // one unit per (256 tokens, 64 neurons): kt = the 64-neuron block
+      const int nblk = 2 * p.n_ktiles;
+      U.kt = u % nblk;
+      U.chunk = u / nblk;
+      U.tile0 = 2 * U.chunk;
+      const bool op = p.mode != kModeADD;   // with an operating-point job
+      U.njobs = op ? 1 + p.H : p.H;
+      U.njobs_pm = STREAM ? (op ? 2 : 1) : U.njobs;
+      return U;
+    }
     case kModeAlpha: {
       U.kt = u % p.n_ktiles;
       U.chunk = u / p.n_ktiles;
       U.tile0 = U.chunk * p.tiles_per_unit;
-      int nt = min(p.tiles_per_unit, p.n_ttiles - U.tile0);
-      const bool op = p.mode == kModeFO || p.mode == kModeLOO;   // with an operating-point job
-      int per = op ? 1 + p.H : (p.mode == kModeADD ? p.H : 1);
-      U.njobs = nt * per;
-      U.njobs_pm = (STREAM && p.mode != kModeAlpha) ? nt * (op ? 2 : 1) : U.njobs;
+      U.njobs = min(p.tiles_per_unit, p.n_ttiles - U.tile0);
+      U.njobs_pm = U.njobs;
       return U;
     }
     case kModeCNorm:   // consecutive units: the heads of one token tile; jobs: column tiles of 256
@@ -113,32 +126,17 @@ __device__ __forceinline__ Job job_next(const TileParams& p, const Unit& U, JobI
   J.kt = U.kt;
   if constexpr (MODE == kModeFold) {
     J.kind = kJobFold; J.nkb = 2 * p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D; J.nt = U.base;
-  } else if constexpr (MODE == kModeFO || MODE == kModeLOO) {
-    J.t0 = (U.tile0 + it.a) * kBlockN;
-    if (STREAM && pm) {
-      if (it.b == 0) {
-        J.kind = kJobGateUp; J.nkb = p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D;
-      } else {
-        J.kind = kJobStream; J.nkb = p.nkb_HD; J.nkb_part = p.nkb_HD; J.last_nks = p.ls_HD;
-      }
-      if (++it.b == 2) { it.b = 0; ++it.a; }
-      return J;
-    }
-    if (it.b == 0) {
+  } else if constexpr (MODE == kModeFO || MODE == kModeLOO || MODE == kModeADD) {
+    J.t0 = U.tile0 * kBlockN;   // 256 tokens
+    const int j = it.b++;
+    const bool op = MODE != kModeADD;
+    if (op && j == 0) {
       J.kind = kJobGateUp; J.nkb = p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D;
-    } else {
-      J.kind = kJobHead; J.head = it.b - 1; J.nkb = p.nkb_dh; J.nkb_part = p.nkb_dh; J.last_nks = p.ls_dh;
-    }
-    if (++it.b == 1 + p.H) { it.b = 0; ++it.a; }
-  } else if constexpr (MODE == kModeADD) {
-    J.t0 = (U.tile0 + it.a) * kBlockN;
-    if (STREAM && pm) {
+    } else if (STREAM && pm) {
       J.kind = kJobStream; J.nkb = p.nkb_HD; J.nkb_part = p.nkb_HD; J.last_nks = p.ls_HD;
-      ++it.a;
-      return J;
+    } else {
+      J.kind = kJobHead; J.head = op ? j - 1 : j; J.nkb = p.nkb_dh; J.nkb_part = p.nkb_dh; J.last_nks = p.ls_dh;
     }
-    J.kind = kJobHead; J.head = it.b; J.nkb = p.nkb_dh; J.nkb_part = p.nkb_dh; J.last_nks = p.ls_dh;
-    if (++it.b == p.H) { it.b = 0; ++it.a; }
   } else if constexpr (MODE == kModeAlpha) {
     J.t0 = (U.tile0 + it.b) * kBlockN;
     J.kind = kJobGateUp; J.nkb = p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D;
@@ -189,9 +187,10 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
   constexpr int NG = EW / 4;              // column groups of a 128-column accumulator
   constexpr int CW = kBlockN / NG;        // columns per epilogue thread (of each accumulator)
   constexpr bool kHeads = MODE == kModeFO || MODE == kModeADD || MODE == kModeLOO;
-  // one N = 256 MMA per K slice (see the file comment)
-  constexpr bool kWide = MODE == kModeAlpha || MODE == kModeXPrime || MODE == kModeCNorm || MODE == kModeQNorm;
-  constexpr int CWW = 2 * kBlockN / NG;   // wide passes: columns of the 256 per epilogue thread
+  // one N = 256 MMA per K slice (see the file comment): A = the first tile for the
+  // head passes, the third for the others
+  constexpr bool kWide = MODE != kModeFold;
+  constexpr int CWW = 2 * kBlockN / NG;   // columns of the 256 per epilogue thread
   const int S = p.stages;
   constexpr int kSB = kStageBytes;        // bytes of one pipeline stage
   constexpr int kBOff = 2 * kTileBytes;   // offset of the third tile within a stage
@@ -263,24 +262,33 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
             const int kx = kb_in * kBlockK;
             mbar_arrive_expect_tx(fb, kStageBytes);
             switch (J.kind) {
-              case kJobGateUp:   // W16 gate / up rows (the MMA's B), n16 token rows (its A)
-                tma_load_2d(st, &map0, fb, kx, J.kt * kBlockM);
-                tma_load_2d(st + kTileBytes, &map0, fb, kx, p.I_pad + J.kt * kBlockM);
-                tma_load_2d(st + kBOff, &map1, fb, kx, J.t0);
+              case kJobGateUp:
+                if (MODE == kModeAlpha) {
+                  // the gate and up rows of 128 neurons (the MMA's B, through the 4-D view
+                  // of W16), n16 token rows (its A)
+                  tma_load_4d(st, &map0, fb, kx, 0, 0, J.kt * 8);
+                  tma_load_4d(st + kTileBytes, &map0, fb, kx, 0, 1, J.kt * 8);
+                  tma_load_2d(st + kBOff, &map1, fb, kx, J.t0);
+                } else {
+                  // A = the 128 interleaved W16 rows of 64 neurons, B = 256 n16 token rows
+                  tma_load_2d(st, &map0, fb, kx, J.kt * kBlockM);
+                  tma_load_2d(st + kTileBytes, &map1, fb, kx, J.t0);
+                  tma_load_2d(st + kBOff, &map1, fb, kx, J.t0 + kBlockN);
+                }
                 break;
-              case kJobStream:   // M16 gate / up planes, a16 tokens; K runs over all heads' columns
+              case kJobStream:   // M16 rows of 64 neurons, 256 a16 tokens; K runs over all heads' columns
                 tma_load_2d(st, &map2, fb, kx, J.kt * kBlockM);
-                tma_load_2d(st + kTileBytes, &map2, fb, kx, p.I_pad + J.kt * kBlockM);
-                tma_load_2d(st + kBOff, &map3, fb, kx, J.t0);
+                tma_load_2d(st + kTileBytes, &map3, fb, kx, J.t0);
+                tma_load_2d(st + kBOff, &map3, fb, kx, J.t0 + kBlockN);
                 break;
-              case kJobHead:     // M16 (gate, up) of head h, a16 head h tokens
-                tma_load_3d(st, &map2, fb, kx, J.kt * kBlockM, 2 * J.head);
-                tma_load_3d(st + kTileBytes, &map2, fb, kx, J.kt * kBlockM, 2 * J.head + 1);
-                tma_load_3d(st + kBOff, &map3, fb, kx, J.head, J.t0);
+              case kJobHead:     // M16 rows of 64 neurons for head h, 256 a16 head h tokens
+                tma_load_3d(st, &map2, fb, kx, J.kt * kBlockM, J.head);
+                tma_load_3d(st + kTileBytes, &map3, fb, kx, J.head, J.t0);
+                tma_load_3d(st + kBOff, &map3, fb, kx, J.head, J.t0 + kBlockN);
                 break;
-              case kJobFold:     // A = W16 rows, B = gamma*Wo^T (hi part, then lo part)
-                tma_load_2d(st, &map0, fb, kx, J.kt * kBlockM);
-                tma_load_2d(st + kTileBytes, &map0, fb, kx, p.I_pad + J.kt * kBlockM);
+              case kJobFold:     // A1 / A2 = gate / up rows of 128 neurons (4-D view), B = gamma*Wo^T (hi, then lo)
+                tma_load_4d(st, &map0, fb, kx, 0, 0, J.kt * 8);
+                tma_load_4d(st + kTileBytes, &map0, fb, kx, 0, 1, J.kt * 8);
                 tma_load_3d(st + kBOff, &map1, fb, kx, part, J.nt * kBlockN);
                 break;
               case kJobXPrime:   // Wd16 rows d (256, the MMA's B), alpha16 token rows (its A)
@@ -320,8 +328,7 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
     // A lean loop: this one thread must issue MMAs as fast as the tensor pipe
     // retires them, so no divisions, and descriptors advance by constants.
     if (lane == 0) {
-      // wide passes: M = 128 (the third tile), N = 256 (the first two); one such
-      // MMA reads 12 KB of shared memory where a D1 / D2 pair reads 16 KB
+      // N = 256: one MMA reads 12 KB of shared memory where a D1 / D2 pair reads 16 KB
       constexpr uint32_t idesc = kWide ? idesc_f16(kBlockM, 2 * kBlockN, 0) : idesc_f16(kBlockM, kBlockN, 0);
       const uint64_t dbase = smem_desc_k_sw128(smem_u32(sm.stage0));   // first tile of stage 0
       constexpr uint64_t kStageDesc = (uint64_t)(kSB >> 4);             // descriptor step per stage
@@ -345,16 +352,13 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
             for (int kb = 0; ok && kb < J.nkb; ++kb) {
               if (!mbar_wait(&sm.full[s], ph, sm.abort_flag, p.status)) { ok = false; break; }
               tc_fence_after();
-              const uint64_t da1 = dbase + (uint64_t)s * kStageDesc;
-              const uint64_t da2 = da1 + kA2, db = da1 + kB;
+              const uint64_t da = dbase + (uint64_t)s * kStageDesc, dt = da + kA2;
               const int nks = (kb == J.nkb - 1) ? J.last_nks : 4;
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks) {
                 if (ks < nks && heads_left > 0) {
-                  const uint32_t d1 = tmem + (uint32_t)(b * 2 * kBlockN);
-                  const uint32_t acc = sih > 0 ? 1u : 0u;
-                  mma_f16_ss(d1, da1 + 2 * ks, db + 2 * ks, idesc, acc);
-                  mma_f16_ss(d1 + kBlockN, da2 + 2 * ks, db + 2 * ks, idesc, acc);
+                  const uint32_t d = tmem + (uint32_t)(b * 2 * kBlockN);
+                  mma_f16_ss(d, da + 2 * ks, dt + 2 * ks, idesc, sih > 0 ? 1u : 0u);
                   if (++sih == p.spp) {
                     mma_commit(&sm.tfull[b]);
                     if (++b == 2) { b = 0; tph ^= 1u; }
@@ -384,7 +388,9 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               if (ks < nks) {
-                if constexpr (kWide) {
+                if constexpr (kHeads) {   // A = weights (first tile), B = 256 tokens
+                  mma_f16_ss(d1, da1 + 2 * ks, da2 + 2 * ks, idesc, acc);
+                } else if constexpr (kWide) {
                   mma_f16_ss(d1, db + 2 * ks, da1 + 2 * ks, idesc, acc);
                 } else {
                   mma_f16_ss(d1, da1 + 2 * ks, db + 2 * ks, idesc, acc);
@@ -412,9 +418,14 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // TMEM lane quarter this warp may read
     const int hf = (warp - 2) >> 2;    // which group of CW columns of the tile
-    const int row = q * 32 + lane;     // TMEM lane = row of the MMA's A: an A1 row, or a token (alpha)
+    const int row = q * 32 + lane;     // TMEM lane = row of the MMA's A
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
-    // FO: f32x2 pairs of silu'(g)u and silu(g) of this neuron, CW tokens; LOO: g and u
+    // Head passes: thread l and thread l + 16 both work on neuron 16q + l of the unit's
+    // 64, on the first and the last CW tokens of the column group.
+    const bool upl = lane >= 16;
+    const uint32_t tg = tmem + ((uint32_t)(q * 32) << 16);        // the quarter's gate lanes
+    const uint32_t tu = tmem + ((uint32_t)(q * 32 + 16) << 16);   // ... and its up lanes
+    // FO: f32x2 pairs of silu'(g)u and silu(g), CW tokens; LOO: g and u
     uint64_t abA[CW / 2], abB[CW / 2];
 #pragma unroll
     for (int i = 0; i < CW / 2; ++i) { abA[i] = 0ull; abB[i] = 0ull; }
@@ -441,27 +452,22 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
             // Phase 1: stash g, u in the registers that will hold A', B' and hand the
             // accumulator buffer back at once, so the MMAs of the next two head
             // jobs run while phase 2 (exp + reciprocal per element) computes.
-            constexpr int kG = CW == 64 ? 16 : 8;   // TMEM columns per read
+            const uint32_t col = (uint32_t)(b * 2 * kBlockN + hf * CWW);
 #pragma unroll
-            for (int c = 0; c < CW / kG; ++c) {
-              uint32_t gr[kG], ur[kG];
-              if constexpr (kG == 16) {
-                tmem_ld16(c1 + c * kG, gr);
-                tmem_ld16(c2 + c * kG, ur);
-              } else {
-                tmem_ld8(c1 + c * kG, gr);
-                tmem_ld8(c2 + c * kG, ur);
-              }
+            for (int c = 0; c < CW / 8; ++c) {
+              uint32_t gr[8], ur[8];
+              tmem_ld8_x2<CW>(tg + col + c * 8, gr);
+              tmem_ld8_x2<CW>(tu + col + c * 8, ur);
               tmem_ld_wait();
-              if (c == CW / kG - 1) {
+              if (c == CW / 8 - 1) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.tempty[b]);
               }
 #pragma unroll
-              for (int i = 0; i < kG; i += 2) {
-                abA[(c * kG + i) / 2] = pk_u(gr[i], gr[i + 1]);
-                abB[(c * kG + i) / 2] = pk_u(ur[i], ur[i + 1]);
+              for (int i = 0; i < 8; i += 2) {
+                abA[(c * 8 + i) / 2] = pk_u(gr[i], gr[i + 1]);
+                abB[(c * 8 + i) / 2] = pk_u(ur[i], ur[i + 1]);
               }
             }
             // Phase 2 (FO): (g, u) -> (A', B') = (silu'(g) u, silu(g)) in place; LOO keeps g and u.
@@ -520,21 +526,32 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
           }
         }
         if constexpr (kHeads) {
-          // kJobHead: per token Delta = A' pg + B' pu (FO) or pg^2 + pu^2 (ADD), summed over tokens;
-          // LOO: g - g^(-h) = g (1 - rho) + rho pg = g + rho (pg - g) with rho = r / rms(x - c_h),
-          // likewise for u
+          // kJobHead.  FO: Delta = A' pg + B' pu per token, Delta^2 summed over the thread's CW
+          // tokens; LOO: g - g^(-h) = g + rho (pg - g) with rho = r / rms(x - c_h), likewise
+          // for u, both squared; ADD: each lane sums the squares of its own 2 CW values.
+          const uint32_t col = (uint32_t)(b * 2 * kBlockN + hf * CWW);
           uint64_t acc = pk(0.f, 0.f);
           // TMEM columns per read: 8, or 4 in LOO mode (its arithmetic needs more registers)
           constexpr int kW = MODE == kModeLOO ? 4 : 8;
+          // LOO: rho of the thread's tokens, 4 at a time
+          const float* rho_t = p.rho + (size_t)J.head * p.T_pad + J.t0 + hf * CWW + (upl ? CW : 0);
 #pragma unroll
           for (int c = 0; c < CW / kW; ++c) {
             uint32_t pg[kW], pu[kW];
-            if constexpr (kW == 8) {
-              tmem_ld8(c1 + c * kW, pg);
-              tmem_ld8(c2 + c * kW, pu);
+            if constexpr (MODE == kModeADD) {   // own lane: 32x32b, both halves of the group
+              if constexpr (kW == 8) {
+                tmem_ld8(tl + col + c * kW, pg);
+                tmem_ld8(tl + col + CW + c * kW, pu);
+              } else {
+                tmem_ld4(tl + col + c * kW, pg);
+                tmem_ld4(tl + col + CW + c * kW, pu);
+              }
+            } else if constexpr (kW == 8) {
+              tmem_ld8_x2<CW>(tg + col + c * kW, pg);
+              tmem_ld8_x2<CW>(tu + col + c * kW, pu);
             } else {
-              tmem_ld4(c1 + c * kW, pg);
-              tmem_ld4(c2 + c * kW, pu);
+              tmem_ld4_x2<CW>(tg + col + c * kW, pg);
+              tmem_ld4_x2<CW>(tu + col + c * kW, pu);
             }
             tmem_ld_wait();
             if (c == CW / kW - 1) {
@@ -542,9 +559,8 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
               __syncwarp();
               if (lane == 0) mbar_arrive(&sm.tempty[b]);
             }
-            float4 rq = make_float4(0.f, 0.f, 0.f, 0.f);   // LOO: rho of the chunk's 4 tokens
-            if constexpr (MODE == kModeLOO)   // the same address in every lane: a broadcast
-              rq = __ldg(reinterpret_cast<const float4*>(p.rho + (size_t)J.head * p.T_pad + J.t0 + hf * CW) + c);
+            float4 rq = make_float4(0.f, 0.f, 0.f, 0.f);
+            if constexpr (MODE == kModeLOO) rq = __ldg(reinterpret_cast<const float4*>(rho_t) + c);
 #pragma unroll
             for (int i = 0; i < kW; i += 2) {
               const uint64_t vg = pk_u(pg[i], pg[i + 1]);
@@ -599,13 +615,15 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
                 vu.y = pack_h2(__uint_as_float(mu[i + 2]), __uint_as_float(mu[i + 3]));
                 vu.z = pack_h2(__uint_as_float(mu[i + 4]), __uint_as_float(mu[i + 5]));
                 vu.w = pack_h2(__uint_as_float(mu[i + 6]), __uint_as_float(mu[i + 7]));
-                if (p.stream_heads) {   // [2][I_pad][H*dh]: heads back to back along K
+                // rows in groups of 16 neurons: 16 gate rows, then their 16 up rows
+                const size_t rg = (size_t)(kk >> 4) * 32 + (kk & 15), ru = rg + 16;
+                if (p.stream_heads) {   // [2 I_pad][H*dh]: heads back to back along K
                   const size_t HD = (size_t)p.H * p.dh;
-                  *reinterpret_cast<uint4*>(p.M16 + (size_t)kk * HD + n) = vg;
-                  *reinterpret_cast<uint4*>(p.M16 + ((size_t)p.I_pad + kk) * HD + n) = vu;
-                } else {                // [2H][I_pad][dh]
-                  *reinterpret_cast<uint4*>(p.M16 + ((size_t)(2 * h) * p.I_pad + kk) * p.dh + jj) = vg;
-                  *reinterpret_cast<uint4*>(p.M16 + ((size_t)(2 * h + 1) * p.I_pad + kk) * p.dh + jj) = vu;
+                  *reinterpret_cast<uint4*>(p.M16 + rg * HD + n) = vg;
+                  *reinterpret_cast<uint4*>(p.M16 + ru * HD + n) = vu;
+                } else {                // [H][2 I_pad][dh]
+                  *reinterpret_cast<uint4*>(p.M16 + ((size_t)h * 2 * p.I_pad + rg) * p.dh + jj) = vg;
+                  *reinterpret_cast<uint4*>(p.M16 + ((size_t)h * 2 * p.I_pad + ru) * p.dh + jj) = vu;
                 }
               }
             }
@@ -684,12 +702,16 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
       if (!ok) break;
       // ---- end of unit
       if constexpr (kHeads) {
-        // [chunk][column group][H][I_pad]
-        float* dst = p.partial + ((size_t)(U.chunk * NG + hf) * p.H) * p.I_pad + U.kt * kBlockM + row;
+        // [chunk][column group][H][I_pad]: threads l and l + 16 add their sums (the same
+        // value in both) and thread l writes it
+        const int k = U.kt * 64 + q * 16 + (lane & 15);
+        float* dst = p.partial + ((size_t)(U.chunk * NG + hf) * p.H) * p.I_pad + k;
         for (int h = 0; h < p.H; ++h) {
           float* sp = &sm.sacc[(hf * p.H + h) * kBlockM + row];
-          dst[(size_t)h * p.I_pad] = *sp;
+          const float v = *sp;
           *sp = 0.f;
+          const float t = v + __shfl_xor_sync(0xffffffffu, v, 16);
+          if (!upl) dst[(size_t)h * p.I_pad] = t;
         }
       }
       if constexpr (MODE == kModeXPrime) {

@@ -8,11 +8,12 @@
 namespace aff {
 
 // A job of the tile kernel stages, per K block of 64 fp16 elements (128-byte
-// rows), three 128-row tiles.  The FO / ADD / LOO passes and the fold run two
-// N = 128 MMAs per K slice, D1 = A1 * B^T and D2 = A2 * B^T, sharing the third
-// tile as B: TMEM lanes are A rows (neurons).  The other passes run one
-// N = 256 MMA: A = the third tile, B = the first two back to back, so their
-// lanes are the third tile's rows (tokens; neurons for ||b_gk||^2).
+// rows), three 128-row tiles, and runs one N = 256 MMA per K slice (the fold
+// runs two N = 128 MMAs, D1 = A1 * B^T and D2 = A2 * B^T).  Head passes (FO,
+// ADD, LOO): A = 128 interleaved gate / up weight rows of 64 neurons, B = 256
+// tokens.  Alpha, x', c_h, ||b_gk||^2: A = the third tile (tokens; neurons for
+// ||b_gk||^2), B = the first two.  Gate / up weights (W16, M16) are stored in
+// groups of 16 neurons: 16 gate rows, then the same neurons' 16 up rows.
 constexpr int kBlockM = 128;      // rows per tile (TMEM lanes)
 constexpr int kBlockN = 128;      // TMEM columns per tile of the accumulator
 constexpr int kBlockK = 64;       // fp16 elements per K block (one 128 B swizzle row)
@@ -33,14 +34,14 @@ constexpr int kTmemCols = 512;                        // 2 accumulator buffers x
 constexpr int kMaxDynSmem = 232448;                   // 227 KB opt-in limit per block
 
 enum TileMode : int {
-  kModeFold = 0,   // M_h = Wg/Wu * diag(gamma) * Wo^(h)   -> fp16 [2H][I_pad][dh]
-  kModeFO = 1,     // per token tile: operating point, then every head's Delta^2
-  kModeADD = 2,    // per token tile: every head's (p.w^g)^2 + (p.w^u)^2
+  kModeFold = 0,   // M_h = Wg/Wu * diag(gamma) * Wo^(h)   -> fp16 [H][2 I_pad][dh], interleaved rows
+  kModeFO = 1,     // per (256 tokens, 64 neurons): operating point, then every head's Delta^2
+  kModeADD = 2,    // per (256 tokens, 64 neurons): every head's (p.w^g)^2 + (p.w^u)^2
   kModeAlpha = 3,  // per token tile: alpha = silu(g) u  -> fp16 [T_pad][I_pad]
   kModeXPrime = 4, // x' = x + alpha Wd^T per (token tile, 256 columns d): partial sums of x'^2
   kModeQNorm = 5,  // ||b_gk||^2 = sum over group g's q/k/v rows r of ((Wqkv' diag(gamma'))_r . w^d_k)^2
   kModeCNorm = 6,  // per (token tile, head h): c_h/r = (a_h/r) Wo^(h)^T; sum_d (c/r)^2 and sum_d x (c/r)
-  kModeLOO = 7     // per token tile: operating point g, u, then every head's exact leave-one-out change
+  kModeLOO = 7     // per (256 tokens, 64 neurons): g, u, then every head's exact leave-one-out change
 };
 
 struct TileParams {
@@ -48,7 +49,7 @@ struct TileParams {
   int32_t n_units;
   int32_t stages;
   int32_t T, D, H, G, dh, I, I_pad, T_pad;
-  int32_t n_ktiles;        // neuron tiles of 128 (I_pad / 128)
+  int32_t n_ktiles;        // neuron tiles of 128 (I_pad / 128); head passes: blocks of 64 = 2 n_ktiles
   int32_t n_ttiles;        // token tiles of 128 (T_pad / 128)
   int32_t tiles_per_unit;  // token tiles per FO/ADD/alpha unit
   int32_t n_ntiles;        // fold: column tiles of 128 over H*dh; x', c_h: tiles of 256 over D; qnorm: row tiles of 256 per group
@@ -56,7 +57,7 @@ struct TileParams {
   int32_t nkb_D, nkb_dh, nkb_I;
   int32_t ls_D, ls_dh;     // 16-wide K slices in the last K block of D and of dh
   int32_t stream_heads;    // FO / ADD / LOO: 1 = the heads' K ranges are streamed back to back
-                           // (d_head % 16 == 0 but not % 64): M16 is [2][I_pad][H*dh], a16 read as [T][H*dh]
+                           // (d_head % 16 == 0 but not % 64): M16 is [2 I_pad][H*dh], a16 read as [T][H*dh]
   int32_t nkb_HD, ls_HD;   // streaming: K blocks over H*dh, 16-wide slices in the last one
   int32_t spp;             // streaming: 16-wide K slices per head (d_head / 16)
   uint32_t* status;

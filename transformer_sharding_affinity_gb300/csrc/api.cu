@@ -67,7 +67,7 @@ aff_status aff::check_device(int* sm_count) {
 namespace {
 
 constexpr int64_t kMaxDim = (int64_t)1 << 30;
-constexpr int kTilesPerUnit = 2;      // token tiles (of 128) per FO / ADD unit
+constexpr int kTilesPerUnit = 2;      // token tiles (of 128) per alpha unit
 constexpr int kDownTokenChunk = 256;  // tokens per partial sum of E_t[alpha^2 / r'^2]
 
 inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
@@ -121,11 +121,11 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
   L.status = L.take(256);
   if (d.dtype == AFF_BF16) {
     L.I_pad = round_up(I, 256);
-    L.T_pad = round_up(T, down ? 128 : 256);   // head passes take 256 tokens at a time
+    L.T_pad = round_up(T, down ? 128 : 256 * kHeadSets);   // head-pass units take 512 tokens
     L.W16 = L.take((size_t)2 * L.I_pad * D * 2);
     L.n16 = L.take((size_t)T * D * 2);
     if (!down) {
-      L.n_chunks = ceil_div(L.T_pad / 128, kTilesPerUnit);
+      L.n_chunks = L.T_pad / (256 * kHeadSets);
       L.GWo16 = L.take((size_t)H * dh * 2 * D * 2);
       L.M16 = L.take((size_t)2 * H * L.I_pad * dh * 2);
       L.a16 = L.take((size_t)T * H * dh * 2);
@@ -535,7 +535,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     }
     TileParams p = base_params(d, L, ws, fo ? kModeFO : (loo ? kModeLOO : kModeADD));
     p.rho = rho;
-    p.n_units = (int)(L.n_chunks * 2 * p.n_ktiles);   // (256 tokens, 64 neurons)
+    p.n_units = (int)(L.n_chunks * 2 * p.n_ktiles);   // (512 tokens, 64 neurons)
     p.partial = partial;
     epi_groups = epi_warps(p.mode) / 4;
     if ((st = run_tile(maps, p, s, true)) != AFF_OK) return st;

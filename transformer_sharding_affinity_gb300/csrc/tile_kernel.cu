@@ -72,14 +72,14 @@ __device__ __forceinline__ Unit unit_info(const TileParams& p, int u) {
       break;
     case kModeFO:
     case kModeLOO:
-    case kModeADD: {   // one unit per (256 tokens, 64 neurons): kt = the 64-neuron block
+    case kModeADD: {   // one unit per (kHeadSets x 256 tokens, 64 neurons): kt = the 64-neuron block
       const int nblk = 2 * p.n_ktiles;
       U.kt = u % nblk;
       U.chunk = u / nblk;
-      U.tile0 = 2 * U.chunk;
+      U.tile0 = 2 * kHeadSets * U.chunk;
       const bool op = p.mode != kModeADD;   // with an operating-point job
-      U.njobs = op ? 1 + p.H : p.H;
-      U.njobs_pm = STREAM ? (op ? 2 : 1) : U.njobs;
+      U.njobs = kHeadSets * (op ? 1 + p.H : p.H);
+      U.njobs_pm = STREAM ? kHeadSets * (op ? 2 : 1) : U.njobs;
       return U;
     }
     case kModeAlpha: {
@@ -127,9 +127,12 @@ __device__ __forceinline__ Job job_next(const TileParams& p, const Unit& U, JobI
   if constexpr (MODE == kModeFold) {
     J.kind = kJobFold; J.nkb = 2 * p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D; J.nt = U.base;
   } else if constexpr (MODE == kModeFO || MODE == kModeLOO || MODE == kModeADD) {
-    J.t0 = U.tile0 * kBlockN;   // 256 tokens
-    const int j = it.b++;
+    // a = the unit's set of 256 tokens, b = the job within the set
+    J.t0 = (U.tile0 + 2 * it.a) * kBlockN;
     const bool op = MODE != kModeADD;
+    const int j = it.b;
+    const int per = (STREAM && pm) ? (op ? 2 : 1) : (op ? 1 + p.H : p.H);
+    if (++it.b == per) { it.b = 0; ++it.a; }
     if (op && j == 0) {
       J.kind = kJobGateUp; J.nkb = p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D;
     } else if (STREAM && pm) {

@@ -30,18 +30,20 @@ constexpr __host__ __device__ int epi_warps(int mode) {
   return (mode == 4 || mode == 6 || mode == 7) ? kWideEpiWarps : kEpiWarps;
 }
 constexpr __host__ __device__ int block_threads(int mode) { return 64 + 32 * epi_warps(mode); }
+// FO / ADD / LOO units: sets of 256 tokens per unit (one partial sum per unit)
+constexpr int kHeadSets = 2;
 constexpr int kTmemCols = 512;                        // 2 accumulator buffers x 256 columns
 constexpr int kMaxDynSmem = 232448;                   // 227 KB opt-in limit per block
 
 enum TileMode : int {
   kModeFold = 0,   // M_h = Wg/Wu * diag(gamma) * Wo^(h)   -> fp16 [H][2 I_pad][dh], interleaved rows
-  kModeFO = 1,     // per (256 tokens, 64 neurons): operating point, then every head's Delta^2
-  kModeADD = 2,    // per (256 tokens, 64 neurons): every head's (p.w^g)^2 + (p.w^u)^2
+  kModeFO = 1,     // per (512 tokens, 64 neurons): operating point, then every head's Delta^2
+  kModeADD = 2,    // per (512 tokens, 64 neurons): every head's (p.w^g)^2 + (p.w^u)^2
   kModeAlpha = 3,  // per token tile: alpha = silu(g) u  -> fp16 [T_pad][I_pad]
   kModeXPrime = 4, // x' = x + alpha Wd^T per (token tile, 256 columns d): partial sums of x'^2
   kModeQNorm = 5,  // ||b_gk||^2 = sum over group g's q/k/v rows r of ((Wqkv' diag(gamma'))_r . w^d_k)^2
   kModeCNorm = 6,  // per (token tile, head h): c_h/r = (a_h/r) Wo^(h)^T; sum_d (c/r)^2 and sum_d x (c/r)
-  kModeLOO = 7     // per (256 tokens, 64 neurons): g, u, then every head's exact leave-one-out change
+  kModeLOO = 7     // per (512 tokens, 64 neurons): g, u, then every head's exact leave-one-out change
 };
 
 struct TileParams {

@@ -75,6 +75,10 @@ inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 // Partial sums of x'^2 per token that the x' pass writes: one per column tile
 // of 256 and column group of its epilogue.
 inline int xprime_groups(int64_t D) { return (int)((D + 255) / 256) * (epi_warps(kModeXPrime) / 4); }
+
+// Partial sums per (token, head) that the c_h pass writes: one per column tile of 256
+// and column group of its epilogue.
+inline int cnorm_groups(int64_t D) { return (int)((D + 255) / 256) * (epi_warps(kModeCNorm) / 4); }
 inline int64_t ceil_div(int64_t v, int64_t m) { return (v + m - 1) / m; }
 
 aff_status check_dims(const aff_dims* d) {
@@ -135,7 +139,7 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
       if (mode == AFF_MODE_FO) L.wdn = L.take((size_t)L.I_pad * 4);
       if (mode == AFF_MODE_LOO) {
         L.Wo16 = L.take((size_t)D * H * dh * 2);
-        L.cn = L.take((size_t)2 * (epi_warps(kModeCNorm) / 4) * H * L.T_pad * 4);
+        L.cn = L.take((size_t)2 * cnorm_groups(D) * H * L.T_pad * 4);
         L.rho = L.take((size_t)H * L.T_pad * 4);
         L.inv_r = L.take((size_t)L.T_pad * 4);
       }
@@ -504,11 +508,11 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     maps[3] = maps[0];
     TileParams p = base_params(d, L, ws, kModeCNorm);
     p.n_ntiles = (int)ceil_div(D, 256);
-    p.n_units = (int)(L.T_pad / 128 * H);
+    p.n_units = (int)(L.T_pad / 128 * p.n_ntiles);
     p.partial = cn;
     p.x_bf16 = x_b;
     if ((st = run_tile(maps, p, s)) != AFF_OK) return st;
-    AFF_CUDA(launch_loo_rho(cn, inv_r, rho, T, (int)L.T_pad, H, D, epi_warps(kModeCNorm) / 4, s));
+    AFF_CUDA(launch_loo_rho(cn, inv_r, rho, T, (int)L.T_pad, H, D, cnorm_groups(D), s));
   }
   int epi_groups = 2;   // column groups per token tile in the partial sums (set below)
   // FO / ADD / LOO: per (256 tokens, 64 neurons), operating point (FO, LOO) then every head

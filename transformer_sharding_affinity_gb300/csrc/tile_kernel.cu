@@ -90,10 +90,10 @@ __device__ __forceinline__ Unit unit_info(const TileParams& p, int u) {
       U.njobs_pm = U.njobs;
       return U;
     }
-    case kModeCNorm:   // consecutive units: the heads of one token tile; jobs: column tiles of 256
-      U.head = u % p.H;
-      U.base = (u / p.H) * kBlockM;
-      U.njobs = p.n_ntiles;
+    case kModeCNorm:   // one unit per (token tile, 256 columns d); jobs: the H heads
+      U.kt = u % p.n_ntiles;   // the column tile
+      U.base = (u / p.n_ntiles) * kBlockM;
+      U.njobs = p.H;
       break;
     case kModeXPrime:   // one unit per (token tile, 256 columns d)
       U.base = (u / p.n_ntiles) * kBlockM;
@@ -149,7 +149,7 @@ __device__ __forceinline__ Job job_next(const TileParams& p, const Unit& U, JobI
     J.t0 = U.base; J.nt = U.head;
   } else if constexpr (MODE == kModeCNorm) {
     J.kind = kJobCNorm; J.nkb = p.nkb_dh; J.nkb_part = p.nkb_dh; J.last_nks = p.ls_dh;
-    J.t0 = U.base; J.head = U.head; J.nt = it.b++;
+    J.t0 = U.base; J.head = it.b++; J.nt = U.kt;
   } else {   // kModeQNorm
     J.kind = kJobQNorm; J.nkb = 2 * p.nkb_D; J.nkb_part = p.nkb_D; J.last_nks = p.ls_D;
     J.g = U.head; J.nt = it.b++;
@@ -432,8 +432,9 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
     uint64_t abA[CW / 2], abB[CW / 2];
 #pragma unroll
     for (int i = 0; i < CW / 2; ++i) { abA[i] = 0ull; abB[i] = 0ull; }
-    float ss1 = 0.f;                   // x' / qnorm / cnorm running sums
-    float xd1 = 0.f;                   // cnorm: sum_d x (c/r)
+    float ss1 = 0.f;                   // x' / qnorm running sums
+    // c_h pass: x of the thread's token and CWW columns, loaded at a unit's first head
+    uint32_t xr[MODE == kModeCNorm ? CWW / 2 : 1];
     int b = 0;
     uint32_t tph = 0;                  // TMEM buffer phase (flips every second job)
     bool ok = true;
@@ -632,11 +633,56 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
             }
           }
         }
-        if constexpr (MODE == kModeXPrime || MODE == kModeCNorm) {
-          // lane = token t; columns d = J.nt * 256 + hf * CWW + ...: x' pass: (alpha Wd^T)[t][d],
-          // x' = x + that, accumulate x'^2 over d; c_h pass: (c_h / r)[t][d], accumulate (c/r)^2
-          // and x (c/r) over d.  Columns past D hold zeros (the B tiles were zero-filled), so
-          // only x needs a guard; D % 8 == 0, so an 8-column group is wholly inside or past D.
+        if constexpr (MODE == kModeCNorm) {
+          // lane = token t; columns d = J.nt * 256 + hf * CWW + ... of (c_h / r)[t][d] for head
+          // J.head: sum (c/r)^2 and x (c/r) over them.  x is read once per unit.  Columns past
+          // D hold zeros (the B tiles were zero-filled), so only x needs a guard; D % 8 == 0,
+          // so an 8-column group is wholly inside or wholly past D.
+          const int t = J.t0 + row;
+          if (j == 0) {
+#pragma unroll
+            for (int q8 = 0; q8 < CWW / 8; ++q8) {
+              const int d = J.nt * 2 * kBlockN + hf * CWW + q8 * 8;
+              uint4 w = make_uint4(0u, 0u, 0u, 0u);
+              if (d < p.D && t < p.T) w = __ldg(reinterpret_cast<const uint4*>(p.x_bf16 + (size_t)t * p.D + d));
+              xr[q8 * 4 + 0] = w.x;
+              xr[q8 * 4 + 1] = w.y;
+              xr[q8 * 4 + 2] = w.z;
+              xr[q8 * 4 + 3] = w.w;
+            }
+          }
+          const uint32_t c0 = tl + (uint32_t)(b * 2 * kBlockN + hf * CWW);
+          float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+          for (int c = 0; c < CWW / 16; ++c) {
+            uint32_t v[16];
+            tmem_ld16(c0 + c * 16, v);
+            tmem_ld_wait();
+            if (c == CWW / 16 - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&sm.tempty[b]);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+              const uint32_t e = xr[(c * 16 + i) / 2];
+              const float va = __uint_as_float(v[i]), vb = __uint_as_float(v[i + 1]);
+              s1 = fmaf(va, va, s1);
+              s1 = fmaf(vb, vb, s1);
+              s2 = fmaf(__uint_as_float(e << 16), va, s2);
+              s2 = fmaf(__uint_as_float(e & 0xFFFF0000u), vb, s2);
+            }
+          }
+          // [column tile][column group][quantity][H][T_pad]: quantity 0 = sum (c/r)^2, 1 = sum x (c/r)
+          float* dst = p.partial + ((size_t)((U.kt * NG + hf) * 2) * p.H + J.head) * p.T_pad + t;
+          dst[0] = s1;
+          dst[(size_t)p.H * p.T_pad] = s2;
+        }
+        if constexpr (MODE == kModeXPrime) {
+          // lane = token t; columns d = J.nt * 256 + hf * CWW + ...: (alpha Wd^T)[t][d],
+          // x' = x + that, accumulate x'^2 over d.  Columns past D hold zeros (the B tiles were
+          // zero-filled), so only x needs a guard; D % 8 == 0, so an 8-column group is wholly
+          // inside or wholly past D.
           const int t = J.t0 + row;
           const uint32_t c0 = tl + (uint32_t)(b * 2 * kBlockN + hf * CWW);
 #pragma unroll
@@ -649,10 +695,6 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
               __syncwarp();
               if (lane == 0) mbar_arrive(&sm.tempty[b]);
             }
-            if constexpr (MODE == kModeCNorm) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) ss1 = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), ss1);
-            }
             const int d0 = J.nt * 2 * kBlockN + hf * CWW + c * 16;
 #pragma unroll
             for (int q8 = 0; q8 < 2; ++q8) {
@@ -664,14 +706,9 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
                 for (int i = 0; i < 4; ++i) {
                   const float xa = __uint_as_float(e[i] << 16), xb = __uint_as_float(e[i] & 0xFFFF0000u);
                   const float va = __uint_as_float(v[q8 * 8 + 2 * i]), vb = __uint_as_float(v[q8 * 8 + 2 * i + 1]);
-                  if constexpr (MODE == kModeXPrime) {
-                    const float ya = xa + va, yb = xb + vb;
-                    ss1 = fmaf(ya, ya, ss1);
-                    ss1 = fmaf(yb, yb, ss1);
-                  } else {
-                    xd1 = fmaf(xa, va, xd1);
-                    xd1 = fmaf(xb, vb, xd1);
-                  }
+                  const float ya = xa + va, yb = xb + vb;
+                  ss1 = fmaf(ya, ya, ss1);
+                  ss1 = fmaf(yb, yb, ss1);
                 }
               }
             }
@@ -721,13 +758,6 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
         // [column tile][column group][T_pad]; token tiles are whole, so t < T_pad
         p.partial[(size_t)(U.head * NG + hf) * p.T_pad + U.base + row] = ss1;
         ss1 = 0.f;
-      }
-      if constexpr (MODE == kModeCNorm) {
-        // [column group][quantity][H][T_pad]: quantity 0 = sum (c/r)^2, 1 = sum x (c/r)
-        const int t = U.base + row;
-        p.partial[((size_t)(hf * 2 + 0) * p.H + U.head) * p.T_pad + t] = ss1;
-        p.partial[((size_t)(hf * 2 + 1) * p.H + U.head) * p.T_pad + t] = xd1;
-        ss1 = xd1 = 0.f;
       }
     }
   }

@@ -19,11 +19,12 @@ constexpr int kBlockN = 128;      // TMEM columns per tile of the accumulator
 constexpr int kBlockK = 64;       // fp16 elements per K block (one 128 B swizzle row)
 constexpr int kTileBytes = kBlockM * kBlockK * 2;     // 16 KB
 constexpr int kStageBytes = 3 * kTileBytes;           // three tiles = 48 KB
-// Epilogue warps: 8 (two per TMEM lane quarter), or 16 for the x' pass of the
-// down edge and the leave-one-out passes (four per lane quarter): the x' and
-// c_h passes wait on x loads and the LOO pass on its heavier per-token
-// arithmetic, all latency-bound with 8.  The block is one TMA warp, one MMA
-// warp and the epilogue warps.
+// Epilogue warps: 8 (two per TMEM lane quarter), or 16 (four per lane
+// quarter) for the x' pass of the down edge and the two leave-one-out passes:
+// the x' and c_h passes wait on loads of x and the LOO pass on its heavier
+// per-token arithmetic, all latency-bound with 8 (LOO 2.09 ms with 16 warps,
+// 2.98 ms with 8).  The block is one TMA warp, one MMA warp and the epilogue
+// warps.
 constexpr int kWideEpiWarps = 16;
 constexpr int kEpiWarps = 8;
 constexpr __host__ __device__ int epi_warps(int mode) {

@@ -514,7 +514,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     if ((st = run_tile(maps, p, s)) != AFF_OK) return st;
     AFF_CUDA(launch_loo_rho(cn, inv_r, rho, T, (int)L.T_pad, H, D, cnorm_groups(D), s));
   }
-  int epi_groups = 2;   // column groups per token tile in the partial sums (set below)
+  int epi_groups = 2;   // column groups of the epilogue in the partial sums (set below)
   // FO / ADD / LOO: per (256 tokens, 64 neurons), operating point (FO, LOO) then every head
   {
     const uint32_t brows = 128u;

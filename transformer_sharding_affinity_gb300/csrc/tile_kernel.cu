@@ -35,7 +35,7 @@ namespace aff {
 
 enum JobKind : int {
   kJobGateUp = 0, kJobHead = 1, kJobFold = 2, kJobXPrime = 3, kJobQNorm = 4, kJobCNorm = 5,
-  kJobStream = 6   // producer / MMA view of all H head jobs of a token tile, K ranges back to back
+  kJobStream = 6   // producer / MMA view of all H head jobs of a 256-token set, K ranges back to back
 };
 
 struct Job {
@@ -110,16 +110,16 @@ __device__ __forceinline__ Unit unit_info(const TileParams& p, int u) {
   return U;
 }
 
-// Position within a unit's job list, advanced without divisions: FO / ADD:
-// a = token tile of the unit, b = job within the tile; qnorm: a = group,
-// b = row tile; the other modes count jobs in b.
+// Position within a unit's job list, advanced without divisions: FO / ADD /
+// LOO: a = the unit's set of 256 tokens, b = job within the set; the other
+// modes count jobs in b.
 struct JobIter {
   int a, b;
 };
 
 // The next job of unit U.  Every role walks the same sequence, except that
 // with streamed heads the producer and the MMA issuer (pm) see one kJobStream
-// where the epilogue sees the H head jobs of a token tile.
+// where the epilogue sees the H head jobs of a 256-token set.
 template <int MODE, bool STREAM = false>
 __device__ __forceinline__ Job job_next(const TileParams& p, const Unit& U, JobIter& it, bool pm = false) {
   Job J{};
@@ -537,8 +537,11 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
           uint64_t acc = pk(0.f, 0.f);
           // TMEM columns per read: 8, or 4 in LOO mode (its arithmetic needs more registers)
           constexpr int kW = MODE == kModeLOO ? 4 : 8;
-          // LOO: rho of the thread's tokens, 4 at a time
-          const float* rho_t = p.rho + (size_t)J.head * p.T_pad + J.t0 + hf * CWW + (upl ? CW : 0);
+          // LOO: rho of the thread's tokens, 4 at a time, each float4 fetched one slice ahead
+          const float4* rho4 =
+              reinterpret_cast<const float4*>(p.rho + (size_t)J.head * p.T_pad + J.t0 + hf * CWW + (upl ? CW : 0));
+          float4 rq_next = make_float4(0.f, 0.f, 0.f, 0.f);
+          if constexpr (MODE == kModeLOO) rq_next = __ldg(rho4);
 #pragma unroll
           for (int c = 0; c < CW / kW; ++c) {
             uint32_t pg[kW], pu[kW];
@@ -563,8 +566,10 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
               __syncwarp();
               if (lane == 0) mbar_arrive(&sm.tempty[b]);
             }
-            float4 rq = make_float4(0.f, 0.f, 0.f, 0.f);
-            if constexpr (MODE == kModeLOO) rq = __ldg(reinterpret_cast<const float4*>(rho_t) + c);
+            const float4 rq = rq_next;
+            if constexpr (MODE == kModeLOO) {
+              if (c + 1 < CW / kW) rq_next = __ldg(rho4 + c + 1);
+            }
 #pragma unroll
             for (int i = 0; i < kW; i += 2) {
               const uint64_t vg = pk_u(pg[i], pg[i + 1]);

@@ -43,7 +43,7 @@ enum TileMode : int {
   kModeAlpha = 3,  // per token tile: alpha = silu(g) u  -> fp16 [T_pad][I_pad]
   kModeXPrime = 4, // x' = x + alpha Wd^T per (token tile, 256 columns d): partial sums of x'^2
   kModeQNorm = 5,  // ||b_gk||^2 = sum over group g's q/k/v rows r of ((Wqkv' diag(gamma'))_r . w^d_k)^2
-  kModeCNorm = 6,  // per (token tile, head h): c_h/r = (a_h/r) Wo^(h)^T; sum_d (c/r)^2 and sum_d x (c/r)
+  kModeCNorm = 6,  // per (token tile, 256 columns d), every head h: c_h/r = (a_h/r) Wo^(h)^T; sums of (c/r)^2, x (c/r)
   kModeLOO = 7     // per (512 tokens, 64 neurons): g, u, then every head's exact leave-one-out change
 };
 
@@ -54,7 +54,7 @@ struct TileParams {
   int32_t T, D, H, G, dh, I, I_pad, T_pad;
   int32_t n_ktiles;        // neuron tiles of 128 (I_pad / 128); head passes: blocks of 64 = 2 n_ktiles
   int32_t n_ttiles;        // token tiles of 128 (T_pad / 128)
-  int32_t tiles_per_unit;  // token tiles per FO/ADD/alpha unit
+  int32_t tiles_per_unit;  // token tiles per alpha unit
   int32_t n_ntiles;        // fold: column tiles of 128 over H*dh; x', c_h: tiles of 256 over D; qnorm: row tiles of 256 per group
   int32_t rows_per_group;  // qnorm: (H/G + 2) * dh
   int32_t nkb_D, nkb_dh, nkb_I;

@@ -535,6 +535,28 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
           // for u, both squared; ADD: each lane sums the squares of its own 2 CW values.
           const uint32_t col = (uint32_t)(b * 2 * kBlockN + hf * CWW);
           uint64_t acc = pk(0.f, 0.f);
+          if constexpr (MODE == kModeADD) {
+            // own lane, both halves of the group, 16 columns per read: ADD has registers to
+            // spare, and fewer, wider reads leave fewer TMEM load latencies in the job
+#pragma unroll
+            for (int c = 0; c < CW / 16; ++c) {
+              uint32_t v1[16], v2[16];
+              tmem_ld16(tl + col + c * 16, v1);
+              tmem_ld16(tl + col + CW + c * 16, v2);
+              tmem_ld_wait();
+              if (c == CW / 16 - 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.tempty[b]);
+              }
+#pragma unroll
+              for (int i = 0; i < 16; i += 2) {
+                const uint64_t w1 = pk_u(v1[i], v1[i + 1]), w2 = pk_u(v2[i], v2[i + 1]);
+                acc = fma2(w1, w1, acc);
+                acc = fma2(w2, w2, acc);
+              }
+            }
+          } else {
           // TMEM columns per read: 8, or 4 in LOO mode (its arithmetic needs more registers)
           constexpr int kW = MODE == kModeLOO ? 4 : 8;
           // LOO: rho of the thread's tokens, 4 at a time, each float4 fetched one slice ahead
@@ -545,15 +567,7 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
 #pragma unroll
           for (int c = 0; c < CW / kW; ++c) {
             uint32_t pg[kW], pu[kW];
-            if constexpr (MODE == kModeADD) {   // own lane: 32x32b, both halves of the group
-              if constexpr (kW == 8) {
-                tmem_ld8(tl + col + c * kW, pg);
-                tmem_ld8(tl + col + CW + c * kW, pu);
-              } else {
-                tmem_ld4(tl + col + c * kW, pg);
-                tmem_ld4(tl + col + CW + c * kW, pu);
-              }
-            } else if constexpr (kW == 8) {
+            if constexpr (kW == 8) {
               tmem_ld8_x2<CW>(tg + col + c * kW, pg);
               tmem_ld8_x2<CW>(tu + col + c * kW, pu);
             } else {
@@ -579,17 +593,15 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
                 uint64_t d = mul2(abA[ai], vg);
                 d = fma2(abB[ai], vu, d);
                 acc = fma2(d, d, acc);
-              } else if constexpr (MODE == kModeLOO) {
+              } else {   // LOO
                 const uint64_t rr = i == 0 ? pk(rq.x, rq.y) : pk(rq.z, rq.w), neg1 = pk(-1.0f, -1.0f);
                 const uint64_t dg = fma2(rr, fma2(abA[ai], neg1, vg), abA[ai]);
                 const uint64_t du = fma2(rr, fma2(abB[ai], neg1, vu), abB[ai]);
                 acc = fma2(dg, dg, acc);
                 acc = fma2(du, du, acc);
-              } else {
-                acc = fma2(vg, vg, acc);
-                acc = fma2(vu, vu, acc);
               }
             }
+          }
           }
           const float2 s2 = unpk(acc);
           sm.sacc[(hf * p.H + J.head) * kBlockM + row] += s2.x + s2.y;

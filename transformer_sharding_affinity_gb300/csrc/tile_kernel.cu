@@ -443,6 +443,14 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
       JobIter jt{0, 0};
       for (int j = 0; j < U.njobs; ++j, b ^= 1, tph ^= (uint32_t)(b == 0)) {
         const Job J = job_next<MODE, STREAM>(p, U, jt);
+        // LOO head job: lanes 0..15 fetch rho of the column group's CWW tokens (one float4
+        // each) before the accumulator wait, which hides the load; the token loop takes
+        // its values from them with shuffles
+        float4 rho_v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (MODE == kModeLOO) {
+          if (J.kind == kJobHead && lane < CWW / 4)
+            rho_v = __ldg(reinterpret_cast<const float4*>(p.rho + (size_t)J.head * p.T_pad + J.t0 + hf * CWW) + lane);
+        }
         int w_ok = 1;
         if (lane == 0) w_ok = mbar_wait(&sm.tfull[b], tph, sm.abort_flag, p.status) ? 1 : 0;
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
@@ -559,11 +567,6 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
           } else {
           // TMEM columns per read: 8, or 4 in LOO mode (its arithmetic needs more registers)
           constexpr int kW = MODE == kModeLOO ? 4 : 8;
-          // LOO: rho of the thread's tokens, 4 at a time, each float4 fetched one slice ahead
-          const float4* rho4 =
-              reinterpret_cast<const float4*>(p.rho + (size_t)J.head * p.T_pad + J.t0 + hf * CWW + (upl ? CW : 0));
-          float4 rq_next = make_float4(0.f, 0.f, 0.f, 0.f);
-          if constexpr (MODE == kModeLOO) rq_next = __ldg(rho4);
 #pragma unroll
           for (int c = 0; c < CW / kW; ++c) {
             uint32_t pg[kW], pu[kW];
@@ -580,9 +583,14 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
               __syncwarp();
               if (lane == 0) mbar_arrive(&sm.tempty[b]);
             }
-            const float4 rq = rq_next;
+            float4 rq = make_float4(0.f, 0.f, 0.f, 0.f);   // LOO: rho of the slice's 4 tokens
             if constexpr (MODE == kModeLOO) {
-              if (c + 1 < CW / kW) rq_next = __ldg(rho4 + c + 1);
+              static_assert(kW == 4, "one float4 of rho per slice");
+              const int src = (upl ? CW / 4 : 0) + c;
+              rq.x = __shfl_sync(0xffffffffu, rho_v.x, src);
+              rq.y = __shfl_sync(0xffffffffu, rho_v.y, src);
+              rq.z = __shfl_sync(0xffffffffu, rho_v.z, src);
+              rq.w = __shfl_sync(0xffffffffu, rho_v.w, src);
             }
 #pragma unroll
             for (int i = 0; i < kW; i += 2) {

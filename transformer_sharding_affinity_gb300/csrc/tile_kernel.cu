@@ -20,8 +20,8 @@
 // epilogue reads them with the 16x32bx2 TMEM shape: thread l and thread l + 16
 // of a warp both get neuron 16q + l's gate and up values, for the first and
 // the second half of the warp's columns, so the sum over tokens stays within
-// a thread.  The alpha, x', c_h and ||b_gk||^2
-// passes: A = the third tile (tokens, or neurons), B = the first two.
+// a thread.  The alpha, x', c_h and ||b_gk||^2 passes: A = the third tile
+// (tokens, or neurons), B = the first two.
 // Work is a fixed list of units, each a short list of jobs; CTAs take units
 // round-robin.  Which CTA computes a unit never changes its result, and
 // every unit writes its own partial sums, so the outputs do not depend on
@@ -44,8 +44,8 @@ struct Job {
   int nkb_part;  // K blocks per part (fold / qnorm run the K range twice: hi then lo)
   int last_nks;  // 16-wide K slices in the last block of a part
   int head;      // head index (kJobHead)
-  int t0;        // first token (row of the B tile, or of A1 for x')
-  int kt;        // neuron tile
+  int t0;        // first token
+  int kt;        // neuron tile of 128 (fold, alpha) or block of 64 (head passes)
   int nt;        // column / row tile
   int g;         // KV group (qnorm)
 };
@@ -53,11 +53,11 @@ struct Job {
 struct Unit {
   int njobs;     // jobs as the epilogue sees them
   int njobs_pm;  // jobs as the producer and the MMA issuer see them (fewer when heads are streamed)
-  int chunk;    // FO/ADD/LOO: token chunk index
-  int kt;
+  int chunk;    // FO/ADD/LOO/alpha: token chunk index
+  int kt;       // as Job::kt; cnorm: the column tile of 256
   int tile0;    // FO/ADD/LOO/alpha: first token tile
   int base;     // x', cnorm: first token; qnorm: first neuron
-  int head;     // cnorm: head; qnorm: KV group
+  int head;     // x': the column tile of 256; qnorm: KV group
 };
 
 // Unit u of the schedule.

@@ -47,8 +47,8 @@ def fo_flops(s) -> dict:
 KERNEL_SOURCES = ("tile_kernel.cu", "tile_kernel.cuh", "sm103_primitives.cuh")
 TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass), third FO launch of
-    # `python bench.py --steps 2 --warmup 3 --no-cpu-baseline --e2e-steps 0`: 468.37 + 50.80 MB
-    ("qwen3_0p6b_layer", "fo", 65536): {"bytes": 519.17e6, "src": "ebdb69f7f4fbabde"},
+    # `python bench.py --steps 2 --warmup 3 --no-cpu-baseline --e2e-steps 0`: 467.99 + 50.57 MB
+    ("qwen3_0p6b_layer", "fo", 65536): {"bytes": 518.55e6, "src": "b10f3384ed8b35b1"},
 }
 
 

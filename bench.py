@@ -45,6 +45,7 @@ def fo_flops(s) -> dict:
 # the FO tile kernel, from an ncu capture of this bench's workload; valid only
 # while the kernel sources hash to the recorded value (otherwise null).
 KERNEL_SOURCES = ("tile_kernel.cu", "tile_kernel.cuh", "sm103_primitives.cuh")
+MOMENT_SOURCES = ("moment_kernel.cu", "moment_kernel.cuh", "sm103_primitives.cuh")
 TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass), third FO launch of
     # `python bench.py --steps 2 --warmup 3 --no-cpu-baseline --e2e-steps 0`: 467.99 + 50.57 MB
@@ -52,10 +53,10 @@ TRAFFIC = {
 }
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources:
         with open(os.path.join(ROOT, "transformer_sharding_affinity_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -63,7 +64,7 @@ def kernel_source_hash() -> str:
 
 def measured_traffic(workload: str, mode: str, T: int):
     rec = TRAFFIC.get((workload, mode, T))
-    if rec is None or rec["src"] != kernel_source_hash():
+    if rec is None or rec["src"] != kernel_source_hash(MOMENT_SOURCES if mode == "add" else KERNEL_SOURCES):
         return None
     return rec["bytes"]
 
@@ -278,6 +279,8 @@ def main() -> None:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_0p6b_layer")
     ap.add_argument("--mode", default="fo", choices=["fo", "add", "loo", "down"])
+    ap.add_argument("--add-form", default="moment", choices=["moment", "direct"],
+                    help="ADD through each head's second moment (d_head <= 128) or the direct contraction")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -318,7 +321,10 @@ def main() -> None:
     layer = W.make_layer(shape, with_next=down)
     host = {k: DV.host_tensor(layer, k, shape.dtype).pin_memory() for k in keys}
     dev = {k: v.to("cuda") for k, v in host.items()}
-    d = B.dims(shape.T, shape.D, shape.H, shape.G, shape.dh, shape.I, shape.eps)
+    moment = args.mode == "add" and args.add_form == "moment" and shape.dh <= 128
+    direct_add = args.mode == "add" and not moment
+    d = B.dims(shape.T, shape.D, shape.H, shape.G, shape.dh, shape.I, shape.eps,
+               flags=B.AFF_FLAG_ADD_DIRECT if direct_add else 0)
     mode = 0 if down else B.MODES[args.mode]
     work = torch.empty(B.workspace_size(d, mode, down=down), dtype=torch.uint8, device="cuda")
     S = torch.empty((shape.I, shape.G) if down else (shape.G, shape.I), device="cuda")
@@ -435,6 +441,9 @@ def main() -> None:
     heads = 2 * shape.T * shape.H * shape.dh * 2 * shape.I
     if args.mode == "fo":
         flops_per_step, tile_flops = fl["total"], fl["tile_kernel"]
+    elif moment:   # fold, C_h = sum_t a~ a~^T, then m^T C_h m (hi and lo halves of C_h)
+        tile_flops = 2 * shape.T * shape.H * shape.dh ** 2
+        flops_per_step = fl["fold"] + tile_flops + 2 * 2 * 2 * shape.I * shape.H * shape.dh ** 2
     elif args.mode == "add":
         flops_per_step, tile_flops = fl["fold"] + heads, heads
     elif args.mode == "loo":   # the FO-shaped pass plus c_h / r = (a_h / r) Wo^(h)^T for the rms of x - c_h
@@ -446,29 +455,42 @@ def main() -> None:
             2 * 2 * (shape.H + 2 * shape.G) * shape.dh * shape.D * shape.I
     achieved = tile_flops / (kern_ms * 1e-3) / 1e12
     tokens = shape.T * ws
+    if moment:
+        # the Gram pass reads every token's a~ once (fp16): HBM-bound
+        gram_bytes = shape.T * shape.H * shape.dh * 2
+        gbs = gram_bytes / (kern_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": "moment_kernel<GRAM> (C_h = sum_t a~_t a~_t^T, tcgen05)",
+                "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+                "peak_source": pk["source"] + " HBM copy bandwidth", "kernel_ms": kern_ms,
+                "algorithmic_bytes_per_launch": gram_bytes, "algorithmic_flops_per_launch": tile_flops,
+                "traffic": measured_traffic(args.workload, args.mode, shape.T)}
+    else:
+        roof = {"bound": "tensor",
+                "kernel": ("affinity_tile_kernel<ALPHA> (gate/up GEMM, alpha = silu(g) u)" if down else
+                           f"affinity_tile_kernel<{args.mode.upper()}> (operating point + per-head contraction)"),
+                "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_tflops"],
+                "frac_sustained": achieved / pk["bf16_tflops_sustained"] if pk["bf16_tflops_sustained"] else None,
+                "peak_source": pk["source"] + " bf16 dense (fp16 runs at the bf16 rate)",
+                "kernel_ms": kern_ms, "algorithmic_flops_per_launch": tile_flops,
+                "traffic": measured_traffic(args.workload, "add_direct" if direct_add else args.mode, shape.T)}
     line = {
         "metric": METRIC, "value": tokens / (ms_step * 1e-3), "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp16 operands, fp32 accumulate (bf16 inputs)",
         "data": "synthetic",
         "config": {"workload": args.workload, "T": shape.T, "D": shape.D, "H": shape.H, "G": shape.G,
-                   "d_head": shape.dh, "I": shape.I, "mode": args.mode, "parallelism": f"dp{ws} (token shards)",
+                   "d_head": shape.dh, "I": shape.I, "mode": args.mode,
+                   **({"add_form": "moment" if moment else "direct"} if args.mode == "add" else {}),
+                   "parallelism": f"dp{ws} (token shards)",
                    "launch": "CUDA graph replay of one step" if graph is not None else "direct calls",
                    "l2": "inputs larger than L2 (a + x = %.0f MB per step); no flush" %
                          ((shape.T * (shape.H * shape.dh + shape.D) * 2) / 2**20)},
         "step_flops": flops_per_step,
         "step_tflops": flops_per_step / (ms_step * 1e-3) / 1e12,
         "step_frac_of_peak": flops_per_step / (ms_step * 1e-3) / 1e12 / pk["bf16_tflops"],
-        "roofline": {"bound": "tensor",
-                     "kernel": ("affinity_tile_kernel<ALPHA> (gate/up GEMM, alpha = silu(g) u)" if down else
-                                f"affinity_tile_kernel<{args.mode.upper()}> (operating point + per-head contraction)"),
-                     "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / pk["bf16_tflops"],
-                     "frac_sustained": achieved / pk["bf16_tflops_sustained"] if pk["bf16_tflops_sustained"] else None,
-                     "peak_source": pk["source"] + " bf16 dense (fp16 runs at the bf16 rate)",
-                     "kernel_ms": kern_ms, "algorithmic_flops_per_launch": tile_flops,
-                     "traffic": measured_traffic(args.workload, args.mode, shape.T)},
-        "gpu_launches": {"fo": 7, "add": 6, "loo": 9, "down": 9}[args.mode] * args.steps,
+        "roofline": roof,
+        "gpu_launches": (8 if moment else {"fo": 7, "add": 6, "loo": 9, "down": 9}[args.mode]) * args.steps,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": shape.G * shape.I * 4, "ms_per_step": e2e_ms},
         "clocks": clocks.summary(),

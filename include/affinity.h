@@ -90,9 +90,21 @@ typedef enum {
 typedef enum { AFF_BF16 = 0, AFF_FP32 = 1 } aff_dtype;
 
 /*
+ * aff_dims.flags bits.
+ *   AFF_FLAG_ADD_DIRECT: ADD mode contracts every token with every folded
+ *     neuron row (T x 2I x d_head multiply-adds per head).  Without it, AFF_BF16
+ *     ADD with d_head <= 128 takes the second-moment form: per head the d_head x
+ *     d_head matrix C_h = sum_t (a_h/r)(a_h/r)^T on the tensor cores, then
+ *     m^T C_h m for every folded row m -- the same sum in a different rounding
+ *     order (E_t[(p_h.w)^2] = m^T E_t[a~ a~^T] m).  Other modes ignore the bit.
+ */
+#define AFF_FLAG_ADD_DIRECT 1u
+
+/*
  * Layer shape.  T tokens, model width D, H query heads in G KV groups of
  * H/G heads, head width d_head, I FFN neurons; eps is the rms epsilon
- * (r = sqrt(mean_d x_d^2 + eps)); dtype an aff_dtype; flags must be 0.
+ * (r = sqrt(mean_d x_d^2 + eps)); dtype an aff_dtype; flags 0 or AFF_FLAG_ADD_DIRECT
+ * (any other bit is AFF_ERR_INVALID_ARG).
  *
  * Constraints: all sizes >= 1, H % G == 0.  AFF_BF16 additionally needs
  * D % 8 == 0, d_head % 8 == 0 and I % 8 == 0 (16-byte row strides for the

@@ -47,23 +47,33 @@ def topk_agrees(got_row: np.ndarray, ref_row: np.ndarray, k: int = TOPK, tie: fl
     return True
 
 
-def dims_of(B, shape):
+def dims_of(B, shape, flags=0):
     return B.dims(shape.T, shape.D, shape.H, shape.G, shape.dh, shape.I, shape.eps,
-                  B.AFF_BF16 if shape.dtype == "bf16" else B.AFF_FP32)
+                  B.AFF_BF16 if shape.dtype == "bf16" else B.AFF_FP32, flags)
+
+
+def mode_of(B, mode: str):
+    """(aff_mode, flags) for a test mode name; "add_direct" is ADD in its direct form."""
+    if mode == "add_direct":
+        return B.AFF_MODE_ADD, B.AFF_FLAG_ADD_DIRECT
+    return B.MODES[mode], 0
 
 
 def run_up(B, DV, shape, layer, mode: str, runs: int = 1, per_head: bool = True):
     import torch
     dev = DV.to_device(layer, shape.dtype)
-    d = dims_of(B, shape)
-    ws = torch.empty(B.workspace_size(d, B.MODES[mode]), dtype=torch.uint8, device="cuda")
+    m, flags = mode_of(B, mode)
+    d = dims_of(B, shape, flags)
+    ws = torch.empty(B.workspace_size(d, m), dtype=torch.uint8, device="cuda")
     S = torch.empty(shape.G, shape.I, device="cuda")
     Sh = torch.empty(shape.H, shape.I, device="cuda") if per_head else None
     outs = []
     for _ in range(runs):
         S.fill_(float("nan"))
+        if Sh is not None:
+            Sh.fill_(float("nan"))
         B.affinity_up(dev["a"], dev["x"], dev["Wo"], dev["gamma"], dev["Wg"], dev["Wu"], dev["Wd"], d,
-                      B.MODES[mode], S, Sh, ws)
+                      m, S, Sh, ws)
         st = B.device_status(ws)
         assert st == 0, f"device status {st}: {B.strerror(st)}"
         outs.append((S.cpu().numpy().copy(), None if Sh is None else Sh.cpu().numpy().copy()))
@@ -88,6 +98,7 @@ def run_down(B, DV, shape, layer, runs: int = 1):
 
 
 def oracle_up(O, shape, layer, mode, neurons=None):
+    mode = "add" if mode == "add_direct" else mode
     return O.s_up(layer["a"], layer["x"], layer["Wo"], layer["gamma"], layer["Wg"], layer["Wu"], layer["Wd"],
                   shape.H, shape.G, shape.dh, shape.eps, mode, neurons=neurons)
 

@@ -58,8 +58,10 @@ def _ws(d, mode=0, down=0):
 def test_workspace_size(lib):
     st, n_fo = _ws(_d())
     assert st == B.AFF_OK and n_fo > 0 and n_fo % 1024 == 0
-    st, n_add = _ws(_d(), 1)
+    st, n_add = _ws(_d(flags=B.AFF_FLAG_ADD_DIRECT), 1)
     assert st == B.AFF_OK and 0 < n_add < n_fo          # ADD needs no operating point / Wd norms
+    st, n_add_m = _ws(_d(), 1)                           # second-moment form: 128 x 128 per head and chunk
+    assert st == B.AFF_OK and n_add_m > 0 and n_add_m % 1024 == 0
     st, n_dn = _ws(_d(), 0, 1)
     assert st == B.AFF_OK and n_dn > 0
     st, n_big = _ws(_d(T=65536, D=1024, H=16, G=8, d_head=128, I=3072))
@@ -84,14 +86,38 @@ def test_bad_dims(lib, kw, code):
     assert _ws(_d(**kw))[0] == code
 
 
+def test_flag_constant_matches_header(lib):
+    src = open(os.path.join(ROOT, "include", "affinity.h")).read()
+    m = re.search(r"#define\s+AFF_FLAG_ADD_DIRECT\s+(\d+)u", src)
+    assert m and int(m.group(1)) == B.AFF_FLAG_ADD_DIRECT
+
+
+def test_add_forms_size_their_own_workspace(lib):
+    """The second-moment ADD form keeps one d_head x d_head matrix per head (and
+    per token chunk) instead of the direct form's per-chunk neuron partials."""
+    d = _d(T=65536, D=1024, H=16, G=8, d_head=128, I=3072)
+    st, moment = _ws(d, B.AFF_MODE_ADD)
+    d.flags = B.AFF_FLAG_ADD_DIRECT
+    st2, direct = _ws(d, B.AFF_MODE_ADD)
+    assert st == st2 == B.AFF_OK and moment < direct
+    # d_head > 128 has no second-moment form: the flag changes nothing
+    w = _d(T=4096, D=512, H=2, G=2, d_head=256, I=264)
+    a = _ws(w, B.AFF_MODE_ADD)
+    w.flags = B.AFF_FLAG_ADD_DIRECT
+    assert _ws(w, B.AFF_MODE_ADD) == a
+
+
 def test_fp32_relaxes_alignment_constraints(lib):
     assert _ws(_d(D=60, d_head=12, I=100, dtype=B.AFF_FP32))[0] == B.AFF_OK
 
 
 def test_flags_and_mode_are_checked(lib):
     d = _d()
-    d.flags = 1
-    assert _ws(d)[0] == B.AFF_ERR_INVALID_ARG
+    d.flags = B.AFF_FLAG_ADD_DIRECT
+    assert _ws(d, B.AFF_MODE_ADD)[0] == B.AFF_OK
+    for bad in (2, 1 << 31, B.AFF_FLAG_ADD_DIRECT | 4):
+        d.flags = bad
+        assert _ws(d)[0] == B.AFF_ERR_INVALID_ARG
     assert _ws(_d(), 5)[0] == B.AFF_ERR_INVALID_ARG
 
 
@@ -305,7 +331,7 @@ def test_loo_mode_is_bf16_only(lib):
     n = ctypes.c_size_t(0)
     assert lib.affinity_workspace_size(ctypes.byref(d), B.AFF_MODE_LOO, 0, ctypes.byref(n)) == \
         B.AFF_ERR_UNSUPPORTED_DTYPE
-    db = B.dims(256, 64, 4, 2, 16, 128, 1e-6, B.AFF_BF16)
+    db = B.dims(256, 64, 4, 2, 16, 128, 1e-6, B.AFF_BF16, B.AFF_FLAG_ADD_DIRECT)
     assert B.workspace_size(db, B.AFF_MODE_LOO) > B.workspace_size(db, B.AFF_MODE_ADD)
 
 

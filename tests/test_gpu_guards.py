@@ -15,7 +15,7 @@ from transformer_sharding_affinity_gb300 import binding as B  # noqa: E402
 from transformer_sharding_affinity_gb300 import device as DV  # noqa: E402
 from transformer_sharding_affinity_gb300 import workloads as W  # noqa: E402
 
-from parity_util import TOL, dims_of, oracle_up, rel_err  # noqa: E402
+from parity_util import TOL, dims_of, mode_of, oracle_up, rel_err  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -42,14 +42,15 @@ def test_bounded_wait_times_out_and_the_context_stays_usable():
     assert rel_err(S.cpu().numpy(), S_ref) <= TOL
 
 
-@pytest.mark.parametrize("mode", ["fo", "add", "loo", "down"])
+@pytest.mark.parametrize("mode", ["fo", "add", "add_direct", "loo", "down"])
 def test_nothing_is_written_past_the_workspace_or_the_outputs(mode):
     layer = W.make_layer(SHAPE, with_next=(mode == "down"))
-    d = dims_of(B, SHAPE)
     down = mode == "down"
+    m, flags = (0, 0) if down else mode_of(B, mode)
+    d = dims_of(B, SHAPE, flags)
     keys = DV.DOWN_KEYS if down else DV.UP_KEYS
     dev = DV.to_device(layer, "bf16", keys=keys)
-    n = B.workspace_size(d, B.MODES.get(mode, 0), down=down)
+    n = B.workspace_size(d, m, down=down)
     buf = torch.full((n + TAIL,), CANARY, dtype=torch.uint8, device="cuda")
     ws = buf[:n]
     out_n = SHAPE.G * SHAPE.I
@@ -60,7 +61,7 @@ def test_nothing_is_written_past_the_workspace_or_the_outputs(mode):
                         dev["Wk_next"], dev["Wv_next"], d, out[:out_n], ws)
     else:
         B.affinity_up(dev["a"], dev["x"], dev["Wo"], dev["gamma"], dev["Wg"], dev["Wu"], dev["Wd"], d,
-                      B.MODES[mode], out[:out_n], head[:SHAPE.H * SHAPE.I], ws)
+                      m, out[:out_n], head[:SHAPE.H * SHAPE.I], ws)
     assert B.device_status(ws) == B.AFF_OK
     assert torch.all(buf[n:] == CANARY).item(), "bytes past the workspace were written"
     assert torch.all(out[out_n:] == -7.0).item(), "floats past S_out were written"

@@ -51,7 +51,7 @@ def _assert_up(shape, mode, tol=TOL, record=None):
     return e
 
 
-@pytest.mark.parametrize("mode", ["fo", "add", "loo"])
+@pytest.mark.parametrize("mode", ["fo", "add", "add_direct", "loo"])
 @pytest.mark.parametrize("shape", SMALL, ids=[s.name for s in SMALL])
 def test_up_small(shape, mode):
     _assert_up(shape, mode)
@@ -62,7 +62,7 @@ def test_up_tiny_fp32(mode, record_property):
     _assert_up(W.CONFIGS["tiny"], mode, tol=TOL_F32, record=record_property)
 
 
-@pytest.mark.parametrize("mode", ["fo", "add", "loo"])
+@pytest.mark.parametrize("mode", ["fo", "add", "add_direct", "loo"])
 def test_up_medium(mode, record_property):
     _assert_up(MEDIUM, mode, record=record_property)
 
@@ -74,6 +74,23 @@ def test_loo_is_deterministic_and_differs_from_add():
     assert np.array_equal(outs[0][0].view(np.uint32), outs[1][0].view(np.uint32))
     (S_add, _), = run_up(B, DV, shape, layer, "add")
     assert np.max(np.abs(outs[0][0] / S_add - 1)) > 1e-2
+
+
+def test_add_second_moment_form():
+    """ADD through each head's second moment: bit-for-bit repeatable, a = 0 gives
+    exactly 0, and it agrees with the direct contraction (both are checked
+    against the oracle elsewhere; here against each other on a 4096-token slice)."""
+    layer = W.make_layer(MEDIUM)
+    outs = run_up(B, DV, MEDIUM, layer, "add", runs=2)
+    assert np.array_equal(outs[0][0].view(np.uint32), outs[1][0].view(np.uint32))
+    assert np.array_equal(outs[0][1].view(np.uint32), outs[1][1].view(np.uint32))
+    (S_dir, Sh_dir), = run_up(B, DV, MEDIUM, layer, "add_direct")
+    assert rel_err(outs[0][0], S_dir) <= TOL and rel_err(outs[0][1], Sh_dir) <= TOL
+    z = dict(layer)
+    z["a"] = np.zeros_like(layer["a"])
+    z["a_bits"] = np.zeros_like(layer["a_bits"])
+    (S0, Sh0), = run_up(B, DV, MEDIUM, z, "add")
+    assert np.all(S0 == 0.0) and np.all(Sh0 == 0.0)
 
 
 def test_up_deterministic():
@@ -158,7 +175,8 @@ def test_up_full_size_sampled(name, record_property):
     GPU's top-8 per group."""
     shape = W.CONFIGS[name]
     layer = W.make_layer(shape)
-    modes = {"danube3_500m_layer": ["fo", "add"], "qwen3_0p6b_layer": ["fo", "loo"]}.get(name, ["fo"])
+    modes = {"danube3_500m_layer": ["fo", "add", "add_direct"],
+             "qwen3_0p6b_layer": ["fo", "add", "loo"]}.get(name, ["fo"])
     rng = np.random.default_rng(99)
     for mode in modes:
         (S_gpu, _), = run_up(B, DV, shape, layer, mode, per_head=False)
@@ -191,7 +209,7 @@ _SWEEP = [W.random_small_shape(np.random.default_rng(1000 + i), name=f"rand{i}")
 def test_up_random_shapes(shape):
     """Seeded random small shapes (ragged T, D, d_head and I; 1-12 heads in
     1-4 groups): every mode against the oracle."""
-    for mode in ("fo", "add", "loo"):
+    for mode in ("fo", "add", "add_direct", "loo"):
         _assert_up(shape, mode)
 
 

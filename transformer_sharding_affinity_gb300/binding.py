@@ -35,6 +35,7 @@ AFF_MODE_ADD = 1
 AFF_MODE_LOO = 2
 AFF_BF16 = 0
 AFF_FP32 = 1
+AFF_FLAG_ADD_DIRECT = 1
 MODES = {"fo": AFF_MODE_FO, "add": AFF_MODE_ADD, "loo": AFF_MODE_LOO}
 
 
@@ -143,8 +144,8 @@ def _check(status: int, where: str) -> None:
         raise AffinityError(status, where, detail)
 
 
-def dims(T, D, H, G, d_head, I, eps=1e-6, dtype=AFF_BF16) -> aff_dims:
-    return aff_dims(int(T), int(D), int(H), int(G), int(d_head), int(I), float(eps), int(dtype), 0)
+def dims(T, D, H, G, d_head, I, eps=1e-6, dtype=AFF_BF16, flags=0) -> aff_dims:
+    return aff_dims(int(T), int(D), int(H), int(G), int(d_head), int(I), float(eps), int(dtype), int(flags))
 
 
 def workspace_size(d: aff_dims, mode: int = AFF_MODE_FO, down: bool = False) -> int:

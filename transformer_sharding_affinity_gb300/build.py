@@ -12,7 +12,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libaffinity.so")
-SOURCES = ["tile_kernel.cu", "aux_kernels.cu", "api.cu", "layout.cu", "assign.cu", "realise.cu", "noalloc.cu"]
+SOURCES = ["tile_kernel.cu", "moment_kernel.cu", "aux_kernels.cu", "api.cu", "layout.cu", "assign.cu", "realise.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

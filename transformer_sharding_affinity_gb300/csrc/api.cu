@@ -5,6 +5,7 @@
 #include "affinity.h"
 #include "aux_kernels.cuh"
 #include "internal.h"
+#include "moment_kernel.cuh"
 #include "tile_kernel.cuh"
 
 #include <cuda.h>
@@ -84,7 +85,7 @@ inline int64_t ceil_div(int64_t v, int64_t m) { return (v + m - 1) / m; }
 aff_status check_dims(const aff_dims* d) {
   if (!d) return AFF_ERR_INVALID_ARG;
   if (d->dtype != AFF_BF16 && d->dtype != AFF_FP32) return AFF_ERR_UNSUPPORTED_DTYPE;
-  if (d->flags != 0) return AFF_ERR_INVALID_ARG;
+  if (d->flags & ~AFF_FLAG_ADD_DIRECT) return AFF_ERR_INVALID_ARG;
   if (d->T < 1 || d->D < 1 || d->H < 1 || d->G < 1 || d->d_head < 1 || d->I < 1) return AFF_ERR_INVALID_ARG;
   if (!(std::isfinite(d->eps) && d->eps >= 0.f)) return AFF_ERR_INVALID_ARG;
   if (d->T > kMaxDim || d->D > kMaxDim || d->H > 4096 || d->d_head > 4096 || d->I > kMaxDim)
@@ -107,6 +108,7 @@ struct Layout {
   size_t W16 = 0, GWo16 = 0, M16 = 0, n16 = 0, a16 = 0, partial = 0, headsum = 0, wdn = 0;
   size_t alpha16 = 0, Wd16 = 0, WdT16 = 0, Wqkv16 = 0, ssx = 0, cpart = 0, bnorm = 0;
   size_t Wo16 = 0, cn = 0, rho = 0, inv_r = 0;   // leave-one-out score
+  size_t aT16 = 0, gram = 0, CC = 0, gscale = 0;  // ADD, second-moment form
   // fp32 path
   size_t n32 = 0, a32 = 0, M32 = 0, ab = 0, alpha32 = 0;
   int64_t I_pad = 0, T_pad = 0, n_chunks = 0, n_tchunks = 0, Rg = 0;
@@ -119,6 +121,12 @@ struct Layout {
   }
 };
 
+// ADD through each head's second moment (moment_kernel.cuh): AFF_BF16, d_head
+// <= 128 (one 128-row tile per head), unless the caller asks for the direct form.
+bool moment_form(const aff_dims& d, int mode) {
+  return d.dtype == AFF_BF16 && mode == AFF_MODE_ADD && !(d.flags & AFF_FLAG_ADD_DIRECT) && d.d_head <= 128;
+}
+
 Layout make_layout(const aff_dims& d, int mode, bool down) {
   Layout L;
   const int64_t T = d.T, D = d.D, H = d.H, G = d.G, dh = d.d_head, I = d.I;
@@ -127,8 +135,18 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
     L.I_pad = round_up(I, 256);
     L.T_pad = round_up(T, down ? 128 : 256 * kHeadSets);   // head-pass units take 512 tokens
     L.W16 = L.take((size_t)2 * L.I_pad * D * 2);
-    L.n16 = L.take((size_t)T * D * 2);
-    if (!down) {
+    if (down || mode != AFF_MODE_ADD) L.n16 = L.take((size_t)T * D * 2);   // ADD has no operating point
+    if (!down && moment_form(d, mode)) {
+      const GramSplit gs = gram_split(T, H);
+      L.n_chunks = 1;
+      L.GWo16 = L.take((size_t)H * dh * 2 * D * 2);
+      L.M16 = L.take((size_t)2 * H * L.I_pad * dh * 2);
+      L.aT16 = L.take((size_t)H * dh * L.T_pad * 2);
+      L.gram = L.take((size_t)gs.n_chunks * H * kMomentRows * kMomentRows * 4);
+      L.CC = L.take((size_t)2 * H * kMomentRows * kMomentRows * 2);
+      L.gscale = L.take((size_t)H * 4);
+      L.partial = L.take((size_t)H * L.I_pad * 4);   // [H][I_pad] token sums
+    } else if (!down) {
       L.n_chunks = L.T_pad / (256 * kHeadSets);
       L.GWo16 = L.take((size_t)H * dh * 2 * D * 2);
       L.M16 = L.take((size_t)2 * H * L.I_pad * dh * 2);
@@ -472,8 +490,13 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   float* inv_r = loo ? reinterpret_cast<float*>(ws + L.inv_r) : nullptr;
   if (loo) AFF_CUDA(launch_to_fp16((const uint16_t*)Wo, Wo16, (size_t)D * H * dh, status, ws2));
   // token side on the caller's stream meanwhile
-  AFF_CUDA(launch_prep_tokens(x_b, a_b, g_b, (fo || loo) ? n16 : nullptr, a16, inv_r, T, D, H * dh, d.eps, status,
-                              sm_count, s));
+  const bool moment = moment_form(d, mode);
+  __half* aT16 = moment ? reinterpret_cast<__half*>(ws + L.aT16) : nullptr;
+  if (moment)
+    AFF_CUDA(launch_prep_tokens_t(x_b, a_b, aT16, T, D, H * dh, d.eps, status, s));
+  else
+    AFF_CUDA(launch_prep_tokens(x_b, a_b, g_b, (fo || loo) ? n16 : nullptr, a16, inv_r, T, D, H * dh, d.eps, status,
+                                sm_count, s));
 
   CUtensorMap maps[4];
   std::memset(maps, 0, sizeof maps);
@@ -491,6 +514,58 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     if ((st = run_tile(maps, p, ws2)) != AFF_OK) return st;
   }
   AFF_CUDA(cudaEventRecord(side->join, ws2));
+  if (moment) {
+    // ADD, second-moment form: C_h over the tokens while the fold runs beside it,
+    // then m^T C_h m for every folded row, then the group sums
+    const GramSplit gs = gram_split(T, H);
+    float* gram = reinterpret_cast<float*>(ws + L.gram);
+    __half* CC = reinterpret_cast<__half*>(ws + L.CC);
+    float* gscale = reinterpret_cast<float*>(ws + L.gscale);
+    CUtensorMap mm[2];
+    std::memset(mm, 0, sizeof mm);
+    {
+      // aT16 as [token block][HD][64]: a box is one head's dh rows of one block
+      uint64_t dt[3] = {64, (uint64_t)H * dh, (uint64_t)gs.nkb}, stt[2] = {128, (uint64_t)H * dh * 128};
+      if ((st = make_map(&mm[0], aT16, 3, dt, stt, (uint32_t)dh, 1)) != AFF_OK) return st;
+      mm[1] = mm[0];
+      MomentParams mp{};
+      mp.mode = kMomentGram;
+      mp.n_units = gs.n_chunks * H;
+      mp.H = H; mp.dh = dh; mp.HD = H * dh; mp.I_pad = I_pad;
+      mp.nkb = gs.nkb; mp.kpc = gs.kpc;
+      mp.status = status;
+      mp.gram = gram;
+      const bool timed = g_timing_start && g_timing_stop;
+      if (timed) AFF_CUDA(cudaEventRecord(g_timing_start, s));
+      AFF_CUDA(launch_moment(mm, mp, s));
+      if (timed) AFF_CUDA(cudaEventRecord(g_timing_stop, s));
+      AFF_CUDA(launch_gram_reduce(gram, CC, gscale, gs.n_chunks, H, dh, status, s));
+    }
+    AFF_CUDA(cudaStreamWaitEvent(s, side->join, 0));
+    {
+      if (stream_heads(d)) {
+        if ((st = map2(&mm[0], M16, (uint64_t)H * dh, (uint64_t)2 * I_pad)) != AFF_OK) return st;
+      } else {
+        uint64_t dm[3] = {(uint64_t)dh, (uint64_t)2 * I_pad, (uint64_t)H};
+        uint64_t sd[2] = {(uint64_t)dh * 2, (uint64_t)2 * I_pad * dh * 2};
+        if ((st = make_map(&mm[0], M16, 3, dm, sd, kMomentRows, 1)) != AFF_OK) return st;
+      }
+      if ((st = map2(&mm[1], CC, (uint64_t)kMomentRows, (uint64_t)2 * H * kMomentRows)) != AFF_OK) return st;
+      MomentParams mp{};
+      mp.mode = kMomentQuad;
+      mp.n_units = (int)(2 * L.I_pad / kMomentRows) * H;
+      mp.H = H; mp.dh = dh; mp.HD = H * dh; mp.I_pad = I_pad;
+      mp.nkb = (int)ceil_div(dh, 64);
+      mp.stream = stream_heads(d) ? 1 : 0;
+      mp.status = status;
+      mp.scale = gscale;
+      mp.M16 = M16;
+      mp.out = partial;
+      AFF_CUDA(launch_moment(mm, mp, s));
+    }
+    AFF_CUDA(launch_moment_finalize(partial, T, H, G, I, I_pad, S_out, S_head_out, s));
+    return AFF_OK;
+  }
   AFF_CUDA(cudaStreamWaitEvent(s, side->join, 0));
   // ||w^d||^2 is needed only by the last kernel: computed after the fold, joined late
   if (fo) AFF_CUDA(launch_wd_colnorm((const uint16_t*)Wd, wdn, D, I, I_pad, ws2));

@@ -219,9 +219,10 @@ __global__ void reduce_partials4_kernel(const float* __restrict__ partial, doubl
 // times the column groups), the 16 phases are added in fp64 in order, and
 //   S_head[h][k] = sum / T (x ||w^d_k||^2 for FO),  S_up[g][k] = sum_{h in g} S_head[h][k].
 // Needs I_pad % 128 == 0.
+template <int GROUPS>
 __global__ void __launch_bounds__(512) reduce_finalize_kernel(const float* __restrict__ partial,
                                                               const float* __restrict__ wdn, int fo, int n_chunks,
-                                                              int groups, int T, int H, int G, int I, int I_pad,
+                                                              int T, int H, int G, int I, int I_pad,
                                                               float* __restrict__ S_out, float* __restrict__ S_head_out) {
   __shared__ double part[16][32][4];
   const int k0 = blockIdx.x * 128 + threadIdx.x * 4;
@@ -230,10 +231,13 @@ __global__ void __launch_bounds__(512) reduce_finalize_kernel(const float* __res
   double total[4] = {0.0, 0.0, 0.0, 0.0};
   for (int h = g * hpg; h < (g + 1) * hpg; ++h) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
+    // chunks in order, column groups in order within a chunk; fully unrolled in groups so
+    // that the loads of several chunks are in flight together
+#pragma unroll 8
     for (int c = threadIdx.y; c < n_chunks; c += 16)
-      for (int q = 0; q < groups; ++q) {
-        const float4 v = *reinterpret_cast<const float4*>(partial + ((size_t)(c * groups + q) * H + h) * I_pad + k0);
+#pragma unroll
+      for (int q = 0; q < GROUPS; ++q) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(partial + ((size_t)(c * GROUPS + q) * H + h) * I_pad + k0));
         acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
       }
     part[threadIdx.y][threadIdx.x][0] = acc.x;
@@ -327,6 +331,7 @@ __global__ void loo_rho_kernel(const float* __restrict__ cn, const float* __rest
   if (t < T) {
     const size_t plane = (size_t)H * T_pad, at = (size_t)h * T_pad + t;
     float cc = 0.f, xd = 0.f;   // column groups in order: [group][quantity][H][T_pad]
+#pragma unroll 8
     for (int g = 0; g < groups; ++g) {
       cc += cn[(size_t)(2 * g) * plane + at];
       xd += cn[(size_t)(2 * g + 1) * plane + at];
@@ -674,8 +679,19 @@ cudaError_t launch_reduce_partials(const float* partial, double* out, int n_chun
 cudaError_t launch_reduce_finalize(const float* partial, const float* wdn, int fo, int n_chunks, int groups, int T,
                                    int H, int G, int I, int I_pad, float* S_out, float* S_head_out, cudaStream_t s) {
   dim3 grid(I_pad / 128, G), block(32, 16);
-  reduce_finalize_kernel<<<grid, block, 0, s>>>(partial, wdn, fo, n_chunks, groups, T, H, G, I, I_pad, S_out,
-                                                S_head_out);
+  switch (groups) {
+    case 1:
+      reduce_finalize_kernel<1><<<grid, block, 0, s>>>(partial, wdn, fo, n_chunks, T, H, G, I, I_pad, S_out, S_head_out);
+      break;
+    case 2:
+      reduce_finalize_kernel<2><<<grid, block, 0, s>>>(partial, wdn, fo, n_chunks, T, H, G, I, I_pad, S_out, S_head_out);
+      break;
+    case 4:
+      reduce_finalize_kernel<4><<<grid, block, 0, s>>>(partial, wdn, fo, n_chunks, T, H, G, I, I_pad, S_out, S_head_out);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

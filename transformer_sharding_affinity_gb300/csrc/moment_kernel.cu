@@ -1,0 +1,416 @@
+// moment_kernel.cu -- the ADD score through each head's second moment (see
+// moment_kernel.cuh): token staging in feature-major fp16, the tcgen05 Gram
+// pass over the tokens, its deterministic reduction, and the tcgen05
+// quadratic-form pass over the folded rows.  Paper: "Affinity-Aware Sharding
+// for Delayed Tensor Parallelism", §3 "Affinity scores" (the ADD score).
+#include "moment_kernel.cuh"
+#include "sm103_primitives.cuh"
+
+namespace aff {
+
+namespace {
+
+__device__ __forceinline__ float bf2f_m(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+__device__ __forceinline__ __half to_h_m(float v, bool& bad) {
+  if (!(fabsf(v) <= 65504.f)) bad = true;
+  return __float2half_rn(v);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- token staging
+// Block = 64 tokens.  Each warp first takes 8 tokens' r_t (one warp per token,
+// two tokens' loads in flight together; per token the same sum order as the
+// token-major staging, so both forms see the same a~), then the block walks
+// the features 128 at a time through a shared-memory transpose, the next
+// tile's loads in flight while the current one is stored.  Reads are 256 B
+// token rows; the block's output, [HD][64], is one contiguous stretch of aT16
+// ([T_pad / 64][HD][64]).
+constexpr int kPrepFT = 128;   // features per transposed tile
+
+__device__ __forceinline__ void prep_load_tile(const uint16_t* __restrict__ a, int t0, int T, int HD, int f0,
+                                               uint4 (&q)[4]) {
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int idx = threadIdx.x + r * 256;
+    const int tl = idx >> 4, f = f0 + (idx & 15) * 8, t = t0 + tl;
+    q[r] = (t < T && f < HD) ? __ldg(reinterpret_cast<const uint4*>(a + (size_t)t * HD + f)) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+__global__ void __launch_bounds__(256) prep_tokens_t_kernel(const uint16_t* __restrict__ x,
+                                                            const uint16_t* __restrict__ a, __half* __restrict__ aT16,
+                                                            int T, int D, int HD, float eps, uint32_t* status) {
+  __shared__ float tile[64][kPrepFT + 1];
+  __shared__ float irs[64];
+  const int t0 = blockIdx.x * 64;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint4 q[4];
+  prep_load_tile(a, t0, T, HD, 0, q);   // the first tile's loads overlap the rms pass
+  for (int j = 0; j < 8; j += 2) {
+    const int tl = warp * 8 + j;
+    const bool v0 = t0 + tl < T, v1 = t0 + tl + 1 < T;
+    const uint4* x0 = reinterpret_cast<const uint4*>(x + (size_t)(v0 ? t0 + tl : 0) * D);
+    const uint4* x1 = reinterpret_cast<const uint4*>(x + (size_t)(v1 ? t0 + tl + 1 : 0) * D);
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+    for (int v = lane; v < D / 8; v += 32) {
+      const uint4 p0 = x0[v], p1 = x1[v];
+      const uint16_t* e0 = reinterpret_cast<const uint16_t*>(&p0);
+      const uint16_t* e1 = reinterpret_cast<const uint16_t*>(&p1);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float f0 = bf2f_m(e0[i]), f1 = bf2f_m(e1[i]);
+        s0 = fmaf(f0, f0, s0);
+        s1 = fmaf(f1, f1, s1);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+    }
+    if (lane == 0) {
+      irs[tl] = v0 ? rsqrtf(s0 / (float)D + eps) : 0.f;
+      irs[tl + 1] = v1 ? rsqrtf(s1 / (float)D + eps) : 0.f;
+    }
+  }
+  __syncthreads();
+  bool bad = false;
+  for (int f0 = 0; f0 < HD; f0 += kPrepFT) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int idx = threadIdx.x + r * 256;
+      const int tl = idx >> 4, c8 = (idx & 15) * 8;
+      const uint16_t* e = reinterpret_cast<const uint16_t*>(&q[r]);
+      const float ir = irs[tl];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) tile[tl][c8 + i] = bf2f_m(e[i]) * ir;
+    }
+    __syncthreads();
+    if (f0 + kPrepFT < HD) prep_load_tile(a, t0, T, HD, f0 + kPrepFT, q);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int idx = threadIdx.x + r * 256;
+      const int fl = idx >> 3, tc = idx & 7, f = f0 + fl;
+      if (f < HD) {
+        __align__(16) __half o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = to_h_m(tile[tc * 8 + i][fl], bad);
+        *reinterpret_cast<uint4*>(aT16 + ((size_t)blockIdx.x * HD + f) * 64 + tc * 8) =
+            *reinterpret_cast<const uint4*>(o);
+      }
+    }
+    __syncthreads();
+  }
+  if (bad) latch_status(status, kStatusRange);
+}
+
+// ---------------------------------------------------------------- Gram reduction
+// Block = (head h, 4 rows n).  Every block of a head first sums the diagonal
+// (the same arithmetic in each, so all agree on s_h), then its rows, each in
+// chunk order, and splits C_h / s_h into an fp16 high part and the fp16
+// rounding of the remainder.  |C_h[n][i]| <= sqrt(C_ii C_nn) <= s_h keeps
+// both in range.
+constexpr int kReduceRows = 4;
+
+__global__ void __launch_bounds__(256) gram_reduce_kernel(const float* __restrict__ gram, __half* __restrict__ CC,
+                                                          float* __restrict__ scale, int n_chunks, int H, int dh,
+                                                          uint32_t* status) {
+  __shared__ float diag[128];
+  __shared__ float s_sh;
+  const int h = blockIdx.x, y = blockIdx.y;
+  const size_t cstride = (size_t)H * 128 * 128;
+  const float* g0 = gram + (size_t)h * 128 * 128;
+  if (threadIdx.x < 128) {
+    const int i = threadIdx.x;
+    float d = 0.f;
+    if (i < dh) {
+#pragma unroll 8
+      for (int c = 0; c < n_chunks; ++c) d += __ldg(g0 + c * cstride + (size_t)i * 129);
+    }
+    diag[i] = d;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = 0.f;
+    bool finite = true;
+    for (int i = 0; i < dh; ++i) {
+      if (!isfinite(diag[i])) finite = false;
+      m = fmaxf(m, diag[i]);
+    }
+    if (!finite) {
+      latch_status(status, kStatusRange);
+      m = 1.f;
+    }
+    if (!(m > 0.f)) m = 1.f;
+    s_sh = m;
+    if (y == 0) scale[h] = m;
+  }
+  __syncthreads();
+  const float s = s_sh;
+  for (int e = threadIdx.x; e < kReduceRows * 128; e += 256) {
+    const int n = y * kReduceRows + (e >> 7), i = e & 127;
+    float v = 0.f;
+    if (n < dh && i < dh) {
+      const float* src = g0 + (size_t)n * 128 + i;
+#pragma unroll 8
+      for (int c = 0; c < n_chunks; ++c) v += __ldg(src + c * cstride);
+      v = v / s;
+    }
+    const __half hi = __float2half_rn(v);
+    const __half lo = __float2half_rn(v - __half2float(hi));
+    CC[((size_t)h * 128 + n) * 128 + i] = hi;
+    CC[((size_t)(H + h) * 128 + n) * 128 + i] = lo;
+  }
+}
+
+// ---------------------------------------------------------------- finishing
+// S_head[h][k] = out[h][k] / T; S_up[g][k] = the sum of S_head over g's heads in
+// head order (fp64).  One thread per (group, neuron).
+__global__ void __launch_bounds__(256) moment_finalize_kernel(const float* __restrict__ out, int T, int H, int G,
+                                                              int I, int I_pad, float* __restrict__ S_out,
+                                                              float* __restrict__ S_head_out) {
+  const int k = blockIdx.x * 256 + threadIdx.x, g = blockIdx.y;
+  if (k >= I) return;
+  const int hpg = H / G;
+  const double invT = 1.0 / (double)T;
+  double total = 0.0;
+  for (int h = g * hpg; h < (g + 1) * hpg; ++h) {
+    const double v = (double)out[(size_t)h * I_pad + k] * invT;
+    if (S_head_out) S_head_out[(size_t)h * I + k] = (float)v;
+    total += v;
+  }
+  S_out[(size_t)g * I + k] = (float)total;
+}
+
+// ---------------------------------------------------------------- tcgen05 passes
+// One unit per CTA: warp 0 issues the TMA copies, warp 1 the MMAs (one
+// 128 x 128 fp32 accumulator in TMEM), warps 2..5 read it back.
+//   Gram: unit (head h, token chunk c); a stage is the head's d_head feature rows
+//         of one 64-token block of aT16 (one contiguous d_head x 128 B copy) in a
+//         128-row tile whose remaining rows are zeroed once; D += A A^T.
+//   Quad: unit (head h, row tile rt of M16); a stage is the tile of 128 M16 rows
+//         (64 neurons, gate and up rows interleaved by 16) and the hi / lo tiles
+//         of C~_h; D += A Chi^T + A Clo^T, then every row's m . D[row] in fp32.
+template <int MODE>
+__global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_constant__ CUtensorMap mapA,
+                                                                const __grid_constant__ CUtensorMap mapB,
+                                                                const MomentParams p) {
+  constexpr int S = MODE == kMomentGram ? kGramStages : kQuadStages;
+  constexpr uint32_t kSB = MODE == kMomentGram ? kMomentTileBytes : 3 * kMomentTileBytes;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  __shared__ uint64_t full[S], empty[S], tfull, drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_s;
+  volatile int* abort_flag = &abort_s;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = (int)blockIdx.x % p.H, c = (int)blockIdx.x / p.H;
+  int kb0 = 0, nkb = p.nkb;
+  if (MODE == kMomentGram) {
+    kb0 = c * p.kpc;
+    nkb = p.nkb - kb0 < p.kpc ? p.nkb - kb0 : p.kpc;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&tfull, 1);
+    mbar_init(&drain, 1);
+    abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&mapA);
+    if (MODE == kMomentQuad) prefetch_tmap(&mapB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, 128);
+    tmem_relinquish();
+  }
+  if (MODE == kMomentGram && warp >= 2 && p.dh < kMomentRows) {
+    // rows dh..127 of every stage are never copied into: zero them for the MMAs
+    const int tail = (kMomentRows - p.dh) * 128 / 16;   // uint4 per stage
+    for (int i = threadIdx.x - 64; i < S * tail; i += 128) {
+      const int s = i / tail, e = i % tail;
+      reinterpret_cast<uint4*>(base + (size_t)s * kSB + (size_t)p.dh * 128)[e] = make_uint4(0, 0, 0, 0);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the tensor-core reads
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      int issued = 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % S;
+        const uint32_t ph = (uint32_t)((kb / S) & 1);
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        uint8_t* st = base + (size_t)s * kSB;
+        if constexpr (MODE == kMomentGram) {
+          mbar_arrive_expect_tx(&full[s], (uint32_t)p.dh * 128u);
+          tma_load_3d(st, &mapA, &full[s], 0, h * p.dh, kb0 + kb);
+        } else {
+          mbar_arrive_expect_tx(&full[s], kSB);
+          if (p.stream)
+            tma_load_2d(st, &mapA, &full[s], h * p.dh + kb * 64, c * kMomentRows);
+          else
+            tma_load_3d(st, &mapA, &full[s], kb * 64, c * kMomentRows, h);
+          tma_load_2d(st + kMomentTileBytes, &mapB, &full[s], kb * 64, h * kMomentRows);
+          tma_load_2d(st + 2 * kMomentTileBytes, &mapB, &full[s], kb * 64, (p.H + h) * kMomentRows);
+        }
+        ++issued;
+      }
+      if (!ok) {
+        // let every copy already issued land before shared memory is released
+        const int n = issued < S ? issued : S;
+        for (int i = 1; i <= n; ++i) {
+          const int q = issued - i;
+          volatile int dummy = 0;
+          mbar_wait(&full[q % S], (uint32_t)((q / S) & 1), &dummy, p.status, 100000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16(128, 128, 0);
+      const uint64_t dbase = smem_desc_k_sw128(smem_u32(base));
+      constexpr uint64_t kT = (uint64_t)(kMomentTileBytes >> 4);
+      bool ok = true;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % S;
+        const uint32_t ph = (uint32_t)((kb / S) & 1);
+        if (!mbar_wait(&full[s], ph, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t da = dbase + (uint64_t)(((uint32_t)s * kSB) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint32_t acc = (kb | ks) != 0 ? 1u : 0u;
+          if constexpr (MODE == kMomentGram) {
+            mma_f16_ss(tmem, da + 2 * ks, da + 2 * ks, idesc, acc);
+          } else {
+            mma_f16_ss(tmem, da + 2 * ks, da + kT + 2 * ks, idesc, acc);
+            mma_f16_ss(tmem, da + 2 * ks, da + 2 * kT + 2 * ks, idesc, 1u);
+          }
+        }
+        mma_commit(&empty[s]);
+      }
+      if (ok) {
+        mma_commit(&tfull);
+      } else {
+        mma_commit(&drain);
+        volatile int dummy = 0;
+        mbar_wait(&drain, 0, &dummy, p.status, 100000000ull);
+      }
+    }
+  } else {
+    const int q = warp & 3;              // TMEM lane quarter this warp may read
+    const int row = q * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
+    int w_ok = 1;
+    if (lane == 0) w_ok = mbar_wait(&tfull, 0, abort_flag, p.status) ? 1 : 0;
+    w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+    if (w_ok) {
+      tc_fence_after();
+      if constexpr (MODE == kMomentGram) {
+        // D[i][j] (i = this lane's feature row) goes to [j][i]: a warp's 32 lanes
+        // write 128 contiguous bytes per column.
+        float* dst = p.gram + (size_t)(c * p.H + h) * kMomentRows * kMomentRows + row;
+        for (int j0 = 0; j0 < p.dh; j0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tl + (uint32_t)j0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) dst[(size_t)(j0 + jj) * kMomentRows] = __uint_as_float(v[jj]);
+        }
+      } else {
+        const int rt = c;
+        const __half* mrow = p.stream
+                                 ? p.M16 + (size_t)(rt * kMomentRows + row) * p.HD + (size_t)h * p.dh
+                                 : p.M16 + ((size_t)h * 2 * p.I_pad + (size_t)rt * kMomentRows + row) * p.dh;
+        float acc = 0.f;
+        for (int n0 = 0; n0 < p.dh; n0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tl + (uint32_t)n0, v);
+          const uint4 m0 = __ldg(reinterpret_cast<const uint4*>(mrow + n0));
+          const uint4 m1 = n0 + 8 < p.dh ? __ldg(reinterpret_cast<const uint4*>(mrow + n0 + 8)) : make_uint4(0, 0, 0, 0);
+          tmem_ld_wait();
+          const __half* e0 = reinterpret_cast<const __half*>(&m0);
+          const __half* e1 = reinterpret_cast<const __half*>(&m1);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc = fmaf(__uint_as_float(v[i]), __half2float(e0[i]), acc);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc = fmaf(__uint_as_float(v[8 + i]), __half2float(e1[i]), acc);
+        }
+        acc *= p.scale[h];
+        // rows 32q + l (gate) and 32q + 16 + l (up) are neuron 64 rt + 16 q + l
+        const float pair = acc + __shfl_xor_sync(0xffffffffu, acc, 16);
+        if (lane < 16) p.out[(size_t)h * p.I_pad + (size_t)rt * 64 + q * 16 + lane] = pair;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+size_t moment_smem_bytes(int mode) {
+  return 1024 + (mode == kMomentGram ? (size_t)kGramStages * kMomentTileBytes
+                                     : (size_t)kQuadStages * 3 * kMomentTileBytes);
+}
+
+cudaError_t launch_moment(const CUtensorMap* maps, const MomentParams& p, cudaStream_t s) {
+  if (p.n_units <= 0 || p.nkb <= 0) return cudaErrorInvalidValue;
+  const size_t smem = moment_smem_bytes(p.mode);
+  cudaError_t e;
+  if (p.mode == kMomentGram) {
+    auto* fn = moment_kernel<kMomentGram>;
+    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+      return e;
+    fn<<<p.n_units, kMomentThreads, smem, s>>>(maps[0], maps[1], p);
+  } else if (p.mode == kMomentQuad) {
+    if (p.nkb > kQuadStages) return cudaErrorInvalidValue;
+    auto* fn = moment_kernel<kMomentQuad>;
+    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+      return e;
+    fn<<<p.n_units, kMomentThreads, smem, s>>>(maps[0], maps[1], p);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep_tokens_t(const uint16_t* x, const uint16_t* a, __half* aT16, int T, int D, int HD, float eps,
+                                 uint32_t* status, cudaStream_t s) {
+  const int blocks = (T + 63) / 64;
+  prep_tokens_t_kernel<<<blocks, 256, 0, s>>>(x, a, aT16, T, D, HD, eps, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gram_reduce(const float* gram, __half* CC, float* scale, int n_chunks, int H, int dh,
+                               uint32_t* status, cudaStream_t s) {
+  gram_reduce_kernel<<<dim3(H, 128 / kReduceRows), 256, 0, s>>>(gram, CC, scale, n_chunks, H, dh, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moment_finalize(const float* out, int T, int H, int G, int I, int I_pad, float* S_out,
+                                   float* S_head_out, cudaStream_t s) {
+  moment_finalize_kernel<<<dim3((I + 255) / 256, G), 256, 0, s>>>(out, T, H, G, I, I_pad, S_out, S_head_out);
+  return cudaGetLastError();
+}
+
+}  // namespace aff

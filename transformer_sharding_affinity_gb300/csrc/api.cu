@@ -108,7 +108,7 @@ struct Layout {
   size_t W16 = 0, GWo16 = 0, M16 = 0, n16 = 0, a16 = 0, partial = 0, headsum = 0, wdn = 0;
   size_t alpha16 = 0, Wd16 = 0, WdT16 = 0, Wqkv16 = 0, ssx = 0, cpart = 0, bnorm = 0;
   size_t Wo16 = 0, cn = 0, rho = 0, inv_r = 0;   // leave-one-out score
-  size_t aT16 = 0, gram = 0, CC = 0, gscale = 0;  // ADD, second-moment form
+  size_t aT16 = 0, gram = 0, cmax = 0, CC = 0, gscale = 0;  // ADD, second-moment form
   // fp32 path
   size_t n32 = 0, a32 = 0, M32 = 0, ab = 0, alpha32 = 0;
   int64_t I_pad = 0, T_pad = 0, n_chunks = 0, n_tchunks = 0, Rg = 0;
@@ -143,6 +143,7 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
       L.M16 = L.take((size_t)2 * H * L.I_pad * dh * 2);
       L.aT16 = L.take((size_t)H * dh * L.T_pad * 2);
       L.gram = L.take((size_t)gs.n_chunks * H * kMomentRows * kMomentRows * 4);
+      L.cmax = L.take((size_t)gs.n_chunks * H * 4);
       L.CC = L.take((size_t)2 * H * kMomentRows * kMomentRows * 2);
       L.gscale = L.take((size_t)H * 4);
       L.partial = L.take((size_t)H * L.I_pad * 4);   // [H][I_pad] token sums
@@ -519,6 +520,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     // then m^T C_h m for every folded row, then the group sums
     const GramSplit gs = gram_split(T, H);
     float* gram = reinterpret_cast<float*>(ws + L.gram);
+    float* cmax = reinterpret_cast<float*>(ws + L.cmax);
     __half* CC = reinterpret_cast<__half*>(ws + L.CC);
     float* gscale = reinterpret_cast<float*>(ws + L.gscale);
     CUtensorMap mm[2];
@@ -535,11 +537,12 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
       mp.nkb = gs.nkb; mp.kpc = gs.kpc;
       mp.status = status;
       mp.gram = gram;
+      mp.cmax = cmax;
       const bool timed = g_timing_start && g_timing_stop;
       if (timed) AFF_CUDA(cudaEventRecord(g_timing_start, s));
       AFF_CUDA(launch_moment(mm, mp, s));
       if (timed) AFF_CUDA(cudaEventRecord(g_timing_stop, s));
-      AFF_CUDA(launch_gram_reduce(gram, CC, gscale, gs.n_chunks, H, dh, status, s));
+      AFF_CUDA(launch_gram_reduce(gram, cmax, CC, gscale, gs.n_chunks, H, dh, status, s));
     }
     AFF_CUDA(cudaStreamWaitEvent(s, side->join, 0));
     {

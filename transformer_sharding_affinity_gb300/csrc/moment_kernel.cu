@@ -108,39 +108,25 @@ __global__ void __launch_bounds__(256) prep_tokens_t_kernel(const uint16_t* __re
 }
 
 // ---------------------------------------------------------------- Gram reduction
-// Block = (head h, 4 rows n).  Every block of a head first sums the diagonal
-// (the same arithmetic in each, so all agree on s_h), then its rows, each in
-// chunk order, and splits C_h / s_h into an fp16 high part and the fp16
-// rounding of the remainder.  |C_h[n][i]| <= sqrt(C_ii C_nn) <= s_h keeps
-// both in range.
+// Block = (head h, 4 rows n).  s_h = the sum over chunks of each chunk's
+// largest diagonal entry (in chunk order; every block computes the same value),
+// an upper bound on max_i C_h[i][i], so |C_h[n][i]| <= sqrt(C_ii C_nn) <= s_h.
+// Each entry is summed in chunk order and C_h / s_h is split into an fp16 high
+// part and the fp16 rounding of the remainder.
 constexpr int kReduceRows = 4;
 
-__global__ void __launch_bounds__(256) gram_reduce_kernel(const float* __restrict__ gram, __half* __restrict__ CC,
+__global__ void __launch_bounds__(256) gram_reduce_kernel(const float* __restrict__ gram,
+                                                          const float* __restrict__ cmax, __half* __restrict__ CC,
                                                           float* __restrict__ scale, int n_chunks, int H, int dh,
                                                           uint32_t* status) {
-  __shared__ float diag[128];
   __shared__ float s_sh;
   const int h = blockIdx.x, y = blockIdx.y;
   const size_t cstride = (size_t)H * 128 * 128;
   const float* g0 = gram + (size_t)h * 128 * 128;
-  if (threadIdx.x < 128) {
-    const int i = threadIdx.x;
-    float d = 0.f;
-    if (i < dh) {
-#pragma unroll 8
-      for (int c = 0; c < n_chunks; ++c) d += __ldg(g0 + c * cstride + (size_t)i * 129);
-    }
-    diag[i] = d;
-  }
-  __syncthreads();
   if (threadIdx.x == 0) {
     float m = 0.f;
-    bool finite = true;
-    for (int i = 0; i < dh; ++i) {
-      if (!isfinite(diag[i])) finite = false;
-      m = fmaxf(m, diag[i]);
-    }
-    if (!finite) {
+    for (int c = 0; c < n_chunks; ++c) m += cmax[(size_t)c * H + h];
+    if (!isfinite(m)) {
       latch_status(status, kStatusRange);
       m = 1.f;
     }
@@ -206,6 +192,7 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
   __shared__ uint64_t full[S], empty[S], tfull, drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_s;
+  __shared__ uint32_t dmax_s;   // Gram: the largest diagonal entry of the unit's block (fp32 bits, >= 0)
   volatile int* abort_flag = &abort_s;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -224,6 +211,7 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
     mbar_init(&tfull, 1);
     mbar_init(&drain, 1);
     abort_s = 0;
+    dmax_s = 0u;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -326,13 +314,21 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
         // D[i][j] (i = this lane's feature row) goes to [j][i]: a warp's 32 lanes
         // write 128 contiguous bytes per column.
         float* dst = p.gram + (size_t)(c * p.H + h) * kMomentRows * kMomentRows + row;
+        float dg = 0.f;   // D[row][row]; rows past dh are zero
         for (int j0 = 0; j0 < p.dh; j0 += 16) {
           uint32_t v[16];
           tmem_ld16(tl + (uint32_t)j0, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) dst[(size_t)(j0 + jj) * kMomentRows] = __uint_as_float(v[jj]);
+          for (int jj = 0; jj < 16; ++jj) {
+            dst[(size_t)(j0 + jj) * kMomentRows] = __uint_as_float(v[jj]);
+            if (j0 + jj == row) dg = __uint_as_float(v[jj]);
+          }
         }
+        // sums of squares: >= 0, so the fp32 bit patterns order like the values
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dg = fmaxf(dg, __shfl_xor_sync(0xffffffffu, dg, o));
+        if (lane == 0) atomicMax(&dmax_s, __float_as_uint(dg));
       } else {
         const int rt = c;
         const __half* mrow = p.stream
@@ -357,6 +353,11 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
         const float pair = acc + __shfl_xor_sync(0xffffffffu, acc, 16);
         if (lane < 16) p.out[(size_t)h * p.I_pad + (size_t)rt * 64 + q * 16 + lane] = pair;
       }
+    }
+    if constexpr (MODE == kMomentGram) {
+      // every epilogue warp arrives here, whether or not its wait succeeded
+      named_barrier_sync(1, 128);
+      if (w_ok && warp == 2 && lane == 0) p.cmax[(size_t)c * p.H + h] = __uint_as_float(dmax_s);
     }
   }
 
@@ -401,9 +402,9 @@ cudaError_t launch_prep_tokens_t(const uint16_t* x, const uint16_t* a, __half* a
   return cudaGetLastError();
 }
 
-cudaError_t launch_gram_reduce(const float* gram, __half* CC, float* scale, int n_chunks, int H, int dh,
-                               uint32_t* status, cudaStream_t s) {
-  gram_reduce_kernel<<<dim3(H, 128 / kReduceRows), 256, 0, s>>>(gram, CC, scale, n_chunks, H, dh, status);
+cudaError_t launch_gram_reduce(const float* gram, const float* cmax, __half* CC, float* scale, int n_chunks, int H,
+                               int dh, uint32_t* status, cudaStream_t s) {
+  gram_reduce_kernel<<<dim3(H, 128 / kReduceRows), 256, 0, s>>>(gram, cmax, CC, scale, n_chunks, H, dh, status);
   return cudaGetLastError();
 }
 

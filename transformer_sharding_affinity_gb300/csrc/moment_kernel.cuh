@@ -42,6 +42,7 @@ struct MomentParams {
   int32_t stream;    // quad: M16 is [2 I_pad][H*dh] (else [H][2 I_pad][dh])
   uint32_t* status;
   float* gram;       // Gram output: [chunk][H][128 (column j)][128 (row i)] fp32
+  float* cmax;       // Gram output: [chunk][H] the block's largest diagonal entry
   const float* scale;   // quad: per-head scale s_h of the staged C~_h = C_h / s_h
   const __half* M16;    // quad epilogue: the rows it contracted, read again as fp16
   float* out;           // quad output: [H][I_pad], m_g^T C_h m_g + m_u^T C_h m_u (token sums)
@@ -69,11 +70,12 @@ cudaError_t launch_moment(const CUtensorMap* maps, const MomentParams& p, cudaSt
 // r_t = sqrt(mean_d x_t,d^2 + eps).
 cudaError_t launch_prep_tokens_t(const uint16_t* x, const uint16_t* a, __half* aT16, int T, int D, int HD, float eps,
                                  uint32_t* status, cudaStream_t s);
-// C_h = sum over chunks of the Gram partials (in chunk order); s_h = max_i C_h[i][i]
-// (1 when that is not positive); CC = [hi; lo] fp16 parts of C_h / s_h:
-// [2][H][128][128], zero outside d_head x d_head.
-cudaError_t launch_gram_reduce(const float* gram, __half* CC, float* scale, int n_chunks, int H, int dh,
-                               uint32_t* status, cudaStream_t s);
+// C_h = sum over chunks of the Gram partials (in chunk order); s_h = the sum over
+// chunks of their largest diagonal entries (>= max_i C_h[i][i]; 1 when not
+// positive); CC = [hi; lo] fp16 parts of C_h / s_h: [2][H][128][128], zero
+// outside d_head x d_head.
+cudaError_t launch_gram_reduce(const float* gram, const float* cmax, __half* CC, float* scale, int n_chunks, int H,
+                               int dh, uint32_t* status, cudaStream_t s);
 // S_head[h][k] = out[h][k] / T, S_up[g][k] = sum of S_head over g's heads (fp64, head order).
 cudaError_t launch_moment_finalize(const float* out, int T, int H, int G, int I, int I_pad, float* S_out,
                                    float* S_head_out, cudaStream_t s);

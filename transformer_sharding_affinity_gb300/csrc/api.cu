@@ -108,7 +108,7 @@ struct Layout {
   size_t W16 = 0, GWo16 = 0, M16 = 0, n16 = 0, a16 = 0, partial = 0, headsum = 0, wdn = 0;
   size_t alpha16 = 0, Wd16 = 0, WdT16 = 0, Wqkv16 = 0, ssx = 0, cpart = 0, bnorm = 0;
   size_t Wo16 = 0, cn = 0, rho = 0, inv_r = 0;   // leave-one-out score
-  size_t aT16 = 0, gram = 0, cmax = 0, CC = 0, gscale = 0;  // ADD, second-moment form
+  size_t ir = 0, gram = 0, cmax = 0, CC = 0, gscale = 0;  // ADD, second-moment form
   // fp32 path
   size_t n32 = 0, a32 = 0, M32 = 0, ab = 0, alpha32 = 0;
   int64_t I_pad = 0, T_pad = 0, n_chunks = 0, n_tchunks = 0, Rg = 0;
@@ -141,7 +141,7 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
       L.n_chunks = 1;
       L.GWo16 = L.take((size_t)H * dh * 2 * D * 2);
       L.M16 = L.take((size_t)2 * H * L.I_pad * dh * 2);
-      L.aT16 = L.take((size_t)H * dh * L.T_pad * 2);
+      L.ir = L.take((size_t)gs.nkb * 64 * 4);
       L.gram = L.take((size_t)gs.n_chunks * H * kMomentRows * kMomentRows * 4);
       L.cmax = L.take((size_t)gs.n_chunks * H * 4);
       L.CC = L.take((size_t)2 * H * kMomentRows * kMomentRows * 2);
@@ -248,6 +248,28 @@ aff_status make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* d
   return AFF_OK;
 }
 
+// 16-bit tensor [rows][inner] (row stride inner * 2 bytes), no swizzle, box
+// (box0 innermost elements, box1 rows); OOB reads zero.
+aff_status map_plain_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box0, uint32_t box1) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    g_last_cuda_error = "cuTensorMapEncodeTiled unavailable";
+    return AFF_ERR_CUDA;
+  }
+  cuuint64_t gd[2] = {inner, rows}, gs[1] = {inner * 2};
+  cuuint32_t bx[2] = {box0, box1}, es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(ptr), gd, gs, bx, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[96];
+    std::snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    g_last_cuda_error = buf;
+    return AFF_ERR_CUDA;
+  }
+  return AFF_OK;
+}
+
 // The gate (part 0) or up (part 1) rows of 128 consecutive neurons of W16
 // ([I_pad / 16][2][16][D]) as one box: dims (D, 16, 2, I_pad / 16), box (64, 16, 1, 8).
 aff_status map_gate_up(CUtensorMap* m, const void* W16, uint64_t D, uint64_t I_pad) {
@@ -269,6 +291,18 @@ int pick_stages(int mode, int H) {
 // Heads whose width is a multiple of 16 but not of 64 (e.g. 96) leave the last
 // 64-wide K block of every head job partly empty.  Streaming all heads' K
 // ranges back to back fills every block; AFFINITY_STREAM_HEADS=0 turns it off.
+// CTAs of the fold when it runs beside the second-moment ADD passes: each fold CTA
+// holds a whole SM's tensor memory, so a smaller fold grid leaves SMs to the
+// HBM-bound Gram pass (3/4 of the SMs measured best).  AFFINITY_FOLD_CTAS
+// overrides (0 = one per SM).
+int moment_fold_ctas(int sm_count) {
+  static const int n = [] {
+    const char* e = std::getenv("AFFINITY_FOLD_CTAS");
+    return e ? std::atoi(e) : -1;
+  }();
+  return n >= 0 ? n : sm_count * 3 / 4;
+}
+
 bool stream_heads(const aff_dims& d) {
   static const bool allowed = [] {
     const char* e = std::getenv("AFFINITY_STREAM_HEADS");
@@ -309,7 +343,7 @@ TileParams base_params(const aff_dims& d, const Layout& L, uint8_t* ws, int mode
   return p;
 }
 
-aff_status run_tile(const CUtensorMap* maps, TileParams& p, cudaStream_t s, bool dominant = false) {
+aff_status run_tile(const CUtensorMap* maps, TileParams& p, cudaStream_t s, bool dominant = false, int max_ctas = 0) {
   if (p.n_units <= 0) return AFF_OK;
   // CTAs resident at once, cached per device and configuration
   static std::mutex mu;
@@ -334,6 +368,7 @@ aff_status run_tile(const CUtensorMap* maps, TileParams& p, cudaStream_t s, bool
     cache.push_back({key, fit});
   }
   int grid = p.n_units < fit ? p.n_units : fit;
+  if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
   const bool timed = dominant && g_timing_start && g_timing_stop;
   if (timed) AFF_CUDA(cudaEventRecord(g_timing_start, s));
   cudaError_t e = launch_tile_kernel(maps, p, &grid, s);
@@ -492,9 +527,9 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   if (loo) AFF_CUDA(launch_to_fp16((const uint16_t*)Wo, Wo16, (size_t)D * H * dh, status, ws2));
   // token side on the caller's stream meanwhile
   const bool moment = moment_form(d, mode);
-  __half* aT16 = moment ? reinterpret_cast<__half*>(ws + L.aT16) : nullptr;
+  float* ir_m = moment ? reinterpret_cast<float*>(ws + L.ir) : nullptr;
   if (moment)
-    AFF_CUDA(launch_prep_tokens_t(x_b, a_b, aT16, T, D, H * dh, d.eps, status, s));
+    AFF_CUDA(launch_inv_r(x_b, ir_m, T, gram_split(T, H).nkb * 64, D, d.eps, sm_count, s));
   else
     AFF_CUDA(launch_prep_tokens(x_b, a_b, g_b, (fo || loo) ? n16 : nullptr, a16, inv_r, T, D, H * dh, d.eps, status,
                                 sm_count, s));
@@ -512,7 +547,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     p.n_ntiles = (int)ceil_div((int64_t)H * dh, 128);
     p.n_units = p.n_ktiles * p.n_ntiles;
     p.M16 = M16;
-    if ((st = run_tile(maps, p, ws2)) != AFF_OK) return st;
+    if ((st = run_tile(maps, p, ws2, false, moment_form(d, mode) ? moment_fold_ctas(sm_count) : 0)) != AFF_OK) return st;
   }
   AFF_CUDA(cudaEventRecord(side->join, ws2));
   if (moment) {
@@ -526,9 +561,8 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     CUtensorMap mm[2];
     std::memset(mm, 0, sizeof mm);
     {
-      // aT16 as [token block][HD][64]: a box is one head's dh rows of one block
-      uint64_t dt[3] = {64, (uint64_t)H * dh, (uint64_t)gs.nkb}, stt[2] = {128, (uint64_t)H * dh * 128};
-      if ((st = make_map(&mm[0], aT16, 3, dt, stt, (uint32_t)dh, 1)) != AFF_OK) return st;
+      // a (bf16 bits) as [T][H*dh], unswizzled boxes of one head's dh columns x 64 tokens
+      if ((st = map_plain_2d(&mm[0], a, (uint64_t)H * dh, (uint64_t)T, (uint32_t)dh, 64)) != AFF_OK) return st;
       mm[1] = mm[0];
       MomentParams mp{};
       mp.mode = kMomentGram;
@@ -538,6 +572,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
       mp.status = status;
       mp.gram = gram;
       mp.cmax = cmax;
+      mp.inv_r = ir_m;
       const bool timed = g_timing_start && g_timing_stop;
       if (timed) AFF_CUDA(cudaEventRecord(g_timing_start, s));
       AFF_CUDA(launch_moment(mm, mp, s));

@@ -1,6 +1,6 @@
 // moment_kernel.cu -- the ADD score through each head's second moment (see
-// moment_kernel.cuh): token staging in feature-major fp16, the tcgen05 Gram
-// pass over the tokens, its deterministic reduction, and the tcgen05
+// moment_kernel.cuh): the per-token rms, the tcgen05 Gram pass that reads the
+// bf16 head outputs itself, its deterministic reduction, and the tcgen05
 // quadratic-form pass over the folded rows.  Paper: "Affinity-Aware Sharding
 // for Delayed Tensor Parallelism", §3 "Affinity scores" (the ADD score).
 #include "moment_kernel.cuh"
@@ -19,44 +19,22 @@ __device__ __forceinline__ __half to_h_m(float v, bool& bad) {
 
 }  // namespace
 
-// ---------------------------------------------------------------- token staging
-// Block = 64 tokens.  Each warp first takes 8 tokens' r_t (one warp per token,
-// two tokens' loads in flight together; per token the same sum order as the
-// token-major staging, so both forms see the same a~), then the block walks
-// the features 128 at a time through a shared-memory transpose, the next
-// tile's loads in flight while the current one is stored.  Reads are 256 B
-// token rows; the block's output, [HD][64], is one contiguous stretch of aT16
-// ([T_pad / 64][HD][64]).
-constexpr int kPrepFT = 128;   // features per transposed tile
-
-__device__ __forceinline__ void prep_load_tile(const uint16_t* __restrict__ a, int t0, int T, int HD, int f0,
-                                               uint4 (&q)[4]) {
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int idx = threadIdx.x + r * 256;
-    const int tl = idx >> 4, f = f0 + (idx & 15) * 8, t = t0 + tl;
-    q[r] = (t < T && f < HD) ? __ldg(reinterpret_cast<const uint4*>(a + (size_t)t * HD + f)) : make_uint4(0, 0, 0, 0);
-  }
-}
-
-__global__ void __launch_bounds__(256) prep_tokens_t_kernel(const uint16_t* __restrict__ x,
-                                                            const uint16_t* __restrict__ a, __half* __restrict__ aT16,
-                                                            int T, int D, int HD, float eps, uint32_t* status) {
-  __shared__ float tile[64][kPrepFT + 1];
-  __shared__ float irs[64];
-  const int t0 = blockIdx.x * 64;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint4 q[4];
-  prep_load_tile(a, t0, T, HD, 0, q);   // the first tile's loads overlap the rms pass
-  for (int j = 0; j < 8; j += 2) {
-    const int tl = warp * 8 + j;
-    const bool v0 = t0 + tl < T, v1 = t0 + tl + 1 < T;
-    const uint4* x0 = reinterpret_cast<const uint4*>(x + (size_t)(v0 ? t0 + tl : 0) * D);
-    const uint4* x1 = reinterpret_cast<const uint4*>(x + (size_t)(v1 ? t0 + tl + 1 : 0) * D);
+// ---------------------------------------------------------------- token rms
+// inv_r[t] = 1 / sqrt(mean_d x_t,d^2 + eps) for t < T, 0 for T <= t < n_pad; one
+// warp per token, two tokens' loads in flight together (per token the same sum
+// order as the token-major staging of the other passes).
+__global__ void __launch_bounds__(256) inv_r_kernel(const uint16_t* __restrict__ x, float* __restrict__ inv_r, int T,
+                                                    int n_pad, int D, float eps) {
+  const int lane = threadIdx.x & 31;
+  const int n_warps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 2; t < n_pad; t += 2 * n_warps) {
+    const bool v0 = t < T, v1 = t + 1 < T;
+    const uint4* x0 = reinterpret_cast<const uint4*>(x + (size_t)(v0 ? t : 0) * D);
+    const uint4* x1 = reinterpret_cast<const uint4*>(x + (size_t)(v1 ? t + 1 : 0) * D);
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll 4
     for (int v = lane; v < D / 8; v += 32) {
-      const uint4 p0 = x0[v], p1 = x1[v];
+      const uint4 p0 = __ldg(x0 + v), p1 = __ldg(x1 + v);
       const uint16_t* e0 = reinterpret_cast<const uint16_t*>(&p0);
       const uint16_t* e1 = reinterpret_cast<const uint16_t*>(&p1);
 #pragma unroll
@@ -72,39 +50,10 @@ __global__ void __launch_bounds__(256) prep_tokens_t_kernel(const uint16_t* __re
       s1 += __shfl_xor_sync(0xffffffffu, s1, o);
     }
     if (lane == 0) {
-      irs[tl] = v0 ? rsqrtf(s0 / (float)D + eps) : 0.f;
-      irs[tl + 1] = v1 ? rsqrtf(s1 / (float)D + eps) : 0.f;
+      inv_r[t] = v0 ? rsqrtf(s0 / (float)D + eps) : 0.f;
+      if (t + 1 < n_pad) inv_r[t + 1] = v1 ? rsqrtf(s1 / (float)D + eps) : 0.f;
     }
   }
-  __syncthreads();
-  bool bad = false;
-  for (int f0 = 0; f0 < HD; f0 += kPrepFT) {
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int idx = threadIdx.x + r * 256;
-      const int tl = idx >> 4, c8 = (idx & 15) * 8;
-      const uint16_t* e = reinterpret_cast<const uint16_t*>(&q[r]);
-      const float ir = irs[tl];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) tile[tl][c8 + i] = bf2f_m(e[i]) * ir;
-    }
-    __syncthreads();
-    if (f0 + kPrepFT < HD) prep_load_tile(a, t0, T, HD, f0 + kPrepFT, q);
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int idx = threadIdx.x + r * 256;
-      const int fl = idx >> 3, tc = idx & 7, f = f0 + fl;
-      if (f < HD) {
-        __align__(16) __half o[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = to_h_m(tile[tc * 8 + i][fl], bad);
-        *reinterpret_cast<uint4*>(aT16 + ((size_t)blockIdx.x * HD + f) * 64 + tc * 8) =
-            *reinterpret_cast<const uint4*>(o);
-      }
-    }
-    __syncthreads();
-  }
-  if (bad) latch_status(status, kStatusRange);
 }
 
 // ---------------------------------------------------------------- Gram reduction
@@ -173,23 +122,48 @@ __global__ void __launch_bounds__(256) moment_finalize_kernel(const float* __res
 
 // ---------------------------------------------------------------- tcgen05 passes
 // One unit per CTA: warp 0 issues the TMA copies, warp 1 the MMAs (one
-// 128 x 128 fp32 accumulator in TMEM), warps 2..5 read it back.
-//   Gram: unit (head h, token chunk c); a stage is the head's d_head feature rows
-//         of one 64-token block of aT16 (one contiguous d_head x 128 B copy) in a
-//         128-row tile whose remaining rows are zeroed once; D += A A^T.
+// 128 x 128 fp32 accumulator in TMEM), warps 2..5 convert (Gram) and read the
+// accumulator back.
+//   Gram: unit (head h, token chunk c).  Per block of 64 tokens the TMA copies the
+//         head's d_head bf16 columns of a ([64][d_head], unswizzled) and the block's
+//         64 values of 1/r into a raw stage; the converter warps write a~ = fp16(a/r)
+//         transposed into a 128-row K-major operand tile (128 B swizzle, rows past
+//         d_head zeroed once), the layout the TMA would have written; then
+//         D += A A^T with A = that tile.  The accumulator goes out once, with its
+//         largest diagonal entry.
 //   Quad: unit (head h, row tile rt of M16); a stage is the tile of 128 M16 rows
 //         (64 neurons, gate and up rows interleaved by 16) and the hi / lo tiles
 //         of C~_h; D += A Chi^T + A Clo^T, then every row's m . D[row] in fp32.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t h2_bits(float lo, float hi, bool& bad) {
+  if (!(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f)) bad = true;
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_constant__ CUtensorMap mapA,
                                                                 const __grid_constant__ CUtensorMap mapB,
                                                                 const MomentParams p) {
-  constexpr int S = MODE == kMomentGram ? kGramStages : kQuadStages;
-  constexpr uint32_t kSB = MODE == kMomentGram ? kMomentTileBytes : 3 * kMomentTileBytes;
+  constexpr bool kGram = MODE == kMomentGram;
+  constexpr int S = kGram ? kGramRawStages : kQuadStages;     // TMA stages
+  constexpr int SO = kGram ? kGramOpStages : 1;                // Gram: operand tiles
+  constexpr uint32_t kSB = kGram ? kGramRawBytes : 3 * kMomentTileBytes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  __shared__ uint64_t full[S], empty[S], tfull, drain;
+  // Gram: operand tiles first (1024-byte aligned), raw stages after them
+  uint8_t* op0 = base;
+  uint8_t* st0 = kGram ? base + (size_t)SO * kMomentTileBytes : base;
+  __shared__ uint64_t full[S], empty[S], ofull[SO], oempty[SO], tfull, drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_s;
   __shared__ uint32_t dmax_s;   // Gram: the largest diagonal entry of the unit's block (fp32 bits, >= 0)
@@ -198,7 +172,7 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = (int)blockIdx.x % p.H, c = (int)blockIdx.x / p.H;
   int kb0 = 0, nkb = p.nkb;
-  if (MODE == kMomentGram) {
+  if (kGram) {
     kb0 = c * p.kpc;
     nkb = p.nkb - kb0 < p.kpc ? p.nkb - kb0 : p.kpc;
   }
@@ -206,7 +180,11 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], kGram ? 4 : 1);   // Gram: one arrival per converter warp
+    }
+    for (int s = 0; s < SO; ++s) {
+      mbar_init(&ofull[s], 4);
+      mbar_init(&oempty[s], 1);
     }
     mbar_init(&tfull, 1);
     mbar_init(&drain, 1);
@@ -216,20 +194,20 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&mapA);
-    if (MODE == kMomentQuad) prefetch_tmap(&mapB);
+    if (!kGram) prefetch_tmap(&mapB);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_slot, 128);
     tmem_relinquish();
   }
-  if (MODE == kMomentGram && warp >= 2 && p.dh < kMomentRows) {
-    // rows dh..127 of every stage are never copied into: zero them for the MMAs
-    const int tail = (kMomentRows - p.dh) * 128 / 16;   // uint4 per stage
-    for (int i = threadIdx.x - 64; i < S * tail; i += 128) {
+  if (kGram && warp >= 2 && p.dh < kMomentRows) {
+    // rows dh..127 of the operand tiles are never written: zero them for the MMAs
+    const int tail = (kMomentRows - p.dh) * 128 / 16;   // uint4 per tile
+    for (int i = threadIdx.x - 64; i < SO * tail; i += 128) {
       const int s = i / tail, e = i % tail;
-      reinterpret_cast<uint4*>(base + (size_t)s * kSB + (size_t)p.dh * 128)[e] = make_uint4(0, 0, 0, 0);
+      reinterpret_cast<uint4*>(op0 + (size_t)s * kMomentTileBytes + (size_t)p.dh * 128)[e] = make_uint4(0, 0, 0, 0);
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the tensor-core reads
+    fence_async_smem();   // visible to the tensor-core reads
   }
   tc_fence_before();
   __syncthreads();
@@ -244,10 +222,11 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
         const int s = kb % S;
         const uint32_t ph = (uint32_t)((kb / S) & 1);
         if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
-        uint8_t* st = base + (size_t)s * kSB;
-        if constexpr (MODE == kMomentGram) {
-          mbar_arrive_expect_tx(&full[s], (uint32_t)p.dh * 128u);
-          tma_load_3d(st, &mapA, &full[s], 0, h * p.dh, kb0 + kb);
+        uint8_t* st = st0 + (size_t)s * kSB;
+        if constexpr (kGram) {
+          mbar_arrive_expect_tx(&full[s], (uint32_t)p.dh * 128u + 256u);
+          tma_load_2d(st, &mapA, &full[s], h * p.dh, (kb0 + kb) * 64);
+          bulk_load(st + kGramRawTile, p.inv_r + (size_t)(kb0 + kb) * 64, 256u, &full[s]);
         } else {
           mbar_arrive_expect_tx(&full[s], kSB);
           if (p.stream)
@@ -272,26 +251,30 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(128, 128, 0);
-      const uint64_t dbase = smem_desc_k_sw128(smem_u32(base));
       constexpr uint64_t kT = (uint64_t)(kMomentTileBytes >> 4);
       bool ok = true;
       for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % S;
-        const uint32_t ph = (uint32_t)((kb / S) & 1);
-        if (!mbar_wait(&full[s], ph, abort_flag, p.status)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t da = dbase + (uint64_t)(((uint32_t)s * kSB) >> 4);
+        if constexpr (kGram) {
+          const int so = kb % SO;
+          if (!mbar_wait(&ofull[so], (uint32_t)((kb / SO) & 1), abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t da = smem_desc_k_sw128(smem_u32(op0 + (size_t)so * kMomentTileBytes));
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t acc = (kb | ks) != 0 ? 1u : 0u;
-          if constexpr (MODE == kMomentGram) {
-            mma_f16_ss(tmem, da + 2 * ks, da + 2 * ks, idesc, acc);
-          } else {
-            mma_f16_ss(tmem, da + 2 * ks, da + kT + 2 * ks, idesc, acc);
+          for (int ks = 0; ks < 4; ++ks)
+            mma_f16_ss(tmem, da + 2 * ks, da + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
+          mma_commit(&oempty[so]);
+        } else {
+          const int s = kb % S;
+          if (!mbar_wait(&full[s], (uint32_t)((kb / S) & 1), abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t da = smem_desc_k_sw128(smem_u32(st0 + (size_t)s * kSB));
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            mma_f16_ss(tmem, da + 2 * ks, da + kT + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
             mma_f16_ss(tmem, da + 2 * ks, da + 2 * kT + 2 * ks, idesc, 1u);
           }
+          mma_commit(&empty[s]);
         }
-        mma_commit(&empty[s]);
       }
       if (ok) {
         mma_commit(&tfull);
@@ -306,11 +289,62 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
     const int row = q * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
     int w_ok = 1;
-    if (lane == 0) w_ok = mbar_wait(&tfull, 0, abort_flag, p.status) ? 1 : 0;
+    if constexpr (kGram) {
+      // ---- converter: raw stage (bf16 [64][dh] + 1/r) -> operand tile
+      const int ct = threadIdx.x - 64;   // 0..127
+      const int P = p.dh / 2;            // 32-bit words (feature pairs) per token row
+      const int njobs = 8 * P;           // (feature pair, group of 8 tokens)
+      bool bad = false;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % S, so = kb % SO;
+        int ok = 1;
+        if (lane == 0)
+          ok = (mbar_wait(&full[s], (uint32_t)((kb / S) & 1), abort_flag, p.status) &&
+                mbar_wait(&oempty[so], (uint32_t)((kb / SO) & 1) ^ 1u, abort_flag, p.status))
+                   ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) { w_ok = 0; break; }
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(st0 + (size_t)s * kSB);
+        const float* irs = reinterpret_cast<const float*>(st0 + (size_t)s * kSB + kGramRawTile);
+        uint8_t* op = op0 + (size_t)so * kMomentTileBytes;
+        for (int j = ct; j < njobs; j += 128) {
+          const int pp = j % P, tc = j / P;
+          uint32_t w[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[i] = src[(tc * 8 + i) * P + pp];
+          const float4 ra = reinterpret_cast<const float4*>(irs)[tc * 2];
+          const float4 rb = reinterpret_cast<const float4*>(irs)[tc * 2 + 1];
+          const float ir[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+          uint32_t lo[4], hi[4];   // features 2pp and 2pp+1, tokens in order
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float a0 = __uint_as_float(w[2 * i] << 16) * ir[2 * i];
+            const float a1 = __uint_as_float(w[2 * i + 1] << 16) * ir[2 * i + 1];
+            const float b0 = __uint_as_float(w[2 * i] & 0xffff0000u) * ir[2 * i];
+            const float b1 = __uint_as_float(w[2 * i + 1] & 0xffff0000u) * ir[2 * i + 1];
+            lo[i] = h2_bits(a0, a1, bad);
+            hi[i] = h2_bits(b0, b1, bad);
+          }
+          const int f = 2 * pp;
+          *reinterpret_cast<uint4*>(op + (size_t)f * 128 + (((uint32_t)tc ^ (uint32_t)(f & 7)) << 4)) =
+              make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          *reinterpret_cast<uint4*>(op + (size_t)(f + 1) * 128 + (((uint32_t)tc ^ (uint32_t)((f + 1) & 7)) << 4)) =
+              make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&ofull[so]);
+          mbar_arrive(&empty[s]);
+        }
+      }
+      if (bad) latch_status(p.status, kStatusRange);
+    }
+    if (w_ok && lane == 0) w_ok = mbar_wait(&tfull, 0, abort_flag, p.status) ? 1 : 0;
     w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
     if (w_ok) {
       tc_fence_after();
-      if constexpr (MODE == kMomentGram) {
+      if constexpr (kGram) {
         // D[i][j] (i = this lane's feature row) goes to [j][i]: a warp's 32 lanes
         // write 128 contiguous bytes per column.
         float* dst = p.gram + (size_t)(c * p.H + h) * kMomentRows * kMomentRows + row;
@@ -354,8 +388,8 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
         if (lane < 16) p.out[(size_t)h * p.I_pad + (size_t)rt * 64 + q * 16 + lane] = pair;
       }
     }
-    if constexpr (MODE == kMomentGram) {
-      // every epilogue warp arrives here, whether or not its wait succeeded
+    if constexpr (kGram) {
+      // every epilogue warp arrives here, whether or not its waits succeeded
       named_barrier_sync(1, 128);
       if (w_ok && warp == 2 && lane == 0) p.cmax[(size_t)c * p.H + h] = __uint_as_float(dmax_s);
     }
@@ -370,7 +404,7 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
 }
 
 size_t moment_smem_bytes(int mode) {
-  return 1024 + (mode == kMomentGram ? (size_t)kGramStages * kMomentTileBytes
+  return 1024 + (mode == kMomentGram ? (size_t)kGramOpStages * kMomentTileBytes + (size_t)kGramRawStages * kGramRawBytes
                                      : (size_t)kQuadStages * 3 * kMomentTileBytes);
 }
 
@@ -395,10 +429,11 @@ cudaError_t launch_moment(const CUtensorMap* maps, const MomentParams& p, cudaSt
   return cudaGetLastError();
 }
 
-cudaError_t launch_prep_tokens_t(const uint16_t* x, const uint16_t* a, __half* aT16, int T, int D, int HD, float eps,
-                                 uint32_t* status, cudaStream_t s) {
-  const int blocks = (T + 63) / 64;
-  prep_tokens_t_kernel<<<blocks, 256, 0, s>>>(x, a, aT16, T, D, HD, eps, status);
+cudaError_t launch_inv_r(const uint16_t* x, float* inv_r, int T, int n_pad, int D, float eps, int sm_count,
+                        cudaStream_t s) {
+  int blocks = (n_pad + 15) / 16;   // 8 warps, two tokens each
+  if (blocks > 8 * sm_count) blocks = 8 * sm_count;
+  inv_r_kernel<<<blocks, 256, 0, s>>>(x, inv_r, T, n_pad, D, eps);
   return cudaGetLastError();
 }
 

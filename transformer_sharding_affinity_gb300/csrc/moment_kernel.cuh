@@ -19,13 +19,16 @@
 namespace aff {
 
 enum MomentMode : int {
-  kMomentGram = 0,   // C_h partial sums: per (head, token chunk), A = B = 128 feature rows x 64 tokens
+  kMomentGram = 0,   // C_h partial sums: per (head, token chunk), A = B = a~^T, 128 feature rows x 64 tokens
   kMomentQuad = 1    // per (head, 128 M_h rows): D = M_h C~_h (hi + lo parts), then m . D row by row
 };
 
 constexpr int kMomentRows = 128;                          // feature rows of a Gram tile, M_h rows of a quad tile
 constexpr int kMomentTileBytes = 128 * 64 * 2;            // one 128-row x 64-element fp16 tile
-constexpr int kGramStages = 6;
+constexpr int kGramRawStages = 3;                         // Gram: bf16 [64][d_head] + 64 floats of 1/r
+constexpr int kGramRawTile = 64 * 128 * 2;                // room for d_head <= 128
+constexpr int kGramRawBytes = kGramRawTile + 256;
+constexpr int kGramOpStages = 2;                          // Gram: fp16 operand tiles
 constexpr int kQuadStages = 2;                            // d_head <= 128: at most two K blocks
 constexpr int kMomentThreads = 192;                       // TMA warp, MMA warp, 4 epilogue warps
 // Units of the Gram pass: H x chunks with at most this many CTAs (two per SM on
@@ -43,6 +46,7 @@ struct MomentParams {
   uint32_t* status;
   float* gram;       // Gram output: [chunk][H][128 (column j)][128 (row i)] fp32
   float* cmax;       // Gram output: [chunk][H] the block's largest diagonal entry
+  const float* inv_r;   // Gram: 1/r per token, [nkb * 64] (0 past T)
   const float* scale;   // quad: per-head scale s_h of the staged C~_h = C_h / s_h
   const __half* M16;    // quad epilogue: the rows it contracted, read again as fp16
   float* out;           // quad output: [H][I_pad], m_g^T C_h m_g + m_u^T C_h m_u (token sums)
@@ -65,11 +69,9 @@ inline GramSplit gram_split(int64_t T, int64_t H) {
 
 size_t moment_smem_bytes(int mode);
 cudaError_t launch_moment(const CUtensorMap* maps, const MomentParams& p, cudaStream_t s);
-// aT16 = fp16(a[t][f] / r_t) in blocks of 64 tokens: [T_pad / 64][HD][64]
-// (tokens past T of the last block written as zero; blocks past it untouched);
-// r_t = sqrt(mean_d x_t,d^2 + eps).
-cudaError_t launch_prep_tokens_t(const uint16_t* x, const uint16_t* a, __half* aT16, int T, int D, int HD, float eps,
-                                 uint32_t* status, cudaStream_t s);
+// inv_r[t] = 1 / sqrt(mean_d x_t,d^2 + eps) for t < T, 0 for T <= t < n_pad.
+cudaError_t launch_inv_r(const uint16_t* x, float* inv_r, int T, int n_pad, int D, float eps, int sm_count,
+                         cudaStream_t s);
 // C_h = sum over chunks of the Gram partials (in chunk order); s_h = the sum over
 // chunks of their largest diagonal entries (>= max_i C_h[i][i]; 1 when not
 // positive); CC = [hi; lo] fp16 parts of C_h / s_h: [2][H][128][128], zero

@@ -143,10 +143,11 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
 
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ uint32_t h2_bits(float lo, float hi, bool& bad) {
-  if (!(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f)) bad = true;
-  const __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
+// Two fp32 values (a packed pair) rounded to fp16 and packed, low half first.
+__device__ __forceinline__ uint32_t h2_bits(uint64_t v) {
+  const float2 f = unpk(v);
+  const __half2 h = __floats2half2_rn(f.x, f.y);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 template <int MODE>
@@ -291,10 +292,25 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
     int w_ok = 1;
     if constexpr (kGram) {
       // ---- converter: raw stage (bf16 [64][dh] + 1/r) -> operand tile
+      // Jobs are (feature pair pp, group tc of 8 tokens), 8 * dh / 2 of them, at most 4 per
+      // thread; a thread's jobs are the same in every K block, so their offsets are set once.
+      // An fp16 overflow needs no check here: it becomes inf in the operand, so the
+      // head's diagonal is not finite and the reduction latches the range error.
       const int ct = threadIdx.x - 64;   // 0..127
       const int P = p.dh / 2;            // 32-bit words (feature pairs) per token row
-      const int njobs = 8 * P;           // (feature pair, group of 8 tokens)
-      bool bad = false;
+      int nj = 0;
+      int src_off[4], ir_off[4];
+      uint32_t dst0[4], dst1[4];
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const int j = ct + 128 * n;
+        const int pp = j % P, tc = j / P, f = 2 * pp;
+        src_off[n] = tc * 8 * P + pp;
+        ir_off[n] = tc * 8;
+        dst0[n] = (uint32_t)f * 128u + (((uint32_t)tc ^ (uint32_t)(f & 7)) << 4);
+        dst1[n] = (uint32_t)(f + 1) * 128u + (((uint32_t)tc ^ (uint32_t)((f + 1) & 7)) << 4);
+        if (j < 8 * P) nj = n + 1;
+      }
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = kb % S, so = kb % SO;
         int ok = 1;
@@ -307,29 +323,24 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
         const uint32_t* src = reinterpret_cast<const uint32_t*>(st0 + (size_t)s * kSB);
         const float* irs = reinterpret_cast<const float*>(st0 + (size_t)s * kSB + kGramRawTile);
         uint8_t* op = op0 + (size_t)so * kMomentTileBytes;
-        for (int j = ct; j < njobs; j += 128) {
-          const int pp = j % P, tc = j / P;
-          uint32_t w[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) w[i] = src[(tc * 8 + i) * P + pp];
-          const float4 ra = reinterpret_cast<const float4*>(irs)[tc * 2];
-          const float4 rb = reinterpret_cast<const float4*>(irs)[tc * 2 + 1];
-          const float ir[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
-          uint32_t lo[4], hi[4];   // features 2pp and 2pp+1, tokens in order
+        for (int n = 0; n < 4; ++n) {
+          if (n < nj) {
+            uint32_t w[8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float a0 = __uint_as_float(w[2 * i] << 16) * ir[2 * i];
-            const float a1 = __uint_as_float(w[2 * i + 1] << 16) * ir[2 * i + 1];
-            const float b0 = __uint_as_float(w[2 * i] & 0xffff0000u) * ir[2 * i];
-            const float b1 = __uint_as_float(w[2 * i + 1] & 0xffff0000u) * ir[2 * i + 1];
-            lo[i] = h2_bits(a0, a1, bad);
-            hi[i] = h2_bits(b0, b1, bad);
+            for (int i = 0; i < 8; ++i) w[i] = src[src_off[n] + i * P];
+            const float4 ra = *reinterpret_cast<const float4*>(irs + ir_off[n]);
+            const float4 rb = *reinterpret_cast<const float4*>(irs + ir_off[n] + 4);
+            const uint64_t ir2[4] = {pk(ra.x, ra.y), pk(ra.z, ra.w), pk(rb.x, rb.y), pk(rb.z, rb.w)};
+            uint32_t lo[4], hi[4];   // features 2pp and 2pp+1, tokens in order
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              lo[i] = h2_bits(mul2(pk_u(w[2 * i] << 16, w[2 * i + 1] << 16), ir2[i]));
+              hi[i] = h2_bits(mul2(pk_u(w[2 * i] & 0xffff0000u, w[2 * i + 1] & 0xffff0000u), ir2[i]));
+            }
+            *reinterpret_cast<uint4*>(op + dst0[n]) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4*>(op + dst1[n]) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           }
-          const int f = 2 * pp;
-          *reinterpret_cast<uint4*>(op + (size_t)f * 128 + (((uint32_t)tc ^ (uint32_t)(f & 7)) << 4)) =
-              make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          *reinterpret_cast<uint4*>(op + (size_t)(f + 1) * 128 + (((uint32_t)tc ^ (uint32_t)((f + 1) & 7)) << 4)) =
-              make_uint4(hi[0], hi[1], hi[2], hi[3]);
         }
         fence_async_smem();
         __syncwarp();
@@ -338,7 +349,6 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
           mbar_arrive(&empty[s]);
         }
       }
-      if (bad) latch_status(p.status, kStatusRange);
     }
     if (w_ok && lane == 0) w_ok = mbar_wait(&tfull, 0, abort_flag, p.status) ? 1 : 0;
     w_ok = __shfl_sync(0xffffffffu, w_ok, 0);

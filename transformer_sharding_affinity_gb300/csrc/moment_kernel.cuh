@@ -25,7 +25,7 @@ enum MomentMode : int {
 
 constexpr int kMomentRows = 128;                          // feature rows of a Gram tile, M_h rows of a quad tile
 constexpr int kMomentTileBytes = 128 * 64 * 2;            // one 128-row x 64-element fp16 tile
-constexpr int kGramRawStages = 3;                         // Gram: bf16 [64][d_head] + 64 floats of 1/r
+constexpr int kGramRawStages = 4;                         // Gram: bf16 [64][d_head] + 64 floats of 1/r
 constexpr int kGramRawTile = 64 * 128 * 2;                // room for d_head <= 128
 constexpr int kGramRawBytes = kGramRawTile + 256;
 constexpr int kGramOpStages = 2;                          // Gram: fp16 operand tiles

@@ -173,6 +173,34 @@ def test_s_up_matches_scalar_loops(mode):
     np.testing.assert_allclose(Sh, Sh_ref, rtol=1e-12)
 
 
+def test_add_equals_quadratic_forms_of_the_second_moment():
+    """ADD per head is a mean of squared linear forms in a_h/r, so it equals
+    m^T E_t[(a_h/r)(a_h/r)^T] m with m = W_o^(h)^T diag(gamma) w for every gate and
+    up row w (the form the GPU evaluates by default).  Built here from the
+    second moment of each head's slice of a and the folded rows, with no per-token
+    p_h; the oracle forms p_h per token."""
+    rng = np.random.default_rng(12)
+    L = _layer(rng, T=40, D=10, H=4, G=2, dh=5, I=9)
+    eps = 1e-6
+    S, Sh = _up(L, "add", eps=eps)
+    a, x, Wo, gm, Wg, Wu = (L[k] for k in ("a", "x", "Wo", "gamma", "Wg", "Wu"))
+    H, G, dh = L["H"], L["G"], L["dh"]
+    T = x.shape[0]
+    r = np.sqrt((x * x).mean(axis=1) + eps)
+    Sh_ref = np.zeros_like(Sh)
+    for h in range(H):
+        at = a[:, h * dh:(h + 1) * dh] / r[:, None]
+        C = at.T @ at / T                                   # d_head x d_head second moment
+        Woh = Wo[:, h * dh:(h + 1) * dh]                    # D x d_head
+        for Wrow in (Wg, Wu):
+            M = Wrow @ (gm[:, None] * Woh)                  # I x d_head folded rows
+            Sh_ref[h] += np.einsum("ki,ij,kj->k", M, C, M)
+    np.testing.assert_allclose(Sh, Sh_ref, rtol=1e-12)
+    np.testing.assert_allclose(S, Sh_ref.reshape(G, H // G, -1).sum(1), rtol=1e-12)
+    # and the second moment is positive semi-definite, so every entry is >= 0
+    assert np.all(Sh >= 0)
+
+
 def test_s_down_matches_scalar_loops():
     rng = np.random.default_rng(5)
     L = _layer(rng, T=3, D=4, H=4, G=2, dh=2, I=3, scale=0.6)

@@ -12,11 +12,6 @@ namespace {
 
 __device__ __forceinline__ float bf2f_m(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
-__device__ __forceinline__ __half to_h_m(float v, bool& bad) {
-  if (!(fabsf(v) <= 65504.f)) bad = true;
-  return __float2half_rn(v);
-}
-
 }  // namespace
 
 // ---------------------------------------------------------------- token rms

@@ -1,4 +1,4 @@
-// moment_kernel.cuh -- the ADD score through each head's second moment of p_h.
+// moment_kernel.cuh -- the ADD score through each head's second moment of a_h / r.
 //
 // ADD (paper "Affinity-Aware Sharding for Delayed Tensor Parallelism", §3
 // "Affinity scores") is S_hk = E_t[(p_h.w^g_k)^2 + (p_h.w^u_k)^2].  With

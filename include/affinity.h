@@ -121,6 +121,8 @@ typedef struct {
 /*
  * Bytes of device workspace that affinity_up (down == 0) or affinity_down
  * (down != 0) needs for this shape and mode (mode is ignored when down != 0).
+ * For AFF_MODE_ADD the size also depends on dims->flags (AFF_FLAG_ADD_DIRECT
+ * selects the direct form, whose per-chunk partial sums are larger).
  * The workspace must be 256-byte aligned.  Returns AFF_ERR_INVALID_ARG /
  * AFF_ERR_UNSUPPORTED_SHAPE / AFF_ERR_UNSUPPORTED_DTYPE for bad dims.
  */

@@ -595,7 +595,6 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
       mp.H = H; mp.dh = dh; mp.HD = H * dh; mp.I_pad = I_pad;
       mp.nkb = (int)ceil_div(dh, 64);
       mp.stream = stream_heads(d) ? 1 : 0;
-      mp.ctas = 2 * sm_count;
       mp.status = status;
       mp.scale = gscale;
       mp.M16 = M16;

@@ -159,16 +159,13 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
   // Gram: operand tiles first (1024-byte aligned), raw stages after them
   uint8_t* op0 = base;
   uint8_t* st0 = kGram ? base + (size_t)SO * kMomentTileBytes : base;
-  constexpr int NB = kGram ? 1 : 2;   // accumulator buffers (quad: one unit's MMAs beside the last one's epilogue)
-  __shared__ uint64_t full[S], empty[S], ofull[SO], oempty[SO], tfull[NB], tempty[NB], drain;
+  __shared__ uint64_t full[S], empty[S], ofull[SO], oempty[SO], tfull, drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_s;
   __shared__ uint32_t dmax_s;   // Gram: the largest diagonal entry of the unit's block (fp32 bits, >= 0)
   volatile int* abort_flag = &abort_s;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Gram: one unit per CTA; quad: a persistent grid walks units blockIdx.x, + gridDim.x, ...
-  const int ustep = kGram ? p.n_units : (int)gridDim.x;
   const int h = (int)blockIdx.x % p.H, c = (int)blockIdx.x / p.H;
   int kb0 = 0, nkb = p.nkb;
   if (kGram) {
@@ -185,10 +182,7 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
       mbar_init(&ofull[s], 4);
       mbar_init(&oempty[s], 1);
     }
-    for (int b = 0; b < NB; ++b) {
-      mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);   // one arrival per epilogue warp
-    }
+    mbar_init(&tfull, 1);
     mbar_init(&drain, 1);
     abort_s = 0;
     dmax_s = 0u;
@@ -199,7 +193,7 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
     if (!kGram) prefetch_tmap(&mapB);
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_slot, 128 * NB);
+    tmem_alloc(&tmem_slot, 128);
     tmem_relinquish();
   }
   if (kGram && warp >= 2 && p.dh < kMomentRows) {
@@ -219,29 +213,26 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
-      int issued = 0;   // stage uses so far (the ring runs on across units)
-      for (int u = (int)blockIdx.x; ok && u < p.n_units; u += ustep) {
-        const int uh = u % p.H, uc = u / p.H;
-        for (int kb = 0; kb < nkb; ++kb) {
-          const int s = issued % S;
-          const uint32_t ph = (uint32_t)((issued / S) & 1);
-          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          uint8_t* st = st0 + (size_t)s * kSB;
-          if constexpr (kGram) {
-            mbar_arrive_expect_tx(&full[s], (uint32_t)p.dh * 128u + 256u);
-            tma_load_2d(st, &mapA, &full[s], uh * p.dh, (kb0 + kb) * 64);
-            bulk_load(st + kGramRawTile, p.inv_r + (size_t)(kb0 + kb) * 64, 256u, &full[s]);
-          } else {
-            mbar_arrive_expect_tx(&full[s], kSB);
-            if (p.stream)
-              tma_load_2d(st, &mapA, &full[s], uh * p.dh + kb * 64, uc * kMomentRows);
-            else
-              tma_load_3d(st, &mapA, &full[s], kb * 64, uc * kMomentRows, uh);
-            tma_load_2d(st + kMomentTileBytes, &mapB, &full[s], kb * 64, uh * kMomentRows);
-            tma_load_2d(st + 2 * kMomentTileBytes, &mapB, &full[s], kb * 64, (p.H + uh) * kMomentRows);
-          }
-          ++issued;
+      int issued = 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % S;
+        const uint32_t ph = (uint32_t)((kb / S) & 1);
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        uint8_t* st = st0 + (size_t)s * kSB;
+        if constexpr (kGram) {
+          mbar_arrive_expect_tx(&full[s], (uint32_t)p.dh * 128u + 256u);
+          tma_load_2d(st, &mapA, &full[s], h * p.dh, (kb0 + kb) * 64);
+          bulk_load(st + kGramRawTile, p.inv_r + (size_t)(kb0 + kb) * 64, 256u, &full[s]);
+        } else {
+          mbar_arrive_expect_tx(&full[s], kSB);
+          if (p.stream)
+            tma_load_2d(st, &mapA, &full[s], h * p.dh + kb * 64, c * kMomentRows);
+          else
+            tma_load_3d(st, &mapA, &full[s], kb * 64, c * kMomentRows, h);
+          tma_load_2d(st + kMomentTileBytes, &mapB, &full[s], kb * 64, h * kMomentRows);
+          tma_load_2d(st + 2 * kMomentTileBytes, &mapB, &full[s], kb * 64, (p.H + h) * kMomentRows);
         }
+        ++issued;
       }
       if (!ok) {
         // let every copy already issued land before shared memory is released
@@ -258,42 +249,32 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
       constexpr uint32_t idesc = idesc_f16(128, 128, 0);
       constexpr uint64_t kT = (uint64_t)(kMomentTileBytes >> 4);
       bool ok = true;
-      int g = 0;   // stage uses so far (quad)
-      for (int u = (int)blockIdx.x, li = 0; ok && u < p.n_units; u += ustep, ++li) {
-        const int b = li % NB;
-        if constexpr (!kGram) {
-          // the buffer's previous unit must have been read out by the epilogue
-          if (!mbar_wait(&tempty[b], (uint32_t)(((li / NB) & 1) ^ 1), abort_flag, p.status)) { ok = false; break; }
+      for (int kb = 0; kb < nkb; ++kb) {
+        if constexpr (kGram) {
+          const int so = kb % SO;
+          if (!mbar_wait(&ofull[so], (uint32_t)((kb / SO) & 1), abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-        }
-        const uint32_t d = tmem + (uint32_t)(b * 128);
-        for (int kb = 0; kb < nkb; ++kb) {
-          if constexpr (kGram) {
-            const int so = kb % SO;
-            if (!mbar_wait(&ofull[so], (uint32_t)((kb / SO) & 1), abort_flag, p.status)) { ok = false; break; }
-            tc_fence_after();
-            const uint64_t da = smem_desc_k_sw128(smem_u32(op0 + (size_t)so * kMomentTileBytes));
+          const uint64_t da = smem_desc_k_sw128(smem_u32(op0 + (size_t)so * kMomentTileBytes));
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              mma_f16_ss(d, da + 2 * ks, da + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
-            mma_commit(&oempty[so]);
-          } else {
-            const int s = g % S;
-            if (!mbar_wait(&full[s], (uint32_t)((g / S) & 1), abort_flag, p.status)) { ok = false; break; }
-            tc_fence_after();
-            const uint64_t da = smem_desc_k_sw128(smem_u32(st0 + (size_t)s * kSB));
+          for (int ks = 0; ks < 4; ++ks)
+            mma_f16_ss(tmem, da + 2 * ks, da + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
+          mma_commit(&oempty[so]);
+        } else {
+          const int s = kb % S;
+          if (!mbar_wait(&full[s], (uint32_t)((kb / S) & 1), abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t da = smem_desc_k_sw128(smem_u32(st0 + (size_t)s * kSB));
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              mma_f16_ss(d, da + 2 * ks, da + kT + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
-              mma_f16_ss(d, da + 2 * ks, da + 2 * kT + 2 * ks, idesc, 1u);
-            }
-            mma_commit(&empty[s]);
-            ++g;
+          for (int ks = 0; ks < 4; ++ks) {
+            mma_f16_ss(tmem, da + 2 * ks, da + kT + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
+            mma_f16_ss(tmem, da + 2 * ks, da + 2 * kT + 2 * ks, idesc, 1u);
           }
+          mma_commit(&empty[s]);
         }
-        if (ok) mma_commit(&tfull[b]);
       }
-      if (!ok) {
+      if (ok) {
+        mma_commit(&tfull);
+      } else {
         mma_commit(&drain);
         volatile int dummy = 0;
         mbar_wait(&drain, 0, &dummy, p.status, 100000000ull);
@@ -363,10 +344,12 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
           mbar_arrive(&empty[s]);
         }
       }
-      if (w_ok && lane == 0) w_ok = mbar_wait(&tfull[0], 0, abort_flag, p.status) ? 1 : 0;
-      w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-      if (w_ok) {
-        tc_fence_after();
+    }
+    if (w_ok && lane == 0) w_ok = mbar_wait(&tfull, 0, abort_flag, p.status) ? 1 : 0;
+    w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+    if (w_ok) {
+      tc_fence_after();
+      if constexpr (kGram) {
         // D[i][j] (i = this lane's feature row) goes to [j][i]: a warp's 32 lanes
         // write 128 contiguous bytes per column.
         float* dst = p.gram + (size_t)(c * p.H + h) * kMomentRows * kMomentRows + row;
@@ -385,28 +368,15 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) dg = fmaxf(dg, __shfl_xor_sync(0xffffffffu, dg, o));
         if (lane == 0) atomicMax(&dmax_s, __float_as_uint(dg));
-      }
-      // every epilogue warp arrives here, whether or not its waits succeeded
-      named_barrier_sync(1, 128);
-      if (w_ok && warp == 2 && lane == 0) p.cmax[(size_t)c * p.H + h] = __uint_as_float(dmax_s);
-    } else {
-      // ---- quad: the units of this CTA, accumulator buffers alternating
-      for (int u = (int)blockIdx.x, li = 0; u < p.n_units; u += ustep, ++li) {
-        const int b = li % NB;
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait(&tfull[b], (uint32_t)((li / NB) & 1), abort_flag, p.status) ? 1 : 0;
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        tc_fence_after();
-        const int uh = u % p.H, rt = u / p.H;
+      } else {
+        const int rt = c;
         const __half* mrow = p.stream
-                                 ? p.M16 + (size_t)(rt * kMomentRows + row) * p.HD + (size_t)uh * p.dh
-                                 : p.M16 + ((size_t)uh * 2 * p.I_pad + (size_t)rt * kMomentRows + row) * p.dh;
-        const uint32_t tb = tl + (uint32_t)(b * 128);
+                                 ? p.M16 + (size_t)(rt * kMomentRows + row) * p.HD + (size_t)h * p.dh
+                                 : p.M16 + ((size_t)h * 2 * p.I_pad + (size_t)rt * kMomentRows + row) * p.dh;
         float acc = 0.f;
         for (int n0 = 0; n0 < p.dh; n0 += 16) {
           uint32_t v[16];
-          tmem_ld16(tb + (uint32_t)n0, v);
+          tmem_ld16(tl + (uint32_t)n0, v);
           const uint4 m0 = __ldg(reinterpret_cast<const uint4*>(mrow + n0));
           const uint4 m1 = n0 + 8 < p.dh ? __ldg(reinterpret_cast<const uint4*>(mrow + n0 + 8)) : make_uint4(0, 0, 0, 0);
           tmem_ld_wait();
@@ -417,15 +387,16 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
 #pragma unroll
           for (int i = 0; i < 8; ++i) acc = fmaf(__uint_as_float(v[8 + i]), __half2float(e1[i]), acc);
         }
-        // the buffer is read out: hand it back to the MMA warp
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[b]);
-        acc *= p.scale[uh];
+        acc *= p.scale[h];
         // rows 32q + l (gate) and 32q + 16 + l (up) are neuron 64 rt + 16 q + l
         const float pair = acc + __shfl_xor_sync(0xffffffffu, acc, 16);
-        if (lane < 16) p.out[(size_t)uh * p.I_pad + (size_t)rt * 64 + q * 16 + lane] = pair;
+        if (lane < 16) p.out[(size_t)h * p.I_pad + (size_t)rt * 64 + q * 16 + lane] = pair;
       }
+    }
+    if constexpr (kGram) {
+      // every epilogue warp arrives here, whether or not its waits succeeded
+      named_barrier_sync(1, 128);
+      if (w_ok && warp == 2 && lane == 0) p.cmax[(size_t)c * p.H + h] = __uint_as_float(dmax_s);
     }
   }
 
@@ -433,7 +404,7 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128 * NB);
+    tmem_dealloc(tmem, 128);
   }
 }
 
@@ -456,8 +427,7 @@ cudaError_t launch_moment(const CUtensorMap* maps, const MomentParams& p, cudaSt
     auto* fn = moment_kernel<kMomentQuad>;
     if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
       return e;
-    const int grid = p.ctas > 0 && p.ctas < p.n_units ? p.ctas : p.n_units;
-    fn<<<grid, kMomentThreads, smem, s>>>(maps[0], maps[1], p);
+    fn<<<p.n_units, kMomentThreads, smem, s>>>(maps[0], maps[1], p);
   } else {
     return cudaErrorInvalidValue;
   }

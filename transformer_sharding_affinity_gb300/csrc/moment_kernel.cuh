@@ -43,7 +43,6 @@ struct MomentParams {
   int32_t nkb;       // Gram: 64-token K blocks in all, ceil(T / 64); quad: K blocks over d_head
   int32_t kpc;       // Gram: K blocks per token chunk
   int32_t stream;    // quad: M16 is [2 I_pad][H*dh] (else [H][2 I_pad][dh])
-  int32_t ctas;      // quad: CTAs of the persistent grid (<= n_units; two fit on an SM)
   uint32_t* status;
   float* gram;       // Gram output: [chunk][H][128 (column j)][128 (row i)] fp32
   float* cmax;       // Gram output: [chunk][H] the block's largest diagonal entry

@@ -93,6 +93,26 @@ def test_add_second_moment_form():
     assert np.all(S0 == 0.0) and np.all(Sh0 == 0.0)
 
 
+def test_add_many_quadratic_form_units():
+    """16 heads x 2048 neurons: 512 quadratic-form units, more than two per SM of a
+    152-SM part, and 16 x 16 Gram units.  Sampled neurons against the oracle over
+    all tokens, both ADD forms, and bit-identical repeats."""
+    shape = S("many_units", T=1536, D=256, H=16, G=8, dh=64, I=2048, dtype="bf16", w_std=0.05,
+              x_dist="normal_outliers", seed=24)
+    layer = W.make_layer(shape)
+    rng = np.random.default_rng(8)
+    for mode in ("add", "add_direct"):
+        outs = run_up(B, DV, shape, layer, mode, runs=2)
+        S_gpu, Sh_gpu = outs[0]
+        assert np.array_equal(S_gpu.view(np.uint32), outs[1][0].view(np.uint32))
+        idx = _candidates(S_gpu, rng, top=8, n_random=48)
+        S_ref, Sh_ref = oracle_up(O, shape, layer, mode, neurons=idx)
+        assert rel_err(S_gpu[:, idx], S_ref) <= TOL, mode
+        assert rel_err(Sh_gpu[:, idx], Sh_ref) <= TOL, mode
+        for g in range(shape.G):
+            assert topk_agrees(S_gpu[g, idx], S_ref[g]), f"{mode}: top-8 of group {g} differs"
+
+
 def test_up_deterministic():
     layer = W.make_layer(MEDIUM)
     outs = run_up(B, DV, MEDIUM, layer, "fo", runs=3)

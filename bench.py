@@ -78,18 +78,73 @@ def peaks() -> dict:
     return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+class _Nvml:
+    """The few read-only NVML queries the clock record needs, through ctypes
+    (no Python NVML package on the GPU host).  Reads clocks, power and the
+    clock-event reasons; changes no setting."""
+    SM = 1   # NVML_CLOCK_SM
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+
+    def __init__(self, cuda_index: int):
+        import ctypes
+        self.c = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.dev = ctypes.c_void_p()
+        ok = False
+        try:   # the CUDA device by UUID (CUDA and NVML may number devices differently)
+            import torch
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(cuda_index).uuid)
+            ok = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) == 0
+        except Exception:
+            ok = False
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(cuda_index), ctypes.byref(self.dev)) != 0:
+            raise OSError("no NVML handle")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.max_mhz = self._uint(lib.nvmlDeviceGetMaxClockInfo, self.SM)
+
+    def _uint(self, fn, *args):
+        v = self.c.c_uint()
+        if fn(self.dev, *args, self.c.byref(v)) != 0:
+            return None
+        return v.value
+
+    def sample(self):
+        r = self.c.c_ulonglong()
+        self.reasons_fn(self.dev, self.c.byref(r))
+        return (self._uint(self.lib.nvmlDeviceGetClockInfo, self.SM),
+                [n for bit, n in self.REASONS.items() if r.value & bit],
+                self._uint(self.lib.nvmlDeviceGetPowerUsage))
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
+    """SM clock, power and throttle reasons sampled while the timed region runs:
+    NVML polled every millisecond or so (the default timed region lasts tens of
+    milliseconds), else nvidia-smi every 100 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_s: float = 0.001):
         self.gpu = gpu_index
+        self.period = period_s
         self.proc = None
+        self.nvml = None
         self.lines = []
+        self.samples = []      # (sm_mhz, reasons, power_mw) from NVML
+        self.stop = threading.Event()
 
     def __enter__(self):
+        try:
+            self.nvml = _Nvml(self.gpu)
+            self.t = threading.Thread(target=self._poll, daemon=True)
+            self.t.start()
+            return self
+        except Exception:
+            self.nvml = None
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
@@ -100,11 +155,19 @@ class ClockSampler:
             self.proc = None
         return self
 
+    def _poll(self):
+        while not self.stop.is_set():
+            self.samples.append(self.nvml.sample())
+            time.sleep(self.period)
+
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
     def __exit__(self, *a):
+        self.stop.set()
+        if self.nvml is not None:
+            self.t.join(timeout=5)
         if self.proc:
             self.proc.terminate()
             try:
@@ -113,6 +176,14 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self) -> dict:
+        if self.nvml is not None:
+            sm = [c for c, _, _ in self.samples if c is not None]
+            reasons = sorted({n for _, rs, _ in self.samples for n in rs})
+            pw = [p for _, _, p in self.samples if p is not None]
+            return {"sm_mhz": float(np.median(sm)) if sm else None,
+                    "sm_mhz_min": float(min(sm)) if sm else None, "sm_max_mhz": self.nvml.max_mhz,
+                    "reasons": reasons, "samples": len(sm),
+                    "power_w_max": max(pw) / 1e3 if pw else None, "source": "NVML"}
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
@@ -128,7 +199,7 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi"}
 
 
 def cpu_oracle_rate(shape, layer, budget_s: float = 10.0, max_tokens: int | None = None) -> dict:
@@ -281,7 +352,7 @@ def main() -> None:
     ap.add_argument("--mode", default="fo", choices=["fo", "add", "loo", "down"])
     ap.add_argument("--add-form", default="moment", choices=["moment", "direct"],
                     help="ADD through each head's second moment (d_head <= 128) or the direct contraction")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=256)
@@ -414,22 +485,23 @@ def main() -> None:
     free = [torch.cuda.Event() for _ in range(2)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    e0.record(stream)
-    copy_stream.wait_stream(stream)
-    for i in range(args.e2e_steps):
-        j = i % 2
-        with torch.cuda.stream(copy_stream):
-            if i >= 2:
-                copy_stream.wait_event(free[j])
-            for k in keys:
-                bufs[j][k].copy_(host[k], non_blocking=True)
-            ready[j].record(copy_stream)
-        stream.wait_event(ready[j])
-        step(bufs=bufs[j])
-        free[j].record(stream)
-        S_host.copy_(S, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks_e2e:
+        e0.record(stream)
+        copy_stream.wait_stream(stream)
+        for i in range(args.e2e_steps):
+            j = i % 2
+            with torch.cuda.stream(copy_stream):
+                if i >= 2:
+                    copy_stream.wait_event(free[j])
+                for k in keys:
+                    bufs[j][k].copy_(host[k], non_blocking=True)
+                ready[j].record(copy_stream)
+            stream.wait_event(ready[j])
+            step(bufs=bufs[j])
+            free[j].record(stream)
+            S_host.copy_(S, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps if args.e2e_steps > 0 else float("nan")
 
     if rank != 0:
@@ -492,7 +564,8 @@ def main() -> None:
         "roofline": roof,
         "gpu_launches": (8 if moment else {"fo": 7, "add": 6, "loo": 9, "down": 9}[args.mode]) * args.steps,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": shape.G * shape.I * 4, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": shape.G * shape.I * 4, "ms_per_step": e2e_ms, "steps": args.e2e_steps,
+                "clocks": clocks_e2e.summary()},
         "clocks": clocks.summary(),
     }
     if down:

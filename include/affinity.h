@@ -169,17 +169,33 @@ AFF_API aff_status affinity_up(const void* a, const void* x, const void* Wo, con
  *     enqueued.
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before
- *     any stream capture.
+ *     any stream capture.  Under CUDA's lazy module loading (the default)
+ *     that lookup is also when the 64 MiB is reserved on the device, not
+ *     when the library is loaded: a caller whose pool is about to take the
+ *     whole device must make its first call (or one
+ *     affinity_static_device_status call) before the pool reserves it;
+ *     otherwise the reservation fails and the call returns AFF_ERR_CUDA.
  *   - All calls share the one array, which keeps the last call's contents
  *     (each call writes every part it reads).  Calls whose work overlaps on
  *     the GPU -- on different streams, or from different host threads --
  *     race on it: serialise them.  The device status word lives in the
- *     array too; affinity_device_status() does not apply to it.
+ *     array too: read it with affinity_static_device_status(), not
+ *     affinity_device_status().
  */
 AFF_API aff_status affinity_up_static(const void* a, const void* x, const void* Wo, const void* gamma,
                               const void* Wg, const void* Wu, const void* Wd,
                               const aff_dims* dims, int32_t mode,
                               float* S_out, float* S_head_out, aff_stream_t stream);
+
+/*
+ * The status word of affinity_up_static's array: synchronises `stream`, then
+ * reads and clears what the kernels of the previous affinity_up_static call
+ * on the current device latched (AFF_ERR_DEVICE_TIMEOUT, AFF_ERR_RANGE);
+ * returns AFF_OK if none was set.  Like affinity_device_status, but for the
+ * array that stands in for the workspace; it allocates nothing either.  The
+ * paper has no counterpart.
+ */
+AFF_API aff_status affinity_static_device_status(aff_stream_t stream);
 
 /*
  * S_down for one layer ("Affinity scores", §3, down edge):

@@ -85,6 +85,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.affinity_down.restype = st
     lib.affinity_device_status.argtypes = [_P, _P]
     lib.affinity_device_status.restype = st
+    lib.affinity_static_device_status.argtypes = [_P]
+    lib.affinity_static_device_status.restype = st
     lib.affinity_score_partitions.argtypes = [_P, ctypes.c_int32, ctypes.c_int32, _P, ctypes.POINTER(ctypes.c_int64),
                                               ctypes.POINTER(ctypes.c_int64), _P]
     lib.affinity_score_partitions.restype = st
@@ -215,6 +217,11 @@ def selftest_timeout(workspace, limit_ns: int = 5_000_000, stream=None, workspac
 def device_status(workspace, stream=None) -> int:
     """Synchronise and return (then clear) the device-latched status of the last call."""
     return int(load().affinity_device_status(_ptr(workspace), _stream(stream)))
+
+
+def static_device_status(stream=None) -> int:
+    """As device_status, for the array affinity_up_static uses in place of a workspace."""
+    return int(load().affinity_static_device_status(_stream(stream)))
 
 
 def score_partitions(C: np.ndarray):

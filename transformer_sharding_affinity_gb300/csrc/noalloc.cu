@@ -9,8 +9,12 @@
 
 namespace {
 
-// Scratch used in place of a caller-provided workspace.  Every GPU that loads
-// the library holds these bytes until the process exits.
+// Scratch used in place of a caller-provided workspace.  Every GPU on which
+// this module is loaded holds these bytes until the process exits.  The
+// module is compiled on its own, so under CUDA's lazy module loading (the
+// default) it is loaded on a device, and the 64 MiB reserved there, at the
+// first symbol lookup below: the first affinity_up_static or
+// affinity_static_device_status call on that device.
 constexpr size_t kStaticScratchBytes = 64ull << 20;  // 64 MiB
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
@@ -56,4 +60,13 @@ extern "C" aff_status affinity_up_static(const void* a, const void* x, const voi
   // in the shared array never reach the result.
   return affinity_up(a, x, Wo, gamma, Wg, Wu, Wd, dims, mode, S_out, S_head_out, scratch, kStaticScratchBytes,
                      stream);
+}
+
+// The status word of the static scratch sits where a workspace keeps it, at
+// offset 0, so reading it is affinity_device_status on the array's address.
+extern "C" aff_status affinity_static_device_status(aff_stream_t stream) {
+  void* scratch = nullptr;
+  const aff_status st = scratch_on_current_device(&scratch);
+  if (st != AFF_OK) return st;
+  return affinity_device_status(scratch, stream);
 }

@@ -40,10 +40,17 @@
  *  from run to run (fixed reduction orders, no floating-point atomics).
  *
  *  bf16 path numerics: tensor-core operands are staged as fp16 (the
- *  normalised FFN input gamma*x/r, a/r, the folded per-head matrices) and
- *  contracted with fp32 accumulation; the SwiGLU operating point stays fp32;
- *  token sums are finished in fp64.  Intermediates must fit fp16's range
- *  (|value| < 65504); an overflow latches AFF_ERR_RANGE.  fp32 path: fp32
+ *  normalised FFN input gamma*x/r, a/r, the gate/up weights, the folded
+ *  per-head matrices) and contracted with fp32 accumulation; the SwiGLU
+ *  operating point stays fp32; token sums are finished in fp64.  Each staged
+ *  tensor is multiplied by a power of two chosen on the device from its
+ *  largest magnitude (or a bound on it) and the fp32 results by the inverse,
+ *  so affinity_up accepts every finite bf16 input: values far outside fp16's
+ *  range (|v| < 65504, normal above 2^-14) give the same scores as in range,
+ *  with the rescaling limited to factors 2^-60 .. 2^60 per tensor.  A
+ *  non-finite input latches AFF_ERR_RANGE.  affinity_down stages without
+ *  rescaling its down-projection side (alpha, W_d, the next layer's q/k/v
+ *  rows): there an fp16 overflow latches AFF_ERR_RANGE.  fp32 path: fp32
  *  arithmetic on the CUDA cores (meant for small shapes).
  */
 #ifndef AFFINITY_H
@@ -74,7 +81,7 @@ typedef enum {
   AFF_ERR_WORKSPACE = 5,          /* workspace NULL, too small or misaligned */
   AFF_ERR_CUDA = 6,               /* a CUDA call failed; see affinity_last_cuda_error() */
   AFF_ERR_DEVICE_TIMEOUT = 7,     /* a kernel's bounded wait expired (device-latched) */
-  AFF_ERR_RANGE = 8,              /* an fp16 intermediate overflowed (device-latched) */
+  AFF_ERR_RANGE = 8,              /* a non-finite input, or an fp16 overflow where nothing rescales (device-latched) */
   AFF_ERR_ALIGNMENT = 9,          /* a pointer is not 16-byte aligned */
   AFF_ERR_NO_CONVERGENCE = 10     /* an iterative solver hit its iteration cap (device-latched) */
 } aff_status;
@@ -216,7 +223,8 @@ AFF_API aff_status affinity_down(const void* x, const void* gamma, const void* W
 /*
  * Synchronises `stream`, then reads and clears the status word that kernels
  * of the previous affinity_up / affinity_down call on this workspace latch
- * (AFF_ERR_DEVICE_TIMEOUT, AFF_ERR_RANGE); returns AFF_OK if none was set.
+ * (AFF_ERR_DEVICE_TIMEOUT; AFF_ERR_RANGE for a non-finite input, or an fp16
+ * overflow on affinity_down's unscaled side); returns AFF_OK if none was set.
  */
 AFF_API aff_status affinity_device_status(void* workspace, aff_stream_t stream);
 

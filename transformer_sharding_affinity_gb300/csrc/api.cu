@@ -104,6 +104,7 @@ aff_status check_dims(const aff_dims* d) {
 struct Layout {
   size_t total = 0;
   size_t status = 0;
+  size_t scales = 0;   // DevScales (bf16 path)
   // bf16 path
   size_t W16 = 0, GWo16 = 0, M16 = 0, n16 = 0, a16 = 0, partial = 0, headsum = 0, wdn = 0;
   size_t alpha16 = 0, Wd16 = 0, WdT16 = 0, Wqkv16 = 0, ssx = 0, cpart = 0, bnorm = 0;
@@ -132,6 +133,7 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
   const int64_t T = d.T, D = d.D, H = d.H, G = d.G, dh = d.d_head, I = d.I;
   L.status = L.take(256);
   if (d.dtype == AFF_BF16) {
+    L.scales = L.take(256);
     L.I_pad = round_up(I, 256);
     L.T_pad = round_up(T, down ? 128 : 256 * kHeadSets);   // head-pass units take 512 tokens
     L.W16 = L.take((size_t)2 * L.I_pad * D * 2);
@@ -156,11 +158,11 @@ Layout make_layout(const aff_dims& d, int mode, bool down) {
       const int tile_mode = mode == AFF_MODE_LOO ? kModeLOO : (mode == AFF_MODE_ADD ? kModeADD : kModeFO);
       L.partial = L.take((size_t)L.n_chunks * (epi_warps(tile_mode) / 4) * H * L.I_pad * 4);
       if (mode == AFF_MODE_FO) L.wdn = L.take((size_t)L.I_pad * 4);
+      L.inv_r = L.take((size_t)L.T_pad * 4);   // 1/r per token (restaging of a16, LOO's rho)
       if (mode == AFF_MODE_LOO) {
         L.Wo16 = L.take((size_t)D * H * dh * 2);
         L.cn = L.take((size_t)2 * cnorm_groups(D) * H * L.T_pad * 4);
         L.rho = L.take((size_t)H * L.T_pad * 4);
-        L.inv_r = L.take((size_t)L.T_pad * 4);
       }
     } else {
       L.Rg = (H / G + 2) * dh;
@@ -339,6 +341,7 @@ TileParams base_params(const aff_dims& d, const Layout& L, uint8_t* ws, int mode
     p.spp = (int)(d.d_head / 16);
   }
   p.status = reinterpret_cast<uint32_t*>(ws + L.status);
+  p.sc = reinterpret_cast<const DevScales*>(ws + L.scales);
   p.eps = d.eps;
   return p;
 }
@@ -440,7 +443,7 @@ const char* affinity_strerror(aff_status s) {
     case AFF_ERR_WORKSPACE: return "workspace missing, misaligned (256 B) or smaller than affinity_workspace_size()";
     case AFF_ERR_CUDA: return "a CUDA call failed (see affinity_last_cuda_error())";
     case AFF_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait expired";
-    case AFF_ERR_RANGE: return "an fp16 intermediate overflowed (|value| >= 65504)";
+    case AFF_ERR_RANGE: return "a non-finite input, or an fp16 intermediate overflowed where nothing rescales it";
     case AFF_ERR_ALIGNMENT: return "a device pointer is not 16-byte aligned";
     case AFF_ERR_NO_CONVERGENCE: return "an iterative solver reached its iteration cap";
   }
@@ -514,25 +517,32 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   const uint16_t* x_b = static_cast<const uint16_t*>(x);
   const uint16_t* g_b = static_cast<const uint16_t*>(gamma);
 
-  // weight side (fp16 gate/up rows, gamma*Wo^T, ||w^d||^2, the fold) on the side stream
+  // Power-of-two scales of the fp16 operands (scales.cuh): their maxima start at zero.
+  DevScales* sc = reinterpret_cast<DevScales*>(ws + L.scales);
+  AFF_CUDA(cudaMemsetAsync(sc, 0, sizeof(DevScales), s));
+  // weight side (weight maxima, fp16 gate/up rows, gamma*Wo^T, ||w^d||^2, the fold) on the side stream
   SideStream* side = nullptr;
   if ((st = side_stream(&side)) != AFF_OK) return st;
   const cudaStream_t ws2 = side->stream;
   AFF_CUDA(cudaEventRecord(side->fork, s));
   AFF_CUDA(cudaStreamWaitEvent(ws2, side->fork, 0));
-  AFF_CUDA(launch_prep_gate_up((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, status, ws2));
-  AFF_CUDA(launch_scaled_transpose_split((const uint16_t*)Wo, g_b, GWo16, D, H * dh, status, ws2));
+  AFF_CUDA(launch_weight_max((const uint16_t*)Wg, (const uint16_t*)Wu, (const uint16_t*)Wo, g_b, I, D, H * dh, sc,
+                             sm_count, ws2));
+  AFF_CUDA(launch_weight_stage((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, (const uint16_t*)Wo, g_b,
+                               GWo16, H * dh, status, sc, sm_count, ws2));
   __half* Wo16 = loo ? reinterpret_cast<__half*>(ws + L.Wo16) : nullptr;
-  float* inv_r = loo ? reinterpret_cast<float*>(ws + L.inv_r) : nullptr;
-  if (loo) AFF_CUDA(launch_to_fp16((const uint16_t*)Wo, Wo16, (size_t)D * H * dh, status, ws2));
-  // token side on the caller's stream meanwhile
   const bool moment = moment_form(d, mode);
+  float* inv_r = moment ? nullptr : reinterpret_cast<float*>(ws + L.inv_r);
+  if (loo) AFF_CUDA(launch_to_fp16((const uint16_t*)Wo, Wo16, (size_t)D * H * dh, status, &sc->womax, ws2));
+  // token side on the caller's stream meanwhile
   float* ir_m = moment ? reinterpret_cast<float*>(ws + L.ir) : nullptr;
-  if (moment)
+  if (moment) {
     AFF_CUDA(launch_inv_r(x_b, ir_m, T, gram_split(T, H).nkb * 64, D, d.eps, sm_count, s));
-  else
+  } else {
     AFF_CUDA(launch_prep_tokens(x_b, a_b, g_b, (fo || loo) ? n16 : nullptr, a16, inv_r, T, D, H * dh, d.eps, status,
-                                sm_count, s));
+                                sm_count, sc, s));
+    AFF_CUDA(launch_restage_a(a_b, inv_r, a16, T, H * dh, sc, status, sm_count, s));
+  }
 
   CUtensorMap maps[4];
   std::memset(maps, 0, sizeof maps);
@@ -577,7 +587,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
       if (timed) AFF_CUDA(cudaEventRecord(g_timing_start, s));
       AFF_CUDA(launch_moment(mm, mp, s));
       if (timed) AFF_CUDA(cudaEventRecord(g_timing_stop, s));
-      AFF_CUDA(launch_gram_reduce(gram, cmax, CC, gscale, gs.n_chunks, H, dh, status, s));
+      AFF_CUDA(launch_gram_reduce(gram, cmax, CC, gscale, gs.n_chunks, H, dh, status, a_b, ir_m, T, sc, s));
     }
     AFF_CUDA(cudaStreamWaitEvent(s, side->join, 0));
     {
@@ -601,7 +611,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
       mp.out = partial;
       AFF_CUDA(launch_moment(mm, mp, s));
     }
-    AFF_CUDA(launch_moment_finalize(partial, T, H, G, I, I_pad, S_out, S_head_out, s));
+    AFF_CUDA(launch_moment_finalize(partial, T, H, G, I, I_pad, S_out, S_head_out, sc, D, s));
     return AFF_OK;
   }
   AFF_CUDA(cudaStreamWaitEvent(s, side->join, 0));
@@ -610,7 +620,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   AFF_CUDA(cudaEventRecord(side->join_late, ws2));
   float* rho = loo ? reinterpret_cast<float*>(ws + L.rho) : nullptr;
   if (loo) {
-    // rho[h][t] = r / rms(x - c_h): tensor-core pass over (a_h / r) Wo^(h)^T with the
+    // sigma[h][t] = 1 - r / rms(x - c_h): tensor-core pass over (a_h / r) Wo^(h)^T with the
     // per-token sums over d in the epilogue, then a small kernel
     float* cn = reinterpret_cast<float*>(ws + L.cn);
     uint64_t da[3] = {(uint64_t)dh, (uint64_t)H, (uint64_t)T};
@@ -625,7 +635,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     p.partial = cn;
     p.x_bf16 = x_b;
     if ((st = run_tile(maps, p, s)) != AFF_OK) return st;
-    AFF_CUDA(launch_loo_rho(cn, inv_r, rho, T, (int)L.T_pad, H, D, cnorm_groups(D), s));
+    AFF_CUDA(launch_loo_rho(cn, inv_r, rho, T, (int)L.T_pad, H, D, cnorm_groups(D), sc, s));
   }
   int epi_groups = 2;   // column groups of the epilogue in the partial sums (set below)
   // FO / ADD / LOO: per (256 tokens, 64 neurons), operating point (FO, LOO) then every head
@@ -659,7 +669,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   }
   AFF_CUDA(cudaStreamWaitEvent(s, side->join_late, 0));
   AFF_CUDA(launch_reduce_finalize(partial, wdn, fo, (int)L.n_chunks, epi_groups, T, H, G, I, I_pad, S_out,
-                                  S_head_out, s));
+                                  S_head_out, reinterpret_cast<const DevScales*>(ws + L.scales), D, s));
   return AFF_OK;
 }
 
@@ -717,15 +727,18 @@ aff_status affinity_down(const void* x, const void* gamma, const void* Wg, const
   SideStream* side = nullptr;
   if ((st = side_stream(&side)) != AFF_OK) return st;
   const cudaStream_t ws2 = side->stream;
+  DevScales* sc = reinterpret_cast<DevScales*>(ws + L.scales);
+  AFF_CUDA(cudaMemsetAsync(sc, 0, sizeof(DevScales), s));
   AFF_CUDA(cudaEventRecord(side->fork, s));
   AFF_CUDA(cudaStreamWaitEvent(ws2, side->fork, 0));
-  AFF_CUDA(launch_prep_gate_up((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, status, ws2));
+  AFF_CUDA(launch_weight_max((const uint16_t*)Wg, (const uint16_t*)Wu, nullptr, nullptr, I, D, 0, sc, sm_count, ws2));
+  AFF_CUDA(launch_prep_gate_up((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, status, sc, ws2));
   AFF_CUDA(launch_prep_wd((const uint16_t*)Wd, Wd16, WdT16, D, I, I_pad, status, ws2));
   AFF_CUDA(launch_prep_qkv((const uint16_t*)Wq_next, (const uint16_t*)Wk_next, (const uint16_t*)Wv_next,
                            (const uint16_t*)gamma_next, Wqkv16, G, H / G, dh, D, status, ws2));
   AFF_CUDA(cudaEventRecord(side->join, ws2));
   AFF_CUDA(launch_prep_tokens((const uint16_t*)x, nullptr, (const uint16_t*)gamma, n16, nullptr, nullptr, T, D, 0,
-                              d.eps, status, sm_count, s));
+                              d.eps, status, sm_count, sc, s));
   AFF_CUDA(cudaStreamWaitEvent(s, side->join, 0));
   CUtensorMap maps[4];
   std::memset(maps, 0, sizeof maps);

@@ -4,6 +4,7 @@
 // Paper: "Affinity-Aware Sharding for Delayed Tensor Parallelism", §3
 // "Affinity scores" (eq. 5 and the FO / ADD / down definitions after it).
 #include "aux_kernels.cuh"
+#include "scales.cuh"
 #include "sm103_primitives.cuh"
 
 #include <cuda_fp16.h>
@@ -19,15 +20,31 @@ __device__ __forceinline__ __half to_h(float v, bool& bad) {
 
 // ---------------------------------------------------------------- token rows
 // One warp per token: r_t = sqrt(mean_d x_td^2 + eps); n16 = gamma*x/r (the
-// FFN's normalised input) and a16 = a/r (so that the head contraction with
-// the folded matrices yields p_h.w directly), both rounded to fp16.
+// FFN's normalised input) times 2^e_n and a16 = a/r (so that the head
+// contraction with the folded matrices yields p_h.w directly), both rounded to
+// fp16, and 1/r.  e_n comes from max|gamma| (every block finds the same value;
+// block 0 records it).  a16 is staged unscaled while the largest |a/r| is
+// recorded; restage_a_kernel rescales it when that maximum calls for it.
 __global__ void prep_tokens_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ a,
                                    const uint16_t* __restrict__ gamma, __half* __restrict__ n16,
                                    __half* __restrict__ a16, float* __restrict__ inv_r, int T, int D, int HD,
-                                   float eps, uint32_t* status) {
+                                   float eps, uint32_t* status, DevScales* sc) {
   const int lane = threadIdx.x & 31;
   const int n_warps = (gridDim.x * blockDim.x) >> 5;
+  __shared__ uint32_t gmax_s;
+  if (threadIdx.x == 0) gmax_s = 0u;
+  __syncthreads();
+  uint32_t gm = 0u;   // |gamma| as fp32 bits: the bf16 magnitude bits, shifted
+  for (int v = threadIdx.x; v < D; v += blockDim.x) gm = max(gm, (uint32_t)(gamma[v] & 0x7FFFu) << 16);
+  gm = __reduce_max_sync(0xffffffffu, gm);
+  if (lane == 0) atomicMax(&gmax_s, gm);
+  __syncthreads();
+  DevScales loc{};
+  loc.gmax = gmax_s;
+  if (blockIdx.x == 0 && threadIdx.x == 0) sc->gmax = gmax_s;
+  const float fn = pow2f(scale_exps(loc, D).e_n);
   bool bad = false;
+  uint32_t am = 0u;   // largest |a / r| this thread staged (fp32 bits)
   for (int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; warp < T; warp += n_warps) {
   const size_t t = (size_t)warp;
   const uint4* xr = reinterpret_cast<const uint4*>(x + t * D);
@@ -46,6 +63,7 @@ __global__ void prep_tokens_kernel(const uint16_t* __restrict__ x, const uint16_
   const float ir = rsqrtf(ss / (float)D + eps);
   if (lane == 0 && inv_r) inv_r[t] = ir;
   if (n16) {
+    const float irn = ir * fn;
     const uint4* gr = reinterpret_cast<const uint4*>(gamma);
     uint4* nr = reinterpret_cast<uint4*>(n16 + t * D);
     for (int v = lane; v < D / 8; v += 32) {
@@ -54,7 +72,7 @@ __global__ void prep_tokens_kernel(const uint16_t* __restrict__ x, const uint16_
       const uint16_t* ge = reinterpret_cast<const uint16_t*>(&g);
       __align__(16) __half o[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = to_h(bf2f(ge[i]) * bf2f(e[i]) * ir, bad);
+      for (int i = 0; i < 8; ++i) o[i] = to_h(bf2f(ge[i]) * (bf2f(e[i]) * irn), bad);
       nr[v] = *reinterpret_cast<uint4*>(o);
     }
   }
@@ -66,20 +84,93 @@ __global__ void prep_tokens_kernel(const uint16_t* __restrict__ x, const uint16_
       const uint16_t* e = reinterpret_cast<const uint16_t*>(&q);
       __align__(16) __half o[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = to_h(bf2f(e[i]) * ir, bad);
+      for (int i = 0; i < 8; ++i) {
+        const float f = bf2f(e[i]) * ir;
+        am = max(am, __float_as_uint(fabsf(f)));
+        o[i] = __float2half_rn(f);
+      }
       orow[v] = *reinterpret_cast<uint4*>(o);
     }
   }
   }
+  if (a16) {
+    am = __reduce_max_sync(0xffffffffu, am);
+    if (lane == 0 && am) atomicMax(&sc->amax, am);
+  }
   if (bad) latch_status(status, kStatusRange);
 }
 
-// ---------------------------------------------------------------- weights
-// W16 = fp16 copy of Wg and Wu, I_pad neurons (zero rows past I), in groups of 16
-// neurons: their 16 gate rows, then their 16 up rows ([I_pad / 16][2][16][D]).
+// a16 = fp16(a / r * 2^e_a) for every token, when the largest |a/r| recorded by
+// prep_tokens_kernel lies outside [2^-6, 2^15) (e_a != 0); otherwise nothing to
+// do.  A non-finite maximum (a non-finite input) latches AFF_ERR_RANGE.
+__global__ void restage_a_kernel(const uint16_t* __restrict__ a, const float* __restrict__ inv_r,
+                                 __half* __restrict__ a16, int T, int HD, const DevScales* __restrict__ sc,
+                                 uint32_t* status) {
+  const float am = bits_f(sc->amax);
+  if (!(am <= 3.4e38f)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) latch_status(status, kStatusRange);
+    return;
+  }
+  const int e = scale_exp_act(am);
+  if (e == 0) return;
+  const float f = pow2f(e);
+  const size_t n8 = (size_t)T * HD / 8;
+  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8; v += (size_t)gridDim.x * blockDim.x) {
+    const size_t t = v * 8 / HD;
+    const float irf = inv_r[t] * f;
+    const uint4 q = *reinterpret_cast<const uint4*>(a + v * 8);
+    const uint16_t* e8 = reinterpret_cast<const uint16_t*>(&q);
+    __align__(16) __half o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = __float2half_rn(bf2f(e8[i]) * irf);
+    *reinterpret_cast<uint4*>(a16 + v * 8) = *reinterpret_cast<uint4*>(o);
+  }
+}
+
+// Largest |value| of up to four bf16 arrays (each n_i % 8 == 0) into out_i (fp32
+// bits, atomicMax).  blockIdx.y picks the array; its blocks grid-stride over it
+// with four 16-byte loads in flight per thread.
+struct MaxJobs {
+  const uint16_t* p[4];
+  size_t n8[4];     // 8-element words of each array (0 = unused)
+  uint32_t* out[4];
+};
+
+__device__ __forceinline__ uint32_t max_abs8(const uint4& q) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  uint32_t mm = 0u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) mm = max(mm, max((w[i] & 0x7FFFu) << 16, w[i] & 0x7FFF0000u));
+  return mm;
+}
+
+__global__ void max_abs_kernel(const __grid_constant__ MaxJobs J) {
+  const int k = blockIdx.y;
+  const uint16_t* __restrict__ p = k == 0 ? J.p[0] : k == 1 ? J.p[1] : k == 2 ? J.p[2] : J.p[3];
+  const size_t n8 = k == 0 ? J.n8[0] : k == 1 ? J.n8[1] : k == 2 ? J.n8[2] : J.n8[3];
+  uint32_t* out = k == 0 ? J.out[0] : k == 1 ? J.out[1] : k == 2 ? J.out[2] : J.out[3];
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  uint32_t m = 0u;
+  size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  for (; v + 3 * stride < n8; v += 4 * stride) {
+    const uint4 a0 = __ldg(q + v), a1 = __ldg(q + v + stride), a2 = __ldg(q + v + 2 * stride),
+                a3 = __ldg(q + v + 3 * stride);
+    m = max(m, max(max(max_abs8(a0), max_abs8(a1)), max(max_abs8(a2), max_abs8(a3))));
+  }
+  for (; v < n8; v += stride) m = max(m, max_abs8(__ldg(q + v)));
+  m = __reduce_max_sync(0xffffffffu, m);
+  if ((threadIdx.x & 31) == 0 && m && out) atomicMax(out, m);
+}
+
+// W16 = fp16 copy of Wg and Wu times 2^e_w, I_pad neurons (zero rows past I), in
+// groups of 16 neurons: their 16 gate rows, then their 16 up rows
+// ([I_pad / 16][2][16][D]).
 __global__ void prep_gate_up_kernel(const uint16_t* __restrict__ Wg, const uint16_t* __restrict__ Wu,
-                                    __half* __restrict__ W16, int I, int I_pad, int D, uint32_t* status) {
+                                    __half* __restrict__ W16, int I, int I_pad, int D, uint32_t* status,
+                                    const DevScales* __restrict__ sc) {
   const size_t n8 = (size_t)2 * I_pad * D / 8;
+  const float f = pow2f(scale_exp_norm(bits_f(sc->wmax)));   // W16 = W 2^e_w
   bool bad = false;
   for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8; v += (size_t)gridDim.x * blockDim.x) {
     const size_t e0 = v * 8;
@@ -92,7 +183,7 @@ __global__ void prep_gate_up_kernel(const uint16_t* __restrict__ Wg, const uint1
       uint4 q = *reinterpret_cast<const uint4*>(src);
       const uint16_t* e = reinterpret_cast<const uint16_t*>(&q);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = to_h(bf2f(e[i]), bad);
+      for (int i = 0; i < 8; ++i) o[i] = to_h(bf2f(e[i]) * f, bad);
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[i] = __float2half_rn(0.f);
@@ -102,27 +193,65 @@ __global__ void prep_gate_up_kernel(const uint16_t* __restrict__ Wg, const uint1
   if (bad) latch_status(status, kStatusRange);
 }
 
-// out[n][part][d] for part 0/1 = fp16 hi / lo of scale_d * W[d][n] (a transposed,
-// split copy: hi + lo carries ~22 significant bits of the exact fp32 product).
-// W is [Drows][Ncols] bf16 row-major.  Tiled through shared memory.
-__global__ void scaled_transpose_split_kernel(const uint16_t* __restrict__ W, const uint16_t* __restrict__ scale,
-                                              __half* __restrict__ out, int Drows, int Ncols, uint32_t* status) {
-  __shared__ float tile[32][33];
-  const int d0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const int d = d0 + i, n = n0 + threadIdx.x;
-    tile[i][threadIdx.x] = (d < Drows && n < Ncols) ? bf2f(scale[d]) * bf2f(W[(size_t)d * Ncols + n]) : 0.f;
-  }
-  __syncthreads();
+// The weight staging of the up pass in one launch: blockIdx.y == 0 stages W16 (as
+// prep_gate_up_kernel, one warp per row, no divisions); blockIdx.y == 1 stages
+// GWo16[n][part][d] for part 0/1 = fp16 hi / lo of gamma_d * Wo[d][n] * 2^e_g (a
+// transposed, split copy through 32 x 32 shared-memory tiles: hi + lo carries
+// ~22 significant bits of the exact fp32 product).  256 threads per block; both
+// parts grid-stride.
+__global__ void __launch_bounds__(256) weight_stage_kernel(const uint16_t* __restrict__ Wg,
+                                                           const uint16_t* __restrict__ Wu, __half* __restrict__ W16,
+                                                           int I, int I_pad, int D, const uint16_t* __restrict__ Wo,
+                                                           const uint16_t* __restrict__ gamma,
+                                                           __half* __restrict__ GWo16, int HD, uint32_t* status,
+                                                           const DevScales* __restrict__ sc) {
   bool bad = false;
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const int n = n0 + i, d = d0 + threadIdx.x;
-    if (n < Ncols && d < Drows) {
-      const float v = tile[threadIdx.x][i];
-      const __half hi = to_h(v, bad);
-      const __half lo = __float2half_rn(v - __half2float(hi));
-      out[((size_t)n * 2 + 0) * Drows + d] = hi;
-      out[((size_t)n * 2 + 1) * Drows + d] = lo;
+  if (blockIdx.y == 0) {
+    const float f = pow2f(scale_exp_norm(bits_f(sc->wmax)));   // W16 = W 2^e_w
+    const int lane = threadIdx.x & 31, nw = gridDim.x * 8;
+    const int D8 = D / 8;
+    for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < 2 * I_pad; r += nw) {
+      // row r: neuron group r / 32, gate (0) or up (1) row, neuron 16 * (r / 32) + r % 16
+      const int blk = (r >> 4) & 1, k = (r >> 5) * 16 + (r & 15);
+      const uint4* src = reinterpret_cast<const uint4*>((blk == 0 ? Wg : Wu) + (size_t)k * D);
+      uint4* dst = reinterpret_cast<uint4*>(W16 + (size_t)r * D);
+      for (int c = lane; c < D8; c += 32) {
+        __align__(16) __half o[8];
+        if (k < I) {
+          const uint4 q = __ldg(src + c);
+          const uint16_t* e = reinterpret_cast<const uint16_t*>(&q);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[i] = to_h(bf2f(e[i]) * f, bad);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[i] = __float2half_rn(0.f);
+        }
+        dst[c] = *reinterpret_cast<uint4*>(o);
+      }
+    }
+  } else {
+    __shared__ float tile[32][33];
+    const float f = pow2f(scale_exps(*sc, D).e_g);
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int tn = (HD + 31) / 32, td = (D + 31) / 32;
+    for (int tt = blockIdx.x; tt < tn * td; tt += gridDim.x) {
+      const int d0 = (tt / tn) * 32, n0 = (tt % tn) * 32;
+      __syncthreads();
+      for (int i = ty; i < 32; i += 8) {
+        const int d = d0 + i, n = n0 + tx;
+        tile[i][tx] = (d < D && n < HD) ? bf2f(gamma[d]) * bf2f(Wo[(size_t)d * HD + n]) : 0.f;
+      }
+      __syncthreads();
+      for (int i = ty; i < 32; i += 8) {
+        const int n = n0 + i, d = d0 + tx;
+        if (n < HD && d < D) {
+          const float v = tile[tx][i] * f;
+          const __half hi = to_h(v, bad);
+          const __half lo = __float2half_rn(v - __half2float(hi));
+          GWo16[((size_t)n * 2 + 0) * D + d] = hi;
+          GWo16[((size_t)n * 2 + 1) * D + d] = lo;
+        }
+      }
     }
   }
   if (bad) latch_status(status, kStatusRange);
@@ -223,7 +352,11 @@ template <int GROUPS>
 __global__ void __launch_bounds__(512) reduce_finalize_kernel(const float* __restrict__ partial,
                                                               const float* __restrict__ wdn, int fo, int n_chunks,
                                                               int T, int H, int G, int I, int I_pad,
-                                                              float* __restrict__ S_out, float* __restrict__ S_head_out) {
+                                                              float* __restrict__ S_out, float* __restrict__ S_head_out,
+                                                              const DevScales* __restrict__ sc, int D) {
+  // the partial sums carry the head operands' 2^2(e_m + e_a) (scales.cuh)
+  const ScaleExps ex = scale_exps(*sc, D);
+  const double fh = (double)pow2f(-(ex.e_m + ex.e_a));
   __shared__ double part[16][32][4];
   const int k0 = blockIdx.x * 128 + threadIdx.x * 4;
   const int g = blockIdx.y;
@@ -251,7 +384,7 @@ __global__ void __launch_bounds__(512) reduce_finalize_kernel(const float* __res
         if (k >= I) continue;
         double t = 0.0;
         for (int i = 0; i < 16; ++i) t += part[i][threadIdx.x][e];
-        const double v = t * ((fo ? (double)wdn[k] : 1.0) / (double)T);
+        const double v = t * fh * fh * ((fo ? (double)wdn[k] : 1.0) / (double)T);
         if (S_head_out) S_head_out[(size_t)h * I + k] = (float)v;
         total[e] += v;
       }
@@ -305,29 +438,37 @@ cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, 
 // ---------------------------------------------------------------- leave-one-out score
 // out = fp16 copy of n bf16 values (n % 8 == 0), 8 per thread.
 __global__ void to_fp16_kernel(const uint16_t* __restrict__ in, __half* __restrict__ out, size_t n,
-                               uint32_t* status) {
+                               uint32_t* status, const uint32_t* __restrict__ maxbits) {
+  const float f = maxbits ? pow2f(scale_exp_norm(bits_f(*maxbits))) : 1.f;
   bool bad = false;
   for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n / 8; v += (size_t)gridDim.x * blockDim.x) {
     uint4 q = *reinterpret_cast<const uint4*>(in + v * 8);
     const uint16_t* e = reinterpret_cast<const uint16_t*>(&q);
     __align__(16) __half o[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = to_h(bf2f(e[i]), bad);
+    for (int i = 0; i < 8; ++i) o[i] = to_h(bf2f(e[i]) * f, bad);
     *reinterpret_cast<uint4*>(out + v * 8) = *reinterpret_cast<uint4*>(o);
   }
   if (bad) latch_status(status, kStatusRange);
 }
 
-// rho[h][t] = r_t / rms(x_t - c_th), from the two column halves of
+// sigma[h][t] = 1 - rho with rho = r_t / rms(x_t - c_th), from the column groups of
 // CC = sum_d (c/r)^2 and XD = sum_d x (c/r):  since mean_d x^2 = r^2 - eps,
-//   rms(x - c)^2 / r^2 = 1 + (CC - 2 XD / r) / D.
-// Padding tokens (t >= T) get rho = 1; they carry no signal.
+//   rms(x - c)^2 / r^2 = 1 + q,  q = (CC - 2 XD / r) / D,
+// and 1 - rho = 1 - 1/s = q / (s (s + 1)) with s = sqrt(1 + q), a form without
+// cancellation when the head's write is small (rho near 1).  The leave-one-out
+// change is then formed as p.w + sigma (g - p.w).  Padding tokens (t >= T) get
+// sigma = 0; they carry no signal.
+// The c_h pass contracted a16 (a/r 2^e_a) with Wo16 (Wo 2^e_o): its sums carry
+// 2^(e_a + e_o) per factor of c/r, removed here.
 __global__ void loo_rho_kernel(const float* __restrict__ cn, const float* __restrict__ inv_r, float* __restrict__ rho,
-                               int T, int T_pad, int H, int D, int groups) {
+                               int T, int T_pad, int H, int D, int groups, const DevScales* __restrict__ sc) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   const int h = blockIdx.y;
   if (t >= T_pad) return;
-  float v = 1.0f;
+  const ScaleExps ex = scale_exps(*sc, D);
+  const float u = pow2f(-(ex.e_a + ex.e_o));
+  float v = 0.0f;
   if (t < T) {
     const size_t plane = (size_t)H * T_pad, at = (size_t)h * T_pad + t;
     float cc = 0.f, xd = 0.f;   // column groups in order: [group][quantity][H][T_pad]
@@ -336,8 +477,16 @@ __global__ void loo_rho_kernel(const float* __restrict__ cn, const float* __rest
       cc += cn[(size_t)(2 * g) * plane + at];
       xd += cn[(size_t)(2 * g + 1) * plane + at];
     }
-    const float q = 1.0f + (cc - 2.0f * xd * inv_r[t]) / (float)D;
-    v = rsqrtf(fmaxf(q, 1e-30f));
+    cc = cc * u * u;
+    xd = xd * u;
+    const float q = (cc - 2.0f * xd * inv_r[t]) / (float)D;
+    const float w = 1.0f + q;
+    if (w > 1e-30f) {
+      const float sq = sqrtf(w);
+      v = q / (sq * (sq + 1.0f));
+    } else {
+      v = 1.0f - rsqrtf(1e-30f);   // x - c_h vanishes: rho at its clamp
+    }
   }
   rho[(size_t)h * T_pad + t] = v;
 }
@@ -627,7 +776,7 @@ static inline int blocks_for(size_t n, int threads, int cap = 8192) {
 // until it drained, which serialised the two.
 cudaError_t launch_prep_tokens(const uint16_t* x, const uint16_t* a, const uint16_t* gamma, __half* n16, __half* a16,
                                float* inv_r, int T, int D, int HD, float eps, uint32_t* status, int sm_count,
-                               cudaStream_t s) {
+                               DevScales* sc, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(prep_tokens_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
@@ -635,20 +784,49 @@ cudaError_t launch_prep_tokens(const uint16_t* x, const uint16_t* a, const uint1
   const int want = (T + warps_per_block - 1) / warps_per_block;
   const int cap = 3 * (sm_count > 0 ? sm_count : 1);
   prep_tokens_kernel<<<want < cap ? want : cap, 32 * warps_per_block, 0, s>>>(x, a, gamma, n16, a16, inv_r, T, D,
-                                                                               HD, eps, status);
+                                                                               HD, eps, status, sc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_restage_a(const uint16_t* a, const float* inv_r, __half* a16, int T, int HD, const DevScales* sc,
+                             uint32_t* status, int sm_count, cudaStream_t s) {
+  restage_a_kernel<<<4 * (sm_count > 0 ? sm_count : 1), 256, 0, s>>>(a, inv_r, a16, T, HD, sc, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_weight_max(const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wo, const uint16_t* gamma,
+                              int I, int D, int HD, DevScales* sc, int sm_count, cudaStream_t s) {
+  MaxJobs J{};
+  J.p[0] = Wg; J.n8[0] = (size_t)I * D / 8; J.out[0] = &sc->wmax;
+  J.p[1] = Wu; J.n8[1] = (size_t)I * D / 8; J.out[1] = &sc->wmax;
+  int arrays = 2;
+  if (Wo) {
+    J.p[2] = Wo; J.n8[2] = (size_t)D * HD / 8; J.out[2] = &sc->womax;
+    J.p[3] = gamma; J.n8[3] = (size_t)D / 8; J.out[3] = &sc->gwmax;
+    arrays = 4;
+  }
+  // per array about 1024 words per block, at most two blocks per SM per array
+  int g = blocks_for(J.n8[0], 1024);
+  if (g > 2 * sm_count) g = 2 * (sm_count > 0 ? sm_count : 1);
+  max_abs_kernel<<<dim3(g, arrays), 256, 0, s>>>(J);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_weight_stage(const uint16_t* Wg, const uint16_t* Wu, __half* W16, int I, int I_pad, int D,
+                                const uint16_t* Wo, const uint16_t* gamma, __half* GWo16, int HD, uint32_t* status,
+                                const DevScales* sc, int sm_count, cudaStream_t s) {
+  int g0 = (2 * I_pad + 7) / 8;                          // one warp per W16 row
+  const int g1 = ((HD + 31) / 32) * ((D + 31) / 32);     // gamma*Wo^T tiles
+  if (g0 < g1) g0 = g1;
+  if (g0 > 4 * sm_count) g0 = 4 * (sm_count > 0 ? sm_count : 1);
+  weight_stage_kernel<<<dim3(g0, 2), 256, 0, s>>>(Wg, Wu, W16, I, I_pad, D, Wo, gamma, GWo16, HD, status, sc);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prep_gate_up(const uint16_t* Wg, const uint16_t* Wu, __half* W16, int I, int I_pad, int D,
-                                uint32_t* status, cudaStream_t s) {
-  prep_gate_up_kernel<<<blocks_for((size_t)2 * I_pad * D / 8, 256), 256, 0, s>>>(Wg, Wu, W16, I, I_pad, D, status);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_scaled_transpose_split(const uint16_t* W, const uint16_t* scale, __half* out, int Drows, int Ncols,
-                                          uint32_t* status, cudaStream_t s) {
-  dim3 grid((Ncols + 31) / 32, (Drows + 31) / 32), block(32, 8);
-  scaled_transpose_split_kernel<<<grid, block, 0, s>>>(W, scale, out, Drows, Ncols, status);
+                                uint32_t* status, const DevScales* sc, cudaStream_t s) {
+  prep_gate_up_kernel<<<blocks_for((size_t)2 * I_pad * D / 8, 256), 256, 0, s>>>(Wg, Wu, W16, I, I_pad, D, status,
+                                                                                 sc);
   return cudaGetLastError();
 }
 
@@ -677,17 +855,21 @@ cudaError_t launch_reduce_partials(const float* partial, double* out, int n_chun
 }
 
 cudaError_t launch_reduce_finalize(const float* partial, const float* wdn, int fo, int n_chunks, int groups, int T,
-                                   int H, int G, int I, int I_pad, float* S_out, float* S_head_out, cudaStream_t s) {
+                                   int H, int G, int I, int I_pad, float* S_out, float* S_head_out,
+                                   const DevScales* sc, int D, cudaStream_t s) {
   dim3 grid(I_pad / 128, G), block(32, 16);
   switch (groups) {
     case 1:
-      reduce_finalize_kernel<1><<<grid, block, 0, s>>>(partial, wdn, fo, n_chunks, T, H, G, I, I_pad, S_out, S_head_out);
+      reduce_finalize_kernel<1><<<grid, block, 0, s>>>(partial, wdn, fo, n_chunks, T, H, G, I, I_pad, S_out,
+                                                          S_head_out, sc, D);
       break;
     case 2:
-      reduce_finalize_kernel<2><<<grid, block, 0, s>>>(partial, wdn, fo, n_chunks, T, H, G, I, I_pad, S_out, S_head_out);
+      reduce_finalize_kernel<2><<<grid, block, 0, s>>>(partial, wdn, fo, n_chunks, T, H, G, I, I_pad, S_out,
+                                                          S_head_out, sc, D);
       break;
     case 4:
-      reduce_finalize_kernel<4><<<grid, block, 0, s>>>(partial, wdn, fo, n_chunks, T, H, G, I, I_pad, S_out, S_head_out);
+      reduce_finalize_kernel<4><<<grid, block, 0, s>>>(partial, wdn, fo, n_chunks, T, H, G, I, I_pad, S_out,
+                                                          S_head_out, sc, D);
       break;
     default:
       return cudaErrorInvalidValue;
@@ -702,15 +884,16 @@ cudaError_t launch_finalize_up(const double* sh, const float* wdn, int fo, int T
   return cudaGetLastError();
 }
 
-cudaError_t launch_to_fp16(const uint16_t* in, __half* out, size_t n, uint32_t* status, cudaStream_t s) {
+cudaError_t launch_to_fp16(const uint16_t* in, __half* out, size_t n, uint32_t* status, const uint32_t* maxbits,
+                           cudaStream_t s) {
   const size_t blocks = (n / 8 + 255) / 256;
-  to_fp16_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(in, out, n, status);
+  to_fp16_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(in, out, n, status, maxbits);
   return cudaGetLastError();
 }
 
 cudaError_t launch_loo_rho(const float* cn, const float* inv_r, float* rho, int T, int T_pad, int H, int D,
-                           int groups, cudaStream_t s) {
-  loo_rho_kernel<<<dim3((T_pad + 255) / 256, H), 256, 0, s>>>(cn, inv_r, rho, T, T_pad, H, D, groups);
+                           int groups, const DevScales* sc, cudaStream_t s) {
+  loo_rho_kernel<<<dim3((T_pad + 255) / 256, H), 256, 0, s>>>(cn, inv_r, rho, T, T_pad, H, D, groups, sc);
   return cudaGetLastError();
 }
 

@@ -5,27 +5,42 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "scales.cuh"
+
 namespace aff {
 
+// n16 = gamma x / r 2^e_n, a16 = a / r (max recorded in sc->amax), inv_r = 1 / r.
 cudaError_t launch_prep_tokens(const uint16_t* x, const uint16_t* a, const uint16_t* gamma, __half* n16, __half* a16,
                                float* inv_r, int T, int D, int HD, float eps, uint32_t* status, int sm_count,
-                               cudaStream_t s);
+                               DevScales* sc, cudaStream_t s);
+// a16 staged again as a / r 2^e_a when sc->amax calls for it (else returns at once).
+cudaError_t launch_restage_a(const uint16_t* a, const float* inv_r, __half* a16, int T, int HD, const DevScales* sc,
+                             uint32_t* status, int sm_count, cudaStream_t s);
+// The weight maxima of DevScales (Wg/Wu; gamma*Wo column sums and maxima when Wo is given).
+cudaError_t launch_weight_max(const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wo, const uint16_t* gamma,
+                              int I, int D, int HD, DevScales* sc, int sm_count, cudaStream_t s);
+// W16 (as launch_prep_gate_up) and gamma*Wo^T hi / lo ([HD][2][D], 2^e_g) in one launch.
+cudaError_t launch_weight_stage(const uint16_t* Wg, const uint16_t* Wu, __half* W16, int I, int I_pad, int D,
+                                const uint16_t* Wo, const uint16_t* gamma, __half* GWo16, int HD, uint32_t* status,
+                                const DevScales* sc, int sm_count, cudaStream_t s);
 cudaError_t launch_prep_gate_up(const uint16_t* Wg, const uint16_t* Wu, __half* W16, int I, int I_pad, int D,
-                                uint32_t* status, cudaStream_t s);
-cudaError_t launch_scaled_transpose_split(const uint16_t* W, const uint16_t* scale, __half* out, int Drows, int Ncols,
-                                          uint32_t* status, cudaStream_t s);
+                                uint32_t* status, const DevScales* sc, cudaStream_t s);
 cudaError_t launch_wd_colnorm(const uint16_t* Wd, float* wdn, int D, int I, int I_pad, cudaStream_t s);
 cudaError_t launch_wd_colnorm_f32(const float* Wd, float* wdn, int D, int I, cudaStream_t s);
 cudaError_t launch_reduce_partials(const float* partial, double* out, int n_chunks, int halves, int H, int I_pad,
                                    cudaStream_t s);
+// The partial sums carry the head operands' 2^2(e_m + e_a) (scales.cuh), removed here.
 cudaError_t launch_reduce_finalize(const float* partial, const float* wdn, int fo, int n_chunks, int groups, int T,
-                                   int H, int G, int I, int I_pad, float* S_out, float* S_head_out, cudaStream_t s);
+                                   int H, int G, int I, int I_pad, float* S_out, float* S_head_out,
+                                   const DevScales* sc, int D, cudaStream_t s);
 cudaError_t launch_finalize_up(const double* sh, const float* wdn, int fo, int T, int H, int G, int I, int I_pad,
                                float* S_out, float* S_head_out, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, cudaStream_t s);
-cudaError_t launch_to_fp16(const uint16_t* in, __half* out, size_t n, uint32_t* status, cudaStream_t s);
+// fp16 copy, times 2^e from the maximum at maxbits (fp32 bits) when given.
+cudaError_t launch_to_fp16(const uint16_t* in, __half* out, size_t n, uint32_t* status, const uint32_t* maxbits,
+                           cudaStream_t s);
 cudaError_t launch_loo_rho(const float* cn, const float* inv_r, float* rho, int T, int T_pad, int H, int D,
-                           int groups, cudaStream_t s);
+                           int groups, const DevScales* sc, cudaStream_t s);
 cudaError_t launch_prep_wd(const uint16_t* Wd, __half* Wd16, __half* WdT16, int D, int I, int I_pad, uint32_t* status,
                            cudaStream_t s);
 cudaError_t launch_prep_qkv(const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* gamma_next,

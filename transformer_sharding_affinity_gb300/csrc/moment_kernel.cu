@@ -4,6 +4,7 @@
 // quadratic-form pass over the folded rows.  Paper: "Affinity-Aware Sharding
 // for Delayed Tensor Parallelism", §3 "Affinity scores" (the ADD score).
 #include "moment_kernel.cuh"
+#include "scales.cuh"
 #include "sm103_primitives.cuh"
 
 namespace aff {
@@ -57,28 +58,63 @@ __global__ void __launch_bounds__(256) inv_r_kernel(const uint16_t* __restrict__
 // an upper bound on max_i C_h[i][i], so |C_h[n][i]| <= sqrt(C_ii C_nn) <= s_h.
 // Each entry is summed in chunk order and C_h / s_h is split into an fp16 high
 // part and the fp16 rounding of the remainder.
+//
+// The Gram pass staged a/r in fp16 unscaled.  If any head's s_h is not finite
+// (an operand overflowed fp16) or every head's s_h is below T 2^-16 (a/r so
+// small that fp16 subnormals would cost precision), the matrices are instead
+// recomputed with a power-of-two scale by moment_fallback_kernel: this kernel
+// then records that decision, adds its share of max |a/r| over all tokens to
+// sc->amax2, and writes nothing else.
 constexpr int kReduceRows = 4;
 
 __global__ void __launch_bounds__(256) gram_reduce_kernel(const float* __restrict__ gram,
                                                           const float* __restrict__ cmax, __half* __restrict__ CC,
                                                           float* __restrict__ scale, int n_chunks, int H, int dh,
-                                                          uint32_t* status) {
+                                                          uint32_t* status, const uint16_t* __restrict__ a,
+                                                          const float* __restrict__ inv_r, int T, DevScales* sc) {
   __shared__ float s_sh;
+  __shared__ int redo_s;
+  __shared__ uint32_t top_s;
   const int h = blockIdx.x, y = blockIdx.y;
   const size_t cstride = (size_t)H * 128 * 128;
   const float* g0 = gram + (size_t)h * 128 * 128;
+  if (threadIdx.x == 0) top_s = 0u;
+  __syncthreads();
+  // every head's s_h (a thread per head, chunks in order): any not finite, and the largest
+  bool nonfinite = false;
+  float top = 0.f;
+  for (int hh = threadIdx.x; hh < H; hh += 256) {
+    float m = 0.f;
+    for (int c = 0; c < n_chunks; ++c) m += cmax[(size_t)c * H + hh];
+    if (isfinite(m)) top = fmaxf(top, m);
+    else nonfinite = true;
+  }
+  atomicMax(&top_s, __float_as_uint(top));   // top >= 0: bit patterns order like the values
+  const int any_nonfinite = __syncthreads_or(nonfinite ? 1 : 0);
   if (threadIdx.x == 0) {
+    redo_s = (any_nonfinite || __uint_as_float(top_s) < (float)T * (1.0f / 65536.0f)) ? 1 : 0;
     float m = 0.f;
     for (int c = 0; c < n_chunks; ++c) m += cmax[(size_t)c * H + h];
-    if (!isfinite(m)) {
-      latch_status(status, kStatusRange);
-      m = 1.f;
-    }
-    if (!(m > 0.f)) m = 1.f;
+    if (!(m > 0.f) || !isfinite(m)) m = 1.f;
     s_sh = m;
-    if (y == 0) scale[h] = m;
+    if (h == 0 && y == 0) sc->redo = (uint32_t)redo_s;
+    if (!redo_s && y == 0) scale[h] = m;
   }
   __syncthreads();
+  if (redo_s) {
+    // this block's share of max |a/r| over every token (HD = H dh columns)
+    const int HD = H * dh;
+    const size_t n = (size_t)T * HD;
+    const size_t nb = (size_t)gridDim.x * gridDim.y, b = (size_t)y * gridDim.x + h;
+    uint32_t am = 0u;
+    for (size_t e = b * 256 + threadIdx.x; e < n; e += nb * 256) {
+      const float v = bf2f_m(a[e]) * inv_r[e / HD];
+      am = max(am, __float_as_uint(fabsf(v)));
+    }
+    am = __reduce_max_sync(0xffffffffu, am);
+    if ((threadIdx.x & 31) == 0 && am) atomicMax(&sc->amax2, am);
+    return;
+  }
   const float s = s_sh;
   for (int e = threadIdx.x; e < kReduceRows * 128; e += 256) {
     const int n = y * kReduceRows + (e >> 7), i = e & 127;
@@ -96,16 +132,81 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float* __restric
   }
 }
 
+// The Gram matrices recomputed with a scale, when gram_reduce_kernel asked for it
+// (otherwise every block returns at once).  One block per head: a~ = a/r 2^e,
+// e from sc->amax2 (a non-finite maximum latches AFF_ERR_RANGE), tokens in order
+// through shared memory in tiles of 32, C_h in fp32 on the CUDA cores; then
+// s = max_i C_h[i][i], CC = [hi; lo] of C_h / s and scale[h] = s 2^-2e, the
+// same outputs as gram_reduce_kernel.  Slow (about a millisecond per head) but
+// only taken for inputs outside fp16's range.
+constexpr int kFbTile = 32;
+
+__global__ void __launch_bounds__(1024) moment_fallback_kernel(const uint16_t* __restrict__ a,
+                                                              const float* __restrict__ inv_r, int T, int H, int dh,
+                                                              __half* __restrict__ CC, float* __restrict__ scale,
+                                                              const DevScales* __restrict__ sc, uint32_t* status) {
+  if (sc->redo == 0u) return;
+  const float am = bits_f(sc->amax2);
+  if (!(am <= 3.4e38f)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) latch_status(status, kStatusRange);
+    return;
+  }
+  const int e = scale_exp_norm(am);
+  const float f = pow2f(e);
+  const int h = blockIdx.x, HD = H * dh;
+  __shared__ float tile[kFbTile][128];
+  __shared__ float dmax_s;
+  const int i = threadIdx.x >> 3, j0 = (threadIdx.x & 7) * 16;   // row i, columns j0 .. j0+15
+  float acc[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+  for (int t0 = 0; t0 < T; t0 += kFbTile) {
+    __syncthreads();
+    for (int v = threadIdx.x; v < kFbTile * 128; v += 1024) {
+      const int tt = v >> 7, c = v & 127, t = t0 + tt;
+      tile[tt][c] = (t < T && c < dh) ? bf2f_m(a[(size_t)t * HD + (size_t)h * dh + c]) * inv_r[t] * f : 0.f;
+    }
+    __syncthreads();
+    if (i < dh) {
+#pragma unroll 4
+      for (int tt = 0; tt < kFbTile; ++tt) {
+        const float ai = tile[tt][i];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) acc[q] = fmaf(ai, tile[tt][j0 + q], acc[q]);
+      }
+    }
+  }
+  if (threadIdx.x == 0) dmax_s = 0.f;
+  __syncthreads();
+  if (i < dh && i >= j0 && i < j0 + 16) atomicMax(reinterpret_cast<unsigned int*>(&dmax_s), __float_as_uint(acc[i - j0]));
+  __syncthreads();
+  float s = dmax_s;
+  if (!(s > 0.f) || !isfinite(s)) s = 1.f;
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int j = j0 + q;
+    const float v = (i < dh && j < dh) ? acc[q] / s : 0.f;
+    const __half hi = __float2half_rn(v);
+    const __half lo = __float2half_rn(v - __half2float(hi));
+    CC[((size_t)h * 128 + i) * 128 + j] = hi;
+    CC[((size_t)(H + h) * 128 + i) * 128 + j] = lo;
+  }
+  if (threadIdx.x == 0) scale[h] = s * pow2f(-e) * pow2f(-e);
+}
+
 // ---------------------------------------------------------------- finishing
 // S_head[h][k] = out[h][k] / T; S_up[g][k] = the sum of S_head over g's heads in
 // head order (fp64).  One thread per (group, neuron).
+// The folded rows were staged times 2^e_m, so the quadratic forms carry 2^2e_m.
 __global__ void __launch_bounds__(256) moment_finalize_kernel(const float* __restrict__ out, int T, int H, int G,
                                                               int I, int I_pad, float* __restrict__ S_out,
-                                                              float* __restrict__ S_head_out) {
+                                                              float* __restrict__ S_head_out,
+                                                              const DevScales* __restrict__ sc, int D) {
   const int k = blockIdx.x * 256 + threadIdx.x, g = blockIdx.y;
   if (k >= I) return;
   const int hpg = H / G;
-  const double invT = 1.0 / (double)T;
+  const double fm = (double)pow2f(-scale_exps(*sc, D).e_m);
+  const double invT = fm * fm / (double)T;
   double total = 0.0;
   for (int h = g * hpg; h < (g + 1) * hpg; ++h) {
     const double v = (double)out[(size_t)h * I_pad + k] * invT;
@@ -443,14 +544,18 @@ cudaError_t launch_inv_r(const uint16_t* x, float* inv_r, int T, int n_pad, int 
 }
 
 cudaError_t launch_gram_reduce(const float* gram, const float* cmax, __half* CC, float* scale, int n_chunks, int H,
-                               int dh, uint32_t* status, cudaStream_t s) {
-  gram_reduce_kernel<<<dim3(H, 128 / kReduceRows), 256, 0, s>>>(gram, cmax, CC, scale, n_chunks, H, dh, status);
+                               int dh, uint32_t* status, const uint16_t* a, const float* inv_r, int T, DevScales* sc,
+                               cudaStream_t s) {
+  gram_reduce_kernel<<<dim3(H, 128 / kReduceRows), 256, 0, s>>>(gram, cmax, CC, scale, n_chunks, H, dh, status, a,
+                                                                  inv_r, T, sc);
+  if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
+  moment_fallback_kernel<<<H, 1024, 0, s>>>(a, inv_r, T, H, dh, CC, scale, sc, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_moment_finalize(const float* out, int T, int H, int G, int I, int I_pad, float* S_out,
-                                   float* S_head_out, cudaStream_t s) {
-  moment_finalize_kernel<<<dim3((I + 255) / 256, G), 256, 0, s>>>(out, T, H, G, I, I_pad, S_out, S_head_out);
+                                   float* S_head_out, const DevScales* sc, int D, cudaStream_t s) {
+  moment_finalize_kernel<<<dim3((I + 255) / 256, G), 256, 0, s>>>(out, T, H, G, I, I_pad, S_out, S_head_out, sc, D);
   return cudaGetLastError();
 }
 

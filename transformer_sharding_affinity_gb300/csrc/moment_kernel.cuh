@@ -16,6 +16,8 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "scales.cuh"
+
 namespace aff {
 
 enum MomentMode : int {
@@ -75,11 +77,16 @@ cudaError_t launch_inv_r(const uint16_t* x, float* inv_r, int T, int n_pad, int 
 // C_h = sum over chunks of the Gram partials (in chunk order); s_h = the sum over
 // chunks of their largest diagonal entries (>= max_i C_h[i][i]; 1 when not
 // positive); CC = [hi; lo] fp16 parts of C_h / s_h: [2][H][128][128], zero
-// outside d_head x d_head.
+// outside d_head x d_head.  When the unscaled fp16 Gram pass overflowed or lost
+// its operands to fp16 subnormals, a second kernel recomputes C_h with a
+// power-of-two scale instead (and scale[h] removes it); it returns at once
+// otherwise.
 cudaError_t launch_gram_reduce(const float* gram, const float* cmax, __half* CC, float* scale, int n_chunks, int H,
-                               int dh, uint32_t* status, cudaStream_t s);
-// S_head[h][k] = out[h][k] / T, S_up[g][k] = sum of S_head over g's heads (fp64, head order).
+                               int dh, uint32_t* status, const uint16_t* a, const float* inv_r, int T, DevScales* sc,
+                               cudaStream_t s);
+// S_head[h][k] = out[h][k] / T (the folded rows' 2^2e_m removed), S_up[g][k] = sum of
+// S_head over g's heads (fp64, head order).
 cudaError_t launch_moment_finalize(const float* out, int T, int H, int G, int I, int I_pad, float* S_out,
-                                   float* S_head_out, cudaStream_t s);
+                                   float* S_head_out, const DevScales* sc, int D, cudaStream_t s);
 
 }  // namespace aff

@@ -246,6 +246,13 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_slot;
+  // Powers of two that undo the operand scales (see scales.cuh): g, u come out of
+  // the gate/up job times 2^(e_n + e_w), head-job values times 2^(e_m + e_a), the
+  // fold's accumulator times 2^(e_w + e_g).
+  // The head-job sums keep their 2^2(e_m + e_a); reduce_finalize removes it.
+  const ScaleExps ex = scale_exps(*p.sc, p.D);
+  const float f_gu = pow2f(-(ex.e_n + ex.e_w));   // -> g, u
+  const float f_up = pow2f(ex.e_m + ex.e_a);      // LOO: g, u onto the head jobs' scale
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -443,7 +450,7 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
       JobIter jt{0, 0};
       for (int j = 0; j < U.njobs; ++j, b ^= 1, tph ^= (uint32_t)(b == 0)) {
         const Job J = job_next<MODE, STREAM>(p, U, jt);
-        // LOO head job: lanes 0..15 fetch rho of the column group's CWW tokens (one float4
+        // LOO head job: lanes 0..15 fetch sigma of the column group's CWW tokens (one float4
         // each) before the accumulator wait, which hides the load; the token loop takes
         // its values from them with shuffles
         float4 rho_v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -480,6 +487,17 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
               for (int i = 0; i < 8; i += 2) {
                 abA[(c * 8 + i) / 2] = pk_u(gr[i], gr[i + 1]);
                 abB[(c * 8 + i) / 2] = pk_u(ur[i], ur[i + 1]);
+              }
+            }
+            {
+              // FO: the accumulators' 2^(e_n + e_w) removed (g, u exact);  LOO: g, u onto the scale
+              // of the head jobs' p_h.w, at which g - g^(-h) is formed
+              const float fs = MODE == kModeLOO ? f_gu * f_up : f_gu;
+              const uint64_t fl = pk(fs, fs);
+#pragma unroll
+              for (int i = 0; i < CW / 2; ++i) {
+                abA[i] = mul2(abA[i], fl);
+                abB[i] = mul2(abB[i], fl);
               }
             }
             // Phase 2 (FO): (g, u) -> (A', B') = (silu'(g) u, silu(g)) in place; LOO keeps g and u.
@@ -524,9 +542,9 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
                 float a2[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                  const float g = __uint_as_float(gr[i + e]);
+                  const float g = __uint_as_float(gr[i + e]) * f_gu;
                   const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
-                  a2[e] = g * sg * __uint_as_float(ur[i + e]);
+                  a2[e] = g * sg * (__uint_as_float(ur[i + e]) * f_gu);
                 }
                 hv[i / 2] = pack_h2(a2[0], a2[1]);
               }
@@ -539,8 +557,8 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
         }
         if constexpr (kHeads) {
           // kJobHead.  FO: Delta = A' pg + B' pu per token, Delta^2 summed over the thread's CW
-          // tokens; LOO: g - g^(-h) = g + rho (pg - g) with rho = r / rms(x - c_h), likewise
-          // for u, both squared; ADD: each lane sums the squares of its own 2 CW values.
+          // tokens; LOO: g - g^(-h) = pg + sigma (g - pg) with sigma = 1 - r / rms(x - c_h),
+          // likewise for u, both squared; ADD: each lane sums the squares of its own 2 CW values.
           const uint32_t col = (uint32_t)(b * 2 * kBlockN + hf * CWW);
           uint64_t acc = pk(0.f, 0.f);
           if constexpr (MODE == kModeADD) {
@@ -583,9 +601,9 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
               __syncwarp();
               if (lane == 0) mbar_arrive(&sm.tempty[b]);
             }
-            float4 rq = make_float4(0.f, 0.f, 0.f, 0.f);   // LOO: rho of the slice's 4 tokens
+            float4 rq = make_float4(0.f, 0.f, 0.f, 0.f);   // LOO: sigma of the slice's 4 tokens
             if constexpr (MODE == kModeLOO) {
-              static_assert(kW == 4, "one float4 of rho per slice");
+              static_assert(kW == 4, "one float4 of sigma per slice");
               const int src = (upl ? CW / 4 : 0) + c;
               rq.x = __shfl_sync(0xffffffffu, rho_v.x, src);
               rq.y = __shfl_sync(0xffffffffu, rho_v.y, src);
@@ -601,10 +619,10 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
                 uint64_t d = mul2(abA[ai], vg);
                 d = fma2(abB[ai], vu, d);
                 acc = fma2(d, d, acc);
-              } else {   // LOO
+              } else {   // LOO: g - g^(-h) = p.w + sigma (g - p.w), sigma = 1 - rho
                 const uint64_t rr = i == 0 ? pk(rq.x, rq.y) : pk(rq.z, rq.w), neg1 = pk(-1.0f, -1.0f);
-                const uint64_t dg = fma2(rr, fma2(abA[ai], neg1, vg), abA[ai]);
-                const uint64_t du = fma2(rr, fma2(abB[ai], neg1, vu), abB[ai]);
+                const uint64_t dg = fma2(rr, fma2(vg, neg1, abA[ai]), vg);
+                const uint64_t du = fma2(rr, fma2(vu, neg1, abB[ai]), vu);
                 acc = fma2(dg, dg, acc);
                 acc = fma2(du, du, acc);
               }
@@ -612,13 +630,15 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
           }
           }
           const float2 s2 = unpk(acc);
-          sm.sacc[(hf * p.H + J.head) * kBlockM + row] += s2.x + s2.y;
+          sm.sacc[(hf * p.H + J.head) * kBlockM + row] += s2.x + s2.y;   // times 2^2(e_m + e_a)
         }
         static_assert(EW == kWideEpiWarps || CW == 64, "the 8-warp epilogues read 64 columns per thread");
 
         if constexpr (MODE == kModeFold) {
-          // D1 = Mg[k][n], D2 = Mu[k][n] for neuron k = kt*128 + row, columns n = nt*128 + hf*64 + ...
+          // D1 = Mg[k][n], D2 = Mu[k][n] for neuron k = kt*128 + row, columns n = nt*128 + hf*64 + ...,
+          // times 2^(e_w + e_g) from the operands; stored times 2^e_m
           const int kk = J.kt * kBlockM + row;
+          const float fm1 = pow2f(ex.e_m), fm2 = pow2f(-(ex.e_w + ex.e_g));
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t mg[16], mu[16];
@@ -636,14 +656,20 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
               if (n < p.H * p.dh) {
                 const int h = n / p.dh, jj = n % p.dh;
                 uint4 vg, vu;
-                vg.x = pack_h2(__uint_as_float(mg[i + 0]), __uint_as_float(mg[i + 1]));
-                vg.y = pack_h2(__uint_as_float(mg[i + 2]), __uint_as_float(mg[i + 3]));
-                vg.z = pack_h2(__uint_as_float(mg[i + 4]), __uint_as_float(mg[i + 5]));
-                vg.w = pack_h2(__uint_as_float(mg[i + 6]), __uint_as_float(mg[i + 7]));
-                vu.x = pack_h2(__uint_as_float(mu[i + 0]), __uint_as_float(mu[i + 1]));
-                vu.y = pack_h2(__uint_as_float(mu[i + 2]), __uint_as_float(mu[i + 3]));
-                vu.z = pack_h2(__uint_as_float(mu[i + 4]), __uint_as_float(mu[i + 5]));
-                vu.w = pack_h2(__uint_as_float(mu[i + 6]), __uint_as_float(mu[i + 7]));
+                float fg[8], fu[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  fg[e] = __uint_as_float(mg[i + e]) * fm1 * fm2;
+                  fu[e] = __uint_as_float(mu[i + e]) * fm1 * fm2;
+                }
+                vg.x = pack_h2(fg[0], fg[1]);
+                vg.y = pack_h2(fg[2], fg[3]);
+                vg.z = pack_h2(fg[4], fg[5]);
+                vg.w = pack_h2(fg[6], fg[7]);
+                vu.x = pack_h2(fu[0], fu[1]);
+                vu.y = pack_h2(fu[2], fu[3]);
+                vu.z = pack_h2(fu[4], fu[5]);
+                vu.w = pack_h2(fu[6], fu[7]);
                 // rows in groups of 16 neurons: 16 gate rows, then their 16 up rows
                 const size_t rg = (size_t)(kk >> 4) * 32 + (kk & 15), ru = rg + 16;
                 if (p.stream_heads) {   // [2 I_pad][H*dh]: heads back to back along K

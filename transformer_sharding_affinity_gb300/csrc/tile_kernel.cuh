@@ -5,6 +5,8 @@
 #include <cuda_fp16.h>
 #include <cstdint>
 
+#include "scales.cuh"
+
 namespace aff {
 
 // A job of the tile kernel stages, per K block of 64 fp16 elements (128-byte
@@ -70,7 +72,8 @@ struct TileParams {
   const uint16_t* x_bf16;  // x' epilogue reads x (bf16 bits) [T][D]
   float* inv_rp2;          // x' output 1/r'^2 [T_pad]
   float* bnorm;            // qnorm output [I_pad][G]
-  const float* rho;        // LOO: r / rms(x - c_h), [H][T_pad]
+  const float* rho;        // LOO: sigma = 1 - r / rms(x - c_h), [H][T_pad]
+  const DevScales* sc;     // maxima that fix the power-of-two scales of the fp16 operands
   float eps;
 };
 

@@ -293,18 +293,6 @@ int pick_stages(int mode, int H) {
 // Heads whose width is a multiple of 16 but not of 64 (e.g. 96) leave the last
 // 64-wide K block of every head job partly empty.  Streaming all heads' K
 // ranges back to back fills every block; AFFINITY_STREAM_HEADS=0 turns it off.
-// CTAs of the fold when it runs beside the second-moment ADD passes: each fold CTA
-// holds a whole SM's tensor memory, so a smaller fold grid leaves SMs to the
-// HBM-bound Gram pass (3/4 of the SMs measured best).  AFFINITY_FOLD_CTAS
-// overrides (0 = one per SM).
-int moment_fold_ctas(int sm_count) {
-  static const int n = [] {
-    const char* e = std::getenv("AFFINITY_FOLD_CTAS");
-    return e ? std::atoi(e) : -1;
-  }();
-  return n >= 0 ? n : sm_count * 3 / 4;
-}
-
 bool stream_heads(const aff_dims& d) {
   static const bool allowed = [] {
     const char* e = std::getenv("AFFINITY_STREAM_HEADS");
@@ -526,19 +514,26 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   const cudaStream_t ws2 = side->stream;
   AFF_CUDA(cudaEventRecord(side->fork, s));
   AFF_CUDA(cudaStreamWaitEvent(ws2, side->fork, 0));
-  AFF_CUDA(launch_weight_max((const uint16_t*)Wg, (const uint16_t*)Wu, (const uint16_t*)Wo, g_b, I, D, H * dh, sc,
-                             sm_count, ws2));
-  AFF_CUDA(launch_weight_stage((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, (const uint16_t*)Wo, g_b,
-                               GWo16, H * dh, status, sc, sm_count, ws2));
-  __half* Wo16 = loo ? reinterpret_cast<__half*>(ws + L.Wo16) : nullptr;
+  // ADD in the second-moment form: the weight side and the fold run on the caller's stream
+  // with the whole GPU while 1/r is computed beside them, and the Gram pass follows.  The
+  // fold and the Gram pass each want every SM (shared memory keeps their CTAs apart), so
+  // they are faster one after the other than side by side.  Otherwise the weight side runs
+  // on the side stream beside the token staging.
   const bool moment = moment_form(d, mode);
-  float* inv_r = moment ? nullptr : reinterpret_cast<float*>(ws + L.inv_r);
-  if (loo) AFF_CUDA(launch_to_fp16((const uint16_t*)Wo, Wo16, (size_t)D * H * dh, status, &sc->womax, ws2));
-  // token side on the caller's stream meanwhile
+  const cudaStream_t wst = moment ? s : ws2;
   float* ir_m = moment ? reinterpret_cast<float*>(ws + L.ir) : nullptr;
-  if (moment) {
-    AFF_CUDA(launch_inv_r(x_b, ir_m, T, gram_split(T, H).nkb * 64, D, d.eps, sm_count, s));
-  } else {
+  if (moment) AFF_CUDA(launch_inv_r(x_b, ir_m, T, gram_split(T, H).nkb * 64, D, d.eps, sm_count, ws2));
+  // weights staged unscaled with their maxima recorded, then staged again only if a
+  // maximum lies outside fp16's comfortable range (scales.cuh)
+  AFF_CUDA(launch_weight_stage((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, (const uint16_t*)Wo, g_b,
+                               GWo16, H * dh, sc, sm_count, wst));
+  __half* Wo16 = loo ? reinterpret_cast<__half*>(ws + L.Wo16) : nullptr;
+  float* inv_r = moment ? nullptr : reinterpret_cast<float*>(ws + L.inv_r);
+  if (loo) AFF_CUDA(launch_to_fp16((const uint16_t*)Wo, Wo16, (size_t)D * H * dh, status, wst));
+  AFF_CUDA(launch_weight_restage((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, (const uint16_t*)Wo, g_b,
+                                 GWo16, Wo16, H * dh, sc, status, sm_count, wst));
+  // token side on the caller's stream meanwhile
+  if (!moment) {
     AFF_CUDA(launch_prep_tokens(x_b, a_b, g_b, (fo || loo) ? n16 : nullptr, a16, inv_r, T, D, H * dh, d.eps, status,
                                 sm_count, sc, s));
     AFF_CUDA(launch_restage_a(a_b, inv_r, a16, T, H * dh, sc, status, sm_count, s));
@@ -557,13 +552,14 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     p.n_ntiles = (int)ceil_div((int64_t)H * dh, 128);
     p.n_units = p.n_ktiles * p.n_ntiles;
     p.M16 = M16;
-    if ((st = run_tile(maps, p, ws2, false, moment_form(d, mode) ? moment_fold_ctas(sm_count) : 0)) != AFF_OK) return st;
+    if ((st = run_tile(maps, p, wst)) != AFF_OK) return st;
   }
   AFF_CUDA(cudaEventRecord(side->join, ws2));
   if (moment) {
     // ADD, second-moment form: C_h over the tokens while the fold runs beside it,
     // then m^T C_h m for every folded row, then the group sums
     const GramSplit gs = gram_split(T, H);
+    AFF_CUDA(cudaStreamWaitEvent(s, side->join, 0));   // 1/r
     float* gram = reinterpret_cast<float*>(ws + L.gram);
     float* cmax = reinterpret_cast<float*>(ws + L.cmax);
     __half* CC = reinterpret_cast<__half*>(ws + L.CC);
@@ -731,8 +727,9 @@ aff_status affinity_down(const void* x, const void* gamma, const void* Wg, const
   AFF_CUDA(cudaMemsetAsync(sc, 0, sizeof(DevScales), s));
   AFF_CUDA(cudaEventRecord(side->fork, s));
   AFF_CUDA(cudaStreamWaitEvent(ws2, side->fork, 0));
-  AFF_CUDA(launch_weight_max((const uint16_t*)Wg, (const uint16_t*)Wu, nullptr, nullptr, I, D, 0, sc, sm_count, ws2));
-  AFF_CUDA(launch_prep_gate_up((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, status, sc, ws2));
+  AFF_CUDA(launch_prep_gate_up((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, sc, ws2));
+  AFF_CUDA(launch_weight_restage((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, nullptr, nullptr, nullptr,
+                                 nullptr, 0, sc, status, sm_count, ws2));
   AFF_CUDA(launch_prep_wd((const uint16_t*)Wd, Wd16, WdT16, D, I, I_pad, status, ws2));
   AFF_CUDA(launch_prep_qkv((const uint16_t*)Wq_next, (const uint16_t*)Wk_next, (const uint16_t*)Wv_next,
                            (const uint16_t*)gamma_next, Wqkv16, G, H / G, dh, D, status, ws2));

@@ -18,6 +18,12 @@ __device__ __forceinline__ __half to_h(float v, bool& bad) {
   return __float2half_rn(v);
 }
 
+// fp16 of v, its magnitude folded into m (fp32 bits) for the staging maxima.
+__device__ __forceinline__ __half to_h_max(float v, uint32_t& m) {
+  m = max(m, __float_as_uint(fabsf(v)));
+  return __float2half_rn(v);
+}
+
 // ---------------------------------------------------------------- token rows
 // One warp per token: r_t = sqrt(mean_d x_td^2 + eps); n16 = gamma*x/r (the
 // FFN's normalised input) times 2^e_n and a16 = a/r (so that the head
@@ -127,134 +133,149 @@ __global__ void restage_a_kernel(const uint16_t* __restrict__ a, const float* __
   }
 }
 
-// Largest |value| of up to four bf16 arrays (each n_i % 8 == 0) into out_i (fp32
-// bits, atomicMax).  blockIdx.y picks the array; its blocks grid-stride over it
-// with four 16-byte loads in flight per thread.
-struct MaxJobs {
-  const uint16_t* p[4];
-  size_t n8[4];     // 8-element words of each array (0 = unused)
-  uint32_t* out[4];
-};
-
-__device__ __forceinline__ uint32_t max_abs8(const uint4& q) {
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-  uint32_t mm = 0u;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) mm = max(mm, max((w[i] & 0x7FFFu) << 16, w[i] & 0x7FFF0000u));
-  return mm;
-}
-
-__global__ void max_abs_kernel(const __grid_constant__ MaxJobs J) {
-  const int k = blockIdx.y;
-  const uint16_t* __restrict__ p = k == 0 ? J.p[0] : k == 1 ? J.p[1] : k == 2 ? J.p[2] : J.p[3];
-  const size_t n8 = k == 0 ? J.n8[0] : k == 1 ? J.n8[1] : k == 2 ? J.n8[2] : J.n8[3];
-  uint32_t* out = k == 0 ? J.out[0] : k == 1 ? J.out[1] : k == 2 ? J.out[2] : J.out[3];
-  const uint4* q = reinterpret_cast<const uint4*>(p);
-  const size_t stride = (size_t)gridDim.x * blockDim.x;
-  uint32_t m = 0u;
-  size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
-  for (; v + 3 * stride < n8; v += 4 * stride) {
-    const uint4 a0 = __ldg(q + v), a1 = __ldg(q + v + stride), a2 = __ldg(q + v + 2 * stride),
-                a3 = __ldg(q + v + 3 * stride);
-    m = max(m, max(max(max_abs8(a0), max_abs8(a1)), max(max_abs8(a2), max_abs8(a3))));
-  }
-  for (; v < n8; v += stride) m = max(m, max_abs8(__ldg(q + v)));
-  m = __reduce_max_sync(0xffffffffu, m);
-  if ((threadIdx.x & 31) == 0 && m && out) atomicMax(out, m);
-}
-
-// W16 = fp16 copy of Wg and Wu times 2^e_w, I_pad neurons (zero rows past I), in
-// groups of 16 neurons: their 16 gate rows, then their 16 up rows
-// ([I_pad / 16][2][16][D]).
-__global__ void prep_gate_up_kernel(const uint16_t* __restrict__ Wg, const uint16_t* __restrict__ Wu,
-                                    __half* __restrict__ W16, int I, int I_pad, int D, uint32_t* status,
-                                    const DevScales* __restrict__ sc) {
-  const size_t n8 = (size_t)2 * I_pad * D / 8;
-  const float f = pow2f(scale_exp_norm(bits_f(sc->wmax)));   // W16 = W 2^e_w
-  bool bad = false;
-  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8; v += (size_t)gridDim.x * blockDim.x) {
-    const size_t e0 = v * 8;
-    const int r = (int)(e0 / D), d = (int)(e0 % D);
+// W16 = fp16 copy of Wg and Wu, I_pad neurons (zero rows past I), in groups of 16
+// neurons: their 16 gate rows, then their 16 up rows ([I_pad / 16][2][16][D]).
+// One warp per row, staged unscaled while the largest magnitude is recorded in
+// sc->wmax; weight_restage_kernel rescales when that maximum calls for it.
+__device__ __forceinline__ void stage_w16_rows(const uint16_t* __restrict__ Wg, const uint16_t* __restrict__ Wu,
+                                               __half* __restrict__ W16, int I, int I_pad, int D, int warp0,
+                                               int nwarps, float f, uint32_t& m) {
+  const int lane = threadIdx.x & 31;
+  const int D8 = D / 8;
+  for (int r = warp0; r < 2 * I_pad; r += nwarps) {
     // row r: neuron group r / 32, gate (0) or up (1) row, neuron 16 * (r / 32) + r % 16
     const int blk = (r >> 4) & 1, k = (r >> 5) * 16 + (r & 15);
-    __align__(16) __half o[8];
-    if (k < I) {
-      const uint16_t* src = (blk == 0 ? Wg : Wu) + (size_t)k * D + d;
-      uint4 q = *reinterpret_cast<const uint4*>(src);
-      const uint16_t* e = reinterpret_cast<const uint16_t*>(&q);
+    const uint4* src = reinterpret_cast<const uint4*>((blk == 0 ? Wg : Wu) + (size_t)k * D);
+    uint4* dst = reinterpret_cast<uint4*>(W16 + (size_t)r * D);
+    for (int c = lane; c < D8; c += 32) {
+      __align__(16) __half o[8];
+      if (k < I) {
+        const uint4 q = __ldg(src + c);
+        const uint16_t* e = reinterpret_cast<const uint16_t*>(&q);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = to_h(bf2f(e[i]) * f, bad);
-    } else {
+        for (int i = 0; i < 8; ++i) o[i] = to_h_max(bf2f(e[i]) * f, m);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = __float2half_rn(0.f);
+        for (int i = 0; i < 8; ++i) o[i] = __float2half_rn(0.f);
+      }
+      dst[c] = *reinterpret_cast<uint4*>(o);
     }
-    *reinterpret_cast<uint4*>(W16 + e0) = *reinterpret_cast<uint4*>(o);
   }
-  if (bad) latch_status(status, kStatusRange);
 }
 
-// The weight staging of the up pass in one launch: blockIdx.y == 0 stages W16 (as
-// prep_gate_up_kernel, one warp per row, no divisions); blockIdx.y == 1 stages
-// GWo16[n][part][d] for part 0/1 = fp16 hi / lo of gamma_d * Wo[d][n] * 2^e_g (a
-// transposed, split copy through 32 x 32 shared-memory tiles: hi + lo carries
-// ~22 significant bits of the exact fp32 product).  256 threads per block; both
+__global__ void __launch_bounds__(256) prep_gate_up_kernel(const uint16_t* __restrict__ Wg,
+                                                           const uint16_t* __restrict__ Wu,
+                                                           __half* __restrict__ W16, int I, int I_pad, int D,
+                                                           DevScales* sc) {
+  uint32_t m = 0u;
+  stage_w16_rows(Wg, Wu, W16, I, I_pad, D, (blockIdx.x * blockDim.x + threadIdx.x) >> 5,
+                 (gridDim.x * blockDim.x) >> 5, 1.0f, m);
+  m = __reduce_max_sync(0xffffffffu, m);
+  if ((threadIdx.x & 31) == 0 && m) atomicMax(&sc->wmax, m);
+}
+
+// GWo16[n][part][d] for part 0/1 = fp16 hi / lo of gamma_d * Wo[d][n] * f (a
+// transposed, split copy through 32 x 32 shared-memory tiles: hi + lo carries ~22
+// significant bits of the exact fp32 product); 256 threads, grid-stride over
+// tiles starting at tile0.  Folds max |gamma_d Wo[d][n]| (before f) into gm and
+// max |Wo[d][n]| into om.
+__device__ __forceinline__ void stage_gwo_tiles(const uint16_t* __restrict__ Wo, const uint16_t* __restrict__ gamma,
+                                                __half* __restrict__ GWo16, int D, int HD, int tile0, int ntiles_step,
+                                                float f, uint32_t& gm, uint32_t& om) {
+  __shared__ float tile[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int tn = (HD + 31) / 32, td = (D + 31) / 32;
+  for (int tt = tile0; tt < tn * td; tt += ntiles_step) {
+    const int d0 = (tt / tn) * 32, n0 = (tt % tn) * 32;
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+      const int d = d0 + i, n = n0 + tx;
+      float gw = 0.f;
+      if (d < D && n < HD) {
+        const float w = bf2f(Wo[(size_t)d * HD + n]);
+        om = max(om, __float_as_uint(fabsf(w)));
+        gw = bf2f(gamma[d]) * w;
+        gm = max(gm, __float_as_uint(fabsf(gw)));
+      }
+      tile[i][tx] = gw * f;
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+      const int n = n0 + i, d = d0 + tx;
+      if (n < HD && d < D) {
+        const float v = tile[tx][i];
+        const __half hi = __float2half_rn(v);
+        const __half lo = __float2half_rn(v - __half2float(hi));
+        GWo16[((size_t)n * 2 + 0) * D + d] = hi;
+        GWo16[((size_t)n * 2 + 1) * D + d] = lo;
+      }
+    }
+  }
+}
+
+// The weight staging of the up pass in one launch, unscaled, recording the maxima
+// of DevScales: blockIdx.y == 0 stages W16, blockIdx.y == 1 stages GWo16.  Both
 // parts grid-stride.
 __global__ void __launch_bounds__(256) weight_stage_kernel(const uint16_t* __restrict__ Wg,
                                                            const uint16_t* __restrict__ Wu, __half* __restrict__ W16,
                                                            int I, int I_pad, int D, const uint16_t* __restrict__ Wo,
                                                            const uint16_t* __restrict__ gamma,
-                                                           __half* __restrict__ GWo16, int HD, uint32_t* status,
-                                                           const DevScales* __restrict__ sc) {
-  bool bad = false;
+                                                           __half* __restrict__ GWo16, int HD, DevScales* sc) {
   if (blockIdx.y == 0) {
-    const float f = pow2f(scale_exp_norm(bits_f(sc->wmax)));   // W16 = W 2^e_w
-    const int lane = threadIdx.x & 31, nw = gridDim.x * 8;
-    const int D8 = D / 8;
-    for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < 2 * I_pad; r += nw) {
-      // row r: neuron group r / 32, gate (0) or up (1) row, neuron 16 * (r / 32) + r % 16
-      const int blk = (r >> 4) & 1, k = (r >> 5) * 16 + (r & 15);
-      const uint4* src = reinterpret_cast<const uint4*>((blk == 0 ? Wg : Wu) + (size_t)k * D);
-      uint4* dst = reinterpret_cast<uint4*>(W16 + (size_t)r * D);
-      for (int c = lane; c < D8; c += 32) {
-        __align__(16) __half o[8];
-        if (k < I) {
-          const uint4 q = __ldg(src + c);
-          const uint16_t* e = reinterpret_cast<const uint16_t*>(&q);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) o[i] = to_h(bf2f(e[i]) * f, bad);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) o[i] = __float2half_rn(0.f);
-        }
-        dst[c] = *reinterpret_cast<uint4*>(o);
-      }
-    }
+    uint32_t m = 0u;
+    stage_w16_rows(Wg, Wu, W16, I, I_pad, D, blockIdx.x * 8 + (threadIdx.x >> 5), gridDim.x * 8, 1.0f, m);
+    m = __reduce_max_sync(0xffffffffu, m);
+    if ((threadIdx.x & 31) == 0 && m) atomicMax(&sc->wmax, m);
   } else {
-    __shared__ float tile[32][33];
-    const float f = pow2f(scale_exps(*sc, D).e_g);
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const int tn = (HD + 31) / 32, td = (D + 31) / 32;
-    for (int tt = blockIdx.x; tt < tn * td; tt += gridDim.x) {
-      const int d0 = (tt / tn) * 32, n0 = (tt % tn) * 32;
-      __syncthreads();
-      for (int i = ty; i < 32; i += 8) {
-        const int d = d0 + i, n = n0 + tx;
-        tile[i][tx] = (d < D && n < HD) ? bf2f(gamma[d]) * bf2f(Wo[(size_t)d * HD + n]) : 0.f;
-      }
-      __syncthreads();
-      for (int i = ty; i < 32; i += 8) {
-        const int n = n0 + i, d = d0 + tx;
-        if (n < HD && d < D) {
-          const float v = tile[tx][i] * f;
-          const __half hi = to_h(v, bad);
-          const __half lo = __float2half_rn(v - __half2float(hi));
-          GWo16[((size_t)n * 2 + 0) * D + d] = hi;
-          GWo16[((size_t)n * 2 + 1) * D + d] = lo;
-        }
-      }
+    uint32_t gm = 0u, om = 0u;
+    stage_gwo_tiles(Wo, gamma, GWo16, D, HD, blockIdx.x, gridDim.x, 1.0f, gm, om);
+    gm = __reduce_max_sync(0xffffffffu, gm);
+    om = __reduce_max_sync(0xffffffffu, om);
+    if ((threadIdx.x & 31) == 0) {
+      if (gm) atomicMax(&sc->gwmax, gm);
+      if (om) atomicMax(&sc->womax, om);
     }
   }
-  if (bad) latch_status(status, kStatusRange);
+}
+
+// The weights staged again at their power-of-two scales (scales.cuh) when the
+// recorded maxima call for it; otherwise every block returns at once.  y = 0:
+// W16 = W 2^e_w; y = 1: GWo16 = gamma Wo^T 2^e_g (when given); y = 2: Wo16 =
+// Wo 2^e_o (when given: the leave-one-out pass).  A non-finite maximum (a
+// non-finite weight) latches AFF_ERR_RANGE.
+__global__ void __launch_bounds__(256) weight_restage_kernel(const uint16_t* __restrict__ Wg,
+                                                             const uint16_t* __restrict__ Wu,
+                                                             __half* __restrict__ W16, int I, int I_pad, int D,
+                                                             const uint16_t* __restrict__ Wo,
+                                                             const uint16_t* __restrict__ gamma,
+                                                             __half* __restrict__ GWo16, __half* __restrict__ Wo16,
+                                                             int HD, DevScales* sc, uint32_t* status) {
+  if (blockIdx.y == 1 && GWo16 == nullptr) return;
+  if (blockIdx.y == 2 && Wo16 == nullptr) return;
+  const float m = bits_f(blockIdx.y == 0 ? sc->wmax : (blockIdx.y == 1 ? sc->gwmax : sc->womax));
+  if (!(m <= 3.4e38f)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) latch_status(status, kStatusRange);
+    return;
+  }
+  const int e = scale_exp_act(m);
+  if (e == 0) return;
+  const float f = pow2f(e);
+  uint32_t m1 = 0u, m2 = 0u;   // maxima seen again here (the recorded ones stay)
+  if (blockIdx.y == 0) {
+    stage_w16_rows(Wg, Wu, W16, I, I_pad, D, blockIdx.x * 8 + (threadIdx.x >> 5), gridDim.x * 8, f, m1);
+  } else if (blockIdx.y == 1) {
+    stage_gwo_tiles(Wo, gamma, GWo16, D, HD, blockIdx.x, gridDim.x, f, m1, m2);
+  } else {
+    const size_t n8 = (size_t)D * HD / 8;
+    for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8; v += (size_t)gridDim.x * blockDim.x) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(Wo) + v);
+      const uint16_t* e8 = reinterpret_cast<const uint16_t*>(&q);
+      __align__(16) __half o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = __float2half_rn(bf2f(e8[i]) * f);
+      reinterpret_cast<uint4*>(Wo16)[v] = *reinterpret_cast<uint4*>(o);
+    }
+  }
 }
 
 // wdn[k] = ||w^d_k||^2 = sum_d Wd[d][k]^2 (fp32; fixed order: 8 row phases, then in order).
@@ -438,15 +459,14 @@ cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, 
 // ---------------------------------------------------------------- leave-one-out score
 // out = fp16 copy of n bf16 values (n % 8 == 0), 8 per thread.
 __global__ void to_fp16_kernel(const uint16_t* __restrict__ in, __half* __restrict__ out, size_t n,
-                               uint32_t* status, const uint32_t* __restrict__ maxbits) {
-  const float f = maxbits ? pow2f(scale_exp_norm(bits_f(*maxbits))) : 1.f;
+                               uint32_t* status) {
   bool bad = false;
   for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n / 8; v += (size_t)gridDim.x * blockDim.x) {
     uint4 q = *reinterpret_cast<const uint4*>(in + v * 8);
     const uint16_t* e = reinterpret_cast<const uint16_t*>(&q);
     __align__(16) __half o[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = to_h(bf2f(e[i]) * f, bad);
+    for (int i = 0; i < 8; ++i) o[i] = __float2half_rn(bf2f(e[i]));
     *reinterpret_cast<uint4*>(out + v * 8) = *reinterpret_cast<uint4*>(o);
   }
   if (bad) latch_status(status, kStatusRange);
@@ -794,39 +814,28 @@ cudaError_t launch_restage_a(const uint16_t* a, const float* inv_r, __half* a16,
   return cudaGetLastError();
 }
 
-cudaError_t launch_weight_max(const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wo, const uint16_t* gamma,
-                              int I, int D, int HD, DevScales* sc, int sm_count, cudaStream_t s) {
-  MaxJobs J{};
-  J.p[0] = Wg; J.n8[0] = (size_t)I * D / 8; J.out[0] = &sc->wmax;
-  J.p[1] = Wu; J.n8[1] = (size_t)I * D / 8; J.out[1] = &sc->wmax;
-  int arrays = 2;
-  if (Wo) {
-    J.p[2] = Wo; J.n8[2] = (size_t)D * HD / 8; J.out[2] = &sc->womax;
-    J.p[3] = gamma; J.n8[3] = (size_t)D / 8; J.out[3] = &sc->gwmax;
-    arrays = 4;
-  }
-  // per array about 1024 words per block, at most two blocks per SM per array
-  int g = blocks_for(J.n8[0], 1024);
-  if (g > 2 * sm_count) g = 2 * (sm_count > 0 ? sm_count : 1);
-  max_abs_kernel<<<dim3(g, arrays), 256, 0, s>>>(J);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_weight_stage(const uint16_t* Wg, const uint16_t* Wu, __half* W16, int I, int I_pad, int D,
-                                const uint16_t* Wo, const uint16_t* gamma, __half* GWo16, int HD, uint32_t* status,
-                                const DevScales* sc, int sm_count, cudaStream_t s) {
+                                const uint16_t* Wo, const uint16_t* gamma, __half* GWo16, int HD, DevScales* sc,
+                                int sm_count, cudaStream_t s) {
   int g0 = (2 * I_pad + 7) / 8;                          // one warp per W16 row
   const int g1 = ((HD + 31) / 32) * ((D + 31) / 32);     // gamma*Wo^T tiles
   if (g0 < g1) g0 = g1;
   if (g0 > 4 * sm_count) g0 = 4 * (sm_count > 0 ? sm_count : 1);
-  weight_stage_kernel<<<dim3(g0, 2), 256, 0, s>>>(Wg, Wu, W16, I, I_pad, D, Wo, gamma, GWo16, HD, status, sc);
+  weight_stage_kernel<<<dim3(g0, 2), 256, 0, s>>>(Wg, Wu, W16, I, I_pad, D, Wo, gamma, GWo16, HD, sc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_weight_restage(const uint16_t* Wg, const uint16_t* Wu, __half* W16, int I, int I_pad, int D,
+                                  const uint16_t* Wo, const uint16_t* gamma, __half* GWo16, __half* Wo16, int HD,
+                                  DevScales* sc, uint32_t* status, int sm_count, cudaStream_t s) {
+  weight_restage_kernel<<<dim3(2 * (sm_count > 0 ? sm_count : 1), 3), 256, 0, s>>>(Wg, Wu, W16, I, I_pad, D, Wo, gamma,
+                                                                                  GWo16, Wo16, HD, sc, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prep_gate_up(const uint16_t* Wg, const uint16_t* Wu, __half* W16, int I, int I_pad, int D,
-                                uint32_t* status, const DevScales* sc, cudaStream_t s) {
-  prep_gate_up_kernel<<<blocks_for((size_t)2 * I_pad * D / 8, 256), 256, 0, s>>>(Wg, Wu, W16, I, I_pad, D, status,
-                                                                                 sc);
+                                DevScales* sc, cudaStream_t s) {
+  prep_gate_up_kernel<<<blocks_for((size_t)2 * I_pad, 8), 256, 0, s>>>(Wg, Wu, W16, I, I_pad, D, sc);
   return cudaGetLastError();
 }
 
@@ -884,10 +893,9 @@ cudaError_t launch_finalize_up(const double* sh, const float* wdn, int fo, int T
   return cudaGetLastError();
 }
 
-cudaError_t launch_to_fp16(const uint16_t* in, __half* out, size_t n, uint32_t* status, const uint32_t* maxbits,
-                           cudaStream_t s) {
+cudaError_t launch_to_fp16(const uint16_t* in, __half* out, size_t n, uint32_t* status, cudaStream_t s) {
   const size_t blocks = (n / 8 + 255) / 256;
-  to_fp16_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(in, out, n, status, maxbits);
+  to_fp16_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(in, out, n, status);
   return cudaGetLastError();
 }
 

@@ -16,15 +16,19 @@ cudaError_t launch_prep_tokens(const uint16_t* x, const uint16_t* a, const uint1
 // a16 staged again as a / r 2^e_a when sc->amax calls for it (else returns at once).
 cudaError_t launch_restage_a(const uint16_t* a, const float* inv_r, __half* a16, int T, int HD, const DevScales* sc,
                              uint32_t* status, int sm_count, cudaStream_t s);
-// The weight maxima of DevScales (Wg/Wu; gamma*Wo column sums and maxima when Wo is given).
-cudaError_t launch_weight_max(const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wo, const uint16_t* gamma,
-                              int I, int D, int HD, DevScales* sc, int sm_count, cudaStream_t s);
-// W16 (as launch_prep_gate_up) and gamma*Wo^T hi / lo ([HD][2][D], 2^e_g) in one launch.
+// W16 (as launch_prep_gate_up) and gamma*Wo^T hi / lo ([HD][2][D]) in one launch, both
+// unscaled, recording the maxima of DevScales.
 cudaError_t launch_weight_stage(const uint16_t* Wg, const uint16_t* Wu, __half* W16, int I, int I_pad, int D,
-                                const uint16_t* Wo, const uint16_t* gamma, __half* GWo16, int HD, uint32_t* status,
-                                const DevScales* sc, int sm_count, cudaStream_t s);
+                                const uint16_t* Wo, const uint16_t* gamma, __half* GWo16, int HD, DevScales* sc,
+                                int sm_count, cudaStream_t s);
+// W16 ([I_pad / 16][2][16][D], gate and up rows of 16 neurons), unscaled; records sc->wmax.
 cudaError_t launch_prep_gate_up(const uint16_t* Wg, const uint16_t* Wu, __half* W16, int I, int I_pad, int D,
-                                uint32_t* status, const DevScales* sc, cudaStream_t s);
+                                DevScales* sc, cudaStream_t s);
+// W16, GWo16 (when given) and Wo16 (when given) staged again at their power-of-two scales
+// when the recorded maxima call for it; otherwise returns at once.
+cudaError_t launch_weight_restage(const uint16_t* Wg, const uint16_t* Wu, __half* W16, int I, int I_pad, int D,
+                                  const uint16_t* Wo, const uint16_t* gamma, __half* GWo16, __half* Wo16, int HD,
+                                  DevScales* sc, uint32_t* status, int sm_count, cudaStream_t s);
 cudaError_t launch_wd_colnorm(const uint16_t* Wd, float* wdn, int D, int I, int I_pad, cudaStream_t s);
 cudaError_t launch_wd_colnorm_f32(const float* Wd, float* wdn, int D, int I, cudaStream_t s);
 cudaError_t launch_reduce_partials(const float* partial, double* out, int n_chunks, int halves, int H, int I_pad,
@@ -36,9 +40,7 @@ cudaError_t launch_reduce_finalize(const float* partial, const float* wdn, int f
 cudaError_t launch_finalize_up(const double* sh, const float* wdn, int fo, int T, int H, int G, int I, int I_pad,
                                float* S_out, float* S_head_out, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, cudaStream_t s);
-// fp16 copy, times 2^e from the maximum at maxbits (fp32 bits) when given.
-cudaError_t launch_to_fp16(const uint16_t* in, __half* out, size_t n, uint32_t* status, const uint32_t* maxbits,
-                           cudaStream_t s);
+cudaError_t launch_to_fp16(const uint16_t* in, __half* out, size_t n, uint32_t* status, cudaStream_t s);
 cudaError_t launch_loo_rho(const float* cn, const float* inv_r, float* rho, int T, int T_pad, int H, int D,
                            int groups, const DevScales* sc, cudaStream_t s);
 cudaError_t launch_prep_wd(const uint16_t* Wd, __half* Wd16, __half* WdT16, int D, int I, int I_pad, uint32_t* status,

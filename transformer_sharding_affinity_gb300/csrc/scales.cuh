@@ -8,15 +8,17 @@
 // rounding (away from the subnormal range), so a result is the same as with
 // no scaling whenever no operand would have overflowed or been subnormal.
 //
-//   weights  W16 = [Wg; Wu] 2^e_w, Wo16 = Wo 2^e_o: e from the tensor's
-//            largest magnitude, always normalised; GWo16 = gamma Wo^T 2^e_g
-//            from the bound |gamma_d Wo[d][j]| <= max|gamma| max|Wo|;
+//   weights  W16 = [Wg; Wu] 2^e_w, GWo16 = gamma Wo^T 2^e_g, Wo16 = Wo 2^e_o:
+//            staged unscaled while their largest magnitudes are recorded,
+//            then staged again (weight_restage_kernel) only when a maximum
+//            lies outside [2^-6, 2^15), so ordinary weights pay for one small
+//            launch;
 //   fold     M16 = M 2^e_m, e_m from the bound
-//            |M[k][j]| <= D max|W| max|gamma| max|Wo|;
+//            |M[k][j]| <= D max|W| max|gamma_d Wo[d][j]|;
 //   n16      gamma x / r * 2^e_n, from the bound |x_d| / r <= sqrt(D);
 //   a16      a / r * 2^e_a, from the largest staged |a / r|: 0 unless that
 //            maximum lies outside [2^-6, 2^15), in which case a16 is staged
-//            again (so ordinary inputs pay for one extra small launch).
+//            again.
 // The maxima live in DevScales inside the workspace; every consumer derives
 // the exponents from them with the same functions, so all kernels agree.
 #pragma once
@@ -28,7 +30,7 @@ namespace aff {
 struct DevScales {
   uint32_t wmax;    // max over Wg and Wu of |value| (fp32 bits; atomicMax over non-negative floats)
   uint32_t womax;   // max |Wo|
-  uint32_t gwmax;   // max |gamma| seen by the weight side (with womax, a bound on |gamma_d Wo[d][j]|)
+  uint32_t gwmax;   // max |gamma_d Wo[d][j]|
   uint32_t gmax;    // max |gamma| recorded by the token side (the scale of n16)
   uint32_t amax;    // max |a_t / r_t| as first staged (FO, LOO, ADD direct)
   uint32_t amax2;   // second-moment ADD fallback: max |a_t / r_t| over every token
@@ -94,14 +96,13 @@ __host__ __device__ inline ScaleExps scale_exps(const DevScales& s, int D) {
   // ceil(log2(D)): D <= 2^lgD
   int lgD = 0;
   while ((int64_t)1 << lgD < (int64_t)D) ++lgD;
-  const int ew = scale_exp_norm(bits_f(s.wmax)), eo = scale_exp_norm(bits_f(s.womax));
-  const int eg = scale_exp_norm(bits_f(s.gwmax));
-  x.e_w = ew;
-  x.e_o = eo;
-  // products of bounds could leave fp32's range: combine exponents instead (each factor
-  // times 2^e lies in [2^13, 2^14), so a product of k factors times 2^(sum e) < 2^14k)
-  x.e_g = clamp_exp(eg + eo - 14);
-  x.e_m = clamp_exp(ew + eg + eo - 28 - lgD);
+  x.e_w = scale_exp_act(bits_f(s.wmax));
+  x.e_g = scale_exp_act(bits_f(s.gwmax));
+  x.e_o = scale_exp_act(bits_f(s.womax));
+  // |M[k][j]| <= D max|W| max|gamma Wo|: the bound's product could leave fp32's range, so
+  // its factors' normalising exponents are combined instead (each factor times its 2^e
+  // lies in [2^13, 2^14))
+  x.e_m = clamp_exp(scale_exp_norm(bits_f(s.wmax)) + scale_exp_norm(bits_f(s.gwmax)) - 14 - lgD);
   // |gamma_d x_d / r| <= max|gamma| sqrt(D) (x_d^2 <= D mean(x^2) <= D r^2); sqrt(D) <= 2^lg
   int lg = 0;
   while ((int64_t)1 << (2 * lg) < (int64_t)D) ++lg;

@@ -44,12 +44,12 @@ def fo_flops(s) -> dict:
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the FO tile kernel, from an ncu capture of this bench's workload; valid only
 # while the kernel sources hash to the recorded value (otherwise null).
-KERNEL_SOURCES = ("tile_kernel.cu", "tile_kernel.cuh", "sm103_primitives.cuh")
-MOMENT_SOURCES = ("moment_kernel.cu", "moment_kernel.cuh", "sm103_primitives.cuh")
+KERNEL_SOURCES = ("tile_kernel.cu", "tile_kernel.cuh", "sm103_primitives.cuh", "scales.cuh")
+MOMENT_SOURCES = ("moment_kernel.cu", "moment_kernel.cuh", "sm103_primitives.cuh", "scales.cuh")
 TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass), third FO launch of
-    # `python bench.py --steps 2 --warmup 3 --no-cpu-baseline --e2e-steps 0`: 467.99 + 50.57 MB
-    ("qwen3_0p6b_layer", "fo", 65536): {"bytes": 518.55e6, "src": "b10f3384ed8b35b1"},
+    # `python bench.py --steps 2 --warmup 3 --no-cpu-baseline --e2e-steps 0`: 458.02 + 50.56 MB
+    ("qwen3_0p6b_layer", "fo", 65536): {"bytes": 508.58e6, "src": "7dccbe638d141e05"},
 }
 
 
@@ -562,7 +562,7 @@ def main() -> None:
         "step_tflops": flops_per_step / (ms_step * 1e-3) / 1e12,
         "step_frac_of_peak": flops_per_step / (ms_step * 1e-3) / 1e12 / pk["bf16_tflops"],
         "roofline": roof,
-        "gpu_launches": (8 if moment else {"fo": 7, "add": 6, "loo": 9, "down": 9}[args.mode]) * args.steps,
+        "gpu_launches": (9 if moment else {"fo": 8, "add": 7, "loo": 10, "down": 10}[args.mode]) * args.steps,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": shape.G * shape.I * 4, "ms_per_step": e2e_ms, "steps": args.e2e_steps,
                 "clocks": clocks_e2e.summary()},

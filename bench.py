@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import subprocess
 import sys
@@ -254,7 +255,8 @@ def run_reference(args) -> None:
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload, "T": shape.T, "D": shape.D, "H": shape.H, "G": shape.G,
-                       "d_head": shape.dh, "I": shape.I, "mode": "fo", "tokens_per_step": tok},
+                       "d_head": shape.dh, "I": shape.I, "mode": "fo"},
+            "tokens_per_step": tok,
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"each step: fp64 oracle FO S_up over all {shape.I} neurons for {tok} tokens "
                                        f"of the {args.workload} workload"},
@@ -345,14 +347,18 @@ def run_layout(args) -> None:
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_0p6b_layer")
     ap.add_argument("--mode", default="fo", choices=["fo", "add", "loo", "down"])
     ap.add_argument("--add-form", default="moment", choices=["moment", "direct"],
                     help="ADD through each head's second moment (d_head <= 128) or the direct contraction")
-    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--e2e-steps", type=int, default=200,
+                    help="at least this many end-to-end steps (0: skip); more when --min-load-s asks for it")
+    ap.add_argument("--min-load-s", type=float, default=5.0,
+                    help="run the end-to-end loop for about this long, so that a clock sampler polling "
+                         "every few hundred ms sees the GPU under load many times")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=256)
@@ -484,11 +490,15 @@ def main() -> None:
     ready = [torch.cuda.Event() for _ in range(2)]
     free = [torch.cuda.Event() for _ in range(2)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = 0
+    if args.e2e_steps > 0:
+        # an end-to-end step takes ~1.1-1.2x the device step
+        n_e2e = max(args.e2e_steps, min(100000, int(math.ceil(args.min_load_s * 1e3 / (1.15 * ms_step)))))
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks_e2e:
         e0.record(stream)
         copy_stream.wait_stream(stream)
-        for i in range(args.e2e_steps):
+        for i in range(n_e2e):
             j = i % 2
             with torch.cuda.stream(copy_stream):
                 if i >= 2:
@@ -502,7 +512,7 @@ def main() -> None:
             S_host.copy_(S, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps if args.e2e_steps > 0 else float("nan")
+    e2e_ms = e0.elapsed_time(e1) / n_e2e if n_e2e > 0 else float("nan")
 
     if rank != 0:
         if ws > 1:
@@ -564,7 +574,7 @@ def main() -> None:
         "roofline": roof,
         "gpu_launches": (9 if moment else {"fo": 8, "add": 7, "loo": 10, "down": 10}[args.mode]) * args.steps,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": shape.G * shape.I * 4, "ms_per_step": e2e_ms, "steps": args.e2e_steps,
+                "d2h_bytes_per_step": shape.G * shape.I * 4, "ms_per_step": e2e_ms, "steps": n_e2e,
                 "clocks": clocks_e2e.summary()},
         "clocks": clocks.summary(),
     }

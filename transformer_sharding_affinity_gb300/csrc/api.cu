@@ -543,14 +543,15 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   std::memset(maps, 0, sizeof maps);
   // fold: M_h = [Wg; Wu] diag(gamma) Wo^(h)
   {
-    if ((st = map_gate_up(&maps[0], W16, (uint64_t)D, (uint64_t)I_pad)) != AFF_OK) return st;
+    // units of (128 rows of W16, 256 columns of H*dh): A = W16 rows, B = gamma*Wo^T hi, then lo
+    if ((st = map2(&maps[0], W16, (uint64_t)D, (uint64_t)2 * I_pad)) != AFF_OK) return st;
     uint64_t dm[3] = {(uint64_t)D, 2, (uint64_t)H * dh}, sd[2] = {(uint64_t)D * 2, (uint64_t)D * 4};
     if ((st = make_map(&maps[1], GWo16, 3, dm, sd, 128, 2)) != AFF_OK) return st;
     maps[2] = maps[0];
     maps[3] = maps[0];
     TileParams p = base_params(d, L, ws, kModeFold);
-    p.n_ntiles = (int)ceil_div((int64_t)H * dh, 128);
-    p.n_units = p.n_ktiles * p.n_ntiles;
+    p.n_ntiles = (int)ceil_div((int64_t)H * dh, 256);
+    p.n_units = 2 * p.n_ktiles * p.n_ntiles;
     p.M16 = M16;
     if ((st = run_tile(maps, p, wst)) != AFF_OK) return st;
   }

@@ -65,10 +65,10 @@ template <bool STREAM = false>
 __device__ __forceinline__ Unit unit_info(const TileParams& p, int u) {
   Unit U{};
   switch (p.mode) {
-    case kModeFold:
-      U.kt = u % p.n_ktiles;
+    case kModeFold:   // one unit per (128 rows of W16 / M16, 256 columns of H*dh)
+      U.kt = u % (2 * p.n_ktiles);
       U.njobs = 1;
-      U.base = u / p.n_ktiles;  // column tile
+      U.base = u / (2 * p.n_ktiles);  // column tile of 256
       break;
     case kModeFO:
     case kModeLOO:
@@ -191,8 +191,8 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
   constexpr int CW = kBlockN / NG;        // columns per epilogue thread (of each accumulator)
   constexpr bool kHeads = MODE == kModeFO || MODE == kModeADD || MODE == kModeLOO;
   // one N = 256 MMA per K slice (see the file comment): A = the first tile for the
-  // head passes, the third for the others
-  constexpr bool kWide = MODE != kModeFold;
+  // head passes and the fold, the third for the others
+  constexpr bool kAFirst = kHeads || MODE == kModeFold;
   constexpr int CWW = 2 * kBlockN / NG;   // columns of the 256 per epilogue thread
   const int S = p.stages;
   constexpr int kSB = kStageBytes;        // bytes of one pipeline stage
@@ -296,10 +296,10 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
                 tma_load_3d(st + kTileBytes, &map3, fb, kx, J.head, J.t0);
                 tma_load_3d(st + kBOff, &map3, fb, kx, J.head, J.t0 + kBlockN);
                 break;
-              case kJobFold:     // A1 / A2 = gate / up rows of 128 neurons (4-D view), B = gamma*Wo^T (hi, then lo)
-                tma_load_4d(st, &map0, fb, kx, 0, 0, J.kt * 8);
-                tma_load_4d(st + kTileBytes, &map0, fb, kx, 0, 1, J.kt * 8);
-                tma_load_3d(st + kBOff, &map1, fb, kx, part, J.nt * kBlockN);
+              case kJobFold:     // A = 128 rows of W16, B = 256 columns of gamma*Wo^T (hi, then lo)
+                tma_load_2d(st, &map0, fb, kx, J.kt * kBlockM);
+                tma_load_3d(st + kTileBytes, &map1, fb, kx, part, J.nt * 2 * kBlockN);
+                tma_load_3d(st + kBOff, &map1, fb, kx, part, J.nt * 2 * kBlockN + kBlockN);
                 break;
               case kJobXPrime:   // Wd16 rows d (256, the MMA's B), alpha16 token rows (its A)
                 tma_load_2d(st, &map1, fb, kx, J.nt * 2 * kBlockN);
@@ -338,8 +338,8 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
     // A lean loop: this one thread must issue MMAs as fast as the tensor pipe
     // retires them, so no divisions, and descriptors advance by constants.
     if (lane == 0) {
-      // N = 256: one MMA reads 12 KB of shared memory where a D1 / D2 pair reads 16 KB
-      constexpr uint32_t idesc = kWide ? idesc_f16(kBlockM, 2 * kBlockN, 0) : idesc_f16(kBlockM, kBlockN, 0);
+      // N = 256: one MMA reads 12 KB of shared memory where two N = 128 MMAs read 16 KB
+      constexpr uint32_t idesc = idesc_f16(kBlockM, 2 * kBlockN, 0);
       const uint64_t dbase = smem_desc_k_sw128(smem_u32(sm.stage0));   // first tile of stage 0
       constexpr uint64_t kStageDesc = (uint64_t)(kSB >> 4);             // descriptor step per stage
       constexpr uint64_t kA2 = (uint64_t)(kTileBytes >> 4), kB = (uint64_t)(kBOff >> 4);
@@ -387,7 +387,6 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
            }
           }
           const uint32_t d1 = tmem + (uint32_t)(b * 2 * kBlockN);
-          const uint32_t d2 = d1 + kBlockN;
           uint32_t acc = 0u;
           for (int kb = 0, kb_in = 0; kb < J.nkb; ++kb) {
             if (!mbar_wait(&sm.full[s], ph, sm.abort_flag, p.status)) { ok = false; break; }
@@ -398,13 +397,10 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               if (ks < nks) {
-                if constexpr (kHeads) {   // A = weights (first tile), B = 256 tokens
+                if constexpr (kAFirst) {   // A = the first tile (weights), B = the next 256 rows
                   mma_f16_ss(d1, da1 + 2 * ks, da2 + 2 * ks, idesc, acc);
-                } else if constexpr (kWide) {
-                  mma_f16_ss(d1, db + 2 * ks, da1 + 2 * ks, idesc, acc);
                 } else {
-                  mma_f16_ss(d1, da1 + 2 * ks, db + 2 * ks, idesc, acc);
-                  mma_f16_ss(d2, da2 + 2 * ks, db + 2 * ks, idesc, acc);
+                  mma_f16_ss(d1, db + 2 * ks, da1 + 2 * ks, idesc, acc);
                 }
                 acc = 1u;
               }
@@ -635,50 +631,41 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
         static_assert(EW == kWideEpiWarps || CW == 64, "the 8-warp epilogues read 64 columns per thread");
 
         if constexpr (MODE == kModeFold) {
-          // D1 = Mg[k][n], D2 = Mu[k][n] for neuron k = kt*128 + row, columns n = nt*128 + hf*64 + ...,
-          // times 2^(e_w + e_g) from the operands; stored times 2^e_m
-          const int kk = J.kt * kBlockM + row;
+          // TMEM lane = row R of W16 and M16 (groups of 16 neurons: 16 gate rows, then the same
+          // neurons' 16 up rows), columns n = nt*256 + hf*128 + ... of H*dh, times 2^(e_w + e_g)
+          // from the operands; stored times 2^e_m.  d_head % 8 == 0, so an 8-column group lies
+          // in one head.
+          const size_t R = (size_t)J.kt * kBlockM + row;
           const float fm1 = pow2f(ex.e_m), fm2 = pow2f(-(ex.e_w + ex.e_g));
+          const uint32_t col = (uint32_t)(b * 2 * kBlockN + hf * CWW);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t mg[16], mu[16];
-            tmem_ld16(c1 + c * 16, mg);
-            tmem_ld16(c2 + c * 16, mu);
+          for (int c = 0; c < CWW / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld16(tl + col + c * 32, *reinterpret_cast<uint32_t(*)[16]>(v));
+            tmem_ld16(tl + col + c * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
             tmem_ld_wait();
-            if (c == 3) {
+            if (c == CWW / 32 - 1) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(&sm.tempty[b]);
             }
 #pragma unroll
-            for (int i = 0; i < 16; i += 8) {
-              const int n = J.nt * kBlockN + hf * 64 + c * 16 + i;
+            for (int i = 0; i < 32; i += 8) {
+              const int n = J.nt * 2 * kBlockN + hf * CWW + c * 32 + i;
               if (n < p.H * p.dh) {
-                const int h = n / p.dh, jj = n % p.dh;
-                uint4 vg, vu;
-                float fg[8], fu[8];
+                float f[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  fg[e] = __uint_as_float(mg[i + e]) * fm1 * fm2;
-                  fu[e] = __uint_as_float(mu[i + e]) * fm1 * fm2;
-                }
-                vg.x = pack_h2(fg[0], fg[1]);
-                vg.y = pack_h2(fg[2], fg[3]);
-                vg.z = pack_h2(fg[4], fg[5]);
-                vg.w = pack_h2(fg[6], fg[7]);
-                vu.x = pack_h2(fu[0], fu[1]);
-                vu.y = pack_h2(fu[2], fu[3]);
-                vu.z = pack_h2(fu[4], fu[5]);
-                vu.w = pack_h2(fu[6], fu[7]);
-                // rows in groups of 16 neurons: 16 gate rows, then their 16 up rows
-                const size_t rg = (size_t)(kk >> 4) * 32 + (kk & 15), ru = rg + 16;
+                for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[i + e]) * fm1 * fm2;
+                uint4 w;
+                w.x = pack_h2(f[0], f[1]);
+                w.y = pack_h2(f[2], f[3]);
+                w.z = pack_h2(f[4], f[5]);
+                w.w = pack_h2(f[6], f[7]);
                 if (p.stream_heads) {   // [2 I_pad][H*dh]: heads back to back along K
-                  const size_t HD = (size_t)p.H * p.dh;
-                  *reinterpret_cast<uint4*>(p.M16 + rg * HD + n) = vg;
-                  *reinterpret_cast<uint4*>(p.M16 + ru * HD + n) = vu;
+                  *reinterpret_cast<uint4*>(p.M16 + R * ((size_t)p.H * p.dh) + n) = w;
                 } else {                // [H][2 I_pad][dh]
-                  *reinterpret_cast<uint4*>(p.M16 + ((size_t)h * 2 * p.I_pad + rg) * p.dh + jj) = vg;
-                  *reinterpret_cast<uint4*>(p.M16 + ((size_t)h * 2 * p.I_pad + ru) * p.dh + jj) = vu;
+                  const int h = n / p.dh, jj = n % p.dh;
+                  *reinterpret_cast<uint4*>(p.M16 + ((size_t)h * 2 * p.I_pad + R) * p.dh + jj) = w;
                 }
               }
             }

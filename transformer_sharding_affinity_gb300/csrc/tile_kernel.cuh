@@ -10,11 +10,12 @@
 namespace aff {
 
 // A job of the tile kernel stages, per K block of 64 fp16 elements (128-byte
-// rows), three 128-row tiles, and runs one N = 256 MMA per K slice (the fold
-// runs two N = 128 MMAs, D1 = A1 * B^T and D2 = A2 * B^T).  Head passes (FO,
-// ADD, LOO): A = 128 interleaved gate / up weight rows of 64 neurons, B = 256
-// tokens.  Alpha, x', c_h, ||b_gk||^2: A = the third tile (tokens; neurons for
-// ||b_gk||^2), B = the first two.  Gate / up weights (W16, M16) are stored in
+// rows), three 128-row tiles, and runs one N = 256 MMA per K slice.  Head
+// passes (FO, ADD, LOO): A = 128 interleaved gate / up weight rows of 64
+// neurons, B = 256 tokens.  Fold: A = the same 128 weight rows, B = 256
+// columns of gamma*Wo^T (its hi part, then its lo part, along K).  Alpha, x',
+// c_h, ||b_gk||^2: A = the third tile (tokens; neurons for ||b_gk||^2), B = the
+// first two.  Gate / up weights (W16, M16) are stored in
 // groups of 16 neurons: 16 gate rows, then the same neurons' 16 up rows.
 constexpr int kBlockM = 128;      // rows per tile (TMEM lanes)
 constexpr int kBlockN = 128;      // TMEM columns per tile of the accumulator
@@ -57,7 +58,7 @@ struct TileParams {
   int32_t n_ktiles;        // neuron tiles of 128 (I_pad / 128); head passes: blocks of 64 = 2 n_ktiles
   int32_t n_ttiles;        // token tiles of 128 (T_pad / 128)
   int32_t tiles_per_unit;  // token tiles per alpha unit
-  int32_t n_ntiles;        // fold: column tiles of 128 over H*dh; x', c_h: tiles of 256 over D; qnorm: row tiles of 256 per group
+  int32_t n_ntiles;        // fold: column tiles of 256 over H*dh; x', c_h: tiles of 256 over D; qnorm: row tiles of 256 per group
   int32_t rows_per_group;  // qnorm: (H/G + 2) * dh
   int32_t nkb_D, nkb_dh, nkb_I;
   int32_t ls_D, ls_dh;     // 16-wide K slices in the last K block of D and of dh

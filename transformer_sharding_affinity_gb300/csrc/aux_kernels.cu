@@ -8,6 +8,7 @@
 #include "sm103_primitives.cuh"
 
 #include <cuda_fp16.h>
+#include "launch.cuh"
 
 namespace aff {
 
@@ -35,6 +36,7 @@ __global__ void prep_tokens_kernel(const uint16_t* __restrict__ x, const uint16_
                                    const uint16_t* __restrict__ gamma, __half* __restrict__ n16,
                                    __half* __restrict__ a16, float* __restrict__ inv_r, int T, int D, int HD,
                                    float eps, uint32_t* status, DevScales* sc) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int n_warps = (gridDim.x * blockDim.x) >> 5;
   __shared__ uint32_t gmax_s;
@@ -112,6 +114,7 @@ __global__ void prep_tokens_kernel(const uint16_t* __restrict__ x, const uint16_
 __global__ void restage_a_kernel(const uint16_t* __restrict__ a, const float* __restrict__ inv_r,
                                  __half* __restrict__ a16, int T, int HD, const DevScales* __restrict__ sc,
                                  uint32_t* status) {
+  pdl_enter();
   const float am = bits_f(sc->amax);
   if (!(am <= 3.4e38f)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) latch_status(status, kStatusRange);
@@ -167,6 +170,7 @@ __global__ void __launch_bounds__(256) prep_gate_up_kernel(const uint16_t* __res
                                                            const uint16_t* __restrict__ Wu,
                                                            __half* __restrict__ W16, int I, int I_pad, int D,
                                                            DevScales* sc) {
+  pdl_enter();
   uint32_t m = 0u;
   stage_w16_rows(Wg, Wu, W16, I, I_pad, D, (blockIdx.x * blockDim.x + threadIdx.x) >> 5,
                  (gridDim.x * blockDim.x) >> 5, 1.0f, m);
@@ -221,6 +225,7 @@ __global__ void __launch_bounds__(256) weight_stage_kernel(const uint16_t* __res
                                                            int I, int I_pad, int D, const uint16_t* __restrict__ Wo,
                                                            const uint16_t* __restrict__ gamma,
                                                            __half* __restrict__ GWo16, int HD, DevScales* sc) {
+  pdl_enter();
   if (blockIdx.y == 0) {
     uint32_t m = 0u;
     stage_w16_rows(Wg, Wu, W16, I, I_pad, D, blockIdx.x * 8 + (threadIdx.x >> 5), gridDim.x * 8, 1.0f, m);
@@ -250,6 +255,7 @@ __global__ void __launch_bounds__(256) weight_restage_kernel(const uint16_t* __r
                                                              const uint16_t* __restrict__ gamma,
                                                              __half* __restrict__ GWo16, __half* __restrict__ Wo16,
                                                              int HD, DevScales* sc, uint32_t* status) {
+  pdl_enter();
   if (blockIdx.y == 1 && GWo16 == nullptr) return;
   if (blockIdx.y == 2 && Wo16 == nullptr) return;
   const float m = bits_f(blockIdx.y == 0 ? sc->wmax : (blockIdx.y == 1 ? sc->gwmax : sc->womax));
@@ -280,6 +286,7 @@ __global__ void __launch_bounds__(256) weight_restage_kernel(const uint16_t* __r
 
 // wdn[k] = ||w^d_k||^2 = sum_d Wd[d][k]^2 (fp32; fixed order: 8 row phases, then in order).
 __global__ void wd_colnorm_kernel(const uint16_t* __restrict__ Wd, float* __restrict__ wdn, int D, int I, int I_pad) {
+  pdl_enter();
   __shared__ float part[8][33];
   const int k = blockIdx.x * 32 + threadIdx.x;
   float s = 0.f;
@@ -375,6 +382,7 @@ __global__ void __launch_bounds__(512) reduce_finalize_kernel(const float* __res
                                                               int T, int H, int G, int I, int I_pad,
                                                               float* __restrict__ S_out, float* __restrict__ S_head_out,
                                                               const DevScales* __restrict__ sc, int D) {
+  pdl_enter();
   // the partial sums carry the head operands' 2^2(e_m + e_a) (scales.cuh)
   const ScaleExps ex = scale_exps(*sc, D);
   const double fh = (double)pow2f(-(ex.e_m + ex.e_a));
@@ -460,6 +468,7 @@ cudaError_t launch_wait_selftest(uint32_t* status, unsigned long long limit_ns, 
 // out = fp16 copy of n bf16 values (n % 8 == 0), 8 per thread.
 __global__ void to_fp16_kernel(const uint16_t* __restrict__ in, __half* __restrict__ out, size_t n,
                                uint32_t* status) {
+  pdl_enter();
   bool bad = false;
   for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n / 8; v += (size_t)gridDim.x * blockDim.x) {
     uint4 q = *reinterpret_cast<const uint4*>(in + v * 8);
@@ -483,6 +492,7 @@ __global__ void to_fp16_kernel(const uint16_t* __restrict__ in, __half* __restri
 // 2^(e_a + e_o) per factor of c/r, removed here.
 __global__ void loo_rho_kernel(const float* __restrict__ cn, const float* __restrict__ inv_r, float* __restrict__ rho,
                                int T, int T_pad, int H, int D, int groups, const DevScales* __restrict__ sc) {
+  pdl_enter();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   const int h = blockIdx.y;
   if (t >= T_pad) return;
@@ -515,6 +525,7 @@ __global__ void loo_rho_kernel(const float* __restrict__ cn, const float* __rest
 // Wd16 [D][I_pad] and WdT16 [I_pad][D]: fp16 copies of Wd (zero padded).
 __global__ void prep_wd_kernel(const uint16_t* __restrict__ Wd, __half* __restrict__ Wd16,
                                __half* __restrict__ WdT16, int D, int I, int I_pad, uint32_t* status) {
+  pdl_enter();
   __shared__ float tile[32][33];
   const int d0 = blockIdx.y * 32, k0 = blockIdx.x * 32;
   bool bad = false;
@@ -538,6 +549,7 @@ __global__ void prep_wd_kernel(const uint16_t* __restrict__ Wd, __half* __restri
 __global__ void prep_qkv_kernel(const uint16_t* __restrict__ Wq, const uint16_t* __restrict__ Wk,
                                 const uint16_t* __restrict__ Wv, const uint16_t* __restrict__ gamma_next,
                                 __half* __restrict__ out, int G, int hpg, int dh, int D, uint32_t* status) {
+  pdl_enter();
   const int Rg = (hpg + 2) * dh;
   const size_t total = (size_t)G * Rg * D;
   bool bad = false;
@@ -565,6 +577,7 @@ __global__ void prep_qkv_kernel(const uint16_t* __restrict__ Wq, const uint16_t*
 __global__ void down_token_weights_kernel(const __half* __restrict__ alpha16, const float* __restrict__ ssx,
                                           float* __restrict__ cpart, int T, int T_pad, int D, int I_pad,
                                           int chunk, float eps, int groups) {
+  pdl_enter();
   extern __shared__ float w_tok[];   // [chunk]
   const int c = blockIdx.y;
   const int t0 = c * chunk, n = min(T, t0 + chunk) - t0;
@@ -610,6 +623,7 @@ __global__ void __launch_bounds__(256) finalize_down_kernel(const float* __restr
                                                             const float* __restrict__ bnorm, int n_chunks,
                                                             int bhalves, int T, int I, int I_pad, int G,
                                                             float* __restrict__ S_out) {
+  pdl_enter();
   __shared__ double part[8][32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int k = blockIdx.x * 32 + lane;
@@ -803,14 +817,17 @@ cudaError_t launch_prep_tokens(const uint16_t* x, const uint16_t* a, const uint1
   const int warps_per_block = 8;
   const int want = (T + warps_per_block - 1) / warps_per_block;
   const int cap = 3 * (sm_count > 0 ? sm_count : 1);
-  prep_tokens_kernel<<<want < cap ? want : cap, 32 * warps_per_block, 0, s>>>(x, a, gamma, n16, a16, inv_r, T, D,
-                                                                               HD, eps, status, sc);
+  if (cudaError_t e_ = launch_pdl(prep_tokens_kernel, want < cap ? want : cap, 32 * warps_per_block, 0, s, x, a,
+                                  gamma, n16, a16, inv_r, T, D, HD, eps, status, sc); e_ != cudaSuccess)
+    return e_;
   return cudaGetLastError();
 }
 
 cudaError_t launch_restage_a(const uint16_t* a, const float* inv_r, __half* a16, int T, int HD, const DevScales* sc,
                              uint32_t* status, int sm_count, cudaStream_t s) {
-  restage_a_kernel<<<4 * (sm_count > 0 ? sm_count : 1), 256, 0, s>>>(a, inv_r, a16, T, HD, sc, status);
+  if (cudaError_t e_ = launch_pdl(restage_a_kernel, 4 * (sm_count > 0 ? sm_count : 1), 256, 0, s, a, inv_r, a16, T,
+                                  HD, sc, status); e_ != cudaSuccess)
+    return e_;
   return cudaGetLastError();
 }
 
@@ -821,27 +838,33 @@ cudaError_t launch_weight_stage(const uint16_t* Wg, const uint16_t* Wu, __half* 
   const int g1 = ((HD + 31) / 32) * ((D + 31) / 32);     // gamma*Wo^T tiles
   if (g0 < g1) g0 = g1;
   if (g0 > 4 * sm_count) g0 = 4 * (sm_count > 0 ? sm_count : 1);
-  weight_stage_kernel<<<dim3(g0, 2), 256, 0, s>>>(Wg, Wu, W16, I, I_pad, D, Wo, gamma, GWo16, HD, sc);
+  if (cudaError_t e_ = launch_pdl(weight_stage_kernel, dim3(g0, 2), 256, 0, s, Wg, Wu, W16, I, I_pad, D, Wo, gamma,
+                                  GWo16, HD, sc); e_ != cudaSuccess)
+    return e_;
   return cudaGetLastError();
 }
 
 cudaError_t launch_weight_restage(const uint16_t* Wg, const uint16_t* Wu, __half* W16, int I, int I_pad, int D,
                                   const uint16_t* Wo, const uint16_t* gamma, __half* GWo16, __half* Wo16, int HD,
                                   DevScales* sc, uint32_t* status, int sm_count, cudaStream_t s) {
-  weight_restage_kernel<<<dim3(2 * (sm_count > 0 ? sm_count : 1), 3), 256, 0, s>>>(Wg, Wu, W16, I, I_pad, D, Wo, gamma,
-                                                                                  GWo16, Wo16, HD, sc, status);
+  if (cudaError_t e_ = launch_pdl(weight_restage_kernel, dim3(2 * (sm_count > 0 ? sm_count : 1), 3), 256, 0, s, Wg,
+                                  Wu, W16, I, I_pad, D, Wo, gamma, GWo16, Wo16, HD, sc, status); e_ != cudaSuccess)
+    return e_;
   return cudaGetLastError();
 }
 
 cudaError_t launch_prep_gate_up(const uint16_t* Wg, const uint16_t* Wu, __half* W16, int I, int I_pad, int D,
                                 DevScales* sc, cudaStream_t s) {
-  prep_gate_up_kernel<<<blocks_for((size_t)2 * I_pad, 8), 256, 0, s>>>(Wg, Wu, W16, I, I_pad, D, sc);
+  if (cudaError_t e_ = launch_pdl(prep_gate_up_kernel, blocks_for((size_t)2 * I_pad, 8), 256, 0, s, Wg, Wu, W16, I,
+                                  I_pad, D, sc); e_ != cudaSuccess)
+    return e_;
   return cudaGetLastError();
 }
 
 cudaError_t launch_wd_colnorm(const uint16_t* Wd, float* wdn, int D, int I, int I_pad, cudaStream_t s) {
   dim3 grid((I_pad + 31) / 32), block(32, 8);
-  wd_colnorm_kernel<<<grid, block, 0, s>>>(Wd, wdn, D, I, I_pad);
+  if (cudaError_t e_ = launch_pdl(wd_colnorm_kernel, grid, block, 0, s, Wd, wdn, D, I, I_pad); e_ != cudaSuccess)
+    return e_;
   return cudaGetLastError();
 }
 
@@ -869,16 +892,19 @@ cudaError_t launch_reduce_finalize(const float* partial, const float* wdn, int f
   dim3 grid(I_pad / 128, G), block(32, 16);
   switch (groups) {
     case 1:
-      reduce_finalize_kernel<1><<<grid, block, 0, s>>>(partial, wdn, fo, n_chunks, T, H, G, I, I_pad, S_out,
-                                                          S_head_out, sc, D);
+      if (cudaError_t e_ = launch_pdl(reduce_finalize_kernel<1>, grid, block, 0, s, partial, wdn, fo, n_chunks, T, H,
+                                      G, I, I_pad, S_out, S_head_out, sc, D); e_ != cudaSuccess)
+        return e_;
       break;
     case 2:
-      reduce_finalize_kernel<2><<<grid, block, 0, s>>>(partial, wdn, fo, n_chunks, T, H, G, I, I_pad, S_out,
-                                                          S_head_out, sc, D);
+      if (cudaError_t e_ = launch_pdl(reduce_finalize_kernel<2>, grid, block, 0, s, partial, wdn, fo, n_chunks, T, H,
+                                      G, I, I_pad, S_out, S_head_out, sc, D); e_ != cudaSuccess)
+        return e_;
       break;
     case 4:
-      reduce_finalize_kernel<4><<<grid, block, 0, s>>>(partial, wdn, fo, n_chunks, T, H, G, I, I_pad, S_out,
-                                                          S_head_out, sc, D);
+      if (cudaError_t e_ = launch_pdl(reduce_finalize_kernel<4>, grid, block, 0, s, partial, wdn, fo, n_chunks, T, H,
+                                      G, I, I_pad, S_out, S_head_out, sc, D); e_ != cudaSuccess)
+        return e_;
       break;
     default:
       return cudaErrorInvalidValue;
@@ -895,41 +921,50 @@ cudaError_t launch_finalize_up(const double* sh, const float* wdn, int fo, int T
 
 cudaError_t launch_to_fp16(const uint16_t* in, __half* out, size_t n, uint32_t* status, cudaStream_t s) {
   const size_t blocks = (n / 8 + 255) / 256;
-  to_fp16_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(in, out, n, status);
+  if (cudaError_t e_ = launch_pdl(to_fp16_kernel, (unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s, in, out, n,
+                                  status); e_ != cudaSuccess)
+    return e_;
   return cudaGetLastError();
 }
 
 cudaError_t launch_loo_rho(const float* cn, const float* inv_r, float* rho, int T, int T_pad, int H, int D,
                            int groups, const DevScales* sc, cudaStream_t s) {
-  loo_rho_kernel<<<dim3((T_pad + 255) / 256, H), 256, 0, s>>>(cn, inv_r, rho, T, T_pad, H, D, groups, sc);
+  if (cudaError_t e_ = launch_pdl(loo_rho_kernel, dim3((T_pad + 255) / 256, H), 256, 0, s, cn, inv_r, rho, T, T_pad,
+                                  H, D, groups, sc); e_ != cudaSuccess)
+    return e_;
   return cudaGetLastError();
 }
 
 cudaError_t launch_prep_wd(const uint16_t* Wd, __half* Wd16, __half* WdT16, int D, int I, int I_pad, uint32_t* status,
                            cudaStream_t s) {
   dim3 grid((I_pad + 31) / 32, (D + 31) / 32), block(32, 8);
-  prep_wd_kernel<<<grid, block, 0, s>>>(Wd, Wd16, WdT16, D, I, I_pad, status);
+  if (cudaError_t e_ = launch_pdl(prep_wd_kernel, grid, block, 0, s, Wd, Wd16, WdT16, D, I, I_pad, status); e_ != cudaSuccess)
+    return e_;
   return cudaGetLastError();
 }
 
 cudaError_t launch_prep_qkv(const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* gamma_next,
                             __half* out, int G, int hpg, int dh, int D, uint32_t* status, cudaStream_t s) {
-  prep_qkv_kernel<<<blocks_for((size_t)G * (hpg + 2) * dh * D, 256), 256, 0, s>>>(Wq, Wk, Wv, gamma_next, out, G, hpg,
-                                                                                 dh, D, status);
+  if (cudaError_t e_ = launch_pdl(prep_qkv_kernel, blocks_for((size_t)G * (hpg + 2) * dh * D, 256), 256, 0, s, Wq, Wk,
+                                  Wv, gamma_next, out, G, hpg, dh, D, status); e_ != cudaSuccess)
+    return e_;
   return cudaGetLastError();
 }
 
 cudaError_t launch_down_token_weights(const __half* alpha16, const float* ssx, float* cpart, int T, int T_pad, int D,
                                       int I_pad, int chunk, float eps, int groups, cudaStream_t s) {
   dim3 grid((I_pad / 8 + 127) / 128, (T + chunk - 1) / chunk);
-  down_token_weights_kernel<<<grid, 128, (size_t)chunk * sizeof(float), s>>>(alpha16, ssx, cpart, T, T_pad, D,
-                                                                             I_pad, chunk, eps, groups);
+  if (cudaError_t e_ = launch_pdl(down_token_weights_kernel, grid, 128, (size_t)chunk * sizeof(float), s, alpha16,
+                                  ssx, cpart, T, T_pad, D, I_pad, chunk, eps, groups); e_ != cudaSuccess)
+    return e_;
   return cudaGetLastError();
 }
 
 cudaError_t launch_finalize_down(const float* cpart, const float* bnorm, int n_chunks, int bhalves, int T, int I,
                                  int I_pad, int G, float* S_out, cudaStream_t s) {
-  finalize_down_kernel<<<(I + 31) / 32, 256, 0, s>>>(cpart, bnorm, n_chunks, bhalves, T, I, I_pad, G, S_out);
+  if (cudaError_t e_ = launch_pdl(finalize_down_kernel, (I + 31) / 32, 256, 0, s, cpart, bnorm, n_chunks, bhalves, T,
+                                  I, I_pad, G, S_out); e_ != cudaSuccess)
+    return e_;
   return cudaGetLastError();
 }
 

@@ -6,6 +6,7 @@
 #include "moment_kernel.cuh"
 #include "scales.cuh"
 #include "sm103_primitives.cuh"
+#include "launch.cuh"
 
 namespace aff {
 
@@ -21,6 +22,7 @@ __device__ __forceinline__ float bf2f_m(uint16_t b) { return __uint_as_float((ui
 // order as the token-major staging of the other passes).
 __global__ void __launch_bounds__(256) inv_r_kernel(const uint16_t* __restrict__ x, float* __restrict__ inv_r, int T,
                                                     int n_pad, int D, float eps) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int n_warps = (gridDim.x * blockDim.x) >> 5;
   for (int t = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 2; t < n_pad; t += 2 * n_warps) {
@@ -72,6 +74,7 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float* __restric
                                                           float* __restrict__ scale, int n_chunks, int H, int dh,
                                                           uint32_t* status, const uint16_t* __restrict__ a,
                                                           const float* __restrict__ inv_r, int T, DevScales* sc) {
+  pdl_enter();
   __shared__ float s_sh;
   __shared__ int redo_s;
   __shared__ uint32_t top_s;
@@ -145,6 +148,7 @@ __global__ void __launch_bounds__(1024) moment_fallback_kernel(const uint16_t* _
                                                               const float* __restrict__ inv_r, int T, int H, int dh,
                                                               __half* __restrict__ CC, float* __restrict__ scale,
                                                               const DevScales* __restrict__ sc, uint32_t* status) {
+  pdl_enter();
   if (sc->redo == 0u) return;
   const float am = bits_f(sc->amax2);
   if (!(am <= 3.4e38f)) {
@@ -202,6 +206,7 @@ __global__ void __launch_bounds__(256) moment_finalize_kernel(const float* __res
                                                               int I, int I_pad, float* __restrict__ S_out,
                                                               float* __restrict__ S_head_out,
                                                               const DevScales* __restrict__ sc, int D) {
+  pdl_enter();
   const int k = blockIdx.x * 256 + threadIdx.x, g = blockIdx.y;
   if (k >= I) return;
   const int hpg = H / G;
@@ -250,6 +255,7 @@ template <int MODE>
 __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_constant__ CUtensorMap mapA,
                                                                 const __grid_constant__ CUtensorMap mapB,
                                                                 const MomentParams p) {
+  pdl_enter();
   constexpr bool kGram = MODE == kMomentGram;
   constexpr int S = kGram ? kGramRawStages : kQuadStages;     // TMA stages
   constexpr int SO = kGram ? kGramOpStages : 1;                // Gram: operand tiles
@@ -522,13 +528,15 @@ cudaError_t launch_moment(const CUtensorMap* maps, const MomentParams& p, cudaSt
     auto* fn = moment_kernel<kMomentGram>;
     if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
       return e;
-    fn<<<p.n_units, kMomentThreads, smem, s>>>(maps[0], maps[1], p);
+    if (cudaError_t e_ = launch_pdl(fn, p.n_units, kMomentThreads, smem, s, maps[0], maps[1], p); e_ != cudaSuccess)
+      return e_;
   } else if (p.mode == kMomentQuad) {
     if (p.nkb > kQuadStages) return cudaErrorInvalidValue;
     auto* fn = moment_kernel<kMomentQuad>;
     if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
       return e;
-    fn<<<p.n_units, kMomentThreads, smem, s>>>(maps[0], maps[1], p);
+    if (cudaError_t e_ = launch_pdl(fn, p.n_units, kMomentThreads, smem, s, maps[0], maps[1], p); e_ != cudaSuccess)
+      return e_;
   } else {
     return cudaErrorInvalidValue;
   }
@@ -539,23 +547,28 @@ cudaError_t launch_inv_r(const uint16_t* x, float* inv_r, int T, int n_pad, int 
                         cudaStream_t s) {
   int blocks = (n_pad + 15) / 16;   // 8 warps, two tokens each
   if (blocks > 8 * sm_count) blocks = 8 * sm_count;
-  inv_r_kernel<<<blocks, 256, 0, s>>>(x, inv_r, T, n_pad, D, eps);
+  if (cudaError_t e_ = launch_pdl(inv_r_kernel, blocks, 256, 0, s, x, inv_r, T, n_pad, D, eps); e_ != cudaSuccess)
+    return e_;
   return cudaGetLastError();
 }
 
 cudaError_t launch_gram_reduce(const float* gram, const float* cmax, __half* CC, float* scale, int n_chunks, int H,
                                int dh, uint32_t* status, const uint16_t* a, const float* inv_r, int T, DevScales* sc,
                                cudaStream_t s) {
-  gram_reduce_kernel<<<dim3(H, 128 / kReduceRows), 256, 0, s>>>(gram, cmax, CC, scale, n_chunks, H, dh, status, a,
-                                                                  inv_r, T, sc);
+  if (cudaError_t e_ = launch_pdl(gram_reduce_kernel, dim3(H, 128 / kReduceRows), 256, 0, s, gram, cmax, CC, scale,
+                                  n_chunks, H, dh, status, a, inv_r, T, sc); e_ != cudaSuccess)
+    return e_;
   if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
-  moment_fallback_kernel<<<H, 1024, 0, s>>>(a, inv_r, T, H, dh, CC, scale, sc, status);
+  if (cudaError_t e_ = launch_pdl(moment_fallback_kernel, H, 1024, 0, s, a, inv_r, T, H, dh, CC, scale, sc, status); e_ != cudaSuccess)
+    return e_;
   return cudaGetLastError();
 }
 
 cudaError_t launch_moment_finalize(const float* out, int T, int H, int G, int I, int I_pad, float* S_out,
                                    float* S_head_out, const DevScales* sc, int D, cudaStream_t s) {
-  moment_finalize_kernel<<<dim3((I + 255) / 256, G), 256, 0, s>>>(out, T, H, G, I, I_pad, S_out, S_head_out, sc, D);
+  if (cudaError_t e_ = launch_pdl(moment_finalize_kernel, dim3((I + 255) / 256, G), 256, 0, s, out, T, H, G, I, I_pad,
+                                  S_out, S_head_out, sc, D); e_ != cudaSuccess)
+    return e_;
   return cudaGetLastError();
 }
 

@@ -30,6 +30,7 @@
 #include "tile_kernel.cuh"
 
 #include <cuda_fp16.h>
+#include "launch.cuh"
 
 namespace aff {
 
@@ -182,6 +183,11 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
     affinity_tile_kernel(const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
                          const __grid_constant__ CUtensorMap map2, const __grid_constant__ CUtensorMap map3,
                          const TileParams p) {
+  pdl_enter();
+  // The next kernel in the stream may be placed beside this one's CTAs at once (it waits
+  // for this kernel to complete before touching memory).  Not in the FO pass: there the
+  // early arrivals (the reduction's 512-thread blocks) measured 10 us slower per launch.
+  if constexpr (MODE != kModeFO) pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -829,7 +835,8 @@ static cudaError_t launch_mode(const CUtensorMap* maps, const TileParams& p, int
     *grid = n;   // shared memory and TMEM allow one CTA per SM
     return e;
   }
-  fn<<<*grid, block_threads(MODE), smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+  if (cudaError_t e_ = launch_pdl(fn, *grid, block_threads(MODE), smem, stream, maps[0], maps[1], maps[2], maps[3], p); e_ != cudaSuccess)
+    return e_;
   return cudaGetLastError();
 }
 

@@ -179,39 +179,58 @@ __global__ void __launch_bounds__(256) prep_gate_up_kernel(const uint16_t* __res
 }
 
 // GWo16[n][part][d] for part 0/1 = fp16 hi / lo of gamma_d * Wo[d][n] * f (a
-// transposed, split copy through 32 x 32 shared-memory tiles: hi + lo carries ~22
-// significant bits of the exact fp32 product); 256 threads, grid-stride over
-// tiles starting at tile0.  Folds max |gamma_d Wo[d][n]| (before f) into gm and
-// max |Wo[d][n]| into om.
+// transposed, split copy through 64 x 64 shared-memory tiles, 16-byte loads and
+// stores: hi + lo carries ~22 significant bits of the exact fp32 product); 256
+// threads, grid-stride over tiles starting at tile0.  D and HD are multiples of
+// 8, so an 8-element chunk is wholly inside or wholly outside.  Folds
+// max |gamma_d Wo[d][n]| (before f) into gm and max |Wo[d][n]| into om.
 __device__ __forceinline__ void stage_gwo_tiles(const uint16_t* __restrict__ Wo, const uint16_t* __restrict__ gamma,
                                                 __half* __restrict__ GWo16, int D, int HD, int tile0, int ntiles_step,
                                                 float f, uint32_t& gm, uint32_t& om) {
-  __shared__ float tile[32][33];
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int tn = (HD + 31) / 32, td = (D + 31) / 32;
+  __shared__ float tile[64][65];   // [d][n], padded: column reads hit distinct banks but for 2-way
+  const int tn = (HD + 63) / 64, td = (D + 63) / 64;
   for (int tt = tile0; tt < tn * td; tt += ntiles_step) {
-    const int d0 = (tt / tn) * 32, n0 = (tt % tn) * 32;
+    const int d0 = (tt / tn) * 64, n0 = (tt % tn) * 64;
     __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
-      const int d = d0 + i, n = n0 + tx;
-      float gw = 0.f;
+    // 64 rows d x 8 chunks of 8 columns n
+    for (int it = threadIdx.x; it < 512; it += 256) {
+      const int i = it >> 3, c = (it & 7) * 8;
+      const int d = d0 + i, n = n0 + c;
+      float gw[8];
       if (d < D && n < HD) {
-        const float w = bf2f(Wo[(size_t)d * HD + n]);
-        om = max(om, __float_as_uint(fabsf(w)));
-        gw = bf2f(gamma[d]) * w;
-        gm = max(gm, __float_as_uint(fabsf(gw)));
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(Wo + (size_t)d * HD + n));
+        const uint16_t* e = reinterpret_cast<const uint16_t*>(&q);
+        const float g = bf2f(gamma[d]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float w = bf2f(e[j]);
+          om = max(om, __float_as_uint(fabsf(w)));
+          gw[j] = g * w;
+          gm = max(gm, __float_as_uint(fabsf(gw[j])));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) gw[j] = 0.f;
       }
-      tile[i][tx] = gw * f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) tile[i][c + j] = gw[j] * f;
     }
     __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
-      const int n = n0 + i, d = d0 + tx;
+    // 64 rows n x 8 chunks of 8 columns d, hi and lo
+    for (int it = threadIdx.x; it < 512; it += 256) {
+      const int i = it >> 3, c = (it & 7) * 8;
+      const int n = n0 + i, d = d0 + c;
       if (n < HD && d < D) {
-        const float v = tile[tx][i];
-        const __half hi = __float2half_rn(v);
-        const __half lo = __float2half_rn(v - __half2float(hi));
-        GWo16[((size_t)n * 2 + 0) * D + d] = hi;
-        GWo16[((size_t)n * 2 + 1) * D + d] = lo;
+        __align__(16) __half hi[8];
+        __align__(16) __half lo[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float v = tile[c + j][i];
+          hi[j] = __float2half_rn(v);
+          lo[j] = __float2half_rn(v - __half2float(hi[j]));
+        }
+        *reinterpret_cast<uint4*>(GWo16 + ((size_t)n * 2 + 0) * D + d) = *reinterpret_cast<const uint4*>(hi);
+        *reinterpret_cast<uint4*>(GWo16 + ((size_t)n * 2 + 1) * D + d) = *reinterpret_cast<const uint4*>(lo);
       }
     }
   }
@@ -835,7 +854,7 @@ cudaError_t launch_weight_stage(const uint16_t* Wg, const uint16_t* Wu, __half* 
                                 const uint16_t* Wo, const uint16_t* gamma, __half* GWo16, int HD, DevScales* sc,
                                 int sm_count, cudaStream_t s) {
   int g0 = (2 * I_pad + 7) / 8;                          // one warp per W16 row
-  const int g1 = ((HD + 31) / 32) * ((D + 31) / 32);     // gamma*Wo^T tiles
+  const int g1 = ((HD + 63) / 64) * ((D + 63) / 64);     // gamma*Wo^T tiles
   if (g0 < g1) g0 = g1;
   if (g0 > 4 * sm_count) g0 = 4 * (sm_count > 0 ? sm_count : 1);
   if (cudaError_t e_ = launch_pdl(weight_stage_kernel, dim3(g0, 2), 256, 0, s, Wg, Wu, W16, I, I_pad, D, Wo, gamma,

@@ -83,12 +83,22 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float* __restric
   const float* g0 = gram + (size_t)h * 128 * 128;
   if (threadIdx.x == 0) top_s = 0u;
   __syncthreads();
-  // every head's s_h (a thread per head, chunks in order): any not finite, and the largest
+  // every head's s_h (a thread per head, chunks in order; the loads eight at a time ahead
+  // of the sum): any not finite, and the largest.  The thread of head h keeps its sum.
   bool nonfinite = false;
   float top = 0.f;
   for (int hh = threadIdx.x; hh < H; hh += 256) {
     float m = 0.f;
-    for (int c = 0; c < n_chunks; ++c) m += cmax[(size_t)c * H + hh];
+    int c = 0;
+    for (; c + 8 <= n_chunks; c += 8) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = cmax[(size_t)(c + j) * H + hh];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m += v[j];
+    }
+    for (; c < n_chunks; ++c) m += cmax[(size_t)c * H + hh];
+    if (hh == h) s_sh = m;
     if (isfinite(m)) top = fmaxf(top, m);
     else nonfinite = true;
   }
@@ -96,8 +106,7 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float* __restric
   const int any_nonfinite = __syncthreads_or(nonfinite ? 1 : 0);
   if (threadIdx.x == 0) {
     redo_s = (any_nonfinite || __uint_as_float(top_s) < (float)T * (1.0f / 65536.0f)) ? 1 : 0;
-    float m = 0.f;
-    for (int c = 0; c < n_chunks; ++c) m += cmax[(size_t)c * H + h];
+    float m = s_sh;
     if (!(m > 0.f) || !isfinite(m)) m = 1.f;
     s_sh = m;
     if (h == 0 && y == 0) sc->redo = (uint32_t)redo_s;

@@ -250,18 +250,18 @@ aff_status make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* d
   return AFF_OK;
 }
 
-// 16-bit tensor [rows][inner] (row stride inner * 2 bytes), no swizzle, box
-// (box0 innermost elements, box1 rows); OOB reads zero.
-aff_status map_plain_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box0, uint32_t box1) {
+// 16-bit tensor [rows][inner] (row stride inner * 2 bytes), box (32 innermost
+// elements = 64 bytes, box1 rows), 64-byte swizzle; OOB reads zero.
+aff_status map_sw64_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box1) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     g_last_cuda_error = "cuTensorMapEncodeTiled unavailable";
     return AFF_ERR_CUDA;
   }
   cuuint64_t gd[2] = {inner, rows}, gs[1] = {inner * 2};
-  cuuint32_t bx[2] = {box0, box1}, es[2] = {1, 1};
+  cuuint32_t bx[2] = {32, box1}, es[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(ptr), gd, gs, bx, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char buf[96];
@@ -568,8 +568,8 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     CUtensorMap mm[2];
     std::memset(mm, 0, sizeof mm);
     {
-      // a (bf16 bits) as [T][H*dh], unswizzled boxes of one head's dh columns x 64 tokens
-      if ((st = map_plain_2d(&mm[0], a, (uint64_t)H * dh, (uint64_t)T, (uint32_t)dh, 64)) != AFF_OK) return st;
+      // a (bf16 bits) as [T][H*dh], boxes of 32 columns x 64 tokens, 64-byte swizzle
+      if ((st = map_sw64_2d(&mm[0], a, (uint64_t)H * dh, (uint64_t)T, 64)) != AFF_OK) return st;
       mm[1] = mm[0];
       MomentParams mp{};
       mp.mode = kMomentGram;
@@ -602,6 +602,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
       mp.H = H; mp.dh = dh; mp.HD = H * dh; mp.I_pad = I_pad;
       mp.nkb = (int)ceil_div(dh, 64);
       mp.stream = stream_heads(d) ? 1 : 0;
+      mp.ctas = 2 * sm_count;
       mp.status = status;
       mp.scale = gscale;
       mp.M16 = M16;

@@ -266,22 +266,26 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
                                                                 const MomentParams p) {
   pdl_enter();
   constexpr bool kGram = MODE == kMomentGram;
-  constexpr int S = kGram ? kGramRawStages : kQuadStages;     // TMA stages
-  constexpr int SO = kGram ? kGramOpStages : 1;                // Gram: operand tiles
-  constexpr uint32_t kSB = kGram ? kGramRawBytes : 3 * kMomentTileBytes;
+  constexpr int S = kGram ? kGramStages : kQuadStages;        // TMA stages
+  constexpr uint32_t kSB = kGram ? kGramStageBytes : 3 * kMomentTileBytes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  // Gram: operand tiles first (1024-byte aligned), raw stages after them
-  uint8_t* op0 = base;
-  uint8_t* st0 = kGram ? base + (size_t)SO * kMomentTileBytes : base;
-  __shared__ uint64_t full[S], empty[S], ofull[SO], oempty[SO], tfull, drain;
+  // stages first (1024-byte aligned); Gram: then 64 floats of 1/r per stage
+  uint8_t* st0 = base;
+  float* irs0 = reinterpret_cast<float*>(base + (size_t)S * kSB);
+  constexpr int NB = kGram ? 1 : 2;   // accumulator buffers (quad: one unit's MMAs beside the last one's epilogue)
+  // Gram: full = the TMA copies landed, cvt = the converter warps rewrote the stage, empty =
+  // the MMAs read it.  Quad: full, empty.
+  __shared__ uint64_t full[S], empty[S], cvt[kGram ? S : 1], tfull[NB], tempty[NB], drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_s;
   __shared__ uint32_t dmax_s;   // Gram: the largest diagonal entry of the unit's block (fp32 bits, >= 0)
   volatile int* abort_flag = &abort_s;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Gram: one unit per CTA; quad: a persistent grid walks units blockIdx.x, + gridDim.x, ...
+  const int ustep = kGram ? p.n_units : (int)gridDim.x;
   const int h = (int)blockIdx.x % p.H, c = (int)blockIdx.x / p.H;
   int kb0 = 0, nkb = p.nkb;
   if (kGram) {
@@ -292,13 +296,13 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kGram ? 4 : 1);   // Gram: one arrival per converter warp
+      mbar_init(&empty[s], 1);
+      if (kGram) mbar_init(&cvt[s], 4);   // one arrival per converter warp
     }
-    for (int s = 0; s < SO; ++s) {
-      mbar_init(&ofull[s], 4);
-      mbar_init(&oempty[s], 1);
+    for (int b = 0; b < NB; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);   // one arrival per epilogue warp
     }
-    mbar_init(&tfull, 1);
     mbar_init(&drain, 1);
     abort_s = 0;
     dmax_s = 0u;
@@ -309,15 +313,17 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
     if (!kGram) prefetch_tmap(&mapB);
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_slot, 128);
+    tmem_alloc(&tmem_slot, 128 * NB);
     tmem_relinquish();
   }
-  if (kGram && warp >= 2 && p.dh < kMomentRows) {
-    // rows dh..127 of the operand tiles are never written: zero them for the MMAs
-    const int tail = (kMomentRows - p.dh) * 128 / 16;   // uint4 per tile
-    for (int i = threadIdx.x - 64; i < SO * tail; i += 128) {
-      const int s = i / tail, e = i % tail;
-      reinterpret_cast<uint4*>(op0 + (size_t)s * kMomentTileBytes + (size_t)p.dh * 128)[e] = make_uint4(0, 0, 0, 0);
+  // Gram: boxes of 32 features per stage; the MMA reads all four, so the ones past
+  // ceil(d_head / 32) are zeroed once (the TMA never writes them)
+  const int gboxes = kGram ? (p.dh + 31) / 32 : 0;
+  if (kGram && warp >= 2 && gboxes < 4) {
+    const int per = (4 - gboxes) * kGramBox / 16;   // uint4 per stage
+    for (int i = threadIdx.x - 64; i < S * per; i += 128) {
+      const int s = i / per, e = i % per;
+      reinterpret_cast<uint4*>(st0 + (size_t)s * kSB + (size_t)gboxes * kGramBox)[e] = make_uint4(0, 0, 0, 0);
     }
     fence_async_smem();   // visible to the tensor-core reads
   }
@@ -329,26 +335,31 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
-      int issued = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % S;
-        const uint32_t ph = (uint32_t)((kb / S) & 1);
-        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
-        uint8_t* st = st0 + (size_t)s * kSB;
-        if constexpr (kGram) {
-          mbar_arrive_expect_tx(&full[s], (uint32_t)p.dh * 128u + 256u);
-          tma_load_2d(st, &mapA, &full[s], h * p.dh, (kb0 + kb) * 64);
-          bulk_load(st + kGramRawTile, p.inv_r + (size_t)(kb0 + kb) * 64, 256u, &full[s]);
-        } else {
-          mbar_arrive_expect_tx(&full[s], kSB);
-          if (p.stream)
-            tma_load_2d(st, &mapA, &full[s], h * p.dh + kb * 64, c * kMomentRows);
-          else
-            tma_load_3d(st, &mapA, &full[s], kb * 64, c * kMomentRows, h);
-          tma_load_2d(st + kMomentTileBytes, &mapB, &full[s], kb * 64, h * kMomentRows);
-          tma_load_2d(st + 2 * kMomentTileBytes, &mapB, &full[s], kb * 64, (p.H + h) * kMomentRows);
+      int issued = 0;   // stage uses so far (the ring runs on across units)
+      for (int u = (int)blockIdx.x; ok && u < p.n_units; u += ustep) {
+        const int uh = u % p.H, uc = u / p.H;
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int s = issued % S;
+          const uint32_t ph = (uint32_t)((issued / S) & 1);
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          uint8_t* st = st0 + (size_t)s * kSB;
+          if constexpr (kGram) {
+            // a's columns uh*dh .. + 32*gboxes (past dh: the next head's, or zeros past H*dh)
+            mbar_arrive_expect_tx(&full[s], (uint32_t)(gboxes * kGramBox) + 256u);
+            for (int bx = 0; bx < gboxes; ++bx)
+              tma_load_2d(st + bx * kGramBox, &mapA, &full[s], uh * p.dh + 32 * bx, (kb0 + kb) * 64);
+            bulk_load(irs0 + s * 64, p.inv_r + (size_t)(kb0 + kb) * 64, 256u, &full[s]);
+          } else {
+            mbar_arrive_expect_tx(&full[s], kSB);
+            if (p.stream)
+              tma_load_2d(st, &mapA, &full[s], uh * p.dh + kb * 64, uc * kMomentRows);
+            else
+              tma_load_3d(st, &mapA, &full[s], kb * 64, uc * kMomentRows, uh);
+            tma_load_2d(st + kMomentTileBytes, &mapB, &full[s], kb * 64, uh * kMomentRows);
+            tma_load_2d(st + 2 * kMomentTileBytes, &mapB, &full[s], kb * 64, (p.H + uh) * kMomentRows);
+          }
+          ++issued;
         }
-        ++issued;
       }
       if (!ok) {
         // let every copy already issued land before shared memory is released
@@ -362,35 +373,46 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16(128, 128, 0);
+      // Gram: A = B = the stage, MN-major (features along M and N, tokens along K)
+      constexpr uint32_t idesc = kGram ? idesc_f16_mn(128, 128, 0) : idesc_f16(128, 128, 0);
       constexpr uint64_t kT = (uint64_t)(kMomentTileBytes >> 4);
       bool ok = true;
-      for (int kb = 0; kb < nkb; ++kb) {
-        if constexpr (kGram) {
-          const int so = kb % SO;
-          if (!mbar_wait(&ofull[so], (uint32_t)((kb / SO) & 1), abort_flag, p.status)) { ok = false; break; }
+      int g = 0;   // stage uses so far (quad)
+      for (int u = (int)blockIdx.x, li = 0; ok && u < p.n_units; u += ustep, ++li) {
+        const int b = li % NB;
+        if constexpr (!kGram) {
+          // the buffer's previous unit must have been read out by the epilogue
+          if (!mbar_wait(&tempty[b], (uint32_t)(((li / NB) & 1) ^ 1), abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t da = smem_desc_k_sw128(smem_u32(op0 + (size_t)so * kMomentTileBytes));
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_f16_ss(tmem, da + 2 * ks, da + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
-          mma_commit(&oempty[so]);
-        } else {
-          const int s = kb % S;
-          if (!mbar_wait(&full[s], (uint32_t)((kb / S) & 1), abort_flag, p.status)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t da = smem_desc_k_sw128(smem_u32(st0 + (size_t)s * kSB));
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            mma_f16_ss(tmem, da + 2 * ks, da + kT + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
-            mma_f16_ss(tmem, da + 2 * ks, da + 2 * kT + 2 * ks, idesc, 1u);
-          }
-          mma_commit(&empty[s]);
         }
+        const uint32_t d = tmem + (uint32_t)(b * 128);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if constexpr (kGram) {
+            const int s = kb % S;
+            if (!mbar_wait(&cvt[s], (uint32_t)((kb / S) & 1), abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t da = smem_desc_mn_sw64(smem_u32(st0 + (size_t)s * kSB), kGramBox);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)   // 16 tokens = 16 rows of 64 B per K slice
+              mma_f16_ss(d, da + 64 * ks, da + 64 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
+            mma_commit(&empty[s]);
+          } else {
+            const int s = g % S;
+            if (!mbar_wait(&full[s], (uint32_t)((g / S) & 1), abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t da = smem_desc_k_sw128(smem_u32(st0 + (size_t)s * kSB));
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              mma_f16_ss(d, da + 2 * ks, da + kT + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
+              mma_f16_ss(d, da + 2 * ks, da + 2 * kT + 2 * ks, idesc, 1u);
+            }
+            mma_commit(&empty[s]);
+            ++g;
+          }
+        }
+        if (ok) mma_commit(&tfull[b]);
       }
-      if (ok) {
-        mma_commit(&tfull);
-      } else {
+      if (!ok) {
         mma_commit(&drain);
         volatile int dummy = 0;
         mbar_wait(&drain, 0, &dummy, p.status, 100000000ull);
@@ -402,70 +424,41 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
     int w_ok = 1;
     if constexpr (kGram) {
-      // ---- converter: raw stage (bf16 [64][dh] + 1/r) -> operand tile
-      // Jobs are (feature pair pp, group tc of 8 tokens), 8 * dh / 2 of them, at most 4 per
-      // thread; a thread's jobs are the same in every K block, so their offsets are set once.
+      // ---- converter: each stage rewritten in place, bf16 a -> fp16 a/r.  A 16-byte chunk
+      // holds 8 features of one token; the 64-byte swizzle only permutes chunks within a
+      // token's 64-byte row, so chunk X of a box belongs to token (X % 256) / 4.
       // An fp16 overflow needs no check here: it becomes inf in the operand, so the
       // head's diagonal is not finite and the reduction latches the range error.
       const int ct = threadIdx.x - 64;   // 0..127
-      const int P = p.dh / 2;            // 32-bit words (feature pairs) per token row
-      int nj = 0;
-      int src_off[4], ir_off[4];
-      uint32_t dst0[4], dst1[4];
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        const int j = ct + 128 * n;
-        const int pp = j % P, tc = j / P, f = 2 * pp;
-        src_off[n] = tc * 8 * P + pp;
-        ir_off[n] = tc * 8;
-        dst0[n] = (uint32_t)f * 128u + (((uint32_t)tc ^ (uint32_t)(f & 7)) << 4);
-        dst1[n] = (uint32_t)(f + 1) * 128u + (((uint32_t)tc ^ (uint32_t)((f + 1) & 7)) << 4);
-        if (j < 8 * P) nj = n + 1;
-      }
+      const int nch = gboxes * (kGramBox / 16);
       for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % S, so = kb % SO;
+        const int s = kb % S;
         int ok = 1;
-        if (lane == 0)
-          ok = (mbar_wait(&full[s], (uint32_t)((kb / S) & 1), abort_flag, p.status) &&
-                mbar_wait(&oempty[so], (uint32_t)((kb / SO) & 1) ^ 1u, abort_flag, p.status))
-                   ? 1 : 0;
+        if (lane == 0) ok = mbar_wait(&full[s], (uint32_t)((kb / S) & 1), abort_flag, p.status) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) { w_ok = 0; break; }
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(st0 + (size_t)s * kSB);
-        const float* irs = reinterpret_cast<const float*>(st0 + (size_t)s * kSB + kGramRawTile);
-        uint8_t* op = op0 + (size_t)so * kMomentTileBytes;
-#pragma unroll
-        for (int n = 0; n < 4; ++n) {
-          if (n < nj) {
-            uint32_t w[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) w[i] = src[src_off[n] + i * P];
-            const float4 ra = *reinterpret_cast<const float4*>(irs + ir_off[n]);
-            const float4 rb = *reinterpret_cast<const float4*>(irs + ir_off[n] + 4);
-            const uint64_t ir2[4] = {pk(ra.x, ra.y), pk(ra.z, ra.w), pk(rb.x, rb.y), pk(rb.z, rb.w)};
-            uint32_t lo[4], hi[4];   // features 2pp and 2pp+1, tokens in order
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              lo[i] = h2_bits(mul2(pk_u(w[2 * i] << 16, w[2 * i + 1] << 16), ir2[i]));
-              hi[i] = h2_bits(mul2(pk_u(w[2 * i] & 0xffff0000u, w[2 * i + 1] & 0xffff0000u), ir2[i]));
-            }
-            *reinterpret_cast<uint4*>(op + dst0[n]) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            *reinterpret_cast<uint4*>(op + dst1[n]) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          }
+        uint4* st = reinterpret_cast<uint4*>(st0 + (size_t)s * kSB);
+        const float* irs = irs0 + s * 64;
+#pragma unroll 2
+        for (int x = ct; x < nch; x += 128) {
+          const uint4 w = st[x];
+          const float ir = irs[(x & 255) >> 2];
+          const uint64_t ir2 = pk(ir, ir);
+          uint4 o;
+          o.x = h2_bits(mul2(pk_u(w.x << 16, w.x & 0xffff0000u), ir2));
+          o.y = h2_bits(mul2(pk_u(w.y << 16, w.y & 0xffff0000u), ir2));
+          o.z = h2_bits(mul2(pk_u(w.z << 16, w.z & 0xffff0000u), ir2));
+          o.w = h2_bits(mul2(pk_u(w.w << 16, w.w & 0xffff0000u), ir2));
+          st[x] = o;
         }
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&ofull[so]);
-          mbar_arrive(&empty[s]);
-        }
+        if (lane == 0) mbar_arrive(&cvt[s]);
       }
-    }
-    if (w_ok && lane == 0) w_ok = mbar_wait(&tfull, 0, abort_flag, p.status) ? 1 : 0;
-    w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-    if (w_ok) {
-      tc_fence_after();
-      if constexpr (kGram) {
+      if (w_ok && lane == 0) w_ok = mbar_wait(&tfull[0], 0, abort_flag, p.status) ? 1 : 0;
+      w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+      if (w_ok) {
+        tc_fence_after();
         // D[i][j] (i = this lane's feature row) goes to [j][i]: a warp's 32 lanes
         // write 128 contiguous bytes per column.
         float* dst = p.gram + (size_t)(c * p.H + h) * kMomentRows * kMomentRows + row;
@@ -484,15 +477,28 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) dg = fmaxf(dg, __shfl_xor_sync(0xffffffffu, dg, o));
         if (lane == 0) atomicMax(&dmax_s, __float_as_uint(dg));
-      } else {
-        const int rt = c;
+      }
+      // every epilogue warp arrives here, whether or not its waits succeeded
+      named_barrier_sync(1, 128);
+      if (w_ok && warp == 2 && lane == 0) p.cmax[(size_t)c * p.H + h] = __uint_as_float(dmax_s);
+    } else {
+      // ---- quad: the units of this CTA, accumulator buffers alternating
+      for (int u = (int)blockIdx.x, li = 0; u < p.n_units; u += ustep, ++li) {
+        const int b = li % NB;
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(&tfull[b], (uint32_t)((li / NB) & 1), abort_flag, p.status) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+        const int uh = u % p.H, rt = u / p.H;
         const __half* mrow = p.stream
-                                 ? p.M16 + (size_t)(rt * kMomentRows + row) * p.HD + (size_t)h * p.dh
-                                 : p.M16 + ((size_t)h * 2 * p.I_pad + (size_t)rt * kMomentRows + row) * p.dh;
+                                 ? p.M16 + (size_t)(rt * kMomentRows + row) * p.HD + (size_t)uh * p.dh
+                                 : p.M16 + ((size_t)uh * 2 * p.I_pad + (size_t)rt * kMomentRows + row) * p.dh;
+        const uint32_t tb = tl + (uint32_t)(b * 128);
         float acc = 0.f;
         for (int n0 = 0; n0 < p.dh; n0 += 16) {
           uint32_t v[16];
-          tmem_ld16(tl + (uint32_t)n0, v);
+          tmem_ld16(tb + (uint32_t)n0, v);
           const uint4 m0 = __ldg(reinterpret_cast<const uint4*>(mrow + n0));
           const uint4 m1 = n0 + 8 < p.dh ? __ldg(reinterpret_cast<const uint4*>(mrow + n0 + 8)) : make_uint4(0, 0, 0, 0);
           tmem_ld_wait();
@@ -503,16 +509,15 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
 #pragma unroll
           for (int i = 0; i < 8; ++i) acc = fmaf(__uint_as_float(v[8 + i]), __half2float(e1[i]), acc);
         }
-        acc *= p.scale[h];
+        // the buffer is read out: hand it back to the MMA warp
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[b]);
+        acc *= p.scale[uh];
         // rows 32q + l (gate) and 32q + 16 + l (up) are neuron 64 rt + 16 q + l
         const float pair = acc + __shfl_xor_sync(0xffffffffu, acc, 16);
-        if (lane < 16) p.out[(size_t)h * p.I_pad + (size_t)rt * 64 + q * 16 + lane] = pair;
+        if (lane < 16) p.out[(size_t)uh * p.I_pad + (size_t)rt * 64 + q * 16 + lane] = pair;
       }
-    }
-    if constexpr (kGram) {
-      // every epilogue warp arrives here, whether or not its waits succeeded
-      named_barrier_sync(1, 128);
-      if (w_ok && warp == 2 && lane == 0) p.cmax[(size_t)c * p.H + h] = __uint_as_float(dmax_s);
     }
   }
 
@@ -520,12 +525,12 @@ __global__ void __launch_bounds__(kMomentThreads) moment_kernel(const __grid_con
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 128 * NB);
   }
 }
 
 size_t moment_smem_bytes(int mode) {
-  return 1024 + (mode == kMomentGram ? (size_t)kGramOpStages * kMomentTileBytes + (size_t)kGramRawStages * kGramRawBytes
+  return 1024 + (mode == kMomentGram ? (size_t)kGramStages * (kGramStageBytes + 256)
                                      : (size_t)kQuadStages * 3 * kMomentTileBytes);
 }
 
@@ -544,7 +549,8 @@ cudaError_t launch_moment(const CUtensorMap* maps, const MomentParams& p, cudaSt
     auto* fn = moment_kernel<kMomentQuad>;
     if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
       return e;
-    if (cudaError_t e_ = launch_pdl(fn, p.n_units, kMomentThreads, smem, s, maps[0], maps[1], p); e_ != cudaSuccess)
+    const int grid = p.ctas > 0 && p.ctas < p.n_units ? p.ctas : p.n_units;
+    if (cudaError_t e_ = launch_pdl(fn, grid, kMomentThreads, smem, s, maps[0], maps[1], p); e_ != cudaSuccess)
       return e_;
   } else {
     return cudaErrorInvalidValue;

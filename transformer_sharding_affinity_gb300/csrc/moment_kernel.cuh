@@ -27,10 +27,12 @@ enum MomentMode : int {
 
 constexpr int kMomentRows = 128;                          // feature rows of a Gram tile, M_h rows of a quad tile
 constexpr int kMomentTileBytes = 128 * 64 * 2;            // one 128-row x 64-element fp16 tile
-constexpr int kGramRawStages = 4;                         // Gram: bf16 [64][d_head] + 64 floats of 1/r
-constexpr int kGramRawTile = 64 * 128 * 2;                // room for d_head <= 128
-constexpr int kGramRawBytes = kGramRawTile + 256;
-constexpr int kGramOpStages = 2;                          // Gram: fp16 operand tiles
+// Gram stage: 64 tokens of one head's columns of a, as up to four TMA boxes of 32
+// features x 64 tokens (64-byte rows, 64-byte swizzle), 4 KB each; the converter
+// warps rewrite them in place as fp16 a/r, which the MMA reads as MN-major operands.
+constexpr int kGramStages = 6;
+constexpr int kGramBox = 64 * 32 * 2;
+constexpr int kGramStageBytes = 4 * kGramBox;
 constexpr int kQuadStages = 2;                            // d_head <= 128: at most two K blocks
 constexpr int kMomentThreads = 192;                       // TMA warp, MMA warp, 4 epilogue warps
 // Units of the Gram pass: H x chunks with at most this many CTAs (two per SM on
@@ -45,6 +47,7 @@ struct MomentParams {
   int32_t nkb;       // Gram: 64-token K blocks in all, ceil(T / 64); quad: K blocks over d_head
   int32_t kpc;       // Gram: K blocks per token chunk
   int32_t stream;    // quad: M16 is [2 I_pad][H*dh] (else [H][2 I_pad][dh])
+  int32_t ctas;      // quad: CTAs of the persistent grid (<= n_units; two fit on an SM)
   uint32_t* status;
   float* gram;       // Gram output: [chunk][H][128 (column j)][128 (row i)] fp32
   float* cmax;       // Gram output: [chunk][H] the block's largest diagonal entry

@@ -219,6 +219,21 @@ __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile written by TMA
+// with 64-byte swizzling: rows of 32 16-bit elements (64 B) along M (or N),
+// one row per K index; 8-row swizzle atoms (512 B) follow each other along K,
+// and groups of 32 M elements lie `mn_group_bytes` apart.  The k-th 16-element
+// K slice starts 16 rows (1024 B) further.  `addr` must be 512-byte aligned.
+__device__ __forceinline__ uint64_t smem_desc_mn_sw64(uint32_t addr, uint32_t mn_group_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);            // start address
+  d |= static_cast<uint64_t>((mn_group_bytes >> 4) & 0x3FFFu) << 16;   // leading byte offset: next 32 M elements
+  d |= static_cast<uint64_t>(512 >> 4) << 32;                     // stride byte offset: next 8 K rows
+  d |= static_cast<uint64_t>(1) << 46;                            // descriptor version for tcgen05
+  d |= static_cast<uint64_t>(4) << 61;                            // swizzle mode: 64 B
+  return d;
+}
+
 // Instruction descriptor of kind::f16 with fp32 accumulation, both operands
 // K-major.  ab_bf16 selects bf16 (1) or fp16 (0) operands.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N, uint32_t ab_bf16) {
@@ -227,6 +242,10 @@ __host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N, uint32_
          | (ab_bf16 << 10)         // B format
          | ((N >> 3) << 17)        // N / 8
          | ((M >> 4) << 24);       // M / 16
+}
+// As idesc_f16 with both operands MN-major (the "transpose A / B" bits).
+__host__ __device__ constexpr uint32_t idesc_f16_mn(uint32_t M, uint32_t N, uint32_t ab_bf16) {
+  return idesc_f16(M, N, ab_bf16) | (1u << 15) | (1u << 16);
 }
 
 // ---------------------------------------------------------------- packed fp32x2 math (sm_100+)

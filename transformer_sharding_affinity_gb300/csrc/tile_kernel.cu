@@ -167,6 +167,7 @@ struct Smem {
   uint32_t* tmem_slot;
   volatile int* abort_flag;
   float* sacc;     // FO / ADD / LOO: the unit's sums [column group][H][128 neurons]
+  float4* rsc;     // LOO: per epilogue warp, sigma of its column group's tokens for the current head job
   uint8_t* stage0;
 };
 
@@ -209,6 +210,8 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
   sm.sacc = reinterpret_cast<float*>(cur);
   const int sacc_floats = kHeads ? NG * p.H * kBlockM : 0;
   cur += (size_t)sacc_floats * 4;
+  sm.rsc = reinterpret_cast<float4*>(cur);
+  if constexpr (MODE == kModeLOO) cur += (size_t)EW * (CWW / 4) * 16;
   sm.full = reinterpret_cast<uint64_t*>(cur);
   sm.empty = sm.full + S;
   sm.tfull = sm.empty + S;
@@ -467,6 +470,14 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
         tc_fence_after();
         const uint32_t c1 = tl + (uint32_t)(b * 2 * kBlockN + hf * CW);
         const uint32_t c2 = c1 + kBlockN;
+        float4* rsw = sm.rsc + (warp - 2) * (CWW / 4);   // LOO: this warp's sigma slots
+        if constexpr (MODE == kModeLOO) {
+          if (J.kind == kJobHead) {
+            __syncwarp();   // the previous head job's reads of the slots are done
+            if (lane < CWW / 4) rsw[lane] = rho_v;
+            __syncwarp();
+          }
+        }
 
         if constexpr (MODE == kModeFO || MODE == kModeLOO) {
           if (J.kind == kJobGateUp) {
@@ -606,11 +617,7 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
             float4 rq = make_float4(0.f, 0.f, 0.f, 0.f);   // LOO: sigma of the slice's 4 tokens
             if constexpr (MODE == kModeLOO) {
               static_assert(kW == 4, "one float4 of sigma per slice");
-              const int src = (upl ? CW / 4 : 0) + c;
-              rq.x = __shfl_sync(0xffffffffu, rho_v.x, src);
-              rq.y = __shfl_sync(0xffffffffu, rho_v.y, src);
-              rq.z = __shfl_sync(0xffffffffu, rho_v.z, src);
-              rq.w = __shfl_sync(0xffffffffu, rho_v.w, src);
+              rq = rsw[(upl ? CW / 4 : 0) + c];   // a broadcast read
             }
 #pragma unroll
             for (int i = 0; i < kW; i += 2) {
@@ -817,7 +824,9 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
 size_t tile_smem_bytes(int mode, int stages, int H) {
   const bool heads = mode == kModeFO || mode == kModeADD || mode == kModeLOO;
   const size_t sacc = heads ? (size_t)(epi_warps(mode) / 4) * H * kBlockM * 4 : 0;
-  return 1024 + (size_t)stages * kStageBytes + sacc + (size_t)(2 * stages + 5) * 8 + 8;
+  // LOO: a 16-byte sigma slot per 4 tokens of each epilogue warp's column group
+  const size_t rsc = mode == kModeLOO ? (size_t)epi_warps(mode) * (2 * kBlockN / (epi_warps(mode) / 4) / 4) * 16 : 0;
+  return 1024 + (size_t)stages * kStageBytes + sacc + rsc + (size_t)(2 * stages + 5) * 8 + 8;
 }
 
 // Launches `grid` CTAs.  With grid == 0 it only reports in *grid how many CTAs

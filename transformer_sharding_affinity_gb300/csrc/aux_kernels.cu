@@ -150,18 +150,25 @@ __device__ __forceinline__ void stage_w16_rows(const uint16_t* __restrict__ Wg, 
     const int blk = (r >> 4) & 1, k = (r >> 5) * 16 + (r & 15);
     const uint4* src = reinterpret_cast<const uint4*>((blk == 0 ? Wg : Wu) + (size_t)k * D);
     uint4* dst = reinterpret_cast<uint4*>(W16 + (size_t)r * D);
-    for (int c = lane; c < D8; c += 32) {
-      __align__(16) __half o[8];
-      if (k < I) {
-        const uint4 q = __ldg(src + c);
-        const uint16_t* e = reinterpret_cast<const uint16_t*>(&q);
+    // four 16-byte loads of the row in flight per lane, then their conversion
+    for (int c0 = lane; c0 < D8; c0 += 4 * 32) {
+      uint4 q[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = to_h_max(bf2f(e[i]) * f, m);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = __float2half_rn(0.f);
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + 32 * j;
+        q[j] = (k < I && c < D8) ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
       }
-      dst[c] = *reinterpret_cast<uint4*>(o);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + 32 * j;
+        if (c < D8) {
+          __align__(16) __half o[8];
+          const uint16_t* e = reinterpret_cast<const uint16_t*>(&q[j]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[i] = to_h_max(bf2f(e[i]) * f, m);
+          dst[c] = *reinterpret_cast<uint4*>(o);
+        }
+      }
     }
   }
 }
@@ -192,28 +199,31 @@ __device__ __forceinline__ void stage_gwo_tiles(const uint16_t* __restrict__ Wo,
   for (int tt = tile0; tt < tn * td; tt += ntiles_step) {
     const int d0 = (tt / tn) * 64, n0 = (tt % tn) * 64;
     __syncthreads();
-    // 64 rows d x 8 chunks of 8 columns n
-    for (int it = threadIdx.x; it < 512; it += 256) {
+    // 64 rows d x 8 chunks of 8 columns n: both of a thread's loads issued first
+    uint4 q[2];
+    uint16_t gb[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int it = threadIdx.x + 256 * u;
+      const int d = d0 + (it >> 3), n = n0 + (it & 7) * 8;
+      const bool in = d < D && n < HD;
+      q[u] = in ? __ldg(reinterpret_cast<const uint4*>(Wo + (size_t)d * HD + n)) : make_uint4(0u, 0u, 0u, 0u);
+      gb[u] = in ? gamma[d] : (uint16_t)0;
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int it = threadIdx.x + 256 * u;
       const int i = it >> 3, c = (it & 7) * 8;
-      const int d = d0 + i, n = n0 + c;
-      float gw[8];
-      if (d < D && n < HD) {
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(Wo + (size_t)d * HD + n));
-        const uint16_t* e = reinterpret_cast<const uint16_t*>(&q);
-        const float g = bf2f(gamma[d]);
+      const uint16_t* e = reinterpret_cast<const uint16_t*>(&q[u]);
+      const float g = bf2f(gb[u]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float w = bf2f(e[j]);
-          om = max(om, __float_as_uint(fabsf(w)));
-          gw[j] = g * w;
-          gm = max(gm, __float_as_uint(fabsf(gw[j])));
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) gw[j] = 0.f;
+      for (int j = 0; j < 8; ++j) {
+        const float w = bf2f(e[j]);
+        om = max(om, __float_as_uint(fabsf(w)));
+        const float gw = g * w;
+        gm = max(gm, __float_as_uint(fabsf(gw)));
+        tile[i][c + j] = gw * f;
       }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) tile[i][c + j] = gw[j] * f;
     }
     __syncthreads();
     // 64 rows n x 8 chunks of 8 columns d, hi and lo
@@ -856,7 +866,7 @@ cudaError_t launch_weight_stage(const uint16_t* Wg, const uint16_t* Wu, __half* 
   int g0 = (2 * I_pad + 7) / 8;                          // one warp per W16 row
   const int g1 = ((HD + 63) / 64) * ((D + 63) / 64);     // gamma*Wo^T tiles
   if (g0 < g1) g0 = g1;
-  if (g0 > 4 * sm_count) g0 = 4 * (sm_count > 0 ? sm_count : 1);
+  if (g0 > 8 * sm_count) g0 = 8 * (sm_count > 0 ? sm_count : 1);
   if (cudaError_t e_ = launch_pdl(weight_stage_kernel, dim3(g0, 2), 256, 0, s, Wg, Wu, W16, I, I_pad, D, Wo, gamma,
                                   GWo16, HD, sc); e_ != cudaSuccess)
     return e_;

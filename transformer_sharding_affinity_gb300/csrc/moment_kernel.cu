@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(256) inv_r_kernel(const uint16_t* __restrict__
 }
 
 // ---------------------------------------------------------------- Gram reduction
-// Block = (head h, 4 rows n).  s_h = the sum over chunks of each chunk's
+// Block = (head h, 2 rows n).  s_h = the sum over chunks of each chunk's
 // largest diagonal entry (in chunk order; every block computes the same value),
 // an upper bound on max_i C_h[i][i], so |C_h[n][i]| <= sqrt(C_ii C_nn) <= s_h.
 // Each entry is summed in chunk order and C_h / s_h is split into an fp16 high
@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(256) inv_r_kernel(const uint16_t* __restrict__
 // recomputed with a power-of-two scale by moment_fallback_kernel: this kernel
 // then records that decision, adds its share of max |a/r| over all tokens to
 // sc->amax2, and writes nothing else.
-constexpr int kReduceRows = 4;
+constexpr int kReduceRows = 2;   // one entry of C_h per thread
 
 __global__ void __launch_bounds__(256) gram_reduce_kernel(const float* __restrict__ gram,
                                                           const float* __restrict__ cmax, __half* __restrict__ CC,

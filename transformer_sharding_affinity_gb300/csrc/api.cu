@@ -376,7 +376,7 @@ aff_status run_tile(const CUtensorMap* maps, TileParams& p, cudaStream_t s, bool
 struct SideStream {
   int dev = -1;
   cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr, join_late = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, join_late = nullptr, mid = nullptr;
 };
 
 aff_status side_stream(SideStream** out) {
@@ -394,6 +394,7 @@ aff_status side_stream(SideStream** out) {
   AFF_CUDA(cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming));
   AFF_CUDA(cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming));
   AFF_CUDA(cudaEventCreateWithFlags(&ss.join_late, cudaEventDisableTiming));
+  AFF_CUDA(cudaEventCreateWithFlags(&ss.mid, cudaEventDisableTiming));
   per_dev.push_back(ss);
   *out = &per_dev.back();
   return AFF_OK;
@@ -514,15 +515,15 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   const cudaStream_t ws2 = side->stream;
   AFF_CUDA(cudaEventRecord(side->fork, s));
   AFF_CUDA(cudaStreamWaitEvent(ws2, side->fork, 0));
-  // ADD in the second-moment form: the weight side and the fold run on the caller's stream
-  // with the whole GPU while 1/r is computed beside them, and the Gram pass follows.  The
-  // fold and the Gram pass each want every SM (shared memory keeps their CTAs apart), so
-  // they are faster one after the other than side by side.  Otherwise the weight side runs
-  // on the side stream beside the token staging.
+  // The weight side (maxima, fp16 gate/up rows, gamma*Wo^T, the fold) runs on the side stream.
+  // FO / LOO / direct ADD: beside the token staging on the caller's stream.  ADD in the
+  // second-moment form: 1/r and then the Gram pass run first on the caller's stream (the Gram
+  // reading a through an L2 that holds no dirty lines of this call yet), and the fold, which
+  // wants every SM as the Gram pass does, follows it beside the Gram reduction.
   const bool moment = moment_form(d, mode);
-  const cudaStream_t wst = moment ? s : ws2;
+  const cudaStream_t wst = ws2;
   float* ir_m = moment ? reinterpret_cast<float*>(ws + L.ir) : nullptr;
-  if (moment) AFF_CUDA(launch_inv_r(x_b, ir_m, T, gram_split(T, H).nkb * 64, D, d.eps, sm_count, ws2));
+  if (moment) AFF_CUDA(launch_inv_r(x_b, ir_m, T, gram_split(T, H).nkb * 64, D, d.eps, sm_count, s));
   // weights staged unscaled with their maxima recorded, then staged again only if a
   // maximum lies outside fp16's comfortable range (scales.cuh)
   AFF_CUDA(launch_weight_stage((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, (const uint16_t*)Wo, g_b,
@@ -537,6 +538,38 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     AFF_CUDA(launch_prep_tokens(x_b, a_b, g_b, (fo || loo) ? n16 : nullptr, a16, inv_r, T, D, H * dh, d.eps, status,
                                 sm_count, sc, s));
     AFF_CUDA(launch_restage_a(a_b, inv_r, a16, T, H * dh, sc, status, sm_count, s));
+  }
+
+  // ADD, second-moment form: C_h over the tokens (Gram pass), then m^T C_h m for every
+  // folded row, then the group sums
+  const GramSplit gs = gram_split(T, H);
+  float* gram = moment ? reinterpret_cast<float*>(ws + L.gram) : nullptr;
+  float* cmax = moment ? reinterpret_cast<float*>(ws + L.cmax) : nullptr;
+  __half* CC = moment ? reinterpret_cast<__half*>(ws + L.CC) : nullptr;
+  float* gscale = moment ? reinterpret_cast<float*>(ws + L.gscale) : nullptr;
+  CUtensorMap mm[2];
+  std::memset(mm, 0, sizeof mm);
+  if (moment) {
+    // a (bf16 bits) as [T][H*dh], boxes of 32 columns x 64 tokens, 64-byte swizzle
+    if ((st = map_sw64_2d(&mm[0], a, (uint64_t)H * dh, (uint64_t)T, 64)) != AFF_OK) return st;
+    mm[1] = mm[0];
+    MomentParams mp{};
+    mp.mode = kMomentGram;
+    mp.n_units = gs.n_chunks * H;
+    mp.H = H; mp.dh = dh; mp.HD = H * dh; mp.I_pad = I_pad;
+    mp.nkb = gs.nkb; mp.kpc = gs.kpc;
+    mp.status = status;
+    mp.gram = gram;
+    mp.cmax = cmax;
+    mp.inv_r = ir_m;
+    const bool timed = g_timing_start && g_timing_stop;
+    if (timed) AFF_CUDA(cudaEventRecord(g_timing_start, s));
+    AFF_CUDA(launch_moment(mm, mp, s));
+    if (timed) AFF_CUDA(cudaEventRecord(g_timing_stop, s));
+    // the fold starts once the Gram pass is done
+    AFF_CUDA(cudaEventRecord(side->mid, s));
+    AFF_CUDA(cudaStreamWaitEvent(ws2, side->mid, 0));
+    AFF_CUDA(launch_gram_reduce(gram, cmax, CC, gscale, gs.n_chunks, H, dh, status, a_b, ir_m, T, sc, s));
   }
 
   CUtensorMap maps[4];
@@ -557,35 +590,6 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   }
   AFF_CUDA(cudaEventRecord(side->join, ws2));
   if (moment) {
-    // ADD, second-moment form: C_h over the tokens while the fold runs beside it,
-    // then m^T C_h m for every folded row, then the group sums
-    const GramSplit gs = gram_split(T, H);
-    AFF_CUDA(cudaStreamWaitEvent(s, side->join, 0));   // 1/r
-    float* gram = reinterpret_cast<float*>(ws + L.gram);
-    float* cmax = reinterpret_cast<float*>(ws + L.cmax);
-    __half* CC = reinterpret_cast<__half*>(ws + L.CC);
-    float* gscale = reinterpret_cast<float*>(ws + L.gscale);
-    CUtensorMap mm[2];
-    std::memset(mm, 0, sizeof mm);
-    {
-      // a (bf16 bits) as [T][H*dh], boxes of 32 columns x 64 tokens, 64-byte swizzle
-      if ((st = map_sw64_2d(&mm[0], a, (uint64_t)H * dh, (uint64_t)T, 64)) != AFF_OK) return st;
-      mm[1] = mm[0];
-      MomentParams mp{};
-      mp.mode = kMomentGram;
-      mp.n_units = gs.n_chunks * H;
-      mp.H = H; mp.dh = dh; mp.HD = H * dh; mp.I_pad = I_pad;
-      mp.nkb = gs.nkb; mp.kpc = gs.kpc;
-      mp.status = status;
-      mp.gram = gram;
-      mp.cmax = cmax;
-      mp.inv_r = ir_m;
-      const bool timed = g_timing_start && g_timing_stop;
-      if (timed) AFF_CUDA(cudaEventRecord(g_timing_start, s));
-      AFF_CUDA(launch_moment(mm, mp, s));
-      if (timed) AFF_CUDA(cudaEventRecord(g_timing_stop, s));
-      AFF_CUDA(launch_gram_reduce(gram, cmax, CC, gscale, gs.n_chunks, H, dh, status, a_b, ir_m, T, sc, s));
-    }
     AFF_CUDA(cudaStreamWaitEvent(s, side->join, 0));
     {
       if (stream_heads(d)) {

@@ -542,6 +542,10 @@ cudaError_t launch_moment(const CUtensorMap* maps, const MomentParams& p, cudaSt
     auto* fn = moment_kernel<kMomentGram>;
     if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
       return e;
+    // two CTAs per SM need the largest shared-memory carve-out
+    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+      return e;
     if (cudaError_t e_ = launch_pdl(fn, p.n_units, kMomentThreads, smem, s, maps[0], maps[1], p); e_ != cudaSuccess)
       return e_;
   } else if (p.mode == kMomentQuad) {

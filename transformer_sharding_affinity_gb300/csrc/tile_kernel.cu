@@ -600,6 +600,13 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
           constexpr int kW = MODE == kModeLOO ? 4 : 8;
 #pragma unroll
           for (int c = 0; c < CW / kW; ++c) {
+            // LOO: sigma of the slice's 4 tokens, a broadcast read issued before the TMEM reads
+            // so that its latency overlaps theirs
+            float4 rq = make_float4(0.f, 0.f, 0.f, 0.f);
+            if constexpr (MODE == kModeLOO) {
+              static_assert(kW == 4, "one float4 of sigma per slice");
+              rq = rsw[(upl ? CW / 4 : 0) + c];
+            }
             uint32_t pg[kW], pu[kW];
             if constexpr (kW == 8) {
               tmem_ld8_x2<CW>(tg + col + c * kW, pg);
@@ -613,11 +620,6 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(&sm.tempty[b]);
-            }
-            float4 rq = make_float4(0.f, 0.f, 0.f, 0.f);   // LOO: sigma of the slice's 4 tokens
-            if constexpr (MODE == kModeLOO) {
-              static_assert(kW == 4, "one float4 of sigma per slice");
-              rq = rsw[(upl ? CW / 4 : 0) + c];   // a broadcast read
             }
 #pragma unroll
             for (int i = 0; i < kW; i += 2) {

@@ -4,11 +4,11 @@
 // Paper: "Affinity-Aware Sharding for Delayed Tensor Parallelism", §3
 // "Affinity scores" (eq. 5 and the FO / ADD / down definitions after it).
 #include "aux_kernels.cuh"
+#include "launch.cuh"
 #include "scales.cuh"
 #include "sm103_primitives.cuh"
 
 #include <cuda_fp16.h>
-#include "launch.cuh"
 
 namespace aff {
 

@@ -4,9 +4,9 @@
 // quadratic-form pass over the folded rows.  Paper: "Affinity-Aware Sharding
 // for Delayed Tensor Parallelism", §3 "Affinity scores" (the ADD score).
 #include "moment_kernel.cuh"
+#include "launch.cuh"
 #include "scales.cuh"
 #include "sm103_primitives.cuh"
-#include "launch.cuh"
 
 namespace aff {
 

@@ -8,8 +8,7 @@
 //                three 128 x 64 tiles (fp16, 128 B swizzle);
 //   warp 1       MMA issuer (one thread): for every K slice of 16 one
 //                tcgen05.mma with M = 128 and N = 256 (two of the tiles back
-//                to back) into an fp32 accumulator of 256 TMEM columns; the
-//                fold issues two with N = 128 (D1 = A1 B^T, D2 = A2 B^T).
+//                to back) into an fp32 accumulator of 256 TMEM columns.
 //                Two accumulator buffers alternate so the epilogue of one job
 //                overlaps the MMAs of the next;
 //   warps 2..    epilogue: TMEM -> registers with tcgen05.ld; warp w reads
@@ -20,17 +19,18 @@
 // epilogue reads them with the 16x32bx2 TMEM shape: thread l and thread l + 16
 // of a warp both get neuron 16q + l's gate and up values, for the first and
 // the second half of the warp's columns, so the sum over tokens stays within
-// a thread.  The alpha, x', c_h and ||b_gk||^2 passes: A = the third tile
+// a thread.  The fold: A = the same 128 weight rows, B = 256 columns of
+// gamma*Wo^T.  The alpha, x', c_h and ||b_gk||^2 passes: A = the third tile
 // (tokens, or neurons), B = the first two.
 // Work is a fixed list of units, each a short list of jobs; CTAs take units
 // round-robin.  Which CTA computes a unit never changes its result, and
 // every unit writes its own partial sums, so the outputs do not depend on
 // the grid size.
+#include "launch.cuh"
 #include "sm103_primitives.cuh"
 #include "tile_kernel.cuh"
 
 #include <cuda_fp16.h>
-#include "launch.cuh"
 
 namespace aff {
 

@@ -45,12 +45,12 @@ def fo_flops(s) -> dict:
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the FO tile kernel, from an ncu capture of this bench's workload; valid only
 # while the kernel sources hash to the recorded value (otherwise null).
-KERNEL_SOURCES = ("tile_kernel.cu", "tile_kernel.cuh", "sm103_primitives.cuh", "scales.cuh")
-MOMENT_SOURCES = ("moment_kernel.cu", "moment_kernel.cuh", "sm103_primitives.cuh", "scales.cuh")
+KERNEL_SOURCES = ("tile_kernel.cu", "tile_kernel.cuh", "sm103_primitives.cuh", "scales.cuh", "launch.cuh")
+MOMENT_SOURCES = ("moment_kernel.cu", "moment_kernel.cuh", "sm103_primitives.cuh", "scales.cuh", "launch.cuh")
 TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass), third FO launch of
-    # `python bench.py --steps 2 --warmup 3 --no-cpu-baseline --e2e-steps 0`: 455.68 + 50.63 MB
-    ("qwen3_0p6b_layer", "fo", 65536): {"bytes": 506.31e6, "src": "f0bf97c29fe4a7d3"},
+    # `python bench.py --steps 2 --warmup 3 --no-cpu-baseline --e2e-steps 0`: 455.01 + 50.68 MB
+    ("qwen3_0p6b_layer", "fo", 65536): {"bytes": 505.68e6, "src": "2a88b611ee175b8a"},
 }
 
 

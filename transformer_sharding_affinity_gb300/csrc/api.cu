@@ -518,8 +518,10 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   // The weight side (maxima, fp16 gate/up rows, gamma*Wo^T, the fold) runs on the side stream.
   // FO / LOO / direct ADD: beside the token staging on the caller's stream.  ADD in the
   // second-moment form: 1/r and then the Gram pass run first on the caller's stream (the Gram
-  // reading a through an L2 that holds no dirty lines of this call yet), and the fold, which
-  // wants every SM as the Gram pass does, follows it beside the Gram reduction.
+  // reading a through an L2 that holds no dirty lines of this call yet); the fold, which wants
+  // every SM as the Gram pass does, follows the Gram on the caller's stream, and the Gram
+  // reduction runs beside it on the side stream, so that the path from the Gram through the
+  // fold to the quadratic forms crosses no stream.
   const bool moment = moment_form(d, mode);
   const cudaStream_t wst = ws2;
   float* ir_m = moment ? reinterpret_cast<float*>(ws + L.ir) : nullptr;
@@ -566,10 +568,14 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     if (timed) AFF_CUDA(cudaEventRecord(g_timing_start, s));
     AFF_CUDA(launch_moment(mm, mp, s));
     if (timed) AFF_CUDA(cudaEventRecord(g_timing_stop, s));
-    // the fold starts once the Gram pass is done
+    // the Gram reduction on the side stream once the Gram pass is done; the fold next on
+    // this stream once the staged weights are ready (recorded before the side stream
+    // waits for the Gram, so that this wait is already met)
     AFF_CUDA(cudaEventRecord(side->mid, s));
+    AFF_CUDA(cudaEventRecord(side->join_late, ws2));
     AFF_CUDA(cudaStreamWaitEvent(ws2, side->mid, 0));
-    AFF_CUDA(launch_gram_reduce(gram, cmax, CC, gscale, gs.n_chunks, H, dh, status, a_b, ir_m, T, sc, s));
+    AFF_CUDA(cudaStreamWaitEvent(s, side->join_late, 0));
+    AFF_CUDA(launch_gram_reduce(gram, cmax, CC, gscale, gs.n_chunks, H, dh, status, a_b, ir_m, T, sc, ws2));
   }
 
   CUtensorMap maps[4];
@@ -586,7 +592,7 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     p.n_ntiles = (int)ceil_div((int64_t)H * dh, 256);
     p.n_units = 2 * p.n_ktiles * p.n_ntiles;
     p.M16 = M16;
-    if ((st = run_tile(maps, p, wst)) != AFF_OK) return st;
+    if ((st = run_tile(maps, p, moment ? s : wst)) != AFF_OK) return st;
   }
   AFF_CUDA(cudaEventRecord(side->join, ws2));
   if (moment) {

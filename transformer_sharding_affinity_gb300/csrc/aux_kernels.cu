@@ -399,12 +399,15 @@ __global__ void reduce_partials4_kernel(const float* __restrict__ partial, doubl
 }
 
 // The chunk partial sums of one KV group's heads, reduced and finalised in one
-// pass: block = 128 neurons (32 threads x 4, 16-byte loads) x 16 chunk phases,
-// one group.  For every head of the group, each thread sums its chunks of the
-// [n_chunks][groups][H][I_pad] partials in fp32 (at most n_chunks / 16 chunks
-// times the column groups), the 16 phases are added in fp64 in order, and
-//   S_head[h][k] = sum / T (x ||w^d_k||^2 for FO),  S_up[g][k] = sum_{h in g} S_head[h][k].
-// Needs I_pad % 128 == 0.
+// pass: block = 128 neurons (32 threads x 4, 16-byte loads) x 16 rows, one
+// group.  The rows take the group's heads R at a time (R = min(H/G, 16)), 16 / R
+// rows to a head, so that the loads of all R heads are in flight together: row
+// y sums, for head R r + y / (16 / R) of the round, the chunks c = y % (16 / R)
+// + j 16 / R of the [n_chunks][groups][H][I_pad] partials in fp32 (column
+// groups in order within a chunk); then one warp per head adds its rows in
+// fp64, in order, and
+//   S_head[h][k] = sum / T (x ||w^d_k||^2 for FO),  S_up[g][k] = sum_{h in g} S_head[h][k]
+// (heads in order).  Needs I_pad % 128 == 0.
 template <int GROUPS>
 __global__ void __launch_bounds__(512) reduce_finalize_kernel(const float* __restrict__ partial,
                                                               const float* __restrict__ wdn, int fo, int n_chunks,
@@ -415,41 +418,61 @@ __global__ void __launch_bounds__(512) reduce_finalize_kernel(const float* __res
   // the partial sums carry the head operands' 2^2(e_m + e_a) (scales.cuh)
   const ScaleExps ex = scale_exps(*sc, D);
   const double fh = (double)pow2f(-(ex.e_m + ex.e_a));
-  __shared__ double part[16][32][4];
+  __shared__ float part[16][32][4];
+  __shared__ double vh[16][32][4];
   const int k0 = blockIdx.x * 128 + threadIdx.x * 4;
   const int g = blockIdx.y;
   const int hpg = H / G;
-  double total[4] = {0.0, 0.0, 0.0, 0.0};
-  for (int h = g * hpg; h < (g + 1) * hpg; ++h) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    // chunks in order, column groups in order within a chunk; fully unrolled in groups so
-    // that the loads of several chunks are in flight together
-#pragma unroll 8
-    for (int c = threadIdx.y; c < n_chunks; c += 16)
+  const int R = hpg < 16 ? hpg : 16;   // heads per round
+  const int P = 16 / R;                // rows per head
+  const int y = threadIdx.y;
+  const double inv_T = 1.0 / (double)T;
+  double scale[4];
 #pragma unroll
-      for (int q = 0; q < GROUPS; ++q) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(partial + ((size_t)(c * GROUPS + q) * H + h) * I_pad + k0));
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-      }
-    part[threadIdx.y][threadIdx.x][0] = acc.x;
-    part[threadIdx.y][threadIdx.x][1] = acc.y;
-    part[threadIdx.y][threadIdx.x][2] = acc.z;
-    part[threadIdx.y][threadIdx.x][3] = acc.w;
+  for (int e = 0; e < 4; ++e) {
+    const int k = k0 + e;
+    scale[e] = fh * fh * ((fo && k < I) ? (double)wdn[k] : 1.0) * inv_T;
+  }
+  double total[4] = {0.0, 0.0, 0.0, 0.0};
+  for (int h0 = g * hpg; h0 < (g + 1) * hpg; h0 += R) {
+    const int r = y / P, ph = y % P;
+    const int h = h0 + r;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < R && h < (g + 1) * hpg) {
+#pragma unroll 8
+      for (int c = ph; c < n_chunks; c += P)
+#pragma unroll
+        for (int q = 0; q < GROUPS; ++q) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(partial + ((size_t)(c * GROUPS + q) * H + h) * I_pad + k0));
+          acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+    }
+    part[y][threadIdx.x][0] = acc.x;
+    part[y][threadIdx.x][1] = acc.y;
+    part[y][threadIdx.x][2] = acc.z;
+    part[y][threadIdx.x][3] = acc.w;
     __syncthreads();
-    if (threadIdx.y == 0) {
+    if (ph == 0 && r < R && h < (g + 1) * hpg) {   // one warp per head of the round
+#pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int k = k0 + e;
-        if (k >= I) continue;
         double t = 0.0;
-        for (int i = 0; i < 16; ++i) t += part[i][threadIdx.x][e];
-        const double v = t * fh * fh * ((fo ? (double)wdn[k] : 1.0) / (double)T);
-        if (S_head_out) S_head_out[(size_t)h * I + k] = (float)v;
-        total[e] += v;
+        for (int i = 0; i < P; ++i) t += part[y + i][threadIdx.x][e];
+        const double v = t * scale[e];
+        vh[r][threadIdx.x][e] = v;
+        const int k = k0 + e;
+        if (S_head_out && k < I) S_head_out[(size_t)h * I + k] = (float)v;
       }
     }
     __syncthreads();
+    if (y == 0) {
+      const int nr = min(R, (g + 1) * hpg - h0);
+      for (int i = 0; i < nr; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) total[e] += vh[i][threadIdx.x][e];
+    }
+    __syncthreads();
   }
-  if (threadIdx.y == 0)
+  if (y == 0)
     for (int e = 0; e < 4; ++e)
       if (k0 + e < I) S_out[(size_t)g * I + k0 + e] = (float)total[e];
 }

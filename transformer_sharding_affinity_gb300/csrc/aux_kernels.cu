@@ -399,17 +399,18 @@ __global__ void reduce_partials4_kernel(const float* __restrict__ partial, doubl
 }
 
 // The chunk partial sums of one KV group's heads, reduced and finalised in one
-// pass: block = 128 neurons (32 threads x 4, 16-byte loads) x 16 rows, one
-// group.  The rows take the group's heads R at a time (R = min(H/G, 16)), 16 / R
-// rows to a head, so that the loads of all R heads are in flight together: row
-// y sums, for head R r + y / (16 / R) of the round, the chunks c = y % (16 / R)
-// + j 16 / R of the [n_chunks][groups][H][I_pad] partials in fp32 (column
-// groups in order within a chunk); then one warp per head adds its rows in
-// fp64, in order, and
+// pass: block = 64 neurons x one group, 512 threads.  The partial sums are laid
+// out [H][I_pad / 64][n_chunks][groups][64], so each (head, 64-neuron block) is
+// one contiguous run of n_chunks * groups rows of 64 floats.  Thread t reads the
+// 4 neurons 4 (t % 16).. of rows ph, ph + P, ... (16-byte loads; a warp reads 512
+// contiguous bytes); the 32 row phases t / 16 are split among the group's heads R
+// at a time (R = min(H/G, 32), P = 32 / R phases a head), so that the loads of R
+// heads are in flight together.  Each phase sums its rows in fp32 in order; the
+// phases are added in fp64, in order, and
 //   S_head[h][k] = sum / T (x ||w^d_k||^2 for FO),  S_up[g][k] = sum_{h in g} S_head[h][k]
-// (heads in order).  Needs I_pad % 128 == 0.
+// (heads in order).  Needs I_pad % 64 == 0.
 template <int GROUPS>
-__global__ void __launch_bounds__(512) reduce_finalize_kernel(const float* __restrict__ partial,
+__global__ void __launch_bounds__(512, 3) reduce_finalize_kernel(const float* __restrict__ partial,
                                                               const float* __restrict__ wdn, int fo, int n_chunks,
                                                               int T, int H, int G, int I, int I_pad,
                                                               float* __restrict__ S_out, float* __restrict__ S_head_out,
@@ -418,63 +419,58 @@ __global__ void __launch_bounds__(512) reduce_finalize_kernel(const float* __res
   // the partial sums carry the head operands' 2^2(e_m + e_a) (scales.cuh)
   const ScaleExps ex = scale_exps(*sc, D);
   const double fh = (double)pow2f(-(ex.e_m + ex.e_a));
-  __shared__ float part[16][32][4];
-  __shared__ double vh[16][32][4];
-  const int k0 = blockIdx.x * 128 + threadIdx.x * 4;
+  __shared__ float part[32][16][4];
+  __shared__ double vh[8][64];
+  const int t = threadIdx.x;
+  const int kb = blockIdx.x;
   const int g = blockIdx.y;
   const int hpg = H / G;
-  const int R = hpg < 16 ? hpg : 16;   // heads per round
-  const int P = 16 / R;                // rows per head
-  const int y = threadIdx.y;
-  const double inv_T = 1.0 / (double)T;
-  double scale[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int k = k0 + e;
-    scale[e] = fh * fh * ((fo && k < I) ? (double)wdn[k] : 1.0) * inv_T;
-  }
-  double total[4] = {0.0, 0.0, 0.0, 0.0};
+  const int R = hpg < 32 ? hpg : 32;   // heads per round
+  const int P = 32 / R;                // row phases per head
+  const int rows = n_chunks * GROUPS;
+  const size_t run = (size_t)rows * 64;
+  const int c4 = t & 15, rest = t >> 4;
+  const int r = rest / P, ph = rest % P;
+  // fp64 stage: thread t < 64 * min(R, 8) takes neuron n of head-in-round rr (more rounds of 8 if R > 8)
+  const int n = t & 63;
+  const int k = kb * 64 + n;
+  double scale = 0.0;
+  if (t < 64 * 8) scale = fh * fh * ((fo && k < I) ? (double)wdn[k] : 1.0) / (double)T;
+  double total = 0.0;
   for (int h0 = g * hpg; h0 < (g + 1) * hpg; h0 += R) {
-    const int r = y / P, ph = y % P;
-    const int h = h0 + r;
+    const int nr = min(R, (g + 1) * hpg - h0);   // heads in this round
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r < R && h < (g + 1) * hpg) {
+    if (r < nr) {
+      const float4* src = reinterpret_cast<const float4*>(partial + ((size_t)(h0 + r) * (I_pad / 64) + kb) * run) + c4;
 #pragma unroll 8
-      for (int c = ph; c < n_chunks; c += P)
-#pragma unroll
-        for (int q = 0; q < GROUPS; ++q) {
-          const float4 v = __ldg(reinterpret_cast<const float4*>(partial + ((size_t)(c * GROUPS + q) * H + h) * I_pad + k0));
-          acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-        }
-    }
-    part[y][threadIdx.x][0] = acc.x;
-    part[y][threadIdx.x][1] = acc.y;
-    part[y][threadIdx.x][2] = acc.z;
-    part[y][threadIdx.x][3] = acc.w;
-    __syncthreads();
-    if (ph == 0 && r < R && h < (g + 1) * hpg) {   // one warp per head of the round
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        double t = 0.0;
-        for (int i = 0; i < P; ++i) t += part[y + i][threadIdx.x][e];
-        const double v = t * scale[e];
-        vh[r][threadIdx.x][e] = v;
-        const int k = k0 + e;
-        if (S_head_out && k < I) S_head_out[(size_t)h * I + k] = (float)v;
+      for (int row = ph; row < rows; row += P) {
+        const float4 v = __ldg(src + (size_t)row * 16);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
       }
     }
+    part[rest][c4][0] = acc.x;
+    part[rest][c4][1] = acc.y;
+    part[rest][c4][2] = acc.z;
+    part[rest][c4][3] = acc.w;
     __syncthreads();
-    if (y == 0) {
-      const int nr = min(R, (g + 1) * hpg - h0);
-      for (int i = 0; i < nr; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) total[e] += vh[i][threadIdx.x][e];
+    for (int rr0 = 0; rr0 < nr; rr0 += 8) {
+      const int rr = rr0 + (t >> 6);
+      if (t < 512 && rr < nr && (t >> 6) < 8) {
+        double s = 0.0;
+        for (int i = 0; i < P; ++i) s += part[rr * P + i][n >> 2][n & 3];
+        const double v = s * scale;
+        vh[t >> 6][n] = v;
+        if (S_head_out && k < I) S_head_out[(size_t)(h0 + rr) * I + k] = (float)v;
+      }
+      __syncthreads();
+      if (t < 64) {
+        const int m = min(8, nr - rr0);
+        for (int i = 0; i < m; ++i) total += vh[i][n];
+      }
+      __syncthreads();
     }
-    __syncthreads();
   }
-  if (y == 0)
-    for (int e = 0; e < 4; ++e)
-      if (k0 + e < I) S_out[(size_t)g * I + k0 + e] = (float)total[e];
+  if (t < 64 && k < I) S_out[(size_t)g * I + k] = (float)total;
 }
 
 // S_head[h][k] = sum_t(...) / T (x ||w^d_k||^2 for FO); S_up[g][k] = sum_{h in g} S_head[h][k].
@@ -941,7 +937,7 @@ cudaError_t launch_reduce_partials(const float* partial, double* out, int n_chun
 cudaError_t launch_reduce_finalize(const float* partial, const float* wdn, int fo, int n_chunks, int groups, int T,
                                    int H, int G, int I, int I_pad, float* S_out, float* S_head_out,
                                    const DevScales* sc, int D, cudaStream_t s) {
-  dim3 grid(I_pad / 128, G), block(32, 16);
+  dim3 grid(I_pad / 64, G), block(512);
   switch (groups) {
     case 1:
       if (cudaError_t e_ = launch_pdl(reduce_finalize_kernel<1>, grid, block, 0, s, partial, wdn, fo, n_chunks, T, H,

@@ -795,16 +795,19 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
       if (!ok) break;
       // ---- end of unit
       if constexpr (kHeads) {
-        // [chunk][column group][H][I_pad]: threads l and l + 16 add their sums (the same
-        // value in both) and thread l writes it
-        const int k = U.kt * 64 + q * 16 + (lane & 15);
-        float* dst = p.partial + ((size_t)(U.chunk * NG + hf) * p.H) * p.I_pad + k;
+        // [H][I_pad / 64][chunk][column group][64]: each (head, 64-neuron block) owns one
+        // contiguous run of its chunks' sums, which the reduction streams.  Threads l and
+        // l + 16 add their sums (the same value in both) and thread l writes it.
+        const int n_chunks = p.n_units / (2 * p.n_ktiles);
+        const size_t run = (size_t)n_chunks * NG * 64;   // floats per (head, neuron block)
+        float* dst = p.partial + (size_t)U.kt * run + ((size_t)U.chunk * NG + hf) * 64 + q * 16 + (lane & 15);
+        const size_t hstride = (size_t)(p.I_pad / 64) * run;
         for (int h = 0; h < p.H; ++h) {
           float* sp = &sm.sacc[(hf * p.H + h) * kBlockM + row];
           const float v = *sp;
           *sp = 0.f;
           const float t = v + __shfl_xor_sync(0xffffffffu, v, 16);
-          if (!upl) dst[(size_t)h * p.I_pad] = t;
+          if (!upl) dst[(size_t)h * hstride] = t;
         }
       }
       if constexpr (MODE == kModeXPrime) {

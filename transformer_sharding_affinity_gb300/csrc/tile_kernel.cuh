@@ -67,7 +67,7 @@ struct TileParams {
   int32_t nkb_HD, ls_HD;   // streaming: K blocks over H*dh, 16-wide slices in the last one
   int32_t spp;             // streaming: 16-wide K slices per head (d_head / 16)
   uint32_t* status;
-  float* partial;          // FO/ADD/LOO: [n_chunks][column group][H][I_pad]; x': [column tile][group][T_pad]
+  float* partial;          // FO/ADD/LOO: [H][I_pad / 64][n_chunks][column group][64]; x': [column tile][group][T_pad]
   __half* M16;             // fold output
   __half* alpha16;         // alpha output
   const uint16_t* x_bf16;  // x' epilogue reads x (bf16 bits) [T][D]

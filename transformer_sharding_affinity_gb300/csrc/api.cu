@@ -301,6 +301,18 @@ bool stream_heads(const aff_dims& d) {
   return allowed && d.d_head % 16 == 0 && d.d_head % 64 != 0;
 }
 
+// ADD in the second-moment form: fold units run before the Gram pass, beside 1/r --
+// those past the last whole round of one unit per SM, so that the rest take whole
+// rounds after it.  AFFINITY_FOLD_EARLY=<n> sets the count (0: none).
+int fold_early_units(int n_units, int sm_count) {
+  static const int forced = [] {
+    const char* e = std::getenv("AFFINITY_FOLD_EARLY");
+    return e ? std::atoi(e) : -1;
+  }();
+  int n = forced >= 0 ? forced : (n_units > sm_count && sm_count > 0 ? n_units % sm_count : 0);
+  return n < n_units ? n : n_units;
+}
+
 TileParams base_params(const aff_dims& d, const Layout& L, uint8_t* ws, int mode) {
   TileParams p{};
   p.mode = mode;
@@ -335,7 +347,7 @@ TileParams base_params(const aff_dims& d, const Layout& L, uint8_t* ws, int mode
 }
 
 aff_status run_tile(const CUtensorMap* maps, TileParams& p, cudaStream_t s, bool dominant = false, int max_ctas = 0) {
-  if (p.n_units <= 0) return AFF_OK;
+  if (p.n_units - p.unit0 <= 0) return AFF_OK;
   // CTAs resident at once, cached per device and configuration
   static std::mutex mu;
   static std::vector<std::pair<std::vector<int>, int>> cache;
@@ -358,7 +370,7 @@ aff_status run_tile(const CUtensorMap* maps, TileParams& p, cudaStream_t s, bool
     std::lock_guard<std::mutex> lk(mu);
     cache.push_back({key, fit});
   }
-  int grid = p.n_units < fit ? p.n_units : fit;
+  int grid = p.n_units - p.unit0 < fit ? p.n_units - p.unit0 : fit;
   if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
   const bool timed = dominant && g_timing_start && g_timing_stop;
   if (timed) AFF_CUDA(cudaEventRecord(g_timing_start, s));
@@ -521,7 +533,8 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   // reading a through an L2 that holds no dirty lines of this call yet); the fold, which wants
   // every SM as the Gram pass does, follows the Gram on the caller's stream, and the Gram
   // reduction runs beside it on the side stream, so that the path from the Gram through the
-  // fold to the quadratic forms crosses no stream.
+  // fold to the quadratic forms crosses no stream.  The fold's units past its last whole round
+  // run before the Gram instead, beside 1/r.
   const bool moment = moment_form(d, mode);
   const cudaStream_t wst = ws2;
   float* ir_m = moment ? reinterpret_cast<float*>(ws + L.ir) : nullptr;
@@ -535,6 +548,33 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
   if (loo) AFF_CUDA(launch_to_fp16((const uint16_t*)Wo, Wo16, (size_t)D * H * dh, status, wst));
   AFF_CUDA(launch_weight_restage((const uint16_t*)Wg, (const uint16_t*)Wu, W16, I, I_pad, D, (const uint16_t*)Wo, g_b,
                                  GWo16, Wo16, H * dh, sc, status, sm_count, wst));
+
+  // fold: M_h = [Wg; Wu] diag(gamma) Wo^(h), units of (128 rows of W16, 256 columns of H*dh):
+  // A = W16 rows, B = gamma*Wo^T hi, then lo
+  CUtensorMap fmaps[4];
+  std::memset(fmaps, 0, sizeof fmaps);
+  if ((st = map2(&fmaps[0], W16, (uint64_t)D, (uint64_t)2 * I_pad)) != AFF_OK) return st;
+  {
+    uint64_t dm[3] = {(uint64_t)D, 2, (uint64_t)H * dh}, sd[2] = {(uint64_t)D * 2, (uint64_t)D * 4};
+    if ((st = make_map(&fmaps[1], GWo16, 3, dm, sd, 128, 2)) != AFF_OK) return st;
+  }
+  fmaps[2] = fmaps[0];
+  fmaps[3] = fmaps[0];
+  TileParams fp = base_params(d, L, ws, kModeFold);
+  fp.n_ntiles = (int)ceil_div((int64_t)H * dh, 256);
+  fp.n_units = 2 * fp.n_ktiles * fp.n_ntiles;
+  fp.M16 = M16;
+  // ADD, second-moment form: the units past the last whole round of the fold run first, on
+  // the side stream beside 1/r (which needs few SMs); the rest follow the Gram pass
+  const int fold_early = moment ? fold_early_units(fp.n_units, sm_count) : 0;
+  if (moment) {
+    AFF_CUDA(cudaEventRecord(side->join_late, ws2));   // the staged weights are ready
+    if (fold_early > 0) {
+      TileParams p1 = fp;
+      p1.unit0 = fp.n_units - fold_early;
+      if ((st = run_tile(fmaps, p1, ws2)) != AFF_OK) return st;
+    }
+  }
   // token side on the caller's stream meanwhile
   if (!moment) {
     AFF_CUDA(launch_prep_tokens(x_b, a_b, g_b, (fo || loo) ? n16 : nullptr, a16, inv_r, T, D, H * dh, d.eps, status,
@@ -572,28 +612,18 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
     // this stream once the staged weights are ready (recorded before the side stream
     // waits for the Gram, so that this wait is already met)
     AFF_CUDA(cudaEventRecord(side->mid, s));
-    AFF_CUDA(cudaEventRecord(side->join_late, ws2));
     AFF_CUDA(cudaStreamWaitEvent(ws2, side->mid, 0));
     AFF_CUDA(cudaStreamWaitEvent(s, side->join_late, 0));
     AFF_CUDA(launch_gram_reduce(gram, cmax, CC, gscale, gs.n_chunks, H, dh, status, a_b, ir_m, T, sc, ws2));
   }
 
+  {
+    TileParams p2 = fp;
+    p2.n_units = fp.n_units - fold_early;   // moment form: the units not run before the Gram pass
+    if ((st = run_tile(fmaps, p2, moment ? s : wst)) != AFF_OK) return st;
+  }
   CUtensorMap maps[4];
   std::memset(maps, 0, sizeof maps);
-  // fold: M_h = [Wg; Wu] diag(gamma) Wo^(h)
-  {
-    // units of (128 rows of W16, 256 columns of H*dh): A = W16 rows, B = gamma*Wo^T hi, then lo
-    if ((st = map2(&maps[0], W16, (uint64_t)D, (uint64_t)2 * I_pad)) != AFF_OK) return st;
-    uint64_t dm[3] = {(uint64_t)D, 2, (uint64_t)H * dh}, sd[2] = {(uint64_t)D * 2, (uint64_t)D * 4};
-    if ((st = make_map(&maps[1], GWo16, 3, dm, sd, 128, 2)) != AFF_OK) return st;
-    maps[2] = maps[0];
-    maps[3] = maps[0];
-    TileParams p = base_params(d, L, ws, kModeFold);
-    p.n_ntiles = (int)ceil_div((int64_t)H * dh, 256);
-    p.n_units = 2 * p.n_ktiles * p.n_ntiles;
-    p.M16 = M16;
-    if ((st = run_tile(maps, p, moment ? s : wst)) != AFF_OK) return st;
-  }
   AFF_CUDA(cudaEventRecord(side->join, ws2));
   if (moment) {
     AFF_CUDA(cudaStreamWaitEvent(s, side->join, 0));

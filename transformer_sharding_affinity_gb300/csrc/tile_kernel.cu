@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
       int s = 0, issued = 0;
       uint32_t ph = 0;                 // phase parity of the current use of stage s
       bool ok = true;
-      for (int u = cid; ok && u < p.n_units; u += ncl) {
+      for (int u = p.unit0 + cid; ok && u < p.n_units; u += ncl) {
         const Unit U = unit_info<STREAM>(p, u);
         JobIter jt{0, 0};
         for (int j = 0; ok && j < U.njobs_pm; ++j) {
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
       int s = 0, b = 0;
       uint32_t ph = 0, tph = 0;        // stage phase; TMEM buffer phase (flips every second job)
       bool ok = true;
-      for (int u = cid; ok && u < p.n_units; u += ncl) {
+      for (int u = p.unit0 + cid; ok && u < p.n_units; u += ncl) {
         const Unit U = unit_info<STREAM>(p, u);
         JobIter jt{0, 0};
         for (int j = 0; ok && j < U.njobs_pm; ++j) {
@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
     int b = 0;
     uint32_t tph = 0;                  // TMEM buffer phase (flips every second job)
     bool ok = true;
-    for (int u = cid; ok && u < p.n_units; u += ncl) {
+    for (int u = p.unit0 + cid; ok && u < p.n_units; u += ncl) {
       const Unit U = unit_info<STREAM>(p, u);
       JobIter jt{0, 0};
       for (int j = 0; j < U.njobs; ++j, b ^= 1, tph ^= (uint32_t)(b == 0)) {

@@ -52,7 +52,8 @@ enum TileMode : int {
 
 struct TileParams {
   int32_t mode;
-  int32_t n_units;
+  int32_t unit0;           // first unit of this launch (a pass may be split over launches)
+  int32_t n_units;         // one past the last unit
   int32_t stages;
   int32_t T, D, H, G, dh, I, I_pad, T_pad;
   int32_t n_ktiles;        // neuron tiles of 128 (I_pad / 128); head passes: blocks of 64 = 2 n_ktiles

@@ -49,9 +49,24 @@ KERNEL_SOURCES = ("tile_kernel.cu", "tile_kernel.cuh", "sm103_primitives.cuh", "
 MOMENT_SOURCES = ("moment_kernel.cu", "moment_kernel.cuh", "sm103_primitives.cuh", "scales.cuh", "launch.cuh")
 TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass), third FO launch of
-    # `python bench.py --steps 2 --warmup 3 --no-cpu-baseline --e2e-steps 0`: 455.01 + 50.68 MB
-    ("qwen3_0p6b_layer", "fo", 65536): {"bytes": 505.68e6, "src": "2a88b611ee175b8a"},
+    # `python bench.py --steps 2 --warmup 3 --no-cpu-baseline --e2e-steps 0`: 456.27 + 49.55 MB
+    ("qwen3_0p6b_layer", "fo", 65536): {"bytes": 505.81e6, "src": "6b86366ad5b8befd"},
 }
+
+
+def moment_launches(shape) -> int:
+    """Kernels of one ADD call in the second-moment form: 1/r, the weight staging and
+    restaging, the Gram pass, its reduction and fallback, the quadratic forms, the finish,
+    and the fold -- two launches when some of its units run before the Gram pass (those
+    past its last whole round of one unit per SM, or AFFINITY_FOLD_EARLY of them)."""
+    import torch
+    i_pad = -(-shape.I // 256) * 256
+    units = 2 * (i_pad // 128) * -(-(shape.H * shape.dh) // 256)
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    early = int(os.environ.get("AFFINITY_FOLD_EARLY", "-1"))
+    if early < 0:
+        early = units % sms if units > sms else 0
+    return 9 if min(early, units) in (0, units) else 10
 
 
 def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
@@ -572,7 +587,8 @@ def main() -> None:
         "step_tflops": flops_per_step / (ms_step * 1e-3) / 1e12,
         "step_frac_of_peak": flops_per_step / (ms_step * 1e-3) / 1e12 / pk["bf16_tflops"],
         "roofline": roof,
-        "gpu_launches": (9 if moment else {"fo": 8, "add": 7, "loo": 10, "down": 10}[args.mode]) * args.steps,
+        "gpu_launches": (moment_launches(shape) if moment else
+                         {"fo": 8, "add": 7, "loo": 10, "down": 10}[args.mode]) * args.steps,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": shape.G * shape.I * 4, "ms_per_step": e2e_ms, "steps": n_e2e,
                 "clocks": clocks_e2e.summary()},

@@ -112,6 +112,22 @@ def test_add_many_quadratic_form_units():
             assert topk_agrees(S_gpu[g, idx], S_ref[g]), f"{mode}: top-8 of group {g} differs"
 
 
+def test_add_fold_split_leaves_results_unchanged(monkeypatch):
+    """ADD in the second-moment form may run some fold units before the Gram pass
+    (beside 1/r) and the rest after it; each unit writes its own M16 tile, so S is
+    bit-identical however the units are split (none early, some, all)."""
+    shape = S("fold_split", T=1536, D=256, H=16, G=8, dh=64, I=2048, dtype="bf16", w_std=0.05,
+              x_dist="normal_outliers", seed=25)
+    layer = W.make_layer(shape)
+    outs = []
+    for early in ("0", "37", "100000"):
+        monkeypatch.setenv("AFFINITY_FOLD_EARLY", early)
+        outs.append(run_up(B, DV, shape, layer, "add")[0])
+    for S_, Sh_ in outs[1:]:
+        assert np.array_equal(S_.view(np.uint32), outs[0][0].view(np.uint32))
+        assert np.array_equal(Sh_.view(np.uint32), outs[0][1].view(np.uint32))
+
+
 def test_up_deterministic():
     layer = W.make_layer(MEDIUM)
     outs = run_up(B, DV, MEDIUM, layer, "fo", runs=3)

@@ -305,10 +305,8 @@ bool stream_heads(const aff_dims& d) {
 // those past the last whole round of one unit per SM, so that the rest take whole
 // rounds after it.  AFFINITY_FOLD_EARLY=<n> sets the count (0: none).
 int fold_early_units(int n_units, int sm_count) {
-  static const int forced = [] {
-    const char* e = std::getenv("AFFINITY_FOLD_EARLY");
-    return e ? std::atoi(e) : -1;
-  }();
+  const char* e = std::getenv("AFFINITY_FOLD_EARLY");   // read per call: tests vary it
+  const int forced = e ? std::atoi(e) : -1;
   int n = forced >= 0 ? forced : (n_units > sm_count && sm_count > 0 ? n_units % sm_count : 0);
   return n < n_units ? n : n_units;
 }

@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
     uint64_t abA[CW / 2], abB[CW / 2];
 #pragma unroll
     for (int i = 0; i < CW / 2; ++i) { abA[i] = 0ull; abB[i] = 0ull; }
-    float ss1 = 0.f;                   // x' / qnorm running sums
+    uint64_t ssp = pk(0.f, 0.f);       // x' / qnorm running sums, a packed pair (even and odd columns)
     // c_h pass: x of the thread's token and CWW columns, loaded at a unit's first head
     uint32_t xr[MODE == kModeCNorm ? CWW / 2 : 1];
     int b = 0;
@@ -705,7 +705,7 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
             }
           }
           const uint32_t c0 = tl + (uint32_t)(b * 2 * kBlockN + hf * CWW);
-          float s1 = 0.f, s2 = 0.f;
+          uint64_t s1p = pk(0.f, 0.f), s2p = pk(0.f, 0.f);   // packed pairs: even and odd columns
 #pragma unroll
           for (int c = 0; c < CWW / 16; ++c) {
             uint32_t v[16];
@@ -719,13 +719,13 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
 #pragma unroll
             for (int i = 0; i < 16; i += 2) {
               const uint32_t e = xr[(c * 16 + i) / 2];
-              const float va = __uint_as_float(v[i]), vb = __uint_as_float(v[i + 1]);
-              s1 = fmaf(va, va, s1);
-              s1 = fmaf(vb, vb, s1);
-              s2 = fmaf(__uint_as_float(e << 16), va, s2);
-              s2 = fmaf(__uint_as_float(e & 0xFFFF0000u), vb, s2);
+              const uint64_t v2 = pk_u(v[i], v[i + 1]);
+              s1p = fma2(v2, v2, s1p);
+              s2p = fma2(pk_u(e << 16, e & 0xFFFF0000u), v2, s2p);
             }
           }
+          const float2 f1 = unpk(s1p), f2 = unpk(s2p);
+          const float s1 = f1.x + f1.y, s2 = f2.x + f2.y;
           // [column tile][column group][quantity][H][T_pad]: quantity 0 = sum (c/r)^2, 1 = sum x (c/r)
           float* dst = p.partial + ((size_t)((U.kt * NG + hf) * 2) * p.H + J.head) * p.T_pad + t;
           dst[0] = s1;
@@ -757,11 +757,10 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
                 const uint32_t e[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                  const float xa = __uint_as_float(e[i] << 16), xb = __uint_as_float(e[i] & 0xFFFF0000u);
-                  const float va = __uint_as_float(v[q8 * 8 + 2 * i]), vb = __uint_as_float(v[q8 * 8 + 2 * i + 1]);
-                  const float ya = xa + va, yb = xb + vb;
-                  ss1 = fmaf(ya, ya, ss1);
-                  ss1 = fmaf(yb, yb, ss1);
+                  // x' = x + alpha Wd^T for two columns at once (x * 1 + v rounds as x + v)
+                  const uint64_t x2 = pk_u(e[i] << 16, e[i] & 0xFFFF0000u);
+                  const uint64_t y2 = fma2(x2, pk(1.0f, 1.0f), pk_u(v[q8 * 8 + 2 * i], v[q8 * 8 + 2 * i + 1]));
+                  ssp = fma2(y2, y2, ssp);
                 }
               }
             }
@@ -782,13 +781,17 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
               if (lane == 0) mbar_arrive(&sm.tempty[b]);
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) ss1 = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), ss1);
+            for (int i = 0; i < 16; i += 2) {
+              const uint64_t v2 = pk_u(v[i], v[i + 1]);
+              ssp = fma2(v2, v2, ssp);
+            }
           }
           if (J.nt == p.n_ntiles - 1) {
             // rows past the group's end were zero-filled, so the sum is this column group's share
             const int k = U.base + row;
-            if (k < p.I_pad) p.bnorm[((size_t)hf * p.I_pad + k) * p.G + J.g] = ss1;
-            ss1 = 0.f;
+            const float2 s2 = unpk(ssp);
+            if (k < p.I_pad) p.bnorm[((size_t)hf * p.I_pad + k) * p.G + J.g] = s2.x + s2.y;
+            ssp = pk(0.f, 0.f);
           }
         }
       }
@@ -812,8 +815,9 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
       }
       if constexpr (MODE == kModeXPrime) {
         // [column tile][column group][T_pad]; token tiles are whole, so t < T_pad
-        p.partial[(size_t)(U.head * NG + hf) * p.T_pad + U.base + row] = ss1;
-        ss1 = 0.f;
+        const float2 s2 = unpk(ssp);
+        p.partial[(size_t)(U.head * NG + hf) * p.T_pad + U.base + row] = s2.x + s2.y;
+        ssp = pk(0.f, 0.f);
       }
     }
   }

@@ -697,6 +697,9 @@ aff_status affinity_up(const void* a, const void* x, const void* Wo, const void*
       if ((st = make_map(&maps[3], a16, 3, da, sa, brows, 2)) != AFF_OK) return st;
     }
     TileParams p = base_params(d, L, ws, fo ? kModeFO : (loo ? kModeLOO : kModeADD));
+    // CTAs claim units from a counter (zeroed with the scales at the start of the call), so
+    // that CTAs on faster SMs take more of them and the pass ends with less of a tail
+    p.ucount = &reinterpret_cast<DevScales*>(ws + L.scales)->units;
     p.rho = rho;
     p.n_units = (int)(L.n_chunks * 2 * p.n_ktiles);   // (512 tokens, 64 neurons)
     p.partial = partial;

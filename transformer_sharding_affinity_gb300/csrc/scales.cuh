@@ -35,7 +35,7 @@ struct DevScales {
   uint32_t amax;    // max |a_t / r_t| as first staged (FO, LOO, ADD direct)
   uint32_t amax2;   // second-moment ADD fallback: max |a_t / r_t| over every token
   uint32_t redo;    // second-moment ADD: 1 when the Gram matrices are recomputed with a scale
-  uint32_t pad;
+  uint32_t units;   // head passes (FO, LOO, direct ADD): units claimed so far by the tile kernel's CTAs
 };
 
 constexpr int kScaleTarget = 13;   // a normalised maximum lands in [2^13, 2^14)

@@ -166,6 +166,9 @@ struct Smem {
   uint64_t* drain;
   uint32_t* tmem_slot;
   volatile int* abort_flag;
+  uint64_t* ufull;         // unit ring: the TMA warp published the slot's unit id
+  uint64_t* uempty;        // unit ring: the MMA thread and every epilogue warp have read it
+  volatile int* uring;     // unit ids (-1: no more units)
   float* sacc;     // FO / ADD / LOO: the unit's sums [column group][H][128 neurons]
   float4* rsc;     // LOO: per epilogue warp, sigma of its column group's tokens for the current head job
   uint8_t* stage0;
@@ -219,6 +222,9 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
   sm.drain = sm.tempty + 2;
   sm.tmem_slot = reinterpret_cast<uint32_t*>(sm.drain + 1);
   sm.abort_flag = reinterpret_cast<volatile int*>(sm.tmem_slot + 1);
+  sm.ufull = reinterpret_cast<uint64_t*>(sm.tmem_slot + 2);   // 8-byte aligned: drain + 16 bytes
+  sm.uempty = sm.ufull + kUnitRing;
+  sm.uring = reinterpret_cast<volatile int*>(sm.uempty + kUnitRing);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -235,6 +241,10 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
       mbar_init(&sm.tempty[b], EW);
     }
     mbar_init(sm.drain, 1);
+    for (int r = 0; r < kUnitRing; ++r) {
+      mbar_init(&sm.ufull[r], 1);
+      mbar_init(&sm.uempty[r], 1 + EW);   // the MMA thread and one lane of every epilogue warp
+    }
     *sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -269,7 +279,17 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
       int s = 0, issued = 0;
       uint32_t ph = 0;                 // phase parity of the current use of stage s
       bool ok = true;
-      for (int u = p.unit0 + cid; ok && u < p.n_units; u += ncl) {
+      int ur = 0;
+      uint32_t urph = 0;               // unit ring slot and its phase parity
+      for (int k = 0; ok; ++k) {
+        // the next unit: claimed from the counter, or every gridDim-th; published to the ring
+        const int u = p.ucount ? p.unit0 + (int)atomicAdd(p.ucount, 1u) : p.unit0 + cid + k * ncl;
+        const bool done = u >= p.n_units;
+        if (!mbar_wait(&sm.uempty[ur], urph ^ 1u, sm.abort_flag, p.status)) { ok = false; break; }
+        sm.uring[ur] = done ? -1 : u;
+        mbar_arrive(&sm.ufull[ur]);
+        if (++ur == kUnitRing) { ur = 0; urph ^= 1u; }
+        if (done) break;
         const Unit U = unit_info<STREAM>(p, u);
         JobIter jt{0, 0};
         for (int j = 0; ok && j < U.njobs_pm; ++j) {
@@ -355,7 +375,14 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
       int s = 0, b = 0;
       uint32_t ph = 0, tph = 0;        // stage phase; TMEM buffer phase (flips every second job)
       bool ok = true;
-      for (int u = p.unit0 + cid; ok && u < p.n_units; u += ncl) {
+      int ur = 0;
+      uint32_t urph = 0;
+      while (ok) {
+        if (!mbar_wait(&sm.ufull[ur], urph, sm.abort_flag, p.status)) { ok = false; break; }
+        const int u = sm.uring[ur];
+        mbar_arrive(&sm.uempty[ur]);
+        if (++ur == kUnitRing) { ur = 0; urph ^= 1u; }
+        if (u < 0) break;
         const Unit U = unit_info<STREAM>(p, u);
         JobIter jt{0, 0};
         for (int j = 0; ok && j < U.njobs_pm; ++j) {
@@ -450,7 +477,22 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
     int b = 0;
     uint32_t tph = 0;                  // TMEM buffer phase (flips every second job)
     bool ok = true;
-    for (int u = p.unit0 + cid; ok && u < p.n_units; u += ncl) {
+    int ur = 0;
+    uint32_t urph = 0;
+    while (ok) {
+      int u = -1, u_ok = 1;
+      if (lane == 0) {
+        u_ok = mbar_wait(&sm.ufull[ur], urph, sm.abort_flag, p.status) ? 1 : 0;
+        if (u_ok) {
+          u = sm.uring[ur];
+          mbar_arrive(&sm.uempty[ur]);
+        }
+      }
+      u_ok = __shfl_sync(0xffffffffu, u_ok, 0);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (!u_ok) { ok = false; break; }
+      if (++ur == kUnitRing) { ur = 0; urph ^= 1u; }
+      if (u < 0) break;
       const Unit U = unit_info<STREAM>(p, u);
       JobIter jt{0, 0};
       for (int j = 0; j < U.njobs; ++j, b ^= 1, tph ^= (uint32_t)(b == 0)) {
@@ -835,7 +877,7 @@ size_t tile_smem_bytes(int mode, int stages, int H) {
   const size_t sacc = heads ? (size_t)(epi_warps(mode) / 4) * H * kBlockM * 4 : 0;
   // LOO: a 16-byte sigma slot per 4 tokens of each epilogue warp's column group
   const size_t rsc = mode == kModeLOO ? (size_t)epi_warps(mode) * (2 * kBlockN / (epi_warps(mode) / 4) / 4) * 16 : 0;
-  return 1024 + (size_t)stages * kStageBytes + sacc + rsc + (size_t)(2 * stages + 5) * 8 + 8;
+  return 1024 + (size_t)stages * kStageBytes + sacc + rsc + (size_t)(2 * stages + 5) * 8 + 8 + (size_t)kUnitRing * 20;
 }
 
 // Launches `grid` CTAs.  With grid == 0 it only reports in *grid how many CTAs

@@ -37,6 +37,7 @@ constexpr __host__ __device__ int block_threads(int mode) { return 64 + 32 * epi
 // FO / ADD / LOO units: sets of 256 tokens per unit (one partial sum per unit)
 constexpr int kHeadSets = 2;
 constexpr int kTmemCols = 512;                        // 2 accumulator buffers x 256 columns
+constexpr int kUnitRing = 4;                          // unit ids the TMA warp publishes ahead of the others
 constexpr int kMaxDynSmem = 232448;                   // 227 KB opt-in limit per block
 
 enum TileMode : int {
@@ -68,6 +69,8 @@ struct TileParams {
   int32_t nkb_HD, ls_HD;   // streaming: K blocks over H*dh, 16-wide slices in the last one
   int32_t spp;             // streaming: 16-wide K slices per head (d_head / 16)
   uint32_t* status;
+  uint32_t* ucount;        // when set, CTAs claim units from this counter (zero at launch) instead of
+                           // taking every gridDim-th unit; each unit writes its own slots either way
   float* partial;          // FO/ADD/LOO: [H][I_pad / 64][n_chunks][column group][64]; x': [column tile][group][T_pad]
   __half* M16;             // fold output
   __half* alpha16;         // alpha output

@@ -22,10 +22,13 @@
 // a thread.  The fold: A = the same 128 weight rows, B = 256 columns of
 // gamma*Wo^T.  The alpha, x', c_h and ||b_gk||^2 passes: A = the third tile
 // (tokens, or neurons), B = the first two.
-// Work is a fixed list of units, each a short list of jobs; CTAs take units
-// round-robin.  Which CTA computes a unit never changes its result, and
-// every unit writes its own partial sums, so the outputs do not depend on
-// the grid size.
+// Work is a fixed list of units, each a short list of jobs.  The TMA warp
+// picks a CTA's next unit -- claimed from a counter in the head passes, so
+// that CTAs on faster SMs take more of them, else every gridDim-th -- and
+// publishes its id through a small shared-memory ring that the MMA thread and
+// the epilogue warps read in order.  Which CTA computes a unit never changes
+// its result, and every unit writes its own partial sums, so the outputs do
+// not depend on the grid size or on which CTA claimed what.
 #include "launch.cuh"
 #include "sm103_primitives.cuh"
 #include "tile_kernel.cuh"

@@ -49,8 +49,8 @@ KERNEL_SOURCES = ("tile_kernel.cu", "tile_kernel.cuh", "sm103_primitives.cuh", "
 MOMENT_SOURCES = ("moment_kernel.cu", "moment_kernel.cuh", "sm103_primitives.cuh", "scales.cuh", "launch.cuh")
 TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass), third FO launch of
-    # `python bench.py --steps 2 --warmup 3 --no-cpu-baseline --e2e-steps 0`: 458.98 + 49.47 MB
-    ("qwen3_0p6b_layer", "fo", 65536): {"bytes": 508.45e6, "src": "177c9d8b85814bf2"},
+    # `python bench.py --steps 2 --warmup 3 --no-cpu-baseline --e2e-steps 0`: 479.66 + 49.72 MB
+    ("qwen3_0p6b_layer", "fo", 65536): {"bytes": 529.38e6, "src": "bcfc3f4ae7ec8d2c"},
 }
 
 

@@ -78,3 +78,81 @@ def test_a_mismatched_permutation_changes_the_function():
     bad = dict(wp)
     bad["Wo"] = w["Wo"]
     assert np.max(np.abs(LF.layer_forward(x, bad, H, G, dh) - LF.layer_forward(x, w, H, G, dh))) > 1e-3
+
+
+def test_attention_is_causal():
+    """Changing later tokens leaves every earlier token's attention output unchanged."""
+    rng = np.random.default_rng(5)
+    T, D, H, G, dh = 7, 16, 4, 2, 8
+    w = _weights(rng, D, H, G, dh, 8)
+    x = rng.standard_normal((T, D))
+    y = x.copy()
+    y[4:] = rng.standard_normal((T - 4, D))
+    a, b = LF.attention_heads(x, w, H, G, dh), LF.attention_heads(y, w, H, G, dh)
+    np.testing.assert_allclose(a[:4], b[:4], rtol=1e-14, atol=1e-14)
+    assert np.max(np.abs(a[4:] - b[4:])) > 1e-3
+
+
+def test_equal_scores_average_the_causal_prefix():
+    """With W_q = 0 every score is 0, so each token's output is the mean of the values
+    of the tokens up to it (its KV group's values)."""
+    rng = np.random.default_rng(6)
+    T, D, H, G, dh = 6, 16, 4, 2, 8
+    w = _weights(rng, D, H, G, dh, 8)
+    w["Wq"] = np.zeros_like(w["Wq"])
+    x = rng.standard_normal((T, D))
+    out = LF.attention_heads(x, w, H, G, dh)
+    v = (LF.rmsnorm(x, w["g_attn"]) @ w["Wv"].T).reshape(T, G, dh)
+    for h in range(H):
+        g = h // (H // G)
+        for t in range(T):
+            np.testing.assert_allclose(out[t, h], v[:t + 1, g].mean(axis=0), rtol=1e-12, atol=1e-14)
+
+
+def test_attention_against_scalar_loops():
+    """Grouped-query causal softmax attention, written out with scalar loops on a tiny
+    layer (no q/k norms): scores q.k / sqrt(d), masked above the diagonal, softmax over
+    the keys, the values of query head h's KV group h // (H / G)."""
+    import math
+    rng = np.random.default_rng(7)
+    T, D, H, G, dh = 5, 6, 4, 2, 4
+    w = _weights(rng, D, H, G, dh, 8, qk_norm=False)
+    x = rng.standard_normal((T, D))
+    z = LF.rmsnorm(x, w["g_attn"])
+    q = LF.rope((z @ w["Wq"].T).reshape(T, H, dh))
+    k = LF.rope((z @ w["Wk"].T).reshape(T, G, dh))
+    v = (z @ w["Wv"].T).reshape(T, G, dh)
+    out = LF.attention_heads(x, w, H, G, dh)
+    for h in range(H):
+        g = h // (H // G)
+        for t in range(T):
+            sc = [sum(q[t, h, i] * k[s, g, i] for i in range(dh)) / math.sqrt(dh) for s in range(t + 1)]
+            m = max(sc)
+            e = [math.exp(c - m) for c in sc]
+            tot = sum(e)
+            for i in range(dh):
+                ref = sum(e[s] / tot * v[s, g, i] for s in range(t + 1))
+                assert abs(out[t, h, i] - ref) <= 1e-12 * (1 + abs(ref))
+
+
+def test_ffn_against_scalar_loops():
+    """With W_o = 0 the attention adds nothing, and the layer is x + FFN(rmsnorm(x) g):
+    SwiGLU written out with scalar loops, rms over the row with eps = 1e-6."""
+    import math
+    rng = np.random.default_rng(8)
+    T, D, H, G, dh, I = 3, 5, 2, 1, 4, 6
+    w = _weights(rng, D, H, G, dh, I, qk_norm=False)
+    w["Wo"] = np.zeros_like(w["Wo"])
+    x = rng.standard_normal((T, D))
+    y = LF.layer_forward(x, w, H, G, dh)
+    for t in range(T):
+        r = math.sqrt(sum(x[t, d] ** 2 for d in range(D)) / D + 1e-6)
+        z = [x[t, d] / r * w["g_ffn"][d] for d in range(D)]
+        act = []
+        for i in range(I):
+            gi = sum(z[d] * w["Wg"][i, d] for d in range(D))
+            ui = sum(z[d] * w["Wu"][i, d] for d in range(D))
+            act.append(gi / (1.0 + math.exp(-gi)) * ui)
+        for j in range(D):
+            ref = x[t, j] + sum(act[i] * w["Wd"][j, i] for i in range(I))
+            assert abs(y[t, j] - ref) <= 1e-12 * (1 + abs(ref))

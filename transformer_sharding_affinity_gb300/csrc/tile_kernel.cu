@@ -23,10 +23,10 @@
 // gamma*Wo^T.  The alpha, x', c_h and ||b_gk||^2 passes: A = the third tile
 // (tokens, or neurons), B = the first two.
 // Work is a fixed list of units, each a short list of jobs.  The TMA warp
-// picks a CTA's next unit -- claimed from a counter in the head passes, so
-// that CTAs on faster SMs take more of them, else every gridDim-th -- and
-// publishes its id through a small shared-memory ring that the MMA thread and
-// the epilogue warps read in order.  Which CTA computes a unit never changes
+// picks a CTA's next unit -- every gridDim-th, except that in the head passes
+// the last two rounds are claimed from a counter, so that CTAs on faster SMs
+// take more of them -- and publishes its id through a small shared-memory ring
+// that the MMA thread and the epilogue warps read in order.  Which CTA computes a unit never changes
 // its result, and every unit writes its own partial sums, so the outputs do
 // not depend on the grid size or on which CTA claimed what.
 #include "launch.cuh"
@@ -284,9 +284,14 @@ __global__ void __launch_bounds__(block_threads(MODE), 1)
       bool ok = true;
       int ur = 0;
       uint32_t urph = 0;               // unit ring slot and its phase parity
+      // With a counter, the units before the last two rounds still go every gridDim-th (the
+      // CTAs then walk the token tiles in step, which keeps them in L2) and the rest are
+      // claimed, which evens out the CTAs' finishing times.
+      const int fixed_rounds = p.ucount ? max(0, (p.n_units - p.unit0) / ncl - 2) : 1 << 30;
       for (int k = 0; ok; ++k) {
-        // the next unit: claimed from the counter, or every gridDim-th; published to the ring
-        const int u = p.ucount ? p.unit0 + (int)atomicAdd(p.ucount, 1u) : p.unit0 + cid + k * ncl;
+        // the next unit, published to the ring
+        const int u = k < fixed_rounds ? p.unit0 + cid + k * ncl
+                                       : p.unit0 + fixed_rounds * ncl + (int)atomicAdd(p.ucount, 1u);
         const bool done = u >= p.n_units;
         if (!mbar_wait(&sm.uempty[ur], urph ^ 1u, sm.abort_flag, p.status)) { ok = false; break; }
         sm.uring[ur] = done ? -1 : u;
